@@ -1,0 +1,272 @@
+/*
+ * rpa.h -- C ABI of the GB300 (sm_103a) ragged paged attention library.
+ *
+ * Four operations, each one asynchronous call on a caller-supplied CUDA stream:
+ *
+ *   rpa_forward          ragged paged attention over a packed prefill+decode batch
+ *                        (tpu-inference "ragged_paged_attention/v2/kernel.py",
+ *                        ref_ragged_paged_attention and ragged_paged_attention).
+ *   rpa_update_kv_cache  scatter of the batch's new K/V tokens into their pages
+ *                        (no counterpart on the pages beyond the v2 wrapper's TODO for a
+ *                        cache-write kernel; defined like the MLA update_kv_cache).
+ *   mla_rpa_forward      MLA latent attention with its cache update
+ *                        (tpu-inference "mla/v1/kernel.py", update_kv_cache and
+ *                        mla_ragged_paged_attention / ref_mla_ragged_paged_attention).
+ *   sparse_mla_forward   DSA sparse MLA over selected units of a paged latent cache
+ *                        (sglang-jax "dsa/sparse_mla_prefill.py", sparse_mla_attention and
+ *                        _sparse_mla_kernel_chunked_hminor).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is a DEVICE pointer owned by the caller; the library
+ *     never frees or retains it.  Row-major, densely packed, 16-byte aligned.
+ *   - The library allocates no memory.  Scratch (work lists, split-KV partials,
+ *     the device error word) lives in a caller-provided workspace whose size the
+ *     matching *_workspace_size() call returns; the workspace must be 256-byte
+ *     aligned, must be zero-filled once after it is allocated (the library keeps it
+ *     consistent from then on), and must not be shared by two calls in flight at once.
+ *   - Calls are asynchronous on `stream` and never synchronise with the host, so
+ *     they can be captured in a CUDA graph.  Sizes read from device memory
+ *     (num_seqs, cu_q_lens, kv_lens, page tables, indices) are validated on the
+ *     device: a bad value sets a bit in the workspace's error word, the offending
+ *     sequence/query is skipped (its output rows are left untouched), and no
+ *     out-of-range address is ever formed.  rpa_check_device_status() reads the word.
+ *   - Host-side arguments (shapes, dtypes, options) are validated before any launch;
+ *     a bad one returns a negative status and launches nothing.
+ *   - Optional values use a "none" encoding: sliding_window = 0, soft_cap = 0,
+ *     k_scale = v_scale = 0, mask_value = NaN (meaning -0.7 * FLT_MAX, the pages'
+ *     DEFAULT_MASK_VALUE).
+ *   - Masked logits are given zero softmax weight.  The pages add (RPA) or
+ *     substitute (MLA) mask_value; with a mask value at or below -1e30 that weight
+ *     underflows to exactly zero in float32 because the key at the query's own
+ *     position is always visible, so the two agree.  A mask_value above -1e30 is
+ *     rejected with RPA_ERR_UNSUPPORTED.
+ */
+#ifndef RPA_GB300_RPA_H_
+#define RPA_GB300_RPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RPA_ABI_VERSION 1
+
+/* Every entry point below is exported from the shared library. */
+#if defined(__GNUC__)
+#define RPA_API __attribute__((visibility("default")))
+#else
+#define RPA_API
+#endif
+
+/* Status codes returned by every call. */
+typedef enum {
+    RPA_OK = 0,
+    RPA_ERR_NULL = -1,          /* a required pointer is NULL */
+    RPA_ERR_SHAPE = -2,         /* inconsistent sizes (Hq % Hkv, odd combined heads, ...) */
+    RPA_ERR_DTYPE = -3,         /* unsupported dtype combination */
+    RPA_ERR_VALUE = -4,         /* bad option value (sliding_window < 0, soft_cap < 0, ...) */
+    RPA_ERR_UNSUPPORTED = -5,   /* valid on the pages but not implemented here */
+    RPA_ERR_CUDA = -6,          /* a CUDA runtime call failed (see rpa_last_error) */
+    RPA_ERR_DEVICE_CHECK = -7,  /* rpa_check_device_status found a device-side error */
+    RPA_ERR_WORKSPACE = -8      /* workspace NULL, misaligned or too small */
+} rpa_status;
+
+/* Element types. */
+typedef enum {
+    RPA_DTYPE_BF16 = 1,
+    RPA_DTYPE_FP8_E4M3 = 2,
+    RPA_DTYPE_F32 = 3
+} rpa_dtype;
+
+/* Bits of the device error word (OR-ed together). */
+#define RPA_DEV_ERR_NUM_SEQS   0x01u  /* num_seqs / distribution outside [0, max_num_seqs] */
+#define RPA_DEV_ERR_Q_LEN      0x02u  /* q_len < 0 or q_len > kv_len for some sequence */
+#define RPA_DEV_ERR_KV_LEN     0x04u  /* cdiv(kv_len, page_size) > pages_per_seq */
+#define RPA_DEV_ERR_PAGE       0x08u  /* a used page index outside [0, total_num_pages) */
+#define RPA_DEV_ERR_TOKENS     0x10u  /* cu_q_lens[num_seqs] > max_num_tokens or not monotone */
+#define RPA_DEV_ERR_POSITION   0x20u  /* sparse: query position outside [0, seq_len) */
+
+/* CUDA stream handle (ABI-compatible with cudaStream_t). */
+typedef struct CUstream_st* rpa_stream_t;
+
+/* ---------------------------------------------------------------------- */
+/* Standard ragged paged attention                                         */
+/* ---------------------------------------------------------------------- */
+
+/* Problem description shared by rpa_forward / rpa_update_kv_cache.
+ * Layouts (tpu-inference RPA v2, ref_ragged_paged_attention):
+ *   q          [max_num_tokens, num_q_heads, head_dim]               q_dtype (bf16)
+ *   kv_pages   [total_num_pages, page_size, num_combined_kv_heads, head_dim]  kv_dtype;
+ *              combined head 2j holds K and 2j+1 holds V of KV head j
+ *   kv_lens    int32 [max_num_seqs]   keys of each sequence, including its new tokens
+ *   page_indices int32 [max_num_seqs, pages_per_seq]   logical -> physical page
+ *   cu_q_lens  int32 [max_num_seqs + 1]   sequence i owns tokens [cu_q_lens[i], cu_q_lens[i+1])
+ *   num_seqs   int32 [1] (device)   only the first num_seqs sequences are processed
+ *   out        [max_num_tokens, num_q_heads, head_dim]   q_dtype; rows of tokens
+ *              >= cu_q_lens[num_seqs] are not written
+ * Query j of sequence i sits at position kv_len - q_len + j; key k is visible when
+ * k <= q_pos and (sliding_window == 0 or k > q_pos - sliding_window).  Q head h reads
+ * KV head h / (num_q_heads / num_kv_heads).  Logits: sm_scale * q.k, then
+ * soft_cap * tanh(x / soft_cap) when soft_cap != 0.  When k_scale (v_scale) != 0 the
+ * keys (values) are dequantised as bf16(float(k) * k_scale) before the dot products. */
+typedef struct {
+    uint32_t struct_size;        /* sizeof(rpa_params) */
+    uint32_t version;            /* RPA_ABI_VERSION */
+    int32_t max_num_tokens;
+    int32_t num_q_heads;
+    int32_t num_combined_kv_heads;
+    int32_t head_dim;            /* 64, 128 or 256 */
+    int32_t total_num_pages;
+    int32_t page_size;
+    int32_t max_num_seqs;
+    int32_t pages_per_seq;
+    int32_t q_dtype;             /* RPA_DTYPE_BF16 */
+    int32_t kv_dtype;            /* RPA_DTYPE_BF16 or RPA_DTYPE_FP8_E4M3 */
+    float sm_scale;
+    int32_t sliding_window;      /* 0 = none */
+    float soft_cap;              /* 0 = none */
+    float mask_value;            /* NaN = default */
+    float k_scale;               /* 0 = none */
+    float v_scale;               /* 0 = none */
+} rpa_params;
+
+/* Bytes of workspace rpa_forward needs for these maxima. */
+RPA_API int rpa_workspace_size(const rpa_params* p, size_t* bytes);
+
+/* Ragged paged attention over the whole batch (every sequence, prefill and decode,
+ * in one call).  `out` must not alias `q` or `kv_pages`. */
+RPA_API int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs,
+                void* out, void* workspace, size_t workspace_bytes, rpa_stream_t stream);
+
+/* Write token j of sequence i (position kv_len - q_len + j) into slot
+ * page_indices[i, pos / page_size], pos % page_size of kv_pages, in place:
+ * new_k[t, g, :] to combined head 2g and new_v[t, g, :] to 2g+1.
+ *   new_k, new_v  [max_num_tokens, num_combined_kv_heads / 2, head_dim]  kv_dtype
+ * Bytes are copied unchanged; every other byte of kv_pages is left as it was.
+ * `workspace` is optional (may be NULL): when given, device-side metadata errors are
+ * recorded in its error word (it needs at least 256 bytes). */
+RPA_API int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const void* new_v, void* kv_pages,
+                        const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
+                        const int32_t* num_seqs, void* workspace, size_t workspace_bytes,
+                        rpa_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* MLA latent ragged paged attention                                       */
+/* ---------------------------------------------------------------------- */
+
+/* Layouts (tpu-inference MLA v1, mla_ragged_paged_attention):
+ *   ql_nope    [max_num_tokens, num_q_heads, lkv_dim]        bf16
+ *   q_pe       [max_num_tokens, num_q_heads, r_dim]          bf16
+ *   new_kv_c   [max_num_tokens, lkv_dim]                     bf16
+ *   new_k_pe   [max_num_tokens, r_dim]                       bf16
+ *   cache_kv_c [total_num_pages, page_size / kv_packing, kv_packing, lkv_dim_pad] bf16
+ *   cache_k_pe [total_num_pages, page_size / kv_packing, kv_packing, r_dim_pad]   bf16
+ *              (token t of a page is row t of the page: same bytes as [P, page_size, D])
+ *   kv_lens    int32 [max_num_seqs]; page_indices int32 [max_num_seqs * pages_per_seq]
+ *   cu_q_lens  int32 [max_num_seqs + 1]; distribution int32 [3] (device):
+ *              (decode_end, prefill_end, num_seqs); only distribution[2] bounds the work
+ *   out        [max_num_tokens, num_q_heads, lkv_dim]        bf16
+ * Key = [kv_c | k_pe], value = kv_c, one latent head shared by all q heads; masked
+ * logits are replaced by mask_value (see the header note on masking). */
+typedef struct {
+    uint32_t struct_size;        /* sizeof(mla_params) */
+    uint32_t version;            /* RPA_ABI_VERSION */
+    int32_t max_num_tokens;
+    int32_t num_q_heads;         /* multiple of 64 */
+    int32_t lkv_dim;             /* 512 */
+    int32_t r_dim;               /* 64 */
+    int32_t lkv_dim_pad;         /* align(lkv_dim, 128) */
+    int32_t r_dim_pad;           /* align(r_dim, 128) */
+    int32_t total_num_pages;
+    int32_t page_size;
+    int32_t kv_packing;          /* 2 for bf16 */
+    int32_t max_num_seqs;
+    int32_t pages_per_seq;
+    float sm_scale;
+    int32_t sliding_window;      /* 0 = none */
+    float soft_cap;              /* 0 = none */
+    float mask_value;            /* NaN = default */
+} mla_params;
+
+RPA_API int mla_workspace_size(const mla_params* p, size_t* bytes);
+
+/* Scatter the batch's new latent rows into the caches, in place (update_kv_cache):
+ * token j of sequence i < distribution[2] goes to position kv_len - q_len + j; its
+ * kv_c row is copied to cache_kv_c and its k_pe row to cache_k_pe with columns
+ * [r_dim, r_dim_pad) written as zero.  `workspace` is optional, as for
+ * rpa_update_kv_cache. */
+RPA_API int mla_update_kv_cache(const mla_params* p, const void* new_kv_c, const void* new_k_pe, void* cache_kv_c,
+                        void* cache_k_pe, const int32_t* kv_lens, const int32_t* page_indices,
+                        const int32_t* cu_q_lens, const int32_t* distribution, void* workspace,
+                        size_t workspace_bytes, rpa_stream_t stream);
+
+/* mla_update_kv_cache followed by attention of every query token over the updated
+ * caches (the caches are modified in place). */
+RPA_API int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, const void* new_kv_c,
+                    const void* new_k_pe, void* cache_kv_c, void* cache_k_pe, const int32_t* kv_lens,
+                    const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* distribution,
+                    void* out, void* workspace, size_t workspace_bytes, rpa_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* DSA sparse MLA                                                           */
+/* ---------------------------------------------------------------------- */
+
+/* Layouts (sglang-jax sparse_mla_attention, paged per-request mode):
+ *   q          [batch, num_queries, num_heads, dk]    bf16 (dk = 576 = 512 + 64)
+ *   cache      [total_num_pages * page_size, row_stride]  bf16 (row_stride >= dk; the
+ *              [P, page_size / packing, packing, row_stride] cache has these bytes)
+ *   indices    int32 [batch, num_queries, topk]   unit ids, -1 = empty slot
+ *   positions  int32 [batch, num_queries]         query positions (causal bound)
+ *   page_table int32 [batch, max_pages]           logical -> physical page
+ *   out        [batch, num_queries, num_heads, dv]  float32 (dv = 512)
+ * A unit u covers tokens [u * read_block, (u + 1) * read_block).  Token kp of slot i
+ * is a key when u >= 0, kp <= position and kp < seq_len; it is read from row
+ * page_table[b, kp / page_size] * page_size + kp % page_size.  Keys form a multiset
+ * (a unit named twice counts twice); a query with no key outputs zeros.
+ * read_block must divide page_size. */
+typedef struct {
+    uint32_t struct_size;        /* sizeof(sparse_params) */
+    uint32_t version;            /* RPA_ABI_VERSION */
+    int32_t batch;
+    int32_t num_queries;
+    int32_t num_heads;           /* multiple of 64 */
+    int32_t dk;                  /* 576 */
+    int32_t dv;                  /* 512 */
+    int32_t row_stride;          /* elements per cache row (640) */
+    int32_t topk;
+    int32_t read_block;
+    int32_t page_size;
+    int32_t max_pages;
+    int32_t total_num_pages;
+    int32_t seq_len;
+    float sm_scale;              /* required, > 0 */
+} sparse_params;
+
+RPA_API int sparse_mla_workspace_size(const sparse_params* p, size_t* bytes);
+
+RPA_API int sparse_mla_forward(const sparse_params* p, const void* q, const void* cache, const int32_t* indices,
+                       const int32_t* positions, const int32_t* page_table, float* out, void* workspace,
+                       size_t workspace_bytes, rpa_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Status and diagnostics                                                   */
+/* ---------------------------------------------------------------------- */
+
+/* Synchronises `stream`, reads the workspace's device error word into *bits (may be
+ * NULL) and clears it.  Returns RPA_ERR_DEVICE_CHECK when any bit was set. */
+RPA_API int rpa_check_device_status(void* workspace, uint32_t* bits, rpa_stream_t stream);
+
+/* Thread-local description of the last failed call ("" if none). */
+RPA_API const char* rpa_last_error(void);
+
+/* RPA_ABI_VERSION of the loaded library. */
+RPA_API int rpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RPA_GB300_RPA_H_ */

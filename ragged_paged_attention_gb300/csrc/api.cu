@@ -1,0 +1,482 @@
+// C ABI of the library (declared in include/rpa.h): host-side validation, workspace
+// layout and kernel launches.  Nothing here touches tensor data on the host.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace rpa;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(RPA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+int num_sms_current() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float resolve_mask(float m) { return isnan(m) ? -0.7f * 3.402823466e38f : m; }
+
+// ---------------------------- RPA ----------------------------------------
+struct RpaLayout {
+    size_t items_dec, items_pre, tickets, pml, po, total;
+    int max_dec, max_pre;
+};
+
+int check_rpa_params(const rpa_params* p) {
+    if (!p) return fail(RPA_ERR_NULL, "params is NULL");
+    if (p->struct_size < sizeof(rpa_params)) return fail(RPA_ERR_VALUE, "rpa_params.struct_size too small");
+    if (p->version != RPA_ABI_VERSION) return fail(RPA_ERR_VALUE, "rpa_params.version %u != %d", p->version, RPA_ABI_VERSION);
+    if (p->max_num_tokens <= 0 || p->num_q_heads <= 0 || p->num_combined_kv_heads <= 0 || p->total_num_pages <= 0 ||
+        p->page_size <= 0 || p->max_num_seqs <= 0 || p->pages_per_seq <= 0)
+        return fail(RPA_ERR_SHAPE, "all sizes must be positive");
+    if (p->num_combined_kv_heads % 2) return fail(RPA_ERR_SHAPE, "num_combined_kv_heads must be even (K and V interleaved)");
+    const int hkv = p->num_combined_kv_heads / 2;
+    if (p->num_q_heads % hkv) return fail(RPA_ERR_SHAPE, "num_q_heads %d not divisible by num_kv_heads %d", p->num_q_heads, hkv);
+    if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
+        return fail(RPA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", p->head_dim);
+    if (p->q_dtype != RPA_DTYPE_BF16) return fail(RPA_ERR_DTYPE, "q_dtype must be bf16");
+    if (p->kv_dtype != RPA_DTYPE_BF16 && p->kv_dtype != RPA_DTYPE_FP8_E4M3)
+        return fail(RPA_ERR_DTYPE, "kv_dtype must be bf16 or fp8 e4m3");
+    if (!isfinite(p->sm_scale)) return fail(RPA_ERR_VALUE, "sm_scale must be finite");
+    if (p->sliding_window < 0) return fail(RPA_ERR_VALUE, "sliding_window must be positive (0 = none)");
+    if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
+    if (!isfinite(p->k_scale) || !isfinite(p->v_scale)) return fail(RPA_ERR_VALUE, "k_scale/v_scale must be finite");
+    if (resolve_mask(p->mask_value) > -1e30f)
+        return fail(RPA_ERR_UNSUPPORTED, "mask_value %g > -1e30: masked keys would carry weight", p->mask_value);
+    if ((long long)p->max_num_seqs * p->pages_per_seq > INT32_MAX) return fail(RPA_ERR_SHAPE, "page table too large");
+    return RPA_OK;
+}
+
+RpaLayout rpa_layout(const rpa_params* p) {
+    RpaLayout L;
+    const int hkv = p->num_combined_kv_heads / 2;
+    const int G = p->num_q_heads / hkv;
+    const int groups = cdiv(hkv, kDecodeHeads);
+    L.max_dec = kDecodeTargetCtas + groups * p->max_num_seqs;
+    L.max_pre = hkv * (int)((long long)p->max_num_tokens * G / kPrefillRows + p->max_num_seqs + 1);
+    size_t off = kWsHeaderBytes;
+    L.items_dec = off;
+    off = align_up(off + sizeof(WorkItem) * (size_t)L.max_dec);
+    L.items_pre = off;
+    off = align_up(off + sizeof(WorkItem) * (size_t)L.max_pre);
+    L.tickets = off;
+    off = align_up(off + sizeof(int) * (size_t)L.max_dec);
+    L.pml = off;
+    off = align_up(off + sizeof(float) * 2 * kDecodeHeads * 16 * (size_t)L.max_dec);
+    L.po = off;
+    off = align_up(off + sizeof(float) * (size_t)p->head_dim * kDecodeHeads * 16 * (size_t)L.max_dec);
+    L.total = off;
+    return L;
+}
+
+int check_workspace(const void* ws, size_t have, size_t need) {
+    if (!ws) return fail(RPA_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(RPA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (have < need) return fail(RPA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", have, need);
+    return RPA_OK;
+}
+
+// ---------------------------- MLA ----------------------------------------
+struct LatLayout {
+    size_t items, tickets, pml, po, total;
+    int max_items;
+};
+
+int check_mla_params(const mla_params* p) {
+    if (!p) return fail(RPA_ERR_NULL, "params is NULL");
+    if (p->struct_size < sizeof(mla_params)) return fail(RPA_ERR_VALUE, "mla_params.struct_size too small");
+    if (p->version != RPA_ABI_VERSION) return fail(RPA_ERR_VALUE, "mla_params.version %u != %d", p->version, RPA_ABI_VERSION);
+    if (p->max_num_tokens <= 0 || p->num_q_heads <= 0 || p->total_num_pages <= 0 || p->page_size <= 0 ||
+        p->max_num_seqs <= 0 || p->pages_per_seq <= 0 || p->kv_packing <= 0)
+        return fail(RPA_ERR_SHAPE, "all sizes must be positive");
+    if (p->page_size % p->kv_packing) return fail(RPA_ERR_SHAPE, "page_size must be divisible by kv_packing");
+    if (p->kv_packing != 2) return fail(RPA_ERR_DTYPE, "kv_packing %d does not match bf16 (2)", p->kv_packing);
+    if (p->lkv_dim_pad != (p->lkv_dim + 127) / 128 * 128 || p->r_dim_pad != (p->r_dim + 127) / 128 * 128)
+        return fail(RPA_ERR_SHAPE, "cache widths must be align(dim, 128)");
+    if (p->lkv_dim % 8 || p->r_dim % 8) return fail(RPA_ERR_SHAPE, "lkv_dim and r_dim must be multiples of 8");
+    if (!isfinite(p->sm_scale)) return fail(RPA_ERR_VALUE, "sm_scale must be finite");
+    if (p->sliding_window < 0) return fail(RPA_ERR_VALUE, "sliding_window must be positive (0 = none)");
+    if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
+    if (resolve_mask(p->mask_value) > -1e30f)
+        return fail(RPA_ERR_UNSUPPORTED, "mask_value %g > -1e30: masked keys would carry weight", p->mask_value);
+    if ((long long)p->max_num_seqs * p->pages_per_seq > INT32_MAX) return fail(RPA_ERR_SHAPE, "page table too large");
+    return RPA_OK;
+}
+
+int check_mla_attn_shape(const mla_params* p) {
+    if (p->lkv_dim != 512 || p->r_dim != 64)
+        return fail(RPA_ERR_UNSUPPORTED, "MLA attention supports lkv_dim 512 and r_dim 64 (got %d, %d)", p->lkv_dim, p->r_dim);
+    if (p->num_q_heads % kLatRows) return fail(RPA_ERR_UNSUPPORTED, "num_q_heads must be a multiple of %d", kLatRows);
+    return RPA_OK;
+}
+
+LatLayout lat_layout(long long max_items) {
+    LatLayout L;
+    L.max_items = (int)max_items;
+    size_t off = kWsHeaderBytes;
+    L.items = off;
+    off = align_up(off + sizeof(WorkItem) * (size_t)max_items);
+    L.tickets = off;
+    off = align_up(off + sizeof(int) * (size_t)max_items);
+    L.pml = off;
+    off = align_up(off + sizeof(float) * 2 * kLatRows * (size_t)max_items);
+    L.po = off;
+    off = align_up(off + sizeof(float) * (size_t)kLatRows * kLatDv * (size_t)max_items);
+    L.total = off;
+    return L;
+}
+
+LatLayout mla_layout(const mla_params* p) {
+    const long long tiles = p->num_q_heads / kLatRows;
+    return lat_layout(kLatTargetCtas + tiles * (long long)p->max_num_tokens + tiles);
+}
+
+// ---------------------------- sparse --------------------------------------
+int check_sparse_params(const sparse_params* p) {
+    if (!p) return fail(RPA_ERR_NULL, "params is NULL");
+    if (p->struct_size < sizeof(sparse_params)) return fail(RPA_ERR_VALUE, "sparse_params.struct_size too small");
+    if (p->version != RPA_ABI_VERSION) return fail(RPA_ERR_VALUE, "sparse_params.version %u != %d", p->version, RPA_ABI_VERSION);
+    if (p->batch <= 0 || p->num_queries <= 0 || p->num_heads <= 0 || p->topk <= 0 || p->read_block <= 0 ||
+        p->page_size <= 0 || p->max_pages <= 0 || p->total_num_pages <= 0 || p->seq_len < 0)
+        return fail(RPA_ERR_SHAPE, "all sizes must be positive");
+    if (p->dk != kLatDk || p->dv != kLatDv)
+        return fail(RPA_ERR_UNSUPPORTED, "sparse MLA supports dk 576 and dv 512 (got %d, %d)", p->dk, p->dv);
+    if (p->row_stride < p->dk || p->row_stride % 8) return fail(RPA_ERR_SHAPE, "row_stride must be >= dk and a multiple of 8");
+    if (p->num_heads % kLatRows) return fail(RPA_ERR_UNSUPPORTED, "num_heads must be a multiple of %d", kLatRows);
+    if (p->page_size % p->read_block) return fail(RPA_ERR_SHAPE, "read_block must divide page_size");
+    if (!(p->sm_scale > 0.f) || !isfinite(p->sm_scale)) return fail(RPA_ERR_VALUE, "sm_scale is required (> 0)");
+    if ((long long)p->topk * p->read_block > INT32_MAX / 2) return fail(RPA_ERR_SHAPE, "topk * read_block too large");
+    if ((long long)p->max_pages * p->page_size < p->seq_len) return fail(RPA_ERR_SHAPE, "max_pages * page_size < seq_len");
+    return RPA_OK;
+}
+
+LatLayout sparse_layout(const sparse_params* p, int* splits) {
+    const int sp = sparse_num_splits(p->batch, p->num_queries, p->num_heads, p->topk * p->read_block);
+    if (splits) *splits = sp;
+    const long long items = (long long)p->batch * p->num_queries * (p->num_heads / kLatRows) * sp;
+    return lat_layout(sp > 1 ? items : 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+int rpa_version(void) { return RPA_ABI_VERSION; }
+
+const char* rpa_last_error(void) { return g_err; }
+
+int rpa_workspace_size(const rpa_params* p, size_t* bytes) {
+    int rc = check_rpa_params(p);
+    if (rc) return rc;
+    if (!bytes) return fail(RPA_ERR_NULL, "bytes is NULL");
+    *bytes = rpa_layout(p).total;
+    return RPA_OK;
+}
+
+int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs, void* out,
+                void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+    int rc = check_rpa_params(p);
+    if (rc) return rc;
+    if (!q || !kv_pages || !kv_lens || !page_indices || !cu_q_lens || !num_seqs || !out)
+        return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
+    if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out)) return fail(RPA_ERR_VALUE, "q, kv_pages and out must be 16-byte aligned");
+    if (out == q || out == kv_pages) return fail(RPA_ERR_VALUE, "out must not alias q or kv_pages");
+    const RpaLayout L = rpa_layout(p);
+    rc = check_workspace(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    RpaArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv_pages = kv_pages;
+    a.kv_lens = kv_lens;
+    a.page_indices = page_indices;
+    a.cu_q_lens = cu_q_lens;
+    a.num_seqs = num_seqs;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.max_num_tokens = p->max_num_tokens;
+    a.num_q_heads = p->num_q_heads;
+    a.num_kv_heads = p->num_combined_kv_heads / 2;
+    a.head_dim = p->head_dim;
+    a.total_num_pages = p->total_num_pages;
+    a.page_size = p->page_size;
+    a.max_num_seqs = p->max_num_seqs;
+    a.pages_per_seq = p->pages_per_seq;
+    a.kv_fp8 = p->kv_dtype == RPA_DTYPE_FP8_E4M3;
+    a.sm_scale = p->sm_scale;
+    a.soft_cap = p->soft_cap;
+    a.sliding_window = p->sliding_window;
+    a.has_scale = p->k_scale != 0.f || p->v_scale != 0.f;
+    a.k_scale_or_one = p->k_scale != 0.f ? p->k_scale : 1.f;
+    a.v_scale_or_one = p->v_scale != 0.f ? p->v_scale : 1.f;
+    a.decode_target_ctas = kDecodeTargetCtas;
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.dec_items = reinterpret_cast<WorkItem*>(ws + L.items_dec);
+    a.pre_items = reinterpret_cast<WorkItem*>(ws + L.items_pre);
+    a.tickets = reinterpret_cast<int*>(ws + L.tickets);
+    a.partial_ml = reinterpret_cast<float*>(ws + L.pml);
+    a.partial_o = reinterpret_cast<float*>(ws + L.po);
+    a.max_dec_items = L.max_dec;
+    a.max_pre_items = L.max_pre;
+    cudaError_t e = launch_rpa_forward(a, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_forward launch");
+    return RPA_OK;
+}
+
+int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const void* new_v, void* kv_pages,
+                        const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
+                        const int32_t* num_seqs, void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+    int rc = check_rpa_params(p);
+    if (rc) return rc;
+    if (!new_k || !new_v || !kv_pages || !kv_lens || !page_indices || !cu_q_lens || !num_seqs)
+        return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
+    if (!aligned16(new_k) || !aligned16(new_v) || !aligned16(kv_pages))
+        return fail(RPA_ERR_VALUE, "new_k, new_v and kv_pages must be 16-byte aligned");
+    if (workspace && workspace_bytes < (size_t)kWsHeaderBytes) return fail(RPA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
+    RpaUpdateArgs a;
+    a.new_k = new_k;
+    a.new_v = new_v;
+    a.kv_pages = kv_pages;
+    a.kv_lens = kv_lens;
+    a.page_indices = page_indices;
+    a.cu_q_lens = cu_q_lens;
+    a.num_seqs = num_seqs;
+    a.err = workspace ? &reinterpret_cast<WsHeader*>(workspace)->error_bits : nullptr;
+    a.max_num_tokens = p->max_num_tokens;
+    a.num_kv_heads = p->num_combined_kv_heads / 2;
+    a.head_dim = p->head_dim;
+    a.esz = p->kv_dtype == RPA_DTYPE_FP8_E4M3 ? 1 : 2;
+    a.total_num_pages = p->total_num_pages;
+    a.page_size = p->page_size;
+    a.max_num_seqs = p->max_num_seqs;
+    a.pages_per_seq = p->pages_per_seq;
+    cudaError_t e = launch_rpa_update(a, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_update_kv_cache launch");
+    return RPA_OK;
+}
+
+int mla_workspace_size(const mla_params* p, size_t* bytes) {
+    int rc = check_mla_params(p);
+    if (rc) return rc;
+    if (!bytes) return fail(RPA_ERR_NULL, "bytes is NULL");
+    *bytes = mla_layout(p).total;
+    return RPA_OK;
+}
+
+static int mla_update_impl(const mla_params* p, const void* new_kv_c, const void* new_k_pe, void* cache_kv_c,
+                           void* cache_k_pe, const int32_t* kv_lens, const int32_t* page_indices,
+                           const int32_t* cu_q_lens, const int32_t* distribution, uint32_t* err, int sms,
+                           cudaStream_t stream) {
+    MlaUpdateArgs a;
+    a.new_kv_c = static_cast<const __nv_bfloat16*>(new_kv_c);
+    a.new_k_pe = static_cast<const __nv_bfloat16*>(new_k_pe);
+    a.cache_kv_c = static_cast<__nv_bfloat16*>(cache_kv_c);
+    a.cache_k_pe = static_cast<__nv_bfloat16*>(cache_k_pe);
+    a.kv_lens = kv_lens;
+    a.page_indices = page_indices;
+    a.cu_q_lens = cu_q_lens;
+    a.distribution = distribution;
+    a.err = err;
+    a.max_num_tokens = p->max_num_tokens;
+    a.lkv_dim = p->lkv_dim;
+    a.r_dim = p->r_dim;
+    a.lkv_pad = p->lkv_dim_pad;
+    a.r_pad = p->r_dim_pad;
+    a.total_num_pages = p->total_num_pages;
+    a.page_size = p->page_size;
+    a.max_num_seqs = p->max_num_seqs;
+    a.pages_per_seq = p->pages_per_seq;
+    cudaError_t e = launch_mla_update(a, sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_update_kv_cache launch");
+    return RPA_OK;
+}
+
+int mla_update_kv_cache(const mla_params* p, const void* new_kv_c, const void* new_k_pe, void* cache_kv_c,
+                        void* cache_k_pe, const int32_t* kv_lens, const int32_t* page_indices,
+                        const int32_t* cu_q_lens, const int32_t* distribution, void* workspace,
+                        size_t workspace_bytes, rpa_stream_t stream) {
+    int rc = check_mla_params(p);
+    if (rc) return rc;
+    if (!new_kv_c || !new_k_pe || !cache_kv_c || !cache_k_pe || !kv_lens || !page_indices || !cu_q_lens ||
+        !distribution)
+        return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
+    if (!aligned16(new_kv_c) || !aligned16(new_k_pe) || !aligned16(cache_kv_c) || !aligned16(cache_k_pe))
+        return fail(RPA_ERR_VALUE, "tensors must be 16-byte aligned");
+    if (workspace && workspace_bytes < (size_t)kWsHeaderBytes) return fail(RPA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
+    return mla_update_impl(p, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
+                           distribution, workspace ? &reinterpret_cast<WsHeader*>(workspace)->error_bits : nullptr,
+                           sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, const void* new_kv_c,
+                    const void* new_k_pe, void* cache_kv_c, void* cache_k_pe, const int32_t* kv_lens,
+                    const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* distribution, void* out,
+                    void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+    int rc = check_mla_params(p);
+    if (rc) return rc;
+    rc = check_mla_attn_shape(p);
+    if (rc) return rc;
+    if (!ql_nope || !q_pe || !new_kv_c || !new_k_pe || !cache_kv_c || !cache_k_pe || !kv_lens || !page_indices ||
+        !cu_q_lens || !distribution || !out)
+        return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
+    if (!aligned16(ql_nope) || !aligned16(q_pe) || !aligned16(new_kv_c) || !aligned16(new_k_pe) ||
+        !aligned16(cache_kv_c) || !aligned16(cache_k_pe) || !aligned16(out))
+        return fail(RPA_ERR_VALUE, "tensors must be 16-byte aligned");
+    if (out == ql_nope || out == cache_kv_c) return fail(RPA_ERR_VALUE, "out must not alias an input");
+    const LatLayout L = mla_layout(p);
+    rc = check_workspace(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    rc = mla_update_impl(p, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
+                         distribution, &reinterpret_cast<WsHeader*>(ws)->error_bits, sms, st);
+    if (rc) return rc;
+    LatentArgs a;
+    memset(&a, 0, sizeof a);
+    a.sparse = 0;
+    a.num_heads = p->num_q_heads;
+    a.sm_scale = p->sm_scale;
+    a.soft_cap = p->soft_cap;
+    a.sliding_window = p->sliding_window;
+    a.ql_nope = static_cast<const __nv_bfloat16*>(ql_nope);
+    a.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+    a.cache_kv_c = static_cast<const __nv_bfloat16*>(cache_kv_c);
+    a.cache_k_pe = static_cast<const __nv_bfloat16*>(cache_k_pe);
+    a.kv_lens = kv_lens;
+    a.page_indices = page_indices;
+    a.cu_q_lens = cu_q_lens;
+    a.distribution = distribution;
+    a.max_num_tokens = p->max_num_tokens;
+    a.max_num_seqs = p->max_num_seqs;
+    a.pages_per_seq = p->pages_per_seq;
+    a.lkv_pad = p->lkv_dim_pad;
+    a.r_pad = p->r_dim_pad;
+    a.out_bf16 = static_cast<__nv_bfloat16*>(out);
+    a.total_num_pages = p->total_num_pages;
+    a.page_size = p->page_size;
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.items = reinterpret_cast<WorkItem*>(ws + L.items);
+    a.tickets = reinterpret_cast<int*>(ws + L.tickets);
+    a.partial_ml = reinterpret_cast<float*>(ws + L.pml);
+    a.partial_o = reinterpret_cast<float*>(ws + L.po);
+    a.max_items = L.max_items;
+    cudaError_t e = launch_mla_forward(a, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_rpa_forward launch");
+    return RPA_OK;
+}
+
+int sparse_mla_workspace_size(const sparse_params* p, size_t* bytes) {
+    int rc = check_sparse_params(p);
+    if (rc) return rc;
+    if (!bytes) return fail(RPA_ERR_NULL, "bytes is NULL");
+    *bytes = sparse_layout(p, nullptr).total;
+    return RPA_OK;
+}
+
+int sparse_mla_forward(const sparse_params* p, const void* q, const void* cache, const int32_t* indices,
+                       const int32_t* positions, const int32_t* page_table, float* out, void* workspace,
+                       size_t workspace_bytes, rpa_stream_t stream) {
+    int rc = check_sparse_params(p);
+    if (rc) return rc;
+    if (!q || !cache || !indices || !positions || !page_table || !out) return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
+    if (!aligned16(q) || !aligned16(cache) || !aligned16(out)) return fail(RPA_ERR_VALUE, "q, cache and out must be 16-byte aligned");
+    int splits = 1;
+    const LatLayout L = sparse_layout(p, &splits);
+    rc = check_workspace(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    LatentArgs a;
+    memset(&a, 0, sizeof a);
+    a.sparse = 1;
+    a.num_heads = p->num_heads;
+    a.sm_scale = p->sm_scale;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.cache = static_cast<const __nv_bfloat16*>(cache);
+    a.indices = indices;
+    a.positions = positions;
+    a.page_table = page_table;
+    a.batch = p->batch;
+    a.num_queries = p->num_queries;
+    a.topk = p->topk;
+    a.read_block = p->read_block;
+    a.max_pages = p->max_pages;
+    a.seq_len = p->seq_len;
+    a.row_stride = p->row_stride;
+    a.sparse_splits = splits;
+    a.out_f32 = out;
+    a.total_num_pages = p->total_num_pages;
+    a.page_size = p->page_size;
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.items = nullptr;
+    a.tickets = reinterpret_cast<int*>(ws + L.tickets);
+    a.partial_ml = reinterpret_cast<float*>(ws + L.pml);
+    a.partial_o = reinterpret_cast<float*>(ws + L.po);
+    a.max_items = L.max_items;
+    cudaError_t e = launch_sparse_forward(a, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_forward launch");
+    return RPA_OK;
+}
+
+int rpa_check_device_status(void* workspace, uint32_t* bits, rpa_stream_t stream) {
+    if (!workspace) return fail(RPA_ERR_NULL, "workspace is NULL");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_check_device_status sync");
+    e = cudaMemcpy(&v, &reinterpret_cast<WsHeader*>(workspace)->error_bits, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_check_device_status read");
+    if (v) {
+        e = cudaMemset(&reinterpret_cast<WsHeader*>(workspace)->error_bits, 0, sizeof v);
+        if (e != cudaSuccess) return cuda_fail(e, "rpa_check_device_status clear");
+    }
+    if (bits) *bits = v;
+    if (v) return fail(RPA_ERR_DEVICE_CHECK, "device-side check failed: bits 0x%x", v);
+    return RPA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Device helpers shared by the attention, plan and scatter kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rpa.h"
+
+namespace rpa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kWsHeaderBytes = 256;  // error word, work counters, item counts
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    uint32_t error_bits;     // RPA_DEV_ERR_* bits, sticky until rpa_check_device_status
+    int32_t next_item[4];    // work-stealing counters, reset by the plan kernel
+    int32_t num_items[4];    // items written by the plan kernel, per work list
+    int32_t chunk_keys;      // split-KV chunk chosen by the plan kernel
+    int32_t pad[54];
+};
+static_assert(sizeof(WsHeader) == kWsHeaderBytes, "header size");
+
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+__host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// Asynchronous copies (cp.async, 16 bytes; src_bytes == 0 writes zeros).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core fragments: ldmatrix + mma.sync m16n8k16 bf16 -> f32.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x on the special-function unit (ex2.approx; relative error ~2^-22).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two e4m3 bytes -> two floats (exact), via the hardware fp8x2 -> f16x2 convert.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+    __half2 hh = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(hh);
+}
+
+// Swizzled byte offset of 16-byte chunk `c` of row `r` in a tile whose rows are
+// `row_bytes` long (a multiple of 128): XOR of the low three chunk bits with the
+// row index keeps eight consecutive rows of one logical chunk on distinct banks.
+__device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
+    return static_cast<uint32_t>(r * row_bytes + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exclusive scan over a block (blockDim.x a multiple of 32, <= 1024); returns the
+// thread's exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        scratch[lane] = w;  // inclusive per-warp totals
+    }
+    __syncthreads();
+    const int warp_off = warp ? scratch[warp - 1] : 0;
+    const int tot = scratch[nw - 1];
+    __syncthreads();
+    *total = tot;
+    return warp_off + x - v;
+}
+
+}  // namespace rpa

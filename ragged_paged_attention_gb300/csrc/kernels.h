@@ -1,0 +1,177 @@
+// Kernel argument blocks and launch entry points shared by the C ABI (api.cu)
+// and the kernel translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rpa {
+
+struct WsHeader;
+
+// Tiling constants of the RPA kernels.
+constexpr int kDecodeHeads = 4;         // KV heads per decode CTA (one warp each)
+constexpr int kDecodeBK = 16;           // keys per decode pipeline stage
+constexpr int kPrefillRows = 64;        // (token, q-head) rows per prefill CTA
+constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
+constexpr int kDecodeTargetCtas = 1024; // split so decode work spreads over about this many CTAs
+
+// One unit of work for a persistent attention CTA (32 bytes).
+struct __align__(16) WorkItem {
+    int seq;         // sequence (RPA/MLA) or flat query b*S+s (sparse)
+    int head;        // first KV head (RPA) or first q head (latent) of the tile
+    int row_begin;   // first row of the tile (RPA prefill) / token in sequence (MLA)
+    int key_begin;   // key range [key_begin, key_end)
+    int key_end;
+    int first_item;  // item index of split 0 of this group (ticket / partial base)
+    int num_splits;
+    int split;
+};
+
+struct RpaArgs {
+    const __nv_bfloat16* q;
+    const void* kv_pages;
+    const int32_t* kv_lens;
+    const int32_t* page_indices;
+    const int32_t* cu_q_lens;
+    const int32_t* num_seqs;
+    __nv_bfloat16* out;
+    int max_num_tokens, num_q_heads, num_kv_heads, head_dim;
+    int total_num_pages, page_size, max_num_seqs, pages_per_seq;
+    int kv_fp8;
+    float sm_scale, soft_cap;
+    int sliding_window;
+    int has_scale;              // k_scale or v_scale given
+    float k_scale_or_one, v_scale_or_one;
+    int decode_target_ctas;
+    // workspace
+    WsHeader* hdr;
+    WorkItem* dec_items;
+    WorkItem* pre_items;
+    int* tickets;
+    float* partial_ml;
+    float* partial_o;
+    int max_dec_items, max_pre_items;
+};
+
+struct RpaUpdateArgs {
+    const void* new_k;
+    const void* new_v;
+    void* kv_pages;
+    const int32_t* kv_lens;
+    const int32_t* page_indices;
+    const int32_t* cu_q_lens;
+    const int32_t* num_seqs;
+    uint32_t* err;  // may be null
+    int max_num_tokens, num_kv_heads, head_dim, esz;
+    int total_num_pages, page_size, max_num_seqs, pages_per_seq;
+};
+
+// Latent (MLA and sparse MLA) attention.
+constexpr int kLatRows = 64;      // q heads per CTA
+constexpr int kLatBK = 32;        // keys per stage
+constexpr int kLatDk = 576;       // 512 latent + 64 rope
+constexpr int kLatDv = 512;
+constexpr int kLatMinChunk = 512;
+constexpr int kLatTargetCtas = 1024;
+
+struct LatentArgs {
+    int sparse;                     // 0 = MLA (paged, causal), 1 = DSA sparse
+    int num_heads;
+    float sm_scale, soft_cap;
+    int sliding_window;
+    // MLA
+    const __nv_bfloat16* ql_nope;   // [T, H, 512]
+    const __nv_bfloat16* q_pe;      // [T, H, 64]
+    const __nv_bfloat16* cache_kv_c;  // rows of lkv_pad
+    const __nv_bfloat16* cache_k_pe;  // rows of r_pad
+    const int32_t* kv_lens;
+    const int32_t* page_indices;
+    const int32_t* cu_q_lens;
+    const int32_t* distribution;
+    int max_num_tokens, max_num_seqs, pages_per_seq, lkv_pad, r_pad;
+    __nv_bfloat16* out_bf16;        // [T, H, 512]
+    // sparse
+    const __nv_bfloat16* q;         // [B, S, H, 576]
+    const __nv_bfloat16* cache;     // rows of row_stride
+    const int32_t* indices;         // [B, S, K]
+    const int32_t* positions;       // [B, S]
+    const int32_t* page_table;      // [B, max_pages]
+    int batch, num_queries, topk, read_block, max_pages, seq_len, row_stride, sparse_splits;
+    float* out_f32;                 // [B, S, H, 512]
+    // common
+    int total_num_pages, page_size;
+    // workspace
+    WsHeader* hdr;
+    WorkItem* items;
+    int* tickets;
+    float* partial_ml;
+    float* partial_o;
+    int max_items;
+};
+
+struct MlaUpdateArgs {
+    const __nv_bfloat16* new_kv_c;
+    const __nv_bfloat16* new_k_pe;
+    __nv_bfloat16* cache_kv_c;
+    __nv_bfloat16* cache_k_pe;
+    const int32_t* kv_lens;
+    const int32_t* page_indices;
+    const int32_t* cu_q_lens;
+    const int32_t* distribution;
+    uint32_t* err;
+    int max_num_tokens, lkv_dim, r_dim, lkv_pad, r_pad;
+    int total_num_pages, page_size, max_num_seqs, pages_per_seq;
+};
+
+cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_sparse_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
+
+// Sparse split count the host chooses from static sizes (no device metadata needed).
+inline int sparse_num_splits(int batch, int num_queries, int heads, int slots) {
+    long long tiles = (long long)batch * num_queries * (heads / kLatRows);
+    long long total = tiles * slots;
+    long long chunk = (total + kLatTargetCtas - 1) / kLatTargetCtas;
+    if (chunk < kLatMinChunk) chunk = kLatMinChunk;
+    chunk = (chunk + kLatBK - 1) / kLatBK * kLatBK;
+    long long n = (slots + chunk - 1) / chunk;
+    return n < 1 ? 1 : (int)n;
+}
+
+}  // namespace rpa
+
+#ifdef __CUDACC__
+#include "common.cuh"
+namespace rpa {
+// Validates one sequence's metadata (the reference's dynamic checks); on failure
+// records the error bit and returns false so the sequence is skipped.
+__device__ __forceinline__ bool seq_shape(const RpaArgs& a, int s, int& ql, int& kl) {
+    const int c0 = a.cu_q_lens[s], c1 = a.cu_q_lens[s + 1];
+    ql = c1 - c0;
+    kl = a.kv_lens[s];
+    uint32_t bad = 0;
+    if (c0 < 0 || c1 < c0 || c1 > a.max_num_tokens)
+        bad = RPA_DEV_ERR_TOKENS;
+    else if (ql > kl)
+        bad = RPA_DEV_ERR_Q_LEN;
+    else if (cdiv(kl, a.page_size) > a.pages_per_seq)
+        bad = RPA_DEV_ERR_KV_LEN;
+    if (bad) {
+        set_error(&a.hdr->error_bits, bad);
+        return false;
+    }
+    return true;
+}
+
+// First key any query of a decode-class sequence can see (aligned down to a stage).
+__device__ __forceinline__ int decode_key_begin(const RpaArgs& a, int ql, int kl) {
+    if (a.sliding_window <= 0) return 0;
+    const int lo = kl - ql - a.sliding_window + 1;
+    return lo <= 0 ? 0 : lo / kDecodeBK * kDecodeBK;
+}
+}  // namespace rpa
+#endif

@@ -19,8 +19,10 @@ Recipe (the shapes follow the workloads the source pages describe):
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 
 import numpy as np
 import torch
@@ -30,9 +32,28 @@ BF16_NAN = 0x7FC0
 E4M3_NAN = 0x7F
 
 
+_CHUNK = 1 << 22  # values per independently seeded block (fixed: results do not depend on threads)
+
+
 def _randn(rng: np.random.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
-    x = torch.from_numpy(rng.standard_normal(size=shape, dtype=np.float32))
-    return x.to(dtype)
+    """N(0, 1) float32 values rounded to ``dtype``.  Large draws are split into fixed
+    blocks, each from its own PCG64 stream spawned from one seed taken from ``rng``,
+    and filled by a thread pool."""
+    n = int(np.prod(shape))
+    if n <= _CHUNK:
+        x = rng.standard_normal(size=n, dtype=np.float32)
+    else:
+        x = np.empty(n, dtype=np.float32)
+        blocks = (n + _CHUNK - 1) // _CHUNK
+        seeds = np.random.SeedSequence(int(rng.integers(0, 2**63))).spawn(blocks)
+
+        def fill(i):
+            g = np.random.Generator(np.random.PCG64(seeds[i]))
+            g.standard_normal(out=x[i * _CHUNK:(i + 1) * _CHUNK], dtype=np.float32)
+
+        with concurrent.futures.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(blocks)))
+    return torch.from_numpy(x).reshape(shape).to(dtype)
 
 
 def _fill_nan(t: torch.Tensor) -> None:

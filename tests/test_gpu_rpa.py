@@ -1,0 +1,158 @@
+"""GPU parity of rpa_forward / rpa_update_kv_cache against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ragged_paged_attention_gb300 import api, workloads
+from parity import TOL_BF16, TOL_FP8, gpu, max_abs, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(b, **over):
+    g = b.to("cuda")
+    opts = b.options()
+    opts.update(over)
+    ws = torch.zeros(api.rpa_workspace_size(api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.full_like(g.q, 7.0)
+    api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, workspace=ws, **opts)
+    bits = api.check_device_status(ws)
+    return out, bits, ws
+
+
+def check(b, tol, tokens=None, **over):
+    out, bits, _ = run_gpu(b, **over)
+    assert bits == 0, f"device error bits {bits:#x}"
+    opts = b.options()
+    opts.update(over)
+    ref = oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=tokens, **opts)
+    T = b.num_tokens
+    rows = list(range(T)) if tokens is None else list(tokens)
+    err = max_abs(out[rows], ref[rows])
+    assert err <= tol, f"max-abs {err} > {tol}"
+    # rows of padding tokens are never written
+    assert (out[T:].float() == 7.0).all()
+    return out
+
+
+def test_tiny_batch():
+    check(workloads.tiny_rpa(), TOL_BF16)
+
+
+def test_llama_mixed_small():
+    check(workloads.llama_mixed(scale=1 / 8), TOL_BF16)
+
+
+def test_gemma_options_small():
+    check(workloads.gemma_options(scale=1 / 8), TOL_FP8)
+
+
+def test_llama_mixed_full_size_sampled():
+    b = workloads.llama_mixed()
+    check(b, TOL_BF16, tokens=sample_tokens(b.q_lens))
+
+
+def test_gemma_options_full_size_sampled():
+    b = workloads.gemma_options()
+    check(b, TOL_FP8, tokens=sample_tokens(b.q_lens))
+
+
+@pytest.mark.parametrize("hq,hkv,d,ps", [(8, 1, 64, 8), (16, 2, 128, 4), (4, 4, 256, 16), (32, 2, 128, 32)])
+def test_head_layouts(hq, hkv, d, ps):
+    b = workloads.make_rpa([1, 3, 17, 70, 2], [1, 40, 17, 150, 9], num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                           page_size=ps, seed=hq * d + ps, max_num_seqs=7, max_num_tokens=100, extra_pages=3)
+    check(b, TOL_BF16)
+
+
+@pytest.mark.parametrize("sw,cap", [(1, None), (5, 30.0), (64, None), (None, 2.0)])
+def test_window_and_cap(sw, cap):
+    b = workloads.make_rpa([1, 4, 40, 1], [300, 33, 120, 1], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                           page_size=16, seed=11, sliding_window=sw, soft_cap=cap)
+    check(b, TOL_BF16)
+
+
+def test_fp8_without_scale_and_bf16_with_scale():
+    b = workloads.make_rpa([1, 9], [77, 30], num_q_heads=8, num_kv_heads=4, head_dim=128, page_size=16, seed=12,
+                           kv_dtype=torch.float8_e4m3fn)
+    check(b, TOL_FP8)
+    b2 = workloads.make_rpa([1, 9], [77, 30], num_q_heads=8, num_kv_heads=4, head_dim=128, page_size=16, seed=13,
+                            k_scale=0.37, v_scale=1.7)
+    check(b2, TOL_BF16)
+
+
+def test_empty_batch_and_zero_length_sequences():
+    b = workloads.make_rpa([0, 2, 0], [5, 2, 0], num_q_heads=4, num_kv_heads=2, head_dim=128, page_size=16, seed=14,
+                           max_num_tokens=8)
+    check(b, TOL_BF16)
+    g = b.to("cuda")
+    g.num_seqs.zero_()
+    out = torch.full_like(g.q, 7.0)
+    api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, **b.options())
+    torch.cuda.synchronize()
+    assert (out.float() == 7.0).all()
+
+
+def test_long_prefill_from_position_zero():
+    b = workloads.make_rpa([300, 1], [300, 600], num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                           seed=15)
+    check(b, TOL_BF16)
+
+
+def test_page_permutation_is_bit_exact():
+    b = workloads.make_rpa([1, 1, 33], [900, 20, 200], num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                           seed=16, extra_pages=5)
+    out1, bits, _ = run_gpu(b)
+    P = b.kv_pages.shape[0]
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(P))
+    pages = torch.empty_like(b.kv_pages)
+    pages[perm] = b.kv_pages
+    table = b.page_indices.clone()
+    ok = table < P
+    table[ok] = perm[table[ok].long()].to(torch.int32)
+    b.kv_pages, b.page_indices = pages, table
+    out2, bits2, _ = run_gpu(b)
+    T = b.num_tokens
+    assert bits == bits2 == 0
+    assert torch.equal(out1[:T].view(torch.int16), out2[:T].view(torch.int16))
+
+
+def test_bad_page_index_sets_device_error():
+    b = workloads.make_rpa([1, 5], [40, 50], num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, seed=17)
+    b.page_indices[1, 1] = b.kv_pages.shape[0] + 3   # out of range: the kernels skip it and report
+    out, bits, _ = run_gpu(b)
+    assert bits & 0x08
+    b.page_indices[1, 1] = 0
+    b.kv_lens[0] = 10**6                             # more pages than pages_per_seq
+    out, bits, _ = run_gpu(b)
+    assert bits & 0x04
+
+
+@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn])
+def test_update_kv_cache_bit_exact(kv_dtype):
+    b = workloads.make_rpa([1, 1, 6, 19], [33, 1, 6, 40], num_q_heads=8, num_kv_heads=4, head_dim=128, page_size=16,
+                           seed=18, kv_dtype=kv_dtype, max_num_seqs=6, max_num_tokens=32, extra_pages=4)
+    ref = oracle.rpa_update_kv_cache(b.new_k[:b.num_tokens].contiguous(), b.new_v[:b.num_tokens].contiguous(),
+                                     b.kv_pages, b.kv_lens[:4], b.page_indices[:4], b.cu_q_lens[:5], 4)
+    g = b.to("cuda")
+    api.rpa_update_kv_cache(g.new_k, g.new_v, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs)
+    torch.cuda.synchronize()
+    assert torch.equal(g.kv_pages.cpu().view(torch.uint8), ref.view(torch.uint8))
+
+
+def test_update_then_attend_full_size():
+    b = workloads.llama_mixed(scale=1 / 4)
+    g = b.to("cuda")
+    api.rpa_update_kv_cache(g.new_k, g.new_v, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs)
+    ref_pages = oracle.rpa_update_kv_cache(b.new_k[:b.num_tokens].contiguous(), b.new_v[:b.num_tokens].contiguous(),
+                                           b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens))
+    torch.cuda.synchronize()
+    assert torch.equal(g.kv_pages.cpu().view(torch.int16), ref_pages.view(torch.int16))
+    out = api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, **b.options())
+    toks = sample_tokens(b.q_lens)
+    ref = oracle.rpa(b.q, ref_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=toks,
+                     **b.options())
+    assert max_abs(out[toks], ref[toks]) <= TOL_BF16

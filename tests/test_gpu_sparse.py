@@ -1,0 +1,62 @@
+"""GPU parity of sparse_mla_forward against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ragged_paged_attention_gb300 import api, workloads
+from parity import TOL_BF16, max_abs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(s, queries=None):
+    ref = oracle.sparse_mla(s.q, s.cache, s.indices, s.positions, s.page_table, queries=queries, **s.options())
+    g = s.to("cuda")
+    prm = api.make_sparse_params(g.q, g.cache, g.indices, g.page_table, read_block=s.read_block,
+                                 page_size=s.page_size, seq_len=s.seq_len, sm_scale=s.sm_scale)
+    ws = torch.zeros(api.sparse_mla_workspace_size(prm), dtype=torch.uint8, device="cuda")
+    out = api.sparse_mla_forward(g.q, g.cache, g.indices, g.positions, g.page_table, workspace=ws, **s.options())
+    assert api.check_device_status(ws) == 0
+    B, S = s.positions.shape
+    flat_out = out.reshape(B * S, *out.shape[2:])
+    flat_ref = ref.reshape(B * S, *ref.shape[2:])
+    rows = list(range(B * S)) if queries is None else list(queries)
+    err = max_abs(flat_out[rows], flat_ref[rows])
+    assert err <= TOL_BF16, f"max-abs {err}"
+
+
+@pytest.mark.parametrize("mode", ["token", "page"])
+@pytest.mark.parametrize("phase", ["prefill", "decode"])
+def test_sparse_small(mode, phase):
+    run_and_check(workloads.dsa_sparse(mode=mode, phase=phase, scale=1 / 16))
+
+
+def test_sparse_early_positions_pad_with_minus_one():
+    # queries near position 0 have fewer causal units than K: their slots are -1 padded
+    pos = np.array([[0, 1, 5, 63, 64, 200]], dtype=np.int32)
+    for rb, k in [(1, 32), (16, 4)]:
+        s = workloads.make_sparse(batch=1, num_queries=6, seq_len=256, positions=pos, topk=k, read_block=rb, seed=31)
+        assert (s.indices == -1).any()
+        run_and_check(s)
+
+
+def test_sparse_duplicates_and_future_units():
+    pos = np.array([[100, 100]], dtype=np.int32)
+    idx = np.array([[[3, 3, 50, 120, 200, -1, 7, 7], [0, 1, 2, 3, 99, 100, 101, -1]]], dtype=np.int32)
+    s = workloads.make_sparse(batch=1, num_queries=2, seq_len=256, positions=pos, topk=8, read_block=1, seed=32,
+                              indices=idx)
+    run_and_check(s)
+
+
+@pytest.mark.parametrize("mode", ["token", "page"])
+def test_sparse_prefill_full_size_sampled(mode):
+    s = workloads.dsa_sparse(mode=mode, phase="prefill")
+    rng = np.random.default_rng(5)
+    run_and_check(s, queries=sorted(rng.choice(s.positions.numel(), size=12, replace=False).tolist()))
+
+
+@pytest.mark.parametrize("mode", ["token", "page"])
+def test_sparse_decode_full_size_sampled(mode):
+    s = workloads.dsa_sparse(mode=mode, phase="decode")
+    run_and_check(s, queries=list(range(0, 64, 5)))
