@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 ragged paged attention library.
+
+One step = one pass of the hot path over one mixed prefill+decode batch shaped like
+Llama-3-8B serving (32 q / 8 kv heads, head_dim 128, page_size 16, 128 decode
+sequences with kv_len U[512, 4096] and 4 prefill chunks of 512 queries with kv_len
+U[512, 2048]): the batch's new K/V rows are written into their pages
+(rpa_update_kv_cache) and attention runs over the whole batch (rpa_forward).
+
+Printed as one JSON line:
+  value      query tokens/s over the whole job, inputs resident in HBM (CUDA events)
+  e2e        the same through the public API from pinned host buffers, with the
+             host->device copy of the step's inputs and the device->host read of
+             its output inside the timed region
+  roofline   the dominant kernel's algorithmic bytes (or flops) per launch over its
+             CUDA-event duration, against the measured HBM / bf16 peak
+  cpu_baseline  the float64 oracle on a bounded sample of the same batch, host cores
+  variants   the Gemma-2-style fp8 batch, the DeepSeek MLA batch and the DSA sparse
+             MLA batches, measured in the same run (parity cases of the test-suite)
+
+``--impl reference`` times the oracle instead (the reference arm).  Under torchrun
+(N > 1) every rank runs an independent replica of the step on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "ragged paged attn tokens/s, HBM GB/s & TFLOP/s as % of GB300 roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment: ranks, peaks, clocks
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.index = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.index], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes and flops (what the method must move / compute)
+# ---------------------------------------------------------------------------
+def _visible(kv_len, q_len, sw):
+    """Per query of a sequence: number of visible keys; and unique keys read."""
+    qpos = kv_len - q_len + np.arange(q_len, dtype=np.int64)
+    lo = np.maximum(0, qpos - sw + 1) if sw else np.zeros_like(qpos)
+    vis = qpos + 1 - lo
+    uniq = kv_len - (int(lo[0]) if q_len else kv_len)
+    return vis, uniq
+
+
+def rpa_accounting(b):
+    Hq, D = b.q.shape[1], b.q.shape[2]
+    C = b.kv_pages.shape[2]
+    esz = b.kv_pages.element_size()
+    G = Hq // (C // 2)
+    acc = {"decode": [0, 0, 0], "prefill": [0, 0, 0]}  # tokens, bytes, flops
+    for ql, kl in zip(b.q_lens, b.kv_lens_list):
+        if ql == 0:
+            continue
+        vis, uniq = _visible(kl, ql, b.sliding_window)
+        part = "decode" if ql * G <= 16 else "prefill"
+        acc[part][0] += ql
+        acc[part][1] += uniq * C * D * esz + ql * Hq * D * 2 * 2
+        acc[part][2] += int(vis.sum()) * 4 * Hq * D
+    return acc
+
+
+def mla_accounting(m):
+    H = m.ql_nope.shape[1]
+    tok = byt = fl = 0
+    dec = [0, 0, 0]
+    for ql, kl in zip(m.q_lens, m.kv_lens_list):
+        vis, uniq = _visible(kl, ql, m.sliding_window)
+        b_ = uniq * 576 * 2 + ql * H * (576 * 2 + 512 * 2) + ql * 576 * 2 * 2
+        f_ = int(vis.sum()) * 2 * H * (576 + 512)
+        tok, byt, fl = tok + ql, byt + b_, fl + f_
+        if ql == 1:
+            dec = [dec[0] + 1, dec[1] + b_, dec[2] + f_]
+    return tok, byt, fl, dec
+
+
+def sparse_accounting(s):
+    B, S, H, _ = s.q.shape
+    RB = s.read_block
+    idx = s.indices.numpy().astype(np.int64)
+    pos = s.positions.numpy().astype(np.int64)
+    units = idx[..., None] * RB + np.arange(RB)  # [B,S,K,RB]
+    valid = (idx[..., None] >= 0) & (units <= pos[..., None, None]) & (units < s.seq_len)
+    pairs = int(valid.sum())
+    rows = 0
+    for b in range(B):
+        rows += np.unique(units[b][valid[b]]).size
+    byt = rows * 576 * 2 + B * S * H * (576 * 2 + 512 * 4)
+    fl = pairs * 2 * H * (576 + 512)
+    return B * S, byt, fl
+
+
+def roof_time(byt, fl, peaks, sustained=False):
+    tf = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return max(byt / (peaks["hbm_gbs"] * 1e9), fl / (tf * 1e12))
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+def time_steps(fn, steps, warmup, world, timer=False):
+    from ragged_paged_attention_gb300 import api
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kt = api.KernelTimer() if timer else None
+    if kt:
+        kt.__enter__()
+    e0.record(st)
+    for _ in range(steps):
+        fn()
+    e1.record(st)
+    torch.cuda.synchronize()
+    if kt:
+        kt.__exit__(None, None, None)
+    barrier(world)
+    ms = e0.elapsed_time(e1) / steps
+    return ms, (kt.result if kt else {})
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """dram bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    m_src = re.search(r"source_file:\s*(\S+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_src and m_b):
+        return None
+    src = os.path.join(ROOT, m_src.group(1))
+    if not os.path.exists(src) or source_sha(src) != m_sha.group(1):
+        return None
+    return float(m_b.group(1))
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def llama_batch():
+    from ragged_paged_attention_gb300 import workloads
+    return workloads.llama_mixed()
+
+
+def cpu_baseline_rpa(b, seconds, seed=0):
+    """The float64 oracle on a random sample of the batch's query tokens."""
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    T = b.num_tokens
+    n_cal = 8
+    t0 = time.perf_counter()
+    oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens),
+               tokens=rng.choice(T, n_cal, replace=False), **b.options())
+    cal = time.perf_counter() - t0
+    n = int(max(8, min(T, n_cal * seconds / max(cal, 1e-3))))
+    toks = np.sort(rng.choice(T, n, replace=False))
+    t0 = time.perf_counter()
+    oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=toks, **b.options())
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {T} query tokens drawn uniformly from the Llama-3-8B mixed batch, all heads, "
+                      f"float64 C oracle with OpenMP, {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the oracle on the host cores, timed per step on a bounded sample."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    b = llama_batch()
+    rng = np.random.default_rng(1)
+    T = b.num_tokens
+    per_step = max(4, int(64 * 8 / max(args.steps + args.warmup, 1)))
+    times, toks_done = [], 0
+    for i in range(args.warmup + args.steps):
+        toks = np.sort(rng.choice(T, per_step, replace=False))
+        t0 = time.perf_counter()
+        oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=toks, **b.options())
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            toks_done += per_step
+    value = toks_done / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3_8b_mixed_batch", "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{per_step} random query tokens of {T} per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    from ragged_paged_attention_gb300 import api
+    from ragged_paged_attention_gb300 import build as rpa_build
+    rpa_build.build()
+    api.load_library()
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    b = llama_batch()
+    acc = rpa_accounting(b)
+    g = b.to(dev)
+    opts = b.options()
+    prm = api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)
+    ws = torch.zeros(api.rpa_workspace_size(prm), dtype=torch.uint8, device=dev)
+    ws_u = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(g.q)
+
+    def step():
+        api.rpa_update_kv_cache(g.new_k, g.new_v, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs,
+                                workspace=ws_u)
+        api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, workspace=ws,
+                        **opts)
+
+    clocks = ClockSampler(local).start()
+    ms, ktimes = time_steps(step, args.steps, args.warmup, world, timer=True)
+    clk = clocks.stop()
+    assert api.check_device_status(ws) == 0 and api.check_device_status(ws_u) == 0
+    ms = max_over_ranks(ms, world)
+    T = b.num_tokens
+    value = T * world / (ms * 1e-3)
+
+    # dominant kernel of the step and its roofline
+    step_total = sum(v[1] for v in ktimes.values())
+    dom = max(ktimes.items(), key=lambda kv: kv[1][1])[0] if ktimes else None
+    kernels = {k: {"launches": v[0], "avg_us": 1e3 * v[1] / max(v[0], 1),
+                   "share": v[1] / step_total if step_total else None} for k, v in ktimes.items()}
+    dec_bytes = acc["decode"][1]
+    pre_flops = acc["prefill"][2]
+    if dom == "rpa_prefill_attn":
+        avg_s = ktimes[dom][1] / ktimes[dom][0] * 1e-3
+        ach = pre_flops / avg_s / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "traffic": profiled_traffic(dom, "llama_mixed")}
+    else:
+        dom = "rpa_decode_attn"
+        avg_s = ktimes[dom][1] / ktimes[dom][0] * 1e-3
+        ach = dec_bytes / avg_s / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": profiled_traffic(dom, "llama_mixed")}
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_bytes_per_launch" if roof["bound"] == "hbm" else "algorithmic_flops_per_launch"] = (
+        dec_bytes if roof["bound"] == "hbm" else pre_flops)
+    step_bytes = acc["decode"][1] + acc["prefill"][1]
+    step_flops = acc["decode"][2] + acc["prefill"][2]
+    t_roof = roof_time(step_bytes, step_flops, peaks)
+
+    # end to end: pinned host inputs -> device, update + attention, output -> host
+    host = {k: v.pin_memory() for k, v in
+            dict(q=b.q, new_k=b.new_k, new_v=b.new_v, kv_lens=b.kv_lens, page_indices=b.page_indices,
+                 cu_q_lens=b.cu_q_lens, num_seqs=b.num_seqs).items()}
+    dq = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dq[k].copy_(v, non_blocking=True)
+        api.rpa_update_kv_cache(dq["new_k"], dq["new_v"], g.kv_pages, dq["kv_lens"], dq["page_indices"],
+                                dq["cu_q_lens"], dq["num_seqs"], workspace=ws_u)
+        api.rpa_forward(dq["q"], g.kv_pages, dq["kv_lens"], dq["page_indices"], dq["cu_q_lens"], dq["num_seqs"],
+                        out=out, workspace=ws, **opts)
+        out_h.copy_(out, non_blocking=True)
+
+    ms_e2e = None
+    if not args.no_e2e:
+        ms_e2e, _ = time_steps(e2e_step, args.steps, args.warmup, world)
+        ms_e2e = max_over_ranks(ms_e2e, world)
+
+    # same-run variants (decode/prefill sub-launches are in `kernels`)
+    variants = {}
+    if not args.no_variants:
+        variants = run_variants(dev, peaks, args, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_rpa(b, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "llama3_8b_mixed_batch", "num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128,
+                       "page_size": 16, "decode_seqs": 128, "prefill_chunks": "4 x 512", "query_tokens": T,
+                       "kv_cache_bytes": g.kv_pages.numel() * g.kv_pages.element_size(),
+                       "step": "rpa_update_kv_cache + rpa_forward",
+                       "l2": "inputs larger than L2 (KV cache >1 GB read each step)", "parallelism": "replicas"},
+            "step_roofline": {"bytes": step_bytes, "flops": step_flops, "roofline_us": t_roof * 1e6,
+                              "frac": t_roof / (ms * 1e-3), "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+                              "tflops": step_flops / (ms * 1e-3) / 1e12},
+            "roofline": roof,
+            "kernels": kernels,
+            "gpu_launches": int(sum(v[0] for v in ktimes.values())),
+            "clocks": clk,
+            "e2e": None if ms_e2e is None else {
+                "value": T * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+            "cpu_baseline": cpu,
+            "variants": variants,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_variants(dev, peaks, args, world):
+    from ragged_paged_attention_gb300 import api, workloads
+    res = {}
+    steps, warm = max(3, args.steps // 2), 3
+
+    def report(name, tok, byt, fl, ms, kt, extra=None):
+        t_roof = roof_time(byt, fl, peaks)
+        r = {"tokens_per_s": tok / (ms * 1e-3), "ms_per_step": ms, "hbm_gbs": byt / (ms * 1e-3) / 1e9,
+             "tflops": fl / (ms * 1e-3) / 1e12, "roofline_frac": t_roof / (ms * 1e-3),
+             "bound": "hbm" if byt / (peaks["hbm_gbs"] * 1e9) >= fl / (peaks["bf16_tflops"] * 1e12) else "tensor",
+             "kernels_us": {k: 1e3 * v[1] / max(v[0], 1) for k, v in kt.items()}}
+        if extra:
+            r.update(extra)
+        res[name] = r
+
+    # Gemma-2-style fp8 KV, sliding window, soft cap
+    b = workloads.gemma_options()
+    acc = rpa_accounting(b)
+    g = b.to(dev)
+    opts = b.options()
+    ws = torch.zeros(api.rpa_workspace_size(api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(g.q)
+    ms, kt = time_steps(lambda: api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs,
+                                                out=out, workspace=ws, **opts), steps, warm, world, timer=True)
+    dec_us = 1e3 * kt["rpa_decode_attn"][1] / kt["rpa_decode_attn"][0]
+    report("gemma2_fp8_sw_cap", b.num_tokens, acc["decode"][1] + acc["prefill"][1],
+           acc["decode"][2] + acc["prefill"][2], ms, kt,
+           {"decode_hbm_frac": acc["decode"][1] / (dec_us * 1e-6) / 1e9 / peaks["hbm_gbs"]})
+    del b, g, out, ws
+    torch.cuda.empty_cache()
+
+    # DeepSeek-V3 MLA with its cache update
+    m = workloads.mla_deepseek()
+    tok, byt, fl, dec = mla_accounting(m)
+    g = m.to(dev)
+    opts = m.options()
+    prm = api.make_mla_params(g.ql_nope, g.q_pe, g.cache_kv_c, g.cache_k_pe, g.kv_lens, g.page_indices, **opts)
+    ws = torch.zeros(api.mla_workspace_size(prm), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(g.ql_nope)
+    ms, kt = time_steps(lambda: api.mla_rpa_forward(g.ql_nope, g.q_pe, g.new_kv_c, g.new_k_pe, g.cache_kv_c,
+                                                    g.cache_k_pe, g.kv_lens, g.page_indices, g.cu_q_lens,
+                                                    g.distribution, out=out, workspace=ws, **opts),
+                        steps, warm, world, timer=True)
+    att_us = 1e3 * kt["mla_attn"][1] / kt["mla_attn"][0]
+    report("mla_deepseek_v3", tok, byt, fl, ms, kt,
+           {"attn_tensor_frac": fl / (att_us * 1e-6) / 1e12 / peaks["bf16_tflops"]})
+    del m, g, out, ws
+    torch.cuda.empty_cache()
+
+    # DSA sparse MLA
+    for phase in ("prefill", "decode"):
+        for mode in ("token", "page"):
+            s = workloads.dsa_sparse(mode=mode, phase=phase)
+            tok, byt, fl = sparse_accounting(s)
+            g = s.to(dev)
+            prm = api.make_sparse_params(g.q, g.cache, g.indices, g.page_table, read_block=s.read_block,
+                                         page_size=s.page_size, seq_len=s.seq_len, sm_scale=s.sm_scale)
+            ws = torch.zeros(api.sparse_mla_workspace_size(prm), dtype=torch.uint8, device=dev)
+            out = torch.empty(s.q.shape[:3] + (512,), dtype=torch.float32, device=dev)
+            ms, kt = time_steps(lambda: api.sparse_mla_forward(g.q, g.cache, g.indices, g.positions, g.page_table,
+                                                               out=out, workspace=ws, **s.options()),
+                                steps if phase == "decode" else max(3, steps // 4), warm, world, timer=True)
+            report(f"dsa_sparse_{phase}_{mode}", tok, byt, fl, ms, kt)
+            del s, g, out, ws
+            torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    main()

@@ -259,6 +259,22 @@ RPA_API int sparse_mla_forward(const sparse_params* p, const void* q, const void
  * NULL) and clears it.  Returns RPA_ERR_DEVICE_CHECK when any bit was set. */
 RPA_API int rpa_check_device_status(void* workspace, uint32_t* bits, rpa_stream_t stream);
 
+/* Per-kernel timing (diagnostics).  While enabled, every kernel the library launches
+ * is bracketed by two CUDA events on its launch stream (a GPU-side timestamp pair; no
+ * host synchronisation).  rpa_profile_read synchronises on the recorded events and
+ * reports, per kernel name, the number of launches and their summed duration since
+ * the last rpa_profile_reset.  Entries are written to out[0 .. max_entries) in name
+ * order; *n_entries receives the total number of kernel names. */
+typedef struct {
+    char name[48];
+    int64_t launches;
+    double total_ms;
+} rpa_kernel_time;
+
+RPA_API int rpa_profile_enable(int on);
+RPA_API int rpa_profile_reset(void);
+RPA_API int rpa_profile_read(rpa_kernel_time* out, int max_entries, int* n_entries);
+
 /* Thread-local description of the last failed call ("" if none). */
 RPA_API const char* rpa_last_error(void);
 

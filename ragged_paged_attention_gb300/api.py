@@ -26,13 +26,18 @@ STATUS = {0: "RPA_OK", -1: "RPA_ERR_NULL", -2: "RPA_ERR_SHAPE", -3: "RPA_ERR_DTY
 
 EXPORTS = ("rpa_workspace_size", "rpa_forward", "rpa_update_kv_cache", "mla_workspace_size",
            "mla_update_kv_cache", "mla_rpa_forward", "sparse_mla_workspace_size", "sparse_mla_forward",
-           "rpa_check_device_status", "rpa_last_error", "rpa_version")
+           "rpa_check_device_status", "rpa_last_error", "rpa_version", "rpa_profile_enable",
+           "rpa_profile_reset", "rpa_profile_read")
 
 
 class RpaError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"{STATUS.get(code, code)}: {msg}")
         self.code = code
+
+
+class rpa_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
 
 class rpa_params(ctypes.Structure):
@@ -90,6 +95,9 @@ def load_library(path: str = LIB_PATH):
         lib.sparse_mla_workspace_size.argtypes = [ctypes.POINTER(sparse_params), szp]
         lib.sparse_mla_forward.argtypes = [ctypes.POINTER(sparse_params), P, P, P, P, P, P, P, sz, P]
         lib.rpa_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+        lib.rpa_profile_enable.argtypes = [ctypes.c_int]
+        lib.rpa_profile_reset.argtypes = []
+        lib.rpa_profile_read.argtypes = [ctypes.POINTER(rpa_kernel_time), ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         for name in EXPORTS:
             if name not in ("rpa_last_error",):
                 getattr(lib, name).restype = ctypes.c_int
@@ -343,3 +351,29 @@ def check_device_status(workspace: torch.Tensor) -> int:
     if rc not in (0, -7):
         _check(rc)
     return bits.value
+
+
+class KernelTimer:
+    """Per-kernel CUDA-event timing of the library's own launches (``rpa_profile_*``).
+
+    ``with KernelTimer() as kt: ...`` then ``kt.result`` maps kernel name to
+    ``(launches, total_ms)``.
+    """
+
+    def __enter__(self):
+        lib = load_library()
+        _check(lib.rpa_profile_reset())
+        _check(lib.rpa_profile_enable(1))
+        self.result = {}
+        return self
+
+    def __exit__(self, *exc):
+        lib = load_library()
+        _check(lib.rpa_profile_enable(0))
+        n = ctypes.c_int(0)
+        buf = (rpa_kernel_time * 64)()
+        _check(lib.rpa_profile_read(buf, 64, ctypes.byref(n)))
+        self.result = {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+                       for i in range(min(n.value, 64))}
+        _check(lib.rpa_profile_reset())
+        return False

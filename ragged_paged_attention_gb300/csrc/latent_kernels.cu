@@ -17,6 +17,7 @@
 // slice of O in registers.  Split items merge through the log-sum-exp rule.
 #include "common.cuh"
 #include "kernels.h"
+#include "profile.h"
 
 namespace rpa {
 
@@ -262,13 +263,16 @@ __global__ void __launch_bounds__(256, 1) latent_attn_kernel(LatentArgs a) {
         const int h0 = w.head;
 
         // per-item query context
-        int qpos = 0, b = 0, seq = 0, t = 0;
+        int qpos = 0, b = 0, seq = 0, t = 0, wlo = 0;
         if (SPARSE) {
             b = w.seq / a.num_queries;
             qpos = a.positions[w.seq];
         } else {
             seq = w.seq;
             t = w.row_begin;
+            const int q_start = a.cu_q_lens[seq];
+            qpos = a.kv_lens[seq] - (a.cu_q_lens[seq + 1] - q_start) + (t - q_start);
+            wlo = a.sliding_window > 0 ? qpos - a.sliding_window + 1 : 0;
         }
         const int kb = w.key_begin, ke = w.key_end;
         const int n_blocks = ke > kb ? cdiv(ke - kb, kLatBK) : 0;
@@ -313,6 +317,8 @@ __global__ void __launch_bounds__(256, 1) latent_attn_kernel(LatentArgs a) {
                                 src = a.cache + ((size_t)page * a.page_size + kp % a.page_size) * a.row_stride + c * 8;
                             }
                         }
+                    } else if (key < wlo) {
+                        v = false;  // outside the sliding window (the causal bound is ke)
                     } else {
                         const int page = a.page_indices[(size_t)seq * a.pages_per_seq + key / a.page_size];
                         if ((unsigned)page >= (unsigned)a.total_num_pages) {
@@ -550,6 +556,7 @@ static cudaError_t launch_latent(const LatentArgs& a, int grid, cudaStream_t str
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    ProfScope ps(SPARSE ? "sparse_attn" : "mla_attn", stream);
     kern<<<grid, 256, kLatSmem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -557,20 +564,29 @@ static cudaError_t launch_latent(const LatentArgs& a, int grid, cudaStream_t str
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream) {
     const int grid = min(cdiv(a.max_num_tokens, 8), num_sms * 8);
     if (grid <= 0) return cudaSuccess;
+    ProfScope ps("mla_update", stream);
     mla_update_kernel<<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream) {
-    mla_plan_kernel<<<1, 1024, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    {
+        ProfScope ps("mla_plan", stream);
+        mla_plan_kernel<<<1, 1024, 0, stream>>>(a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     return launch_latent<false>(a, num_sms, stream);
 }
 
 cudaError_t launch_sparse_forward(const LatentArgs& a, int num_sms, cudaStream_t stream) {
-    sparse_reset_kernel<<<1, 1, 0, stream>>>(a.hdr);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    {
+        ProfScope ps("sparse_reset", stream);
+        sparse_reset_kernel<<<1, 1, 0, stream>>>(a.hdr);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     return launch_latent<true>(a, num_sms, stream);
 }

@@ -1,0 +1,17 @@
+// RAII bracket of one kernel launch for the optional per-kernel timing.
+#pragma once
+#include <cuda_runtime.h>
+
+namespace rpa {
+class ProfScope {
+   public:
+    ProfScope(const char* name, cudaStream_t s);
+    ~ProfScope();
+
+   private:
+    const char* name_;
+    cudaStream_t stream_;
+    void* a_;
+    void* b_;
+};
+}  // namespace rpa

@@ -14,6 +14,7 @@
 //     group (atomic ticket) merges them with the log-sum-exp rule.
 #include "common.cuh"
 #include "kernels.h"
+#include "profile.h"
 
 namespace rpa {
 
@@ -553,11 +554,16 @@ template <int D, int NH, int BK, int STAGES, bool FP8, bool DECODE>
 static cudaError_t launch_attn(const RpaArgs& a, int grid, cudaStream_t stream) {
     using T = RpaTile<D, NH, BK, STAGES, FP8>;
     auto kern = rpa_attn_kernel<D, NH, BK, STAGES, FP8, DECODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, T::kSmem);
-    if (e != cudaSuccess) return e;
+    static int per_sm = 0;  // resident CTAs per SM, computed once per process
+    if (per_sm == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, T::kSmem);
+        if (e != cudaSuccess) return e;
+        per_sm = n > 0 ? n : 1;
+    }
+    ProfScope ps(DECODE ? "rpa_decode_attn" : "rpa_prefill_attn", stream);
     kern<<<grid * (per_sm > 0 ? per_sm : 1), 128, T::kSmem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -572,8 +578,12 @@ static cudaError_t launch_rpa_d(const RpaArgs& a, int num_sms, cudaStream_t stre
 }
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream) {
-    rpa_plan_kernel<<<1, 1024, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    {
+        ProfScope ps("rpa_plan", stream);
+        rpa_plan_kernel<<<1, 1024, 0, stream>>>(a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const bool fp8 = a.kv_fp8 != 0;
     switch (a.head_dim) {
@@ -587,6 +597,7 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream) {
     const int grid = min(a.max_num_tokens, num_sms * 8);
     if (grid <= 0) return cudaSuccess;
+    ProfScope ps("rpa_update", stream);
     rpa_update_kernel<<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
