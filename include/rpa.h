@@ -141,6 +141,28 @@ RPA_API int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages
                 const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs,
                 void* out, void* workspace, size_t workspace_bytes, rpa_stream_t stream);
 
+/* rpa_forward without a workspace argument, for callers that cannot allocate device
+ * memory (for example a plugin inside an application whose memory manager owns the
+ * whole GPU, or a serving loop that must not call cudaMalloc, which can synchronise
+ * the device, once it is running).  The pages have no counterpart: it is a packaging
+ * of rpa_forward, with the same arguments minus the workspace and the same results.
+ *   - Scratch is a fixed array of RPA_NOALLOC_SCRATCH_BYTES inside the library; every
+ *     GPU that loads the library holds it until the process exits.  Problems whose
+ *     rpa_workspace_size() exceeds it are rejected with RPA_ERR_WORKSPACE before any
+ *     launch.  The call allocates nothing itself.
+ *   - The first call on each device looks up that array's device address (with the
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the previous call's contents; the
+ *     kernels reset what they need.  Calls that overlap on the GPU (two streams, or
+ *     two threads) race on it: serialise them.
+ *   - Device-side metadata errors skip the offending sequence as in rpa_forward, but
+ *     the error word is not reported (there is no workspace to pass to
+ *     rpa_check_device_status). */
+#define RPA_NOALLOC_SCRATCH_BYTES (64u << 20)
+RPA_API int rpa_forward_noalloc(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                                const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs,
+                                void* out, rpa_stream_t stream);
+
 /* Write token j of sequence i (position kv_len - q_len + j) into slot
  * page_indices[i, pos / page_size], pos % page_size of kv_pages, in place:
  * new_k[t, g, :] to combined head 2g and new_v[t, g, :] to 2g+1.

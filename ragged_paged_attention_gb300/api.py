@@ -27,7 +27,7 @@ STATUS = {0: "RPA_OK", -1: "RPA_ERR_NULL", -2: "RPA_ERR_SHAPE", -3: "RPA_ERR_DTY
 EXPORTS = ("rpa_workspace_size", "rpa_forward", "rpa_update_kv_cache", "mla_workspace_size",
            "mla_update_kv_cache", "mla_rpa_forward", "sparse_mla_workspace_size", "sparse_mla_forward",
            "rpa_check_device_status", "rpa_last_error", "rpa_version", "rpa_profile_enable",
-           "rpa_profile_reset", "rpa_profile_read")
+           "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc")
 
 
 class RpaError(RuntimeError):
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH):
         lib.rpa_last_error.restype = ctypes.c_char_p
         lib.rpa_workspace_size.argtypes = [ctypes.POINTER(rpa_params), szp]
         lib.rpa_forward.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P, sz, P]
+        lib.rpa_forward_noalloc.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P]
         lib.rpa_update_kv_cache.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P, sz, P]
         lib.mla_workspace_size.argtypes = [ctypes.POINTER(mla_params), szp]
         lib.mla_update_kv_cache.argtypes = [ctypes.POINTER(mla_params), P, P, P, P, P, P, P, P, P, sz, P]
@@ -203,6 +204,35 @@ def rpa_forward(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_s
     _check(lib.rpa_forward(ctypes.byref(prm), _ptr(q), _ptr(kv_pages), _ptr(kv_lens), _ptr(page_indices),
                            _ptr(cu_q_lens), _ptr(num_seqs), _ptr(out), _ptr(workspace), workspace.numel(),
                            _stream()))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def rpa_forward_noalloc(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, out, sm_scale=1.0,
+                        sliding_window=None, soft_cap=None, mask_value=None, k_scale=None, v_scale=None):
+    """rpa_forward through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory (their host application's memory
+    manager owns the GPU, or allocation is not allowed once serving has started): the
+    library uses its own fixed scratch array instead of a workspace, so ``out`` must be
+    given.  Overlapping calls race on that array; problems needing more than
+    ``NOALLOC_SCRATCH_BYTES`` of scratch raise ``RpaError`` (RPA_ERR_WORKSPACE).
+    """
+    lib = load_library()
+    _dev(q, "q", torch.bfloat16)
+    _dev(kv_pages, "kv_pages")
+    _dev(out, "out", torch.bfloat16)
+    for n, t in (("kv_lens", kv_lens), ("page_indices", page_indices), ("cu_q_lens", cu_q_lens),
+                 ("num_seqs", num_seqs)):
+        _dev(t, n, torch.int32)
+    prm = make_rpa_params(q, kv_pages, page_indices, sm_scale=sm_scale, sliding_window=sliding_window,
+                          soft_cap=soft_cap, mask_value=mask_value, k_scale=k_scale, v_scale=v_scale)
+    if kv_lens.numel() != prm.max_num_seqs or cu_q_lens.numel() != prm.max_num_seqs + 1 or num_seqs.numel() != 1:
+        raise ValueError("kv_lens must be [max_num_seqs], cu_q_lens [max_num_seqs + 1], num_seqs [1]")
+    _check(lib.rpa_forward_noalloc(ctypes.byref(prm), _ptr(q), _ptr(kv_pages), _ptr(kv_lens), _ptr(page_indices),
+                                   _ptr(cu_q_lens), _ptr(num_seqs), _ptr(out), _stream()))
     return out
 
 

@@ -480,3 +480,63 @@ int rpa_check_device_status(void* workspace, uint32_t* bits, rpa_stream_t stream
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// rpa_forward_noalloc: rpa_forward for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: a plugin running inside a host application
+// whose memory manager owns all of the device memory, or a serving loop that must not
+// allocate after start-up because cudaMalloc can synchronise the device.  This entry
+// point gives them rpa_forward without a workspace argument: its scratch (work lists,
+// split-KV partials, counters) is the fixed file-scope array below, which every GPU
+// that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = RPA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that device
+// current (the host-side name of the array is only a stand-in, never a device address).
+void* noalloc_scratch_ptr(int* rc) {
+    static std::mutex mu;
+    static void* ptrs[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *rc = e != cudaSuccess ? cuda_fail(e, "rpa_forward_noalloc: cudaGetDevice")
+                               : fail(RPA_ERR_CUDA, "rpa_forward_noalloc: device index %d out of range", dev);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            *rc = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "rpa_forward_noalloc: cudaGetSymbolAddress");
+            return nullptr;
+        }
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" int rpa_forward_noalloc(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                                   const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs,
+                                   void* out, rpa_stream_t stream) {
+    int rc = check_rpa_params(p);
+    if (rc) return rc;
+    const size_t need = rpa_layout(p).total;
+    if (need > kNoAllocScratchBytes)
+        return fail(RPA_ERR_WORKSPACE,
+                    "rpa_forward_noalloc: these maxima need %zu bytes of scratch but the library's static scratch "
+                    "holds %zu; use rpa_forward with a caller-allocated workspace",
+                    need, kNoAllocScratchBytes);
+    rc = RPA_OK;
+    void* scratch = noalloc_scratch_ptr(&rc);
+    if (!scratch) return rc;
+    return rpa_forward(p, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, out, scratch, kNoAllocScratchBytes,
+                       stream);
+}
