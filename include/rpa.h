@@ -87,6 +87,7 @@ typedef enum {
 #define RPA_DEV_ERR_PAGE       0x08u  /* a used page index outside [0, total_num_pages) */
 #define RPA_DEV_ERR_TOKENS     0x10u  /* cu_q_lens[num_seqs] > max_num_tokens or not monotone */
 #define RPA_DEV_ERR_POSITION   0x20u  /* sparse: query position outside [0, seq_len) */
+#define RPA_DEV_ERR_TIMEOUT    0x40u  /* a pipeline wait gave up after its time limit (2 s) */
 
 /* CUDA stream handle (ABI-compatible with cudaStream_t). */
 typedef struct CUstream_st* rpa_stream_t;

@@ -85,7 +85,8 @@ RpaLayout rpa_layout(const rpa_params* p) {
     RpaLayout L;
     const int hkv = p->num_combined_kv_heads / 2;
     const int G = p->num_q_heads / hkv;
-    const int groups = cdiv(hkv, kDecodeHeads);
+    const int dh = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
+    const int groups = cdiv(hkv, dh);
     L.max_dec = kDecodeTargetCtas + groups * p->max_num_seqs;
     L.max_pre = hkv * (int)((long long)p->max_num_tokens * G / kPrefillRows + p->max_num_seqs + 1);
     size_t off = kWsHeaderBytes;
@@ -96,9 +97,9 @@ RpaLayout rpa_layout(const rpa_params* p) {
     L.tickets = off;
     off = align_up(off + sizeof(int) * (size_t)L.max_dec);
     L.pml = off;
-    off = align_up(off + sizeof(float) * 2 * kDecodeHeads * 16 * (size_t)L.max_dec);
+    off = align_up(off + sizeof(float) * 2 * dh * 16 * (size_t)L.max_dec);
     L.po = off;
-    off = align_up(off + sizeof(float) * (size_t)p->head_dim * kDecodeHeads * 16 * (size_t)L.max_dec);
+    off = align_up(off + sizeof(float) * (size_t)p->head_dim * dh * 16 * (size_t)L.max_dec);
     L.total = off;
     return L;
 }
@@ -247,6 +248,7 @@ int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const 
     a.k_scale_or_one = p->k_scale != 0.f ? p->k_scale : 1.f;
     a.v_scale_or_one = p->v_scale != 0.f ? p->v_scale : 1.f;
     a.decode_target_ctas = kDecodeTargetCtas;
+    a.decode_heads = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
     a.hdr = reinterpret_cast<WsHeader*>(ws);
     a.dec_items = reinterpret_cast<WorkItem*>(ws + L.items_dec);
     a.pre_items = reinterpret_cast<WorkItem*>(ws + L.items_pre);

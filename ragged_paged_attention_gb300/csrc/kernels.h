@@ -11,7 +11,7 @@ namespace rpa {
 struct WsHeader;
 
 // Tiling constants of the RPA kernels.
-constexpr int kDecodeHeads = 4;         // KV heads per decode CTA (one warp each)
+constexpr int kMaxDecodeHeads = 4;      // most KV heads a decode CTA covers (one warp each)
 constexpr int kDecodeBK = 16;           // keys per decode pipeline stage
 constexpr int kPrefillRows = 64;        // (token, q-head) rows per prefill CTA
 constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
@@ -45,6 +45,7 @@ struct RpaArgs {
     int has_scale;              // k_scale or v_scale given
     float k_scale_or_one, v_scale_or_one;
     int decode_target_ctas;
+    int decode_heads;           // KV heads per decode item (decode_heads_for)
     // workspace
     WsHeader* hdr;
     WorkItem* dec_items;
@@ -126,6 +127,8 @@ struct MlaUpdateArgs {
 };
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_rpa_decode(const RpaArgs& a, int num_sms, cudaStream_t stream);
+int decode_heads_for(int head_dim, bool fp8);
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream);

@@ -1,0 +1,427 @@
+// Decode-class work of ragged paged attention (tpu-inference "ragged_paged_attention/v2/
+// kernel.py": sequences whose q_len * G query rows fit one 16-row tile), for sm_103a.
+//
+// Decode attention reads every visible key once and does ~2 flops per byte, so it is
+// bound by HBM.  The kernel is a warp-specialised streaming pipeline:
+//   * a producer warp walks the page table (lane t resolves token t of a 16-key stage,
+//     one stage ahead) and issues one bulk (TMA 1-D) copy per token: the contiguous K/V
+//     segment of HG KV heads of that token (HG * 2 * D elements) lands in a padded
+//     shared-memory row (padding keeps ldmatrix conflict free); a full/empty mbarrier
+//     pair per stage orders producer and consumers;
+//   * HG consumer warps, one per KV head, hold their query rows (G heads x q_len
+//     tokens, <= 16) as tensor-core A fragments in registers and run QK^T and PV on
+//     m16n8k16 tiles with an online softmax; fp8 (or scaled bf16) K/V are first
+//     dequantised by the warp into its own bf16 rows as bf16(float(x) * scale);
+//   * slots past kv_len are never copied: the stage memory is zeroed once at start, so
+//     a skipped row holds finite data whose probability is exactly zero.
+// Items split the keys of a sequence (flash-decoding); split partials (m, l, O) are
+// merged by the last CTA of the group (atomic ticket), as in rpa_kernels.cu.
+#include "common.cuh"
+#include "kernels.h"
+#include "profile.h"
+
+namespace rpa {
+
+template <int D, int HG, int ESZ, bool CONV>
+struct DecTile {
+    static constexpr int BK = kDecodeBK;                 // keys per stage
+    static constexpr int kSeg = HG * 2 * D * ESZ;        // bytes of one token's segment
+    static constexpr int kRow = kSeg + 16;               // padded shared-memory row
+    static constexpr int kStage = BK * kRow;
+    static constexpr int kConvRow = 2 * D * 2 + 16;      // one head's K|V in bf16, padded
+    static constexpr int kConv = CONV ? HG * BK * kConvRow : 0;
+    static constexpr int kBudget = 104 * 1024;           // two CTAs per SM
+    static constexpr int kFit = (kBudget - kConv) / kStage;
+    static constexpr int STAGES = kFit < 2 ? 2 : (kFit > 4 ? 4 : kFit);
+    static constexpr int kBarOff = STAGES * kStage + kConv;
+    static constexpr int kSmem = kBarOff + 2 * STAGES * 8;
+    static constexpr int kThreads = (HG + 1) * 32;
+    static_assert(kSeg % 16 == 0, "bulk copies move 16-byte multiples");
+};
+
+// 8 elements (K or V of one head) -> 8 bf16 of bf16(float(x) * scale), packed in a uint4.
+template <int ESZ>
+__device__ __forceinline__ uint4 dequant8(const uint8_t* src, float sc) {
+    uint32_t w[4];
+    if (ESZ == 1) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = e4m3x2_to_float2(h[e]);
+            w[e] = pack_bf16(f.x * sc, f.y * sc);
+        }
+    } else {
+        const uint4 raw = *reinterpret_cast<const uint4*>(src);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            w[e] = pack_bf16(f.x * sc, f.y * sc);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int D, int HG, int ESZ, bool CONV>
+__global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decode_kernel(RpaArgs a) {
+    using T = DecTile<D, HG, ESZ, CONV>;
+    constexpr int BK = T::BK, STAGES = T::STAGES;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    uint8_t* conv = smem + STAGES * T::kStage;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kBarOff);
+    uint64_t* empty = full + STAGES;
+    __shared__ WorkItem s_item;
+    __shared__ int s_item_idx, s_last;
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool producer = warp == HG;
+    WsHeader* hdr = a.hdr;
+    uint32_t* err = &hdr->error_bits;
+    const int Hkv = a.num_kv_heads, G = a.num_q_heads / Hkv, C = 2 * Hkv;
+    const uint8_t* kv = static_cast<const uint8_t*>(a.kv_pages);
+
+    // zero the stages once: rows that are never copied (slots past kv_len) stay finite
+    for (int i = tid * 16; i < STAGES * T::kStage; i += blockDim.x * 16)
+        *reinterpret_cast<uint4*>(stages + i) = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], HG);
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    uint32_t pipe = 0;            // blocks this CTA has pushed through the ring so far
+    uint32_t issued_phase[4] = {0, 0, 0, 0};  // producer: last phase issued per stage (+1)
+
+    while (true) {
+        if (tid == 0) {
+            const int it = atomicAdd(&hdr->next_item[0], 1);
+            s_item.seq = -1;
+            s_item_idx = it;
+            if (it < hdr->num_items[0]) s_item = a.dec_items[it];
+        }
+        __syncthreads();
+        const WorkItem w = s_item;
+        const int self = s_item_idx;
+        if (w.seq < 0 || s_abort) break;
+        const int s = w.seq;
+        const int q_start = a.cu_q_lens[s];
+        const int q_len = a.cu_q_lens[s + 1] - q_start;
+        const int kv_len = a.kv_lens[s];
+        const int n_rows = q_len * G;
+        const int kb = w.key_begin, ke = w.key_end;
+        const int n_blocks = ke > kb ? cdiv(ke - kb, BK) : 0;
+        const int h0 = w.head;
+        const int seg_heads = min(HG, Hkv - h0);
+        const uint32_t seg_bytes = seg_heads * 2 * D * ESZ;
+
+        if (producer) {
+            // lane t < BK owns token t of every stage: it resolves that token's page (the
+            // next stage's entry is fetched while this stage's slot is still busy) and
+            // issues the token's bulk copy, so the 16 copies of a stage go out together.
+            const size_t tbl = (size_t)s * a.pages_per_seq;
+            auto page_of = [&](int blk) -> int {
+                const int key = kb + blk * BK + lane;
+                return (lane < BK && blk < n_blocks && key < ke) ? __ldg(a.page_indices + tbl + key / a.page_size)
+                                                                 : -1;
+            };
+            int page_next = page_of(0);
+            for (int blk = 0; blk < n_blocks; ++blk) {
+                const uint32_t q = pipe + blk, st = q % STAGES, ph = (q / STAGES) & 1;
+                const int page = page_next;
+                page_next = page_of(blk + 1);
+                const int key = kb + blk * BK + lane;
+                const bool want = lane < BK && key < ke;
+                const bool ok = want && (unsigned)page < (unsigned)a.total_num_pages;
+                if (want && !ok) set_error(err, RPA_DEV_ERR_PAGE);
+                const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+                int go = 1;
+                if (lane == 0) {
+                    go = mbar_wait(&empty[st], ph ^ 1, err);
+                    if (go) {
+                        mbar_arrive_expect_tx(&full[st], __popc(mask) * seg_bytes);
+                        issued_phase[st] = ph + 1;
+                    } else {
+                        s_abort = 1;
+                    }
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) break;
+                if (ok) {
+                    const uint8_t* src =
+                        kv + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * h0) * (size_t)(D * ESZ);
+                    bulk_g2s(smem_u32(stages + st * T::kStage + lane * T::kRow), src, seg_bytes, &full[st]);
+                }
+            }
+        } else {
+            // ---------------- consumer warp: KV head h0 + warp ----------------
+            const bool head_ok = warp < seg_heads;
+            const int head = h0 + warp;
+            const int g8 = lane >> 2, q4 = lane & 3;
+            int qpos[2], wlo[2];
+            bool rv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int R = g8 + e * 8;
+                rv[e] = head_ok && R < n_rows;
+                qpos[e] = rv[e] ? kv_len - q_len + R / G : -1;
+                wlo[e] = a.sliding_window > 0 ? qpos[e] - a.sliding_window + 1 : 0;
+            }
+            // query rows as A fragments (row g8 / g8+8, columns 2*q4.. of each 16-wide k-step)
+            uint32_t qa[D / 16][4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int R = g8 + e * 8;
+                const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                    a.q + ((size_t)(q_start + (rv[e] ? R / G : 0)) * a.num_q_heads + head * G + (rv[e] ? R % G : 0)) * D);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    qa[ks][e] = rv[e] ? __ldg(qrow + ks * 8 + q4) : 0u;
+                    qa[ks][e + 2] = rv[e] ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;
+                }
+            }
+            float o[D / 8][4];
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+            const float scale = a.sm_scale, cap = a.soft_cap;
+
+            for (int blk = 0; blk < n_blocks; ++blk) {
+                const uint32_t qn = pipe + blk, st = qn % STAGES, ph = (qn / STAGES) & 1;
+                if (!mbar_wait(&full[st], ph, err)) {
+                    s_abort = 1;
+                    break;
+                }
+                const uint8_t* stg = stages + st * T::kStage;
+                uint32_t kbase, vbase;
+                int rowb;
+                if (CONV) {
+                    uint8_t* cb = conv + warp * BK * T::kConvRow;
+                    if (head_ok) {
+                        constexpr int kChunks = 2 * D / 8;  // 8-element chunks of K|V per key
+                        for (int i = lane; i < BK * kChunks; i += 32) {
+                            const int kk = i / kChunks, c = i % kChunks;
+                            const float sc = c < D / 8 ? a.k_scale_or_one : a.v_scale_or_one;
+                            *reinterpret_cast<uint4*>(cb + kk * T::kConvRow + c * 16) =
+                                dequant8<ESZ>(stg + kk * T::kRow + (warp * 2 * D + c * 8) * ESZ, sc);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);  // the stage is free once converted
+                    kbase = smem_u32(cb);
+                    rowb = T::kConvRow;
+                } else {
+                    kbase = smem_u32(stg) + warp * 2 * D * 2;
+                    rowb = T::kRow;
+                }
+                vbase = kbase + D * 2;
+                if (head_ok) {
+                    const int key0 = kb + blk * BK;
+                    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    {
+                        const uint32_t ka = kbase + (((lane >> 4) << 3) + (lane & 7)) * rowb + ((lane >> 3) & 1) * 16;
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(ka + ks * 32, b0, b1, b2, b3);
+                            mma_bf16(sc[0], qa[ks], b0, b1);
+                            mma_bf16(sc[1], qa[ks], b2, b3);
+                        }
+                    }
+                    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = e >> 1;
+                            const int key = key0 + nt * 8 + 2 * q4 + (e & 1);
+                            float x = sc[nt][e] * scale;
+                            if (cap != 0.f) x = cap * tanhf(x / cap);
+                            x *= kLog2e;
+                            const bool ok = key <= qpos[r] && key >= wlo[r] && key < ke;
+                            x = ok ? x : -INFINITY;
+                            sc[nt][e] = x;
+                            mx[r] = fmaxf(mx[r], x);
+                        }
+                    }
+                    float alpha[2], muse[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                        const float mn = fmaxf(m_run[r], mx[r]);
+                        muse[r] = mn == -INFINITY ? 0.f : mn;
+                        alpha[r] = fast_exp2(m_run[r] - muse[r]);
+                        m_run[r] = mn;
+                        l_run[r] *= alpha[r];
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float p = fast_exp2(sc[nt][e] - muse[e >> 1]);
+                            sc[nt][e] = p;
+                            l_run[e >> 1] += p;
+                        }
+                    uint32_t pf[4];
+                    pf[0] = pack_bf16(sc[0][0], sc[0][1]);
+                    pf[1] = pack_bf16(sc[0][2], sc[0][3]);
+                    pf[2] = pack_bf16(sc[1][0], sc[1][1]);
+                    pf[3] = pack_bf16(sc[1][2], sc[1][3]);
+                    const uint32_t va = vbase + ((lane & 7) + (((lane >> 3) & 1) << 3)) * rowb + (lane >> 4) * 16;
+#pragma unroll
+                    for (int dp = 0; dp < D / 16; ++dp) {
+                        o[2 * dp][0] *= alpha[0];
+                        o[2 * dp][1] *= alpha[0];
+                        o[2 * dp][2] *= alpha[1];
+                        o[2 * dp][3] *= alpha[1];
+                        o[2 * dp + 1][0] *= alpha[0];
+                        o[2 * dp + 1][1] *= alpha[0];
+                        o[2 * dp + 1][2] *= alpha[1];
+                        o[2 * dp + 1][3] *= alpha[1];
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(va + dp * 32, b0, b1, b2, b3);
+                        mma_bf16(o[2 * dp], pf, b0, b1);
+                        mma_bf16(o[2 * dp + 1], pf, b2, b3);
+                    }
+                }
+                if (!CONV) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
+                }
+            }
+            // ---- results of this warp's rows ----
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+            }
+            if (!s_abort) {
+                if (w.num_splits == 1) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (!rv[e]) continue;
+                        const int R = g8 + e * 8;
+                        const float inv = l_run[e] > 0.f ? 1.f / l_run[e] : 0.f;
+                        __nv_bfloat16* dst =
+                            a.out + ((size_t)(q_start + R / G) * a.num_q_heads + head * G + R % G) * D;
+#pragma unroll
+                        for (int dt = 0; dt < D / 8; ++dt)
+                            *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * q4) =
+                                pack_bf16(o[dt][2 * e] * inv, o[dt][2 * e + 1] * inv);
+                    }
+                } else {
+                    float* po = a.partial_o + (size_t)self * (a.decode_heads * 16 * D);
+                    float* pml = a.partial_ml + (size_t)self * (a.decode_heads * 16 * 2);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (!rv[e]) continue;
+                        const int r = warp * 16 + g8 + e * 8;
+#pragma unroll
+                        for (int dt = 0; dt < D / 8; ++dt)
+                            *reinterpret_cast<float2*>(po + (size_t)r * D + dt * 8 + 2 * q4) =
+                                make_float2(o[dt][2 * e], o[dt][2 * e + 1]);
+                        if (q4 == 0) {
+                            pml[r * 2] = m_run[e];
+                            pml[r * 2 + 1] = l_run[e];
+                        }
+                    }
+                }
+            }
+        }
+        pipe += n_blocks;
+        __syncthreads();
+        if (s_abort) break;
+        if (w.num_splits == 1) continue;
+        // ---- split merge: the last CTA of the group combines every split ----
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(&a.tickets[w.first_item], 1) == w.num_splits - 1;
+        __syncthreads();
+        if (!s_last) continue;
+        __threadfence();
+        if (!producer && warp < seg_heads) {
+            const int head = h0 + warp;
+            for (int R = 0; R < min(n_rows, 16); ++R) {
+                const int row = warp * 16 + R;
+                float M = -INFINITY;
+                for (int sp = 0; sp < w.num_splits; ++sp)
+                    M = fmaxf(M, __ldcg(a.partial_ml + (size_t)(w.first_item + sp) * (a.decode_heads * 32) + row * 2));
+                const float Mu = M == -INFINITY ? 0.f : M;
+                float L = 0.f;
+                float acc[D / 32];
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+                for (int sp = 0; sp < w.num_splits; ++sp) {
+                    const size_t it = (size_t)(w.first_item + sp);
+                    const float m = __ldcg(a.partial_ml + it * (a.decode_heads * 32) + row * 2);
+                    const float l = __ldcg(a.partial_ml + it * (a.decode_heads * 32) + row * 2 + 1);
+                    const float f = fast_exp2(m - Mu);
+                    L += f * l;
+                    const float* src = a.partial_o + it * (a.decode_heads * 16 * D) + (size_t)row * D;
+#pragma unroll
+                    for (int i = 0; i < D / 32; ++i) acc[i] += f * __ldcg(src + i * 32 + lane);
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                __nv_bfloat16* dst = a.out + ((size_t)(q_start + R / G) * a.num_q_heads + head * G + R % G) * D;
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i) dst[i * 32 + lane] = __float2bfloat16_rn(acc[i] * inv);
+            }
+        }
+        if (tid == 0) a.tickets[w.first_item] = 0;
+    }
+    // after an abort, wait (bounded) until no bulk copy can still land in this CTA's memory
+    if (producer && lane == 0 && s_abort) {
+        for (int st = 0; st < STAGES; ++st)
+            if (issued_phase[st]) mbar_wait(&full[st], issued_phase[st] - 1, err);
+    }
+}
+
+template <int D, int HG, int ESZ, bool CONV>
+static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    using T = DecTile<D, HG, ESZ, CONV>;
+    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV>;
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::kThreads, T::kSmem);
+        if (e != cudaSuccess) return e;
+        per_sm = n > 0 ? n : 1;
+    }
+    ProfScope ps("rpa_decode_attn", stream);
+    kern<<<num_sms * per_sm, T::kThreads, T::kSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+int decode_heads_for(int head_dim, bool fp8) {
+    (void)fp8;
+    return head_dim >= 256 ? 2 : 4;
+}
+
+template <int D>
+static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    constexpr int HG = D >= 256 ? 2 : 4;
+    if (a.kv_fp8) return launch_decode<D, HG, 1, true>(a, num_sms, stream);
+    if (a.has_scale) return launch_decode<D, HG, 2, true>(a, num_sms, stream);
+    return launch_decode<D, HG, 2, false>(a, num_sms, stream);
+}
+
+cudaError_t launch_rpa_decode(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    switch (a.head_dim) {
+        case 64: return launch_decode_d<64>(a, num_sms, stream);
+        case 128: return launch_decode_d<128>(a, num_sms, stream);
+        case 256: return launch_decode_d<256>(a, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rpa

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     __syncthreads();
     const int num = s_num;
     const int G = a.num_q_heads / a.num_kv_heads;
-    const int n_groups = cdiv(a.num_kv_heads, kDecodeHeads);
+    const int n_groups = cdiv(a.num_kv_heads, a.decode_heads);
 
     // pass 1: total decode work (keys x head groups)
     long long dec_keys = 0;
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
                 if (it >= a.max_dec_items) break;  // cannot happen: the host bound covers it
                 WorkItem w;
                 w.seq = s;
-                w.head = g * kDecodeHeads;
+                w.head = g * a.decode_heads;
                 w.key_begin = klo + i * chunk;
                 w.key_end = min(kl, klo + (i + 1) * chunk);
                 w.first_item = od + g * nsplit;
@@ -571,10 +571,9 @@ static cudaError_t launch_attn(const RpaArgs& a, int grid, cudaStream_t stream) 
 template <int D, bool FP8>
 static cudaError_t launch_rpa_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
     constexpr int kPreBK = D >= 256 ? 32 : 64;
-    constexpr int kDecStages = (D >= 256 && !FP8) ? 2 : 3;
     cudaError_t e = launch_attn<D, 1, kPreBK, 3, FP8, false>(a, num_sms, stream);
     if (e != cudaSuccess) return e;
-    return launch_attn<D, kDecodeHeads, kDecodeBK, kDecStages, FP8, true>(a, num_sms, stream);
+    return launch_rpa_decode(a, num_sms, stream);
 }
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream) {
