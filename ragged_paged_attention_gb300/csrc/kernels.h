@@ -13,7 +13,7 @@ struct WsHeader;
 // Tiling constants of the RPA kernels.
 constexpr int kMaxDecodeHeads = 4;      // most KV heads a decode CTA covers (one warp each)
 constexpr int kDecodeBK = 16;           // keys per decode pipeline stage
-constexpr int kPrefillRows = 64;        // (token, q-head) rows per prefill CTA
+constexpr int kPrefillRows = 128;       // (token, q-head) rows per prefill item (one TMEM tile)
 constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
 constexpr int kDecodeTargetCtas = 1024; // split so decode work spreads over about this many CTAs
 
@@ -128,6 +128,7 @@ struct MlaUpdateArgs {
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_rpa_decode(const RpaArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream);
 int decode_heads_for(int head_dim, bool fp8);
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);

@@ -5,13 +5,11 @@
 //   * rpa_plan_kernel reads the device metadata (num_seqs, cu_q_lens, kv_lens),
 //     validates it, and writes two work lists into the workspace: "decode" items
 //     (sequences whose q_len * G rows fit one 16-row tile, split along the keys) and
-//     "prefill" items (64-row tiles of one KV head over the whole causal key range).
-//   * rpa_attn_kernel<DECODE=true/false> are persistent CTAs that steal items from
-//     their list.  K/V rows are gathered page by page with cp.async into swizzled
-//     shared-memory stages; QK^T and PV run on bf16 tensor-core tiles with fp32
-//     accumulation and an online softmax in the log2 domain.
-//   * Split decode items store (m, l, unnormalised O) partials; the last CTA of a
-//     group (atomic ticket) merges them with the log-sum-exp rule.
+//     "prefill" items (128-row tiles of one KV head over the whole causal key range)
+//     (prefill items are 128 rows of one KV head: kPrefillRows).
+//   * the prefill items run on tcgen05/TMEM (rpa_prefill_tc.cu), the decode items on
+//     the streaming split-KV kernel (rpa_decode.cu); both are persistent CTAs that
+//     steal items from their list.
 #include "common.cuh"
 #include "kernels.h"
 #include "profile.h"
@@ -129,367 +127,6 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Attention
-// ---------------------------------------------------------------------------
-template <int D, int NH, int BK, int STAGES, bool FP8>
-struct RpaTile {
-    static constexpr int kEsz = FP8 ? 1 : 2;
-    static constexpr int kRowBytes = NH * 2 * D * kEsz;          // one key, NH heads, K and V
-    static constexpr int kRowBytesBf16 = NH * 2 * D * 2;
-    static constexpr int kChunksPerPart = D * kEsz / 16;         // 16-byte chunks in one K (or V) row
-    static constexpr int kStageBytes = BK * kRowBytes;
-    static constexpr int kConvBytes = FP8 ? BK * kRowBytesBf16 : 0;
-    static constexpr int kQBytes = 64 * D * 2;
-    static constexpr int kSmem = STAGES * kStageBytes + kConvBytes + kQBytes;
-    static_assert(kRowBytes % 128 == 0, "swizzle needs 128-byte rows");
-};
-
-template <int D, int NH, int BK, int STAGES, bool FP8, bool DECODE>
-__global__ void __launch_bounds__(128) rpa_attn_kernel(RpaArgs a) {
-    using T = RpaTile<D, NH, BK, STAGES, FP8>;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* stages = smem;
-    uint8_t* conv = smem + STAGES * T::kStageBytes;
-    uint8_t* qs = conv + T::kConvBytes;
-    __shared__ WorkItem s_item;
-    __shared__ int s_last;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = a.num_q_heads / a.num_kv_heads;
-    const int C = 2 * a.num_kv_heads;
-    const int list = DECODE ? 0 : 1;
-    const WorkItem* items = DECODE ? a.dec_items : a.pre_items;
-    WsHeader* hdr = a.hdr;
-    const uint8_t* kv = static_cast<const uint8_t*>(a.kv_pages);
-    // the bf16 operand tile the MMAs read: the conversion buffer for fp8, the stage otherwise
-    constexpr int kOpRowBytes = T::kRowBytesBf16;
-
-    while (true) {
-        __syncthreads();
-        if (tid == 0) {
-            const int it = atomicAdd(&hdr->next_item[list], 1);
-            s_item.seq = -1;
-            if (it < hdr->num_items[list]) {
-                s_item = items[it];
-                s_item.first_item = DECODE ? s_item.first_item : it;
-                s_item.row_begin = DECODE ? it : s_item.row_begin;  // decode: remember own index
-            }
-        }
-        __syncthreads();
-        const WorkItem w = s_item;
-        if (w.seq < 0) break;
-        const int s = w.seq;
-        const int q_start = a.cu_q_lens[s];
-        const int q_len = a.cu_q_lens[s + 1] - q_start;
-        const int kv_len = a.kv_lens[s];
-        const int n_rows = q_len * G;  // rows of one KV head in this sequence
-
-        // rows owned by this warp: 16 rows of one KV head
-        const int my_head = DECODE ? w.head + warp : w.head;
-        const int row0 = DECODE ? 0 : w.row_begin + warp * 16;
-        const bool head_ok = my_head < a.num_kv_heads;
-        // per-thread rows (g, g + 8) -> query position and window start
-        int qpos[2], wlo[2];
-        bool rv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int R = row0 + (lane >> 2) + e * 8;
-            rv[e] = head_ok && R < n_rows;
-            const int j = rv[e] ? R / G : 0;
-            qpos[e] = kv_len - q_len + j;
-            wlo[e] = a.sliding_window > 0 ? qpos[e] - a.sliding_window + 1 : 0;
-            if (!rv[e]) qpos[e] = -1;
-        }
-        // key range of the whole CTA
-        int kb, ke;
-        if (DECODE) {
-            kb = w.key_begin;
-            ke = w.key_end;
-        } else {
-            const int R0 = w.row_begin;
-            const int R1 = min(n_rows, w.row_begin + 64) - 1;
-            const int qmin = kv_len - q_len + R0 / G;
-            const int qmax = kv_len - q_len + R1 / G;
-            kb = a.sliding_window > 0 ? max(0, qmin - a.sliding_window + 1) : 0;
-            kb = kb / BK * BK;
-            ke = qmax + 1;
-        }
-        const int n_blocks = ke > kb ? cdiv(ke - kb, BK) : 0;
-
-        // ---- Q tile -> shared (rows of invalid tokens/heads are zero) ----
-        {
-            constexpr int kQChunks = D * 2 / 16;
-            for (int i = tid; i < 64 * kQChunks; i += 128) {
-                const int r = i / kQChunks, c = i % kQChunks;
-                const int wr = r / 16;  // warp that owns the row
-                const int head = DECODE ? w.head + wr : w.head;
-                const int R = (DECODE ? 0 : w.row_begin + wr * 16) + (r % 16);
-                const bool v = head < a.num_kv_heads && R < n_rows;
-                const int j = v ? R / G : 0, g = v ? R % G : 0;
-                const __nv_bfloat16* src = a.q + ((size_t)(q_start + j) * a.num_q_heads + head * G + g) * D + c * 8;
-                cp_async16(smem_u32(qs + swz(r, c, D * 2)), v ? (const void*)src : (const void*)a.q, v);
-            }
-        }
-
-        auto load_block = [&](int blk, int stage) {
-            uint8_t* dst = stages + stage * T::kStageBytes;
-            const int key0 = kb + blk * BK;
-            constexpr int kChunksPerKey = NH * 2 * T::kChunksPerPart;
-            for (int i = tid; i < BK * kChunksPerKey; i += 128) {
-                const int kk = i / kChunksPerKey, c = i % kChunksPerKey;
-                const int hh = c / (2 * T::kChunksPerPart);
-                const int part = (c / T::kChunksPerPart) & 1;
-                const int cc = c % T::kChunksPerPart;
-                const int key = key0 + kk;
-                const int head = (DECODE ? w.head : w.head) + hh;
-                bool v = key < ke && key < kv_len && head < a.num_kv_heads;
-                const uint8_t* src = kv;
-                if (v) {
-                    const int page = a.page_indices[(size_t)s * a.pages_per_seq + key / a.page_size];
-                    if ((unsigned)page >= (unsigned)a.total_num_pages) {
-                        set_error(&hdr->error_bits, RPA_DEV_ERR_PAGE);
-                        v = false;
-                    } else {
-                        src = kv + ((((size_t)page * a.page_size + key % a.page_size) * C + 2 * head + part) * D) *
-                                       T::kEsz +
-                              cc * 16;
-                    }
-                }
-                cp_async16(smem_u32(dst + swz(kk, c, T::kRowBytes)), src, v);
-            }
-        };
-
-        // ---- prologue ----
-#pragma unroll
-        for (int st = 0; st < STAGES - 1; ++st) {
-            if (st < n_blocks) load_block(st, st);
-            cp_async_commit();
-        }
-
-        float o[D / 8][4];
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        const float scale = a.sm_scale;
-        const float cap = a.soft_cap;
-        const uint32_t q_base = smem_u32(qs) ;
-        const int kv_head_chunk = DECODE ? warp * 2 * (D * 2 / 16) : 0;  // chunk offset of this warp's K in a bf16 row
-
-        for (int blk = 0; blk < n_blocks; ++blk) {
-            {
-                const int nb = blk + STAGES - 1;
-                if (nb < n_blocks) load_block(nb, nb % STAGES);
-                cp_async_commit();
-            }
-            cp_async_wait<STAGES - 1>();
-            __syncthreads();
-            const uint8_t* stage = stages + (blk % STAGES) * T::kStageBytes;
-            const uint8_t* op = stage;
-            if (FP8 || a.has_scale) {
-                // dequantise: bf16(float(x) * scale), the reference's K/V conversion
-                constexpr int kIn = T::kRowBytes / 16;  // 16-byte chunks per key row (input)
-                uint8_t* dst = FP8 ? conv : const_cast<uint8_t*>(stage);
-                for (int i = tid; i < BK * kIn; i += 128) {
-                    const int kk = i / kIn, c = i % kIn;
-                    const int part = (c / T::kChunksPerPart) & 1;
-                    const float sc = part ? a.v_scale_or_one : a.k_scale_or_one;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(stage + swz(kk, c, T::kRowBytes));
-                    if (FP8) {
-                        const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
-                        uint32_t outw[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            float2 f = e4m3x2_to_float2(h[e]);
-                            outw[e] = pack_bf16(f.x * sc, f.y * sc);
-                        }
-                        // input chunk c (16 fp8) -> output chunks 2c, 2c+1 (8 bf16 each)
-                        *reinterpret_cast<uint4*>(dst + swz(kk, 2 * c, kOpRowBytes)) =
-                            make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                        *reinterpret_cast<uint4*>(dst + swz(kk, 2 * c + 1, kOpRowBytes)) =
-                            make_uint4(outw[4], outw[5], outw[6], outw[7]);
-                    } else {
-                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                        uint32_t outw[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float2 f = __bfloat1622float2(h[e]);
-                            outw[e] = pack_bf16(f.x * sc, f.y * sc);
-                        }
-                        *reinterpret_cast<uint4*>(dst + swz(kk, c, T::kRowBytes)) =
-                            make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                    }
-                }
-                __syncthreads();
-                op = FP8 ? conv : stage;
-            }
-            const uint32_t op_base = smem_u32(op);
-            const int key0 = kb + blk * BK;
-
-            // ---- S = Q K^T ----
-            float sc[BK / 8][4];
-#pragma unroll
-            for (int i = 0; i < BK / 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t af[4];
-                ldsm_x4(q_base + swz(warp * 16 + (lane & 15), ks * 2 + (lane >> 4), D * 2), af[0], af[1], af[2], af[3]);
-#pragma unroll
-                for (int np = 0; np < BK / 16; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int key = np * 16 + ((lane >> 4) << 3) + (lane & 7);
-                    ldsm_x4(op_base + swz(key, kv_head_chunk + ks * 2 + ((lane >> 3) & 1), kOpRowBytes), b0, b1, b2, b3);
-                    mma_bf16(sc[2 * np], af, b0, b1);
-                    mma_bf16(sc[2 * np + 1], af, b2, b3);
-                }
-            }
-            // ---- scale, soft cap, mask ----
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nt = 0; nt < BK / 8; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = e >> 1;
-                    const int key = key0 + nt * 8 + 2 * (lane & 3) + (e & 1);
-                    float x = sc[nt][e] * scale;
-                    if (cap != 0.f) x = cap * tanhf(x / cap);
-                    x *= kLog2e;
-                    const bool ok = key <= qpos[r] && key >= wlo[r] && key < kv_len;
-                    x = ok ? x : -INFINITY;
-                    sc[nt][e] = x;
-                    mx[r] = fmaxf(mx[r], x);
-                }
-            }
-            float alpha[2], muse[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float mn = fmaxf(m_run[r], mx[r]);
-                muse[r] = mn == -INFINITY ? 0.f : mn;
-                alpha[r] = fast_exp2(m_run[r] - muse[r]);
-                m_run[r] = mn;
-                l_run[r] *= alpha[r];
-            }
-#pragma unroll
-            for (int nt = 0; nt < BK / 8; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p = fast_exp2(sc[nt][e] - muse[e >> 1]);
-                    sc[nt][e] = p;
-                    l_run[e >> 1] += p;
-                }
-            }
-#pragma unroll
-            for (int dt = 0; dt < D / 8; ++dt) {
-                o[dt][0] *= alpha[0];
-                o[dt][1] *= alpha[0];
-                o[dt][2] *= alpha[1];
-                o[dt][3] *= alpha[1];
-            }
-            // ---- O += P V ----
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                uint32_t pf[4];
-                pf[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-                pf[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-                pf[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                pf[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int chunk = kv_head_chunk + (D * 2 / 16) + dp * 2 + (lane >> 4);
-                    ldsm_x4_t(op_base + swz(key, chunk, kOpRowBytes), b0, b1, b2, b3);
-                    mma_bf16(o[2 * dp], pf, b0, b1);
-                    mma_bf16(o[2 * dp + 1], pf, b2, b3);
-                }
-            }
-            __syncthreads();  // the stage (and conversion buffer) may be refilled now
-        }
-        cp_async_wait<0>();
-
-        // ---- finalise ----
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-        }
-        const int g8 = lane >> 2, q4 = lane & 3;
-        if (!DECODE || w.num_splits == 1) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (!rv[e]) continue;
-                const int R = row0 + g8 + e * 8;
-                const int j = R / G, qh = my_head * G + R % G;
-                const float inv = l_run[e] > 0.f ? 1.f / l_run[e] : 0.f;
-                __nv_bfloat16* dst = a.out + ((size_t)(q_start + j) * a.num_q_heads + qh) * D;
-#pragma unroll
-                for (int dt = 0; dt < D / 8; ++dt)
-                    *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * q4) =
-                        pack_bf16(o[dt][2 * e] * inv, o[dt][2 * e + 1] * inv);
-            }
-            continue;
-        }
-        // split decode: store the partial, then the last CTA of the group merges
-        const int self = w.row_begin;  // own item index (set above)
-        float* po = a.partial_o + (size_t)self * (NH * 16 * D);
-        float* pml = a.partial_ml + (size_t)self * (NH * 16 * 2);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = warp * 16 + g8 + e * 8;
-#pragma unroll
-            for (int dt = 0; dt < D / 8; ++dt)
-                *reinterpret_cast<float2*>(po + (size_t)r * D + dt * 8 + 2 * q4) = make_float2(o[dt][2 * e], o[dt][2 * e + 1]);
-            if (q4 == 0) {
-                pml[r * 2 + 0] = m_run[e];
-                pml[r * 2 + 1] = l_run[e];
-            }
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int old = atomicAdd(&a.tickets[w.first_item], 1);
-            s_last = old == w.num_splits - 1;
-        }
-        __syncthreads();
-        if (!s_last) continue;
-        __threadfence();
-        // merge: warp `warp` handles head slot `warp`, rows 0..15 of it
-        if (head_ok) {
-            for (int r = 0; r < 16; ++r) {
-                const int R = r;
-                if (R >= n_rows) break;
-                const int row = warp * 16 + r;
-                float M = -INFINITY;
-                for (int sp = 0; sp < w.num_splits; ++sp)
-                    M = fmaxf(M, __ldcg(a.partial_ml + (size_t)(w.first_item + sp) * (NH * 16 * 2) + row * 2));
-                const float Mu = M == -INFINITY ? 0.f : M;
-                float L = 0.f;
-                float acc[D / 32];
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-                for (int sp = 0; sp < w.num_splits; ++sp) {
-                    const size_t it = (size_t)(w.first_item + sp);
-                    const float m = __ldcg(a.partial_ml + it * (NH * 16 * 2) + row * 2);
-                    const float l = __ldcg(a.partial_ml + it * (NH * 16 * 2) + row * 2 + 1);
-                    const float f = fast_exp2(m - Mu);
-                    L += f * l;
-                    const float* src = a.partial_o + it * (NH * 16 * D) + (size_t)row * D;
-#pragma unroll
-                    for (int i = 0; i < D / 32; ++i) acc[i] += f * __ldcg(src + i * 32 + lane);
-                }
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                const int j = R / G, qh = my_head * G + R % G;
-                __nv_bfloat16* dst = a.out + ((size_t)(q_start + j) * a.num_q_heads + qh) * D;
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) dst[i * 32 + lane] = __float2bfloat16_rn(acc[i] * inv);
-            }
-        }
-        if (tid == 0) a.tickets[w.first_item] = 0;
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Cache write: new K/V rows -> their page slots (16-byte copies, bit exact)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
@@ -550,32 +187,6 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
-template <int D, int NH, int BK, int STAGES, bool FP8, bool DECODE>
-static cudaError_t launch_attn(const RpaArgs& a, int grid, cudaStream_t stream) {
-    using T = RpaTile<D, NH, BK, STAGES, FP8>;
-    auto kern = rpa_attn_kernel<D, NH, BK, STAGES, FP8, DECODE>;
-    static int per_sm = 0;  // resident CTAs per SM, computed once per process
-    if (per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
-        if (e != cudaSuccess) return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, T::kSmem);
-        if (e != cudaSuccess) return e;
-        per_sm = n > 0 ? n : 1;
-    }
-    ProfScope ps(DECODE ? "rpa_decode_attn" : "rpa_prefill_attn", stream);
-    kern<<<grid * (per_sm > 0 ? per_sm : 1), 128, T::kSmem, stream>>>(a);
-    return cudaGetLastError();
-}
-
-template <int D, bool FP8>
-static cudaError_t launch_rpa_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
-    constexpr int kPreBK = D >= 256 ? 32 : 64;
-    cudaError_t e = launch_attn<D, 1, kPreBK, 3, FP8, false>(a, num_sms, stream);
-    if (e != cudaSuccess) return e;
-    return launch_rpa_decode(a, num_sms, stream);
-}
-
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream) {
     cudaError_t e;
     {
@@ -584,13 +195,9 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    const bool fp8 = a.kv_fp8 != 0;
-    switch (a.head_dim) {
-        case 64: return fp8 ? launch_rpa_d<64, true>(a, num_sms, stream) : launch_rpa_d<64, false>(a, num_sms, stream);
-        case 128: return fp8 ? launch_rpa_d<128, true>(a, num_sms, stream) : launch_rpa_d<128, false>(a, num_sms, stream);
-        case 256: return fp8 ? launch_rpa_d<256, true>(a, num_sms, stream) : launch_rpa_d<256, false>(a, num_sms, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    e = launch_rpa_prefill(a, num_sms, stream);
+    if (e != cudaSuccess) return e;
+    return launch_rpa_decode(a, num_sms, stream);
 }
 
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream) {

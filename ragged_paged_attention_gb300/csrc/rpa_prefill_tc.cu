@@ -1,0 +1,607 @@
+// Prefill-class work of ragged paged attention (tpu-inference "ragged_paged_attention/v2/
+// kernel.py": sequences whose q_len * G query rows exceed one 16-row tile) on the
+// 5th-generation tensor cores of sm_103a.
+//
+// A work item is 128 query rows of one KV head (rows are (token, q head of the GQA
+// group), token-major) against its causal / windowed key range.  Per CTA:
+//   * producers gather the item's Q rows and, per key block, the K
+//     and V rows of that KV head page by page into 128-byte-swizzled K-major panels.
+//     bf16 caches go by TMA (one 3-D tensor copy per page-sized box and 64-wide panel,
+//     issued by the lanes of warp 4, pages looked up one block ahead; the partial last
+//     page is copied by that warp through registers); fp8 / scaled
+//     caches go through registers in warps 4-7 and are dequantised there as
+//     bf16(float(x) * scale).  Rows past the key range are never copied: the stage
+//     memory is zeroed at start, so such rows hold finite data with zero probability;
+//   * the last warp issues tcgen05.mma: S = Q K^T into one of two TMEM score buffers, then
+//     O += P V into the TMEM output accumulator (V read MN-major from the same panels);
+//   * warps 0-7 turn S into P, two warps per TMEM lane quarter (one thread per row, each
+//     warp of the pair half of the row's columns; the row max is exchanged through
+//     shared memory): scale, soft cap, mask (only on blocks that cross a row's causal or
+//     window limit), online softmax in the log2 domain with lazy rescaling (the running
+//     max only moves when it grows by more than 2^8, and then O is rescaled in TMEM),
+//     P written as bf16 panels; at the end they read O, divide by l, store bf16 rows.
+// Barriers: k_full/k_empty and v_full/v_empty (producers <-> MMA; separate K and V rings
+// of NS stages, so a K slot frees as soon as its QK is done), s_full/s_empty (MMA <->
+// softmax, per score buffer), p_full/p_empty (softmax <-> MMA, per P buffer), q_full,
+// o_full.  Blocks are 128 keys (64 for D = 256); producers run up to two blocks ahead.
+// Every wait is bounded (common.cuh); on a timeout the CTA records an error and stops.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "profile.h"
+
+namespace rpa {
+
+template <int D>
+struct PreTc {
+    static constexpr int BK = D >= 256 ? 64 : 128;       // keys per block
+    static constexpr int DP = D / 64;                    // 64-wide panels of the head dim
+    static constexpr int KP = BK / 64;                   // 64-wide panels of the key dim (P tile)
+    static constexpr int NS = 2;                         // stages of the K ring and of the V ring
+    static constexpr int kQ = DP * 128 * 128;            // Q tile: DP panels of [128 rows x 128 B]
+    static constexpr int kPanel = BK * 128;              // one K or V panel: [BK rows x 128 B]
+    static constexpr int kStage = DP * kPanel;           // K (or V) of one block
+    static constexpr int kP = KP * 128 * 128;            // P tile: KP panels of [128 rows x 64 keys]
+    static constexpr int kOffK = kQ;
+    static constexpr int kOffV = kOffK + NS * kStage;
+    static constexpr int kOffP = kOffV + NS * kStage;
+    static constexpr int kOffBar = kOffP + 2 * kP;
+    static constexpr int kNumBars = 4 * NS + 11;
+    static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
+    static constexpr int kOffItem = kOffRed + 2 * 2 * 128 * 4;            // WorkItem (16-byte aligned) + abort flag
+    static constexpr int kSmem = kOffItem + 48;
+    static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
+    static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle-atom alignment");
+    static constexpr int kColO = 2 * BK;                 // TMEM: S buffers at 0 and BK, O after
+    static constexpr int kTmemCols = kColO + D <= 256 ? 256 : 512;
+    static constexpr int kSoftWarps = 8;                 // two per TMEM lane quarter (column halves)
+    static constexpr int kHalf = BK / 2;                 // score columns per softmax warp
+    static_assert(kColO + D <= kTmemCols, "TMEM budget");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+// 8 source elements of a K/V row -> 16 bytes of bf16 (dequantised when needed).
+template <bool FP8, bool SCALE>
+__device__ __forceinline__ uint4 kv_chunk(const uint8_t* row, int c, float sc) {
+    if (FP8) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row + c * 8));
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = e4m3x2_to_float2(h[e]);
+            w[e] = pack_bf16(f.x * sc, f.y * sc);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    uint4 v = __ldg(reinterpret_cast<const uint4*>(row + c * 16));
+    if (SCALE) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            w[e] = pack_bf16(f.x * sc, f.y * sc);
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return v;
+}
+
+template <bool TMA>
+constexpr int prefill_warps() { return 8 + (TMA ? 1 : 4) + 1; }  // softmax, producers, MMA
+
+template <int D, bool FP8, bool SCALE, bool TMA>
+__global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
+    rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                          int box_rows, int q_tma) {
+    using T = PreTc<D>;
+    constexpr int BK = T::BK;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
+    constexpr int NS = T::NS;
+    uint64_t* k_full = bars;              // [NS]  K block landed
+    uint64_t* k_empty = bars + NS;        // [NS]  QK of that block done
+    uint64_t* v_full = bars + 2 * NS;     // [NS]  V block landed
+    uint64_t* v_empty = bars + 3 * NS;    // [NS]  PV of that block done
+    uint64_t* s_full = bars + 4 * NS;     // [2]   S buffer written by QK
+    uint64_t* s_empty = bars + 4 * NS + 2;  // [2] S buffer read by the softmax
+    uint64_t* p_full = bars + 4 * NS + 4;   // [2] P buffer written (and O rescaled)
+    uint64_t* p_empty = bars + 4 * NS + 6;  // [2] PV of that P buffer done
+    uint64_t* q_full = bars + 4 * NS + 8;
+    uint64_t* o_full = bars + 4 * NS + 9;
+    uint64_t* fin = bars + 4 * NS + 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
+    float* red = reinterpret_cast<float*>(smem + T::kOffRed);
+    constexpr int kProdW0 = 8, kProdW1 = TMA ? 9 : 12, kMmaW = kProdW1;  // producer warps [8, kProdW1), MMA warp
+    // (no static shared variables: with the 1024-byte aligned dynamic block they would
+    // round up to 1 KB and push the kernel past the 227 KB limit)
+    WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + T::kOffItem);
+    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 32);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    WsHeader* hdr = a.hdr;
+    uint32_t* err = &hdr->error_bits;
+    const int Hkv = a.num_kv_heads, G = a.num_q_heads / Hkv, C = 2 * Hkv;
+    constexpr int kEsz = FP8 ? 1 : 2;
+    const uint8_t* kvp = static_cast<const uint8_t*>(a.kv_pages);
+
+    // zero Q and the K/V stages once: rows no copy ever writes stay finite
+    for (int i = tid * 16; i < T::kOffP; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&k_full[i], TMA ? 32 : 128);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], TMA ? 32 : 128);
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 256);
+            mbar_init(&p_full[i], 256);
+            mbar_init(&p_empty[i], 1);
+        }
+        mbar_init(q_full, TMA ? 32 : 128);
+        mbar_init(o_full, 1);
+        mbar_init(fin, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaW) tmem_alloc(tmem_slot, T::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    uint32_t jb = 0;     // key blocks this CTA has processed (ring positions)
+    uint32_t items = 0;  // items this CTA has processed (q_full / o_full phases)
+    while (true) {
+        if (tid == 0) {
+            const int it = atomicAdd(&hdr->next_item[1], 1);
+            s_item.seq = -1;
+            if (it < hdr->num_items[1]) s_item = a.pre_items[it];
+        }
+        __syncthreads();
+        const WorkItem w = s_item;
+        if (w.seq < 0 || s_abort) break;
+        const int s = w.seq;
+        const int q_start = a.cu_q_lens[s];
+        const int q_len = a.cu_q_lens[s + 1] - q_start;
+        const int kv_len = a.kv_lens[s];
+        const int n_rows = q_len * G;
+        const int kvh = w.head;
+        const int R0 = w.row_begin;
+        const int R1 = min(n_rows, R0 + 128) - 1;
+        const int qmin = kv_len - q_len + R0 / G, qmax = kv_len - q_len + R1 / G;
+        int kb = a.sliding_window > 0 ? max(0, qmin - a.sliding_window + 1) : 0;
+        kb = kb / BK * BK;
+        const int ke = qmax + 1;
+        const int nb = cdiv(ke - kb, BK);
+        const uint32_t iph = items & 1;
+
+        if (warp >= kProdW0 && warp < kProdW1) {
+            // ---------------- producers ----------------
+            const int pt = tid - kProdW0 * 32;
+            if (TMA && q_tma) {
+                // the 128 rows are 128/G consecutive tokens x the G heads of this KV head
+                if (pt == 0) {
+                    mbar_arrive_expect_tx(q_full, D * 256);
+#pragma unroll
+                    for (int p = 0; p < T::DP; ++p)
+                        tma_load_3d(smem_u32(smem + p * 16384), &tm_q, 64 * p, kvh * G, q_start + R0 / G, q_full);
+                } else {
+                    mbar_arrive(q_full);
+                }
+            } else {
+                const int nprod = (kProdW1 - kProdW0) * 32;
+                for (int r = pt; r < 128; r += nprod) {
+                    const int R = R0 + r;
+                    const bool rv = R < n_rows;
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                        a.q + ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D);
+#pragma unroll 8
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint4 v = rv ? __ldg(reinterpret_cast<const uint4*>(src + c * 16)) : make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(smem + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(q_full);
+            }
+            if (TMA) {
+                if (warp == kProdW0) {
+                    // lane l owns box l (box_rows keys of one page, box_rows >= 8) of every
+                    // block; its page is looked up one block ahead.  Per block the K panels go
+                    // first (their slot frees when QK is done), then the V panels.  Full boxes
+                    // are one TMA per panel; the rows of a partial last box are copied by the
+                    // warp through registers.  Each full barrier takes TMA bytes + 32 arrivals.
+                    const int nbox = BK / box_rows;
+                    const size_t tbl = (size_t)s * a.pages_per_seq;
+                    auto page_of = [&](int j) -> int {
+                        const int key = kb + j * BK + lane * box_rows;
+                        return (lane < nbox && j < nb && key < ke) ? __ldg(a.page_indices + tbl + key / a.page_size) : -1;
+                    };
+                    int page_next = page_of(0);
+                    for (int j = 0; j < nb; ++j) {
+                        const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
+                        const int page = page_next;
+                        page_next = page_of(j + 1);
+                        const int kbx = kb + j * BK + lane * box_rows;
+                        int rows = lane < nbox ? min(box_rows, ke - kbx) : 0;
+                        if (rows < 0) rows = 0;
+                        if (rows > 0 && (unsigned)page >= (unsigned)a.total_num_pages) {
+                            set_error(err, RPA_DEV_ERR_PAGE);
+                            rows = 0;
+                        }
+                        const bool full = rows == box_rows;
+                        uint32_t bytes = full ? (uint32_t)box_rows * T::DP * 128 : 0u;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+                        const int z0 = page * a.page_size + kbx % a.page_size;
+                        const uint32_t pmask = __ballot_sync(0xffffffffu, rows > 0 && !full);
+                        bool go = true;
+#pragma unroll 1
+                        for (int part = 0; part < 2 && go; ++part) {
+                            uint64_t* fb = part ? &v_full[slot] : &k_full[slot];
+                            uint64_t* eb = part ? &v_empty[slot] : &k_empty[slot];
+                            int g = 1;
+                            if (lane == 0) {
+                                g = mbar_wait(eb, par ^ 1, err);
+                                if (g)
+                                    mbar_expect_tx(fb, bytes);
+                                else
+                                    s_abort = 1;
+                            }
+                            go = __shfl_sync(0xffffffffu, g, 0) != 0;
+                            if (!go) break;
+                            uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
+                            if (full) {
+#pragma unroll
+                                for (int p = 0; p < T::DP; ++p)
+                                    tma_load_3d(smem_u32(stage + p * T::kPanel + lane * box_rows * 128), &tm_kv, 64 * p,
+                                                2 * kvh + part, z0, fb);
+                            }
+                            uint32_t pm = pmask;
+                            while (pm) {
+                                const int src_lane = __ffs(pm) - 1;
+                                pm &= pm - 1;
+                                const int prow = __shfl_sync(0xffffffffu, rows, src_lane);
+                                const int pz0 = __shfl_sync(0xffffffffu, z0, src_lane);
+                                for (int i = lane; i < prow * (D / 8); i += 32) {
+                                    const int t = i / (D / 8), c = i % (D / 8);
+                                    const int kk = src_lane * box_rows + t;
+                                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                                        kvp + ((size_t)(pz0 + t) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
+                                    *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 +
+                                                              (((c & 7) ^ (kk & 7)) << 4)) = v;
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            mbar_arrive(fb);
+                        }
+                        if (!go) break;
+                    }
+                }
+            } else {
+                bool go = true;
+                for (int j = 0; j < nb && go; ++j) {
+                    const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
+#pragma unroll 1
+                    for (int part = 0; part < 2; ++part) {
+                        uint64_t* fb = part ? &v_full[slot] : &k_full[slot];
+                        if (!mbar_wait(part ? &v_empty[slot] : &k_empty[slot], par ^ 1, err)) {
+                            s_abort = 1;
+                            go = false;
+                            break;
+                        }
+                        uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
+                        const float sc = part ? a.v_scale_or_one : a.k_scale_or_one;
+                        for (int i = pt; i < BK * (D / 8); i += 128) {
+                            const int kk = i / (D / 8), c = i % (D / 8);
+                            const int key = kb + j * BK + kk;
+                            uint4 val = make_uint4(0, 0, 0, 0);
+                            if (key < ke) {
+                                const int page = __ldg(a.page_indices + (size_t)s * a.pages_per_seq + key / a.page_size);
+                                if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                                    set_error(err, RPA_DEV_ERR_PAGE);
+                                } else {
+                                    const uint8_t* row =
+                                        kvp + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * kvh + part) *
+                                                  (size_t)(D * kEsz);
+                                    val = kv_chunk<FP8, SCALE>(row, c, sc);
+                                }
+                            }
+                            *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
+                                val;
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(fb);
+                    }
+                }
+            }
+        } else if (warp == kMmaW) {
+            // ---------------- MMA issuer ----------------
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
+                constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, false, true);
+                const uint32_t q_base = smem_u32(smem);
+                bool ok = mbar_wait(q_full, iph, err);
+                tc_fence_after();
+                auto pv = [&](int i) -> bool {
+                    const uint32_t q = jb + i, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
+                    if (!mbar_wait(&p_full[sb], sp, err) || !mbar_wait(&v_full[slot], par, err)) return false;
+                    tc_fence_after();
+                    const uint32_t p_base = smem_u32(smem + T::kOffP + sb * T::kP);
+                    const uint32_t v_base = smem_u32(smem + T::kOffV + slot * T::kStage);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(p_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, T::kPanel, 1024);
+                        umma_bf16(tmem + T::kColO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&p_empty[sb]);
+                    umma_commit(&v_empty[slot]);
+                    return true;
+                };
+                for (int j = 0; j < nb && ok; ++j) {
+                    const uint32_t q = jb + j, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
+                    ok = mbar_wait(&k_full[slot], par, err) && mbar_wait(&s_empty[sb], sp ^ 1, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_base = smem_u32(smem + T::kOffK + slot * T::kStage);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(k_base + (ks >> 2) * T::kPanel + (ks & 3) * 32, 16, 1024);
+                        umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&s_full[sb]);
+                    umma_commit(&k_empty[slot]);
+                    if (j >= 1) ok = pv(j - 1);
+                }
+                if (ok && nb > 0) ok = pv(nb - 1);
+                umma_commit(o_full);
+                if (!ok) s_abort = 1;
+            }
+        } else if (warp < T::kSoftWarps) {
+            // ------- softmax / epilogue: row = TMEM lane, warps w and w+4 split its columns -------
+            const int quarter = warp & 3, half = warp >> 2;
+            const int r = quarter * 32 + lane;
+            const int R = R0 + r;
+            const bool rv = R < n_rows;
+            const int qpos = rv ? kv_len - q_len + R / G : -1;
+            const int wlo = a.sliding_window > 0 ? qpos - a.sliding_window + 1 : INT_MIN;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
+            constexpr int HB = T::kHalf;
+            float m_use = -INFINITY, l_half = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t q = jb + j, slot = q & 1, par = (q >> 1) & 1;  // S / P double buffers
+                if (!mbar_wait(&s_full[slot], par, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float x[HB];
+#pragma unroll
+                for (int c = 0; c < HB / 32; ++c) {
+                    float t32[32];
+                    tmem_ld32(tmem + lane_off + slot * BK + half * HB + c * 32, t32);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = t32[i];
+                }
+                tc_fence_before();
+                mbar_arrive(&s_empty[slot]);
+                const int key0 = kb + j * BK + half * HB;
+                if (cap != 0.f) {
+#pragma unroll
+                    for (int i = 0; i < HB; ++i) x[i] = cap * tanhf(x[i] * scale / cap) * kLog2e;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HB; ++i) x[i] *= c_log2;
+                }
+                // the causal / window mask only matters on blocks crossing a row's limits
+                const bool inside = key0 >= wlo && key0 + HB - 1 <= qpos;
+                if (__any_sync(0xffffffffu, !inside)) {
+#pragma unroll
+                    for (int i = 0; i < HB; ++i) {
+                        const int key = key0 + i;
+                        x[i] = (key <= qpos && key >= wlo) ? x[i] : -INFINITY;
+                    }
+                }
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < HB; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
+                float* red_j = red + (q & 1) * 256;
+                red_j[half * 128 + r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                const float mx = fmaxf(red_j[r], red_j[128 + r]);
+                float alpha = 1.f;
+                const bool had = m_use > -INFINITY;  // O already holds earlier blocks of this row
+                const bool rescale = mx > m_use + 8.f;
+                if (rescale) {
+                    alpha = fast_exp2(m_use - mx);
+                    m_use = mx;
+                }
+                const float mu = m_use == -INFINITY ? 0.f : m_use;
+                // the P buffer of this slot is free once PV two blocks back has finished
+                if (!mbar_wait(&p_empty[slot], par ^ 1, err)) {
+                    ok = false;
+                    break;
+                }
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint8_t* prow = smem + T::kOffP + slot * T::kP + r * 128;
+#pragma unroll
+                for (int cc = 0; cc < HB / 8; ++cc) {
+                    const int c = half * (HB / 8) + cc;  // 16-byte chunk of the row's BK keys
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = fast_exp2(x[cc * 8 + 2 * e] - mu), p1 = fast_exp2(x[cc * 8 + 2 * e + 1] - mu);
+                        sum4[e] += p0 + p1;
+                        w4[e] = pack_bf16(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(prow + (c >> 3) * 16384 + (((c & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                // O already holds this row's earlier blocks when l was positive before
+                const bool row_rescale = rescale && had;
+                l_half = l_half * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                // tcgen05.ld/st are warp-collective: the warp rescales together when any of its
+                // rows needs it (the others multiply by 1); each warp of the pair owns D/2 columns
+                if (__any_sync(0xffffffffu, row_rescale)) {
+                    const float f = row_rescale ? alpha : 1.f;
+                    const uint32_t qp = q - 1, sp = qp & 1, pp = (qp >> 1) & 1;
+                    if (!mbar_wait(&p_empty[sp], pp, err)) {  // PV(j-1) has finished writing O
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o32[32];
+                        const uint32_t col = T::kColO + half * (D / 2) + c * 32;
+                        tmem_ld32(tmem + lane_off + col, o32);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o32[i] *= f;
+                        tmem_st32(tmem + lane_off + col, o32);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&p_full[slot]);
+            }
+            // epilogue: l = both halves; each warp of the pair writes D/2 output columns
+            float l_run = 0.f;
+            if (ok) {
+                // the other parity's exchange buffer: both warps are past its last use
+                float* red_l = red + ((jb + nb) & 1) * 256;
+                red_l[half * 128 + r] = l_half;
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                l_run = red_l[r] + red_l[128 + r];
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+            }
+            if (ok && mbar_wait(o_full, iph, err)) {
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                __nv_bfloat16* dst = a.out +
+                                     ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D +
+                                     half * (D / 2);
+                // every lane runs the (warp-collective) TMEM loads; only real rows store
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                    float o32[32];
+                    tmem_ld32(tmem + lane_off + T::kColO + half * (D / 2) + c * 32, o32);
+                    if (rv) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o32[2 * i] * inv, o32[2 * i + 1] * inv);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+            } else {
+                s_abort = 1;
+            }
+            tc_fence_before();
+        }
+        jb += nb;
+        ++items;
+        __syncthreads();
+        tc_fence_after();
+    }
+    // drain: every MMA this CTA issued has completed before TMEM is released
+    if (warp == kMmaW) {
+        if (lane == 0) {
+            umma_commit(fin);
+            mbar_wait(fin, 0, err);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, T::kTmemCols);
+    }
+}
+
+// Tensor maps (built on the host per call: they embed the caller's pointers).
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) with a box of {64, b1, b2}, 128-byte swizzle.
+static bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
+                           uint32_t b2) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {64, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool FP8, bool SCALE, bool TMA>
+static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
+                              const CUtensorMap& tq, int box_rows, int q_tma) {
+    using T = PreTc<D>;
+    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    ProfScope ps("rpa_prefill_attn", stream);
+    kern<<<num_sms, prefill_warps<TMA>() * 32, T::kSmem, stream>>>(a, tkv, tq, box_rows, q_tma);
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    constexpr int BK = PreTc<D>::BK;
+    CUtensorMap tkv, tq;
+    memset(&tkv, 0, sizeof tkv);
+    memset(&tq, 0, sizeof tq);
+    const int ps = a.page_size, G = a.num_q_heads / a.num_kv_heads, C = 2 * a.num_kv_heads;
+    // box of one page (or of one block when pages are longer); page sizes that do not tile
+    // the block, or boxes too small for one lane each, take the register path
+    const int box_rows = ps < BK ? ps : BK;
+    // (boxes of >= 8 rows keep every TMA destination on a 1024-byte swizzle-atom boundary)
+    bool tma = !a.kv_fp8 && !a.has_scale && (ps & (ps - 1)) == 0 && box_rows >= 8 && BK / box_rows <= 32;
+    const uint64_t tokens = (uint64_t)a.total_num_pages * ps;
+    if (tma) tma = make_tmap_bf16(&tkv, a.kv_pages, D, C, tokens, 1, box_rows);
+    int q_tma = 0;
+    if (tma && 128 % G == 0)
+        q_tma = make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
+    if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma);
+    if (a.kv_fp8) return launch_pre<D, true, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0);
+    if (a.has_scale) return launch_pre<D, false, true, false>(a, num_sms, stream, tkv, tq, box_rows, 0);
+    return launch_pre<D, false, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0);
+}
+
+cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    switch (a.head_dim) {
+        case 64: return launch_pre_d<64>(a, num_sms, stream);
+        case 128: return launch_pre_d<128>(a, num_sms, stream);
+        case 256: return launch_pre_d<256>(a, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rpa
