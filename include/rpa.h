@@ -198,7 +198,7 @@ typedef struct {
     uint32_t struct_size;        /* sizeof(mla_params) */
     uint32_t version;            /* RPA_ABI_VERSION */
     int32_t max_num_tokens;
-    int32_t num_q_heads;         /* multiple of 64 */
+    int32_t num_q_heads;         /* multiple of 128 (one two-CTA tile) */
     int32_t lkv_dim;             /* 512 */
     int32_t r_dim;               /* 64 */
     int32_t lkv_dim_pad;         /* align(lkv_dim, 128) */
@@ -255,7 +255,7 @@ typedef struct {
     uint32_t version;            /* RPA_ABI_VERSION */
     int32_t batch;
     int32_t num_queries;
-    int32_t num_heads;           /* multiple of 64 */
+    int32_t num_heads;           /* multiple of 128 (one two-CTA tile) */
     int32_t dk;                  /* 576 */
     int32_t dv;                  /* 512 */
     int32_t row_stride;          /* elements per cache row (640) */

@@ -152,7 +152,7 @@ LatLayout lat_layout(long long max_items) {
     L.items = off;
     off = align_up(off + sizeof(WorkItem) * (size_t)max_items);
     L.tickets = off;
-    off = align_up(off + sizeof(int) * (size_t)max_items);
+    off = align_up(off + sizeof(int) * 2 * (size_t)max_items);  // one ticket per CTA of a pair
     L.pml = off;
     off = align_up(off + sizeof(float) * 2 * kLatRows * (size_t)max_items);
     L.po = off;

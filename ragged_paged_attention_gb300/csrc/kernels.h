@@ -70,12 +70,12 @@ struct RpaUpdateArgs {
 };
 
 // Latent (MLA and sparse MLA) attention.
-constexpr int kLatRows = 64;      // q heads per CTA
-constexpr int kLatBK = 32;        // keys per stage
+constexpr int kLatRows = 128;     // q heads per (two-CTA) tile
+constexpr int kLatBK = 64;        // keys per block
 constexpr int kLatDk = 576;       // 512 latent + 64 rope
 constexpr int kLatDv = 512;
 constexpr int kLatMinChunk = 512;
-constexpr int kLatTargetCtas = 1024;
+constexpr int kLatTargetCtas = 512;
 
 struct LatentArgs {
     int sparse;                     // 0 = MLA (paged, causal), 1 = DSA sparse
@@ -134,6 +134,8 @@ cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t 
 cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_sparse_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_mla_attention(const LatentArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_sparse_attention(const LatentArgs& a, int num_sms, cudaStream_t stream);
 
 // Sparse split count the host chooses from static sizes (no device metadata needed).
 inline int sparse_num_splits(int batch, int num_queries, int heads, int slots) {

@@ -1,0 +1,692 @@
+// MLA latent attention (tpu-inference "mla/v1/kernel.py") and DSA sparse MLA (sglang-jax
+// "dsa/sparse_mla_prefill.py") on the 5th-generation tensor cores of sm_103a.
+//
+// Both are MQA over one latent head: the 128 q heads of a query read the same key rows
+// [kv_c (512) | k_pe (64)] and the value is kv_c.  A 128-head Q slice of 576 bf16 is 144 KB
+// and the fp32 output [128 x 512] fills all of TMEM, so one query is worked by a cluster
+// of two CTAs that split the latent dimensions:
+//   rank 0: score dims 0-255 and the 64 rope dims, output dims 0-255;
+//   rank 1: score dims 256-511,                    output dims 256-511.
+// Each CTA keeps its Q slice in shared memory, gathers only its dims of each key row and
+// computes a partial score tile S_r = Q_r K_r^T (tcgen05, 128 x 64 per block).  The two
+// partials are exchanged through distributed shared memory (remote stores + cluster-scope
+// mbarriers), so both CTAs hold the same S = S_0 + S_1, run the same online softmax and
+// write the same P; each then accumulates O_r += P V_r into its own 256 TMEM columns.
+// Warps per CTA: 0-7 softmax (two per TMEM lane quarter, 32 of the 64 columns each),
+// 8-11 producers, 12 MMA issuer.  MLA keys are the causal (windowed) prefix gathered page
+// by page with 2-D TMA boxes (the partial last page through registers); sparse keys are
+// the selected units' rows, gathered through registers with their validity recorded for
+// the softmax.  Items split long key ranges; partials merge by the log-sum-exp rule.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "profile.h"
+
+namespace rpa {
+
+namespace lat {
+constexpr int BK = 64;                        // keys per block
+constexpr int NQP_MAX = 5;                    // score panels of rank 0 (4 latent + 1 rope)
+constexpr int kQ = NQP_MAX * 16384;           // Q slice: panels of [128 rows x 64 dims]
+constexpr int kPanel = BK * 128;              // one key panel: [64 rows x 64 dims]
+constexpr int kStage = NQP_MAX * kPanel;
+constexpr int NS = 2;                         // key stages
+constexpr int kP = 128 * 128;                 // P tile [128 rows x 64 keys] bf16
+constexpr int kRecv = 128 * BK * 4;           // the peer's partial scores, fp32
+constexpr int kOffKV = kQ;
+constexpr int kOffP = kOffKV + NS * kStage;
+constexpr int kOffRecv = kOffP + 2 * kP;
+constexpr int kOffBar = kOffRecv + kRecv;
+constexpr int kNumBars = 19;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;
+constexpr int kOffVld = kOffRed + 2 * 2 * 128 * 4;
+constexpr int kOffItem = kOffVld + NS * BK;
+constexpr int kSmem = kOffItem + 48;
+constexpr int kColO = 2 * BK;                 // TMEM: S at columns 0 and 64, O half at 128..383
+constexpr int kTmemCols = 512;
+constexpr int kWarps = 13;
+constexpr int kProdW0 = 8, kMmaW = 12;
+static_assert(kSmem <= 232448, "shared memory budget");
+static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0 && kOffItem % 16 == 0, "alignment");
+}  // namespace lat
+
+// Column (in elements) of latent row data that panel p of CTA `rank` holds.
+__device__ __forceinline__ int lat_panel_col(int rank, int p) { return rank == 0 ? (p < 4 ? 64 * p : 512) : 256 + 64 * p; }
+
+template <bool SPARSE>
+__global__ void __launch_bounds__(lat::kWarps * 32, 1)
+    latent_tc_kernel(LatentArgs a, const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_qb,
+                     const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_kr, int kv_tma,
+                     int box_rows) {
+    using namespace lat;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* kv_full = bars + 0;     // [2] this CTA's key panels landed
+    uint64_t* kv_empty = bars + 2;    // [2] PV of that block done
+    uint64_t* vld_full = bars + 4;    // [2] (sparse) key validity written
+    uint64_t* s_full = bars + 6;      // [2] partial S written by QK
+    uint64_t* s_empty = bars + 8;     // [2] partial S read by the softmax
+    uint64_t* p_full = bars + 10;     // [2] P written (and O rescaled)
+    uint64_t* p_empty = bars + 12;    // [2] PV done with that P buffer
+    uint64_t* q_full = bars + 14;
+    uint64_t* o_full = bars + 15;
+    uint64_t* fin = bars + 16;
+    uint64_t* recv_full = bars + 17;  // the peer has written its partial S into recv
+    uint64_t* peer_done = bars + 18;  // the peer has read my partial S out of its recv
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    uint8_t* vld = smem + kOffVld;
+    WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + kOffItem);
+    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + kOffItem + 32);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+    const int nqp = rank == 0 ? 5 : 4;
+    WsHeader* hdr = a.hdr;
+    uint32_t* err = &hdr->error_bits;
+    const int H = a.num_heads;
+    const int tiles = H / 128;
+
+    for (int i = tid * 16; i < kOffP; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], kv_tma ? 32 : 128);  // TMA: warp 8; registers: all producers
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&vld_full[i], 128);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 256);
+            mbar_init(&p_full[i], 256);
+            mbar_init(&p_empty[i], 1);
+        }
+        mbar_init(q_full, 32);
+        mbar_init(o_full, 1);
+        mbar_init(fin, 1);
+        mbar_init(recv_full, 256);
+        mbar_init(peer_done, 256);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaW) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // items are dealt round-robin to clusters: both CTAs of a cluster see the same sequence
+    int sparse_items = 0, slots = 0, sparse_chunk = 0;
+    if (SPARSE) {
+        slots = a.topk * a.read_block;
+        sparse_items = a.batch * a.num_queries * tiles * a.sparse_splits;
+        sparse_chunk = cdiv(cdiv(slots, a.sparse_splits), BK) * BK;
+    }
+    const int n_items = SPARSE ? sparse_items : hdr->num_items[2];
+    uint32_t jb = 0, items = 0;
+    for (int it = (int)cluster_id_x(); it < n_items; it += (int)cluster_count_x()) {
+        if (tid == 0) {
+            WorkItem w;
+            if (SPARSE) {
+                const int per_q = tiles * a.sparse_splits;
+                const int bs = it / per_q, rem = it % per_q;
+                const int tile = rem / a.sparse_splits, sp = rem % a.sparse_splits;
+                w.seq = bs;
+                w.head = tile * 128;
+                w.row_begin = 0;
+                w.key_begin = sp * sparse_chunk;
+                w.key_end = min(slots, (sp + 1) * sparse_chunk);
+                w.first_item = it - sp;
+                w.num_splits = a.sparse_splits;
+                w.split = sp;
+            } else {
+                w = a.items[it];
+            }
+            s_item = w;
+        }
+        __syncthreads();
+        const WorkItem w = s_item;
+        if (s_abort) break;
+        const int h0 = w.head;
+        int qpos, b = 0, seq = 0, t = 0, wlo = INT_MIN, q_start = 0;
+        if (SPARSE) {
+            b = w.seq / a.num_queries;
+            qpos = a.positions[w.seq];
+        } else {
+            seq = w.seq;
+            t = w.row_begin;
+            q_start = a.cu_q_lens[seq];
+            qpos = a.kv_lens[seq] - (a.cu_q_lens[seq + 1] - q_start) + (t - q_start);
+            if (a.sliding_window > 0) wlo = qpos - a.sliding_window + 1;
+        }
+        const int kb = w.key_begin, ke = w.key_end;
+        const int nb = ke > kb ? cdiv(ke - kb, BK) : 0;
+        const uint32_t iph = items & 1;
+        const int qrow0 = (SPARSE ? w.seq : t) * H + h0;  // first Q row of the tile
+
+        if (warp >= kProdW0 && warp < kMmaW) {
+            // ---------------- producers ----------------
+            const int pt = tid - kProdW0 * 32;
+            if (warp == kProdW0) {
+                // Q slice: one 2-D TMA per panel
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, nqp * 16384);
+                    for (int p = 0; p < nqp; ++p) {
+                        const uint32_t dst = smem_u32(smem + p * 16384);
+                        if (SPARSE)
+                            tma_load_2d(dst, &tm_qa, lat_panel_col(rank, p), qrow0, q_full);
+                        else if (rank == 0 && p == 4)
+                            tma_load_2d(dst, &tm_qb, 0, qrow0, q_full);
+                        else
+                            tma_load_2d(dst, &tm_qa, lat_panel_col(rank, p), qrow0, q_full);
+                    }
+                } else {
+                    mbar_arrive(q_full);
+                }
+            }
+            if (!SPARSE && kv_tma) {
+                if (warp == kProdW0) {
+                    const int nbox = BK / box_rows;
+                    const size_t tbl = (size_t)seq * a.pages_per_seq;
+                    auto page_of = [&](int j) -> int {
+                        const int key = kb + j * BK + lane * box_rows;
+                        return (lane < nbox && j < nb && key < ke) ? __ldg(a.page_indices + tbl + key / a.page_size) : -1;
+                    };
+                    int page_next = page_of(0);
+                    for (int j = 0; j < nb; ++j) {
+                        const uint32_t q = jb + j, st = q & 1, par = (q >> 1) & 1;
+                        const int page = page_next;
+                        page_next = page_of(j + 1);
+                        const int kbx = kb + j * BK + lane * box_rows;
+                        int rows = lane < nbox ? min(box_rows, ke - kbx) : 0;
+                        if (rows < 0) rows = 0;
+                        if (rows > 0 && (unsigned)page >= (unsigned)a.total_num_pages) {
+                            set_error(err, RPA_DEV_ERR_PAGE);
+                            rows = 0;
+                        }
+                        const bool full = rows == box_rows;
+                        uint32_t bytes = full ? (uint32_t)box_rows * nqp * 128 : 0u;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+                        int g = 1;
+                        if (lane == 0) {
+                            g = mbar_wait(&kv_empty[st], par ^ 1, err);
+                            if (g)
+                                mbar_expect_tx(&kv_full[st], bytes);
+                            else
+                                s_abort = 1;
+                        }
+                        if (!__shfl_sync(0xffffffffu, g, 0)) break;
+                        uint8_t* stage = smem + kOffKV + st * kStage;
+                        const int row0 = page * a.page_size + kbx % a.page_size;
+                        if (full) {
+                            for (int p = 0; p < nqp; ++p) {
+                                const uint32_t dst = smem_u32(stage + p * kPanel + lane * box_rows * 128);
+                                if (rank == 0 && p == 4)
+                                    tma_load_2d(dst, &tm_kr, 0, row0, &kv_full[st]);
+                                else
+                                    tma_load_2d(dst, &tm_kc, lat_panel_col(rank, p), row0, &kv_full[st]);
+                            }
+                        }
+                        uint32_t pm = __ballot_sync(0xffffffffu, rows > 0 && !full);
+                        while (pm) {
+                            const int src = __ffs(pm) - 1;
+                            pm &= pm - 1;
+                            const int prow = __shfl_sync(0xffffffffu, rows, src);
+                            const int pr0 = __shfl_sync(0xffffffffu, row0, src);
+                            for (int i = lane; i < prow * nqp * 8; i += 32) {
+                                const int r = i / (nqp * 8), rem = i % (nqp * 8), p = rem / 8, c = rem % 8;
+                                const int kk = src * box_rows + r;
+                                const __nv_bfloat16* s_row = (rank == 0 && p == 4)
+                                                                  ? a.cache_k_pe + (size_t)(pr0 + r) * a.r_pad
+                                                                  : a.cache_kv_c + (size_t)(pr0 + r) * a.lkv_pad + lat_panel_col(rank, p);
+                                const uint4 v = __ldg(reinterpret_cast<const uint4*>(s_row + c * 8));
+                                *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)) = v;
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(&kv_full[st]);
+                    }
+                }
+            } else {
+                // register gather: 128 producer threads, chunk-parallel over the block's rows
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t q = jb + j, st = q & 1, par = (q >> 1) & 1;
+                    if (!mbar_wait(&kv_empty[st], par ^ 1, err)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    uint8_t* stage = smem + kOffKV + st * kStage;
+                    for (int i = pt; i < BK * nqp * 8; i += 128) {
+                        const int kk = i / (nqp * 8), rem = i % (nqp * 8), p = rem / 8, c = rem % 8;
+                        const int key = kb + j * BK + kk;
+                        bool v = key < ke;
+                        const __nv_bfloat16* s_row = nullptr;
+                        if (v) {
+                            if (SPARSE) {
+                                const int u = __ldg(a.indices + (size_t)w.seq * a.topk + key / a.read_block);
+                                const long long kp = (long long)u * a.read_block + key % a.read_block;
+                                v = u >= 0 && kp <= qpos && kp < a.seq_len;
+                                if (v) {
+                                    const int lp = (int)(kp / a.page_size);
+                                    const int page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
+                                    if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                                        set_error(err, RPA_DEV_ERR_PAGE);
+                                        v = false;
+                                    } else {
+                                        s_row = a.cache + ((size_t)page * a.page_size + kp % a.page_size) * a.row_stride +
+                                                lat_panel_col(rank, p);
+                                    }
+                                }
+                            } else {
+                                const int page = __ldg(a.page_indices + (size_t)seq * a.pages_per_seq + key / a.page_size);
+                                if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                                    set_error(err, RPA_DEV_ERR_PAGE);
+                                    v = false;
+                                } else {
+                                    const size_t slot = (size_t)page * a.page_size + key % a.page_size;
+                                    s_row = (rank == 0 && p == 4) ? a.cache_k_pe + slot * a.r_pad
+                                                                  : a.cache_kv_c + slot * a.lkv_pad + lat_panel_col(rank, p);
+                                }
+                            }
+                        }
+                        if (SPARSE && rem == 0) vld[st * BK + kk] = v ? 1 : 0;
+                        if (v)
+                            *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)) =
+                                __ldg(reinterpret_cast<const uint4*>(s_row + c * 8));
+                    }
+                    fence_proxy_async_smem();
+                    if (SPARSE) mbar_arrive(&vld_full[st]);
+                    mbar_arrive(&kv_full[st]);
+                }
+            }
+        } else if (warp == kMmaW) {
+            // ---------------- MMA issuer ----------------
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
+                constexpr uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
+                const uint32_t q_base = smem_u32(smem);
+                bool ok = mbar_wait(q_full, iph, err);
+                tc_fence_after();
+                auto pv = [&](int i) -> bool {
+                    const uint32_t q = jb + i, sb = q & 1, sp = (q >> 1) & 1;
+                    if (!mbar_wait(&p_full[sb], sp, err)) return false;
+                    tc_fence_after();
+                    const uint32_t p_base = smem_u32(smem + kOffP + sb * kP);
+                    const uint32_t v_base = smem_u32(smem + kOffKV + sb * kStage);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(p_base + kk * 32, 16, 1024);
+                        const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, kPanel, 1024);
+                        umma_bf16(tmem + kColO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&p_empty[sb]);
+                    umma_commit(&kv_empty[sb]);
+                    return true;
+                };
+                for (int j = 0; j < nb && ok; ++j) {
+                    const uint32_t q = jb + j, sb = q & 1, sp = (q >> 1) & 1;
+                    ok = mbar_wait(&kv_full[sb], sp, err) && mbar_wait(&s_empty[sb], sp ^ 1, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t k_base = smem_u32(smem + kOffKV + sb * kStage);
+                    for (int p = 0; p < nqp; ++p)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ad = umma_desc_sw128(q_base + p * 16384 + ks * 32, 16, 1024);
+                            const uint64_t bd = umma_desc_sw128(k_base + p * kPanel + ks * 32, 16, 1024);
+                            umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, (p > 0 || ks > 0) ? 1u : 0u);
+                        }
+                    umma_commit(&s_full[sb]);
+                    if (j >= 1) ok = pv(j - 1);
+                }
+                if (ok && nb > 0) ok = pv(nb - 1);
+                umma_commit(o_full);
+                if (!ok) s_abort = 1;
+            }
+        } else {
+            // ------- softmax: row = TMEM lane, warps w and w+4 take 32 of the 64 columns each -------
+            const int quarter = warp & 3, half = warp >> 2;
+            const int r = quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
+            const uint32_t recv_self = smem_u32(smem + kOffRecv) + r * (BK * 4) + half * 128;
+            const uint32_t recv_peer = mapa_shared(recv_self, peer);
+            const uint32_t recv_full_peer = mapa_shared(smem_u32(recv_full), peer);
+            const uint32_t peer_done_peer = mapa_shared(smem_u32(peer_done), peer);
+            float m_use = -INFINITY, l_half = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t q = jb + j, sb = q & 1, sp = (q >> 1) & 1;
+                if (!mbar_wait(&s_full[sb], sp, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float x[32];
+                tmem_ld32(tmem + lane_off + sb * BK + half * 32, x);
+                tc_fence_before();
+                mbar_arrive(&s_empty[sb]);
+                // exchange partial scores with the peer CTA
+                if (!mbar_wait_cluster(peer_done, (q & 1) ^ 1, err)) {  // the peer has read my previous block
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st_cluster_v4(recv_peer + i * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                mbar_arrive_cluster(recv_full_peer);
+                if (!mbar_wait_cluster(recv_full, q & 1, err)) {
+                    ok = false;
+                    break;
+                }
+                {
+                    const float4* src = reinterpret_cast<const float4*>(smem + kOffRecv + r * (BK * 4) + half * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 v = src[i];
+                        x[4 * i] += v.x;
+                        x[4 * i + 1] += v.y;
+                        x[4 * i + 2] += v.z;
+                        x[4 * i + 3] += v.w;
+                    }
+                }
+                mbar_arrive_cluster(peer_done_peer);
+                // scale, soft cap, key validity
+                if (cap != 0.f) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = cap * tanhf(x[i] * scale / cap) * kLog2e;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] *= c_log2;
+                }
+                const int key0 = kb + j * BK + half * 32;
+                if (SPARSE) {
+                    if (!mbar_wait(&vld_full[sb], sp, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* vb = vld + sb * BK + half * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = vb[i] ? x[i] : -INFINITY;
+                } else if (!(key0 >= wlo && key0 + 31 < ke)) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int key = key0 + i;
+                        x[i] = (key < ke && key >= wlo) ? x[i] : -INFINITY;
+                    }
+                }
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
+                float* red_j = red + (q & 1) * 256;
+                red_j[half * 128 + r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                const float mx = fmaxf(red_j[r], red_j[128 + r]);
+                float alpha = 1.f;
+                const bool had = m_use > -INFINITY;
+                const bool rescale = mx > m_use + 8.f;
+                if (rescale) {
+                    alpha = fast_exp2(m_use - mx);
+                    m_use = mx;
+                }
+                const float mu = m_use == -INFINITY ? 0.f : m_use;
+                if (!mbar_wait(&p_empty[sb], sp ^ 1, err)) {
+                    ok = false;
+                    break;
+                }
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint8_t* prow = smem + kOffP + sb * kP + r * 128;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = half * 4 + cc;
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = fast_exp2(x[cc * 8 + 2 * e] - mu), p1 = fast_exp2(x[cc * 8 + 2 * e + 1] - mu);
+                        sum4[e] += p0 + p1;
+                        w4[e] = pack_bf16(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                const bool row_rescale = rescale && had;
+                l_half = l_half * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                if (__any_sync(0xffffffffu, row_rescale)) {
+                    const float f = row_rescale ? alpha : 1.f;
+                    const uint32_t qp = q - 1, spp = qp & 1, ppp = (qp >> 1) & 1;
+                    if (!mbar_wait(&p_empty[spp], ppp, err)) {  // PV of the previous block has written O
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o32[32];
+                        const uint32_t col = kColO + half * 128 + c * 32;
+                        tmem_ld32(tmem + lane_off + col, o32);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o32[i] *= f;
+                        tmem_st32(tmem + lane_off + col, o32);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&p_full[sb]);
+            }
+            // ---- this CTA's output half: 256 columns, 128 per warp of the pair ----
+            float l_run = 0.f;
+            if (ok) {
+                float* red_l = red + ((jb + nb) & 1) * 256;
+                red_l[half * 128 + r] = l_half;
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                l_run = red_l[r] + red_l[128 + r];
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+            }
+            if (ok && mbar_wait(o_full, iph, err)) {
+                tc_fence_after();
+                const bool row_ok = h0 + r < H;
+                const int col0 = (int)rank * 256 + half * 128;
+                if (w.num_splits == 1) {
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o32[32];
+                        tmem_ld32(tmem + lane_off + kColO + half * 128 + c * 32, o32);
+                        if (row_ok) {
+                            if (SPARSE) {
+                                float4* d4 = reinterpret_cast<float4*>(a.out_f32 + ((size_t)w.seq * H + h0 + r) * kLatDv + col0 + c * 32);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    d4[i] = make_float4(o32[4 * i] * inv, o32[4 * i + 1] * inv, o32[4 * i + 2] * inv,
+                                                        o32[4 * i + 3] * inv);
+                            } else {
+                                uint32_t pk[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o32[2 * i] * inv, o32[2 * i + 1] * inv);
+                                uint4* d4 = reinterpret_cast<uint4*>(a.out_bf16 + ((size_t)t * H + h0 + r) * kLatDv + col0 + c * 32);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                            }
+                        }
+                    }
+                } else {
+                    // split: unnormalised O half + (m, l) to the workspace
+                    float* po = a.partial_o + ((size_t)it * 128 + r) * kLatDv + col0;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o32[32];
+                        tmem_ld32(tmem + lane_off + kColO + half * 128 + c * 32, o32);
+                        float4* d4 = reinterpret_cast<float4*>(po + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) d4[i] = make_float4(o32[4 * i], o32[4 * i + 1], o32[4 * i + 2], o32[4 * i + 3]);
+                    }
+                    if (half == 0) {
+                        a.partial_ml[((size_t)it * 128 + r) * 2] = m_use;
+                        a.partial_ml[((size_t)it * 128 + r) * 2 + 1] = l_run;
+                    }
+                }
+            } else {
+                s_abort = 1;
+            }
+            tc_fence_before();
+        }
+        jb += nb;
+        ++items;
+        __syncthreads();
+        tc_fence_after();
+        if (w.num_splits > 1 && !s_abort) {
+            // the last CTA of this rank to finish a split group merges the group's halves
+            volatile int& s_last = *reinterpret_cast<volatile int*>(smem + kOffItem + 36);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) s_last = atomicAdd(&a.tickets[w.first_item * 2 + rank], 1) == w.num_splits - 1;
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                if (warp < 8) {
+                    const int r = (warp & 3) * 32 + lane, half = warp >> 2;
+                    const int col0 = (int)rank * 256 + half * 128;
+                    float M = -INFINITY;
+                    for (int sp = 0; sp < w.num_splits; ++sp)
+                        M = fmaxf(M, __ldcg(a.partial_ml + ((size_t)(w.first_item + sp) * 128 + r) * 2));
+                    const float Mu = M == -INFINITY ? 0.f : M;
+                    float L = 0.f;
+                    for (int sp = 0; sp < w.num_splits; ++sp) {
+                        const size_t base = ((size_t)(w.first_item + sp) * 128 + r) * 2;
+                        L += fast_exp2(__ldcg(a.partial_ml + base) - Mu) * __ldcg(a.partial_ml + base + 1);
+                    }
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    if (h0 + r < H) {
+                        for (int c4 = 0; c4 < 32; ++c4) {
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int sp = 0; sp < w.num_splits; ++sp) {
+                                const size_t base = (size_t)(w.first_item + sp) * 128 + r;
+                                const float f = fast_exp2(__ldcg(a.partial_ml + base * 2) - Mu);
+                                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.partial_o + base * kLatDv + col0 + c4 * 4));
+                                acc.x += f * v.x;
+                                acc.y += f * v.y;
+                                acc.z += f * v.z;
+                                acc.w += f * v.w;
+                            }
+                            if (SPARSE) {
+                                *reinterpret_cast<float4*>(a.out_f32 + ((size_t)w.seq * H + h0 + r) * kLatDv + col0 + c4 * 4) =
+                                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                            } else {
+                                *reinterpret_cast<uint2*>(a.out_bf16 + ((size_t)t * H + h0 + r) * kLatDv + col0 + c4 * 4) =
+                                    make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+                            }
+                        }
+                    }
+                }
+                if (tid == 0) a.tickets[w.first_item * 2 + rank] = 0;
+            }
+            __syncthreads();
+        }
+    }
+    // drain the tensor core, then make sure the peer no longer touches this CTA's memory
+    if (warp == kMmaW) {
+        if (lane == 0) {
+            umma_commit(fin);
+            mbar_wait(fin, 0, err);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    __syncthreads();
+    cluster_sync_all();
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 lat_tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 [rows][cols] with a row stride of `stride` elements; box {64, box_rows}, 128-byte swizzle.
+static bool make_tmap_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t stride,
+                         uint32_t box_rows) {
+    auto enc = lat_tmap_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {stride * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SPARSE>
+static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream_t stream) {
+    using namespace lat;
+    CUtensorMap qa, qb, kc, kr;
+    memset(&qa, 0, sizeof qa);
+    memset(&qb, 0, sizeof qb);
+    memset(&kc, 0, sizeof kc);
+    memset(&kr, 0, sizeof kr);
+    int kv_tma = 0, box_rows = 0;
+    bool ok;
+    if (SPARSE) {
+        ok = make_tmap_2d(&qa, a.q, kLatDk, (uint64_t)a.batch * a.num_queries * a.num_heads, kLatDk, 128);
+    } else {
+        ok = make_tmap_2d(&qa, a.ql_nope, 512, (uint64_t)a.max_num_tokens * a.num_heads, 512, 128) &&
+             make_tmap_2d(&qb, a.q_pe, 64, (uint64_t)a.max_num_tokens * a.num_heads, 64, 128);
+        const int ps = a.page_size;
+        box_rows = ps < BK ? ps : BK;
+        if ((ps & (ps - 1)) == 0 && box_rows >= 8) {
+            const uint64_t rows = (uint64_t)a.total_num_pages * ps;
+            kv_tma = make_tmap_2d(&kc, a.cache_kv_c, a.lkv_pad, rows, a.lkv_pad, box_rows) &&
+                     make_tmap_2d(&kr, a.cache_k_pe, a.r_pad, rows, a.r_pad, box_rows);
+        }
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    auto kern = latent_tc_kernel<SPARSE>;
+    static int max_clusters = 0;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        max_clusters = n > 0 ? n : 1;
+    }
+    cfg.gridDim = dim3(2 * max_clusters);
+    ProfScope ps(SPARSE ? "sparse_attn" : "mla_attn", stream);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, qa, qb, kc, kr, kv_tma, box_rows);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mla_attention(const LatentArgs& a, int num_sms, cudaStream_t stream) {
+    return launch_latent_tc<false>(a, num_sms, stream);
+}
+cudaError_t launch_sparse_attention(const LatentArgs& a, int num_sms, cudaStream_t stream) {
+    return launch_latent_tc<true>(a, num_sms, stream);
+}
+
+}  // namespace rpa
