@@ -251,52 +251,73 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     }
                 }
             } else {
-                // register gather: 128 producer threads, chunk-parallel over the block's rows
+                // register gather: two threads per key row, each half of the row's panels.
+                // The row of the next block is resolved (index -> token -> page) while this
+                // block's slot is still busy; then all of a thread's chunk loads are issued
+                // before any store, so one block costs one memory latency per thread.
+                const int kk = pt >> 1, hh = pt & 1;
+                const int nch = nqp * 4;  // chunks of this thread (20 or 16)
+                auto resolve = [&](int j, bool& v) -> const __nv_bfloat16* {
+                    const int key = kb + j * BK + kk;
+                    v = j < nb && key < ke;
+                    if (!v) return nullptr;
+                    if (SPARSE) {
+                        const int u = __ldg(a.indices + (size_t)w.seq * a.topk + key / a.read_block);
+                        const long long kp = (long long)u * a.read_block + key % a.read_block;
+                        v = u >= 0 && kp <= qpos && kp < a.seq_len;
+                        if (!v) return nullptr;
+                        const int lp = (int)(kp / a.page_size);
+                        const int page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
+                        if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                            set_error(err, RPA_DEV_ERR_PAGE);
+                            v = false;
+                            return nullptr;
+                        }
+                        return a.cache + ((size_t)page * a.page_size + kp % a.page_size) * a.row_stride;
+                    }
+                    const int page = __ldg(a.page_indices + (size_t)seq * a.pages_per_seq + key / a.page_size);
+                    if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                        set_error(err, RPA_DEV_ERR_PAGE);
+                        v = false;
+                        return nullptr;
+                    }
+                    return a.cache_kv_c + ((size_t)page * a.page_size + key % a.page_size) * a.lkv_pad;
+                };
+                bool v_next;
+                const __nv_bfloat16* row_next = resolve(0, v_next);
                 for (int j = 0; j < nb; ++j) {
                     const uint32_t q = jb + j, st = q & 1, par = (q >> 1) & 1;
+                    const bool v = v_next;
+                    const __nv_bfloat16* row = row_next;
+                    row_next = resolve(j + 1, v_next);
                     if (!mbar_wait(&kv_empty[st], par ^ 1, err)) {
                         s_abort = 1;
                         break;
                     }
                     uint8_t* stage = smem + kOffKV + st * kStage;
-                    for (int i = pt; i < BK * nqp * 8; i += 128) {
-                        const int kk = i / (nqp * 8), rem = i % (nqp * 8), p = rem / 8, c = rem % 8;
-                        const int key = kb + j * BK + kk;
-                        bool v = key < ke;
-                        const __nv_bfloat16* s_row = nullptr;
-                        if (v) {
-                            if (SPARSE) {
-                                const int u = __ldg(a.indices + (size_t)w.seq * a.topk + key / a.read_block);
-                                const long long kp = (long long)u * a.read_block + key % a.read_block;
-                                v = u >= 0 && kp <= qpos && kp < a.seq_len;
-                                if (v) {
-                                    const int lp = (int)(kp / a.page_size);
-                                    const int page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
-                                    if ((unsigned)page >= (unsigned)a.total_num_pages) {
-                                        set_error(err, RPA_DEV_ERR_PAGE);
-                                        v = false;
-                                    } else {
-                                        s_row = a.cache + ((size_t)page * a.page_size + kp % a.page_size) * a.row_stride +
-                                                lat_panel_col(rank, p);
-                                    }
-                                }
-                            } else {
-                                const int page = __ldg(a.page_indices + (size_t)seq * a.pages_per_seq + key / a.page_size);
-                                if ((unsigned)page >= (unsigned)a.total_num_pages) {
-                                    set_error(err, RPA_DEV_ERR_PAGE);
-                                    v = false;
-                                } else {
-                                    const size_t slot = (size_t)page * a.page_size + key % a.page_size;
-                                    s_row = (rank == 0 && p == 4) ? a.cache_k_pe + slot * a.r_pad
-                                                                  : a.cache_kv_c + slot * a.lkv_pad + lat_panel_col(rank, p);
-                                }
+                    if (v) {
+                        // MLA rope panel (rank 0, panel 4) comes from the k_pe cache row
+                        const __nv_bfloat16* pe_row =
+                            SPARSE ? nullptr : a.cache_k_pe + (size_t)((row - a.cache_kv_c) / a.lkv_pad) * a.r_pad;
+                        uint4 buf[20];
+#pragma unroll
+                        for (int i = 0; i < 20; ++i) {
+                            if (i < nch) {
+                                const int c = hh * nch + i, p = c >> 3, cc = c & 7;
+                                const __nv_bfloat16* src = (!SPARSE && rank == 0 && p == 4) ? pe_row + cc * 8
+                                                                                           : row + lat_panel_col(rank, p) + cc * 8;
+                                buf[i] = __ldg(reinterpret_cast<const uint4*>(src));
                             }
                         }
-                        if (SPARSE && rem == 0) vld[st * BK + kk] = v ? 1 : 0;
-                        if (v)
-                            *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)) =
-                                __ldg(reinterpret_cast<const uint4*>(s_row + c * 8));
+#pragma unroll
+                        for (int i = 0; i < 20; ++i) {
+                            if (i < nch) {
+                                const int c = hh * nch + i, p = c >> 3, cc = c & 7;
+                                *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((cc ^ (kk & 7)) << 4)) = buf[i];
+                            }
+                        }
                     }
+                    if (SPARSE && hh == 0) vld[st * BK + kk] = v ? 1 : 0;
                     fence_proxy_async_smem();
                     if (SPARSE) mbar_arrive(&vld_full[st]);
                     mbar_arrive(&kv_full[st]);

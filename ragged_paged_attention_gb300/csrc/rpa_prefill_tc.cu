@@ -287,9 +287,31 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     }
                 }
             } else {
+                // register path (fp8 / scaled caches): 128 / BK threads per key row, each a
+                // share of the row's chunks; the page of the next block is looked up ahead, and all of
+                // a thread's loads are issued before it converts and stores.
+                constexpr int kRowChunks = D / 8;            // 8-element chunks per K (or V) row
+                constexpr int kTpr = 128 / BK;               // producer threads per key row
+                constexpr int kPer = kRowChunks / kTpr;      // chunks per thread per block
+                static_assert(128 % BK == 0 && kRowChunks % kTpr == 0, "producer split");
+                const int kk = pt / kTpr, hh = pt % kTpr;
+                auto page_of = [&](int j) -> int {
+                    const int key = kb + j * BK + kk;
+                    return (j < nb && key < ke) ? __ldg(a.page_indices + (size_t)s * a.pages_per_seq + key / a.page_size)
+                                                : -1;
+                };
+                int page_next = page_of(0);
                 bool go = true;
                 for (int j = 0; j < nb && go; ++j) {
                     const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
+                    const int page = page_next;
+                    page_next = page_of(j + 1);
+                    const int key = kb + j * BK + kk;
+                    bool v = key < ke;
+                    if (v && (unsigned)page >= (unsigned)a.total_num_pages) {
+                        set_error(err, RPA_DEV_ERR_PAGE);
+                        v = false;
+                    }
 #pragma unroll 1
                     for (int part = 0; part < 2; ++part) {
                         uint64_t* fb = part ? &v_full[slot] : &k_full[slot];
@@ -300,23 +322,25 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                         }
                         uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
                         const float sc = part ? a.v_scale_or_one : a.k_scale_or_one;
-                        for (int i = pt; i < BK * (D / 8); i += 128) {
-                            const int kk = i / (D / 8), c = i % (D / 8);
-                            const int key = kb + j * BK + kk;
-                            uint4 val = make_uint4(0, 0, 0, 0);
-                            if (key < ke) {
-                                const int page = __ldg(a.page_indices + (size_t)s * a.pages_per_seq + key / a.page_size);
-                                if ((unsigned)page >= (unsigned)a.total_num_pages) {
-                                    set_error(err, RPA_DEV_ERR_PAGE);
-                                } else {
-                                    const uint8_t* row =
-                                        kvp + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * kvh + part) *
-                                                  (size_t)(D * kEsz);
-                                    val = kv_chunk<FP8, SCALE>(row, c, sc);
-                                }
+                        if (v) {
+                            const uint8_t* row = kvp + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * kvh + part) *
+                                                           (size_t)(D * kEsz);
+                            uint4 buf[kPer];
+#pragma unroll
+                            for (int i = 0; i < kPer; ++i) buf[i] = kv_chunk<FP8, SCALE>(row, hh * kPer + i, sc);
+#pragma unroll
+                            for (int i = 0; i < kPer; ++i) {
+                                const int c = hh * kPer + i;
+                                *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
+                                    buf[i];
                             }
-                            *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
-                                val;
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < kPer; ++i) {
+                                const int c = hh * kPer + i;
+                                *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
+                                    make_uint4(0, 0, 0, 0);
+                            }
                         }
                         fence_proxy_async_smem();
                         mbar_arrive(fb);
