@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default="llama_mixed",
+                    choices=["llama_mixed", "gemma2_fp8_sw_cap", "mla_deepseek_v3", "dsa_sparse_prefill_token",
+                             "dsa_sparse_prefill_page", "dsa_sparse_decode_token", "dsa_sparse_decode_page"],
+                    help="the headline step is llama_mixed; the others time one variant alone (profiling runs)")
     return ap.parse_args()
 
 
@@ -340,6 +344,16 @@ def main():
     api.load_library()
     peaks, peak_src = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.workload != "llama_mixed":
+        res = run_variants(dev, peaks, args, world, only=args.workload)
+        if rank == 0:
+            v = res[args.workload]
+            print(json.dumps({"metric": METRIC, "value": v["tokens_per_s"] * world, "unit": "tokens/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": v["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                              "config": {"workload": args.workload}, "detail": v}), flush=True)
+        return
 
     b = llama_batch()
     acc = rpa_accounting(b)
@@ -447,10 +461,13 @@ def main():
         print(json.dumps(line), flush=True)
 
 
-def run_variants(dev, peaks, args, world):
+def run_variants(dev, peaks, args, world, only=None):
     from ragged_paged_attention_gb300 import api, workloads
     res = {}
-    steps, warm = max(3, args.steps // 2), 3
+    steps, warm = (max(3, args.steps // 2), 3) if only is None else (args.steps, args.warmup)
+
+    def want(name):
+        return only is None or only == name
 
     def report(name, tok, byt, fl, ms, kt, extra=None):
         t_roof = roof_time(byt, fl, peaks)
@@ -463,6 +480,18 @@ def run_variants(dev, peaks, args, world):
         res[name] = r
 
     # Gemma-2-style fp8 KV, sliding window, soft cap
+    if want("gemma2_fp8_sw_cap"):
+        _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report)
+    if want("mla_deepseek_v3"):
+        _variant_mla(dev, peaks, api, workloads, steps, warm, world, report)
+    for phase in ("prefill", "decode"):
+        for mode in ("token", "page"):
+            if want(f"dsa_sparse_{phase}_{mode}"):
+                _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report)
+    return res
+
+
+def _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report):
     b = workloads.gemma_options()
     acc = rpa_accounting(b)
     g = b.to(dev)
@@ -479,7 +508,8 @@ def run_variants(dev, peaks, args, world):
     del b, g, out, ws
     torch.cuda.empty_cache()
 
-    # DeepSeek-V3 MLA with its cache update
+
+def _variant_mla(dev, peaks, api, workloads, steps, warm, world, report):
     m = workloads.mla_deepseek()
     tok, byt, fl, dec = mla_accounting(m)
     g = m.to(dev)
@@ -497,23 +527,21 @@ def run_variants(dev, peaks, args, world):
     del m, g, out, ws
     torch.cuda.empty_cache()
 
-    # DSA sparse MLA
-    for phase in ("prefill", "decode"):
-        for mode in ("token", "page"):
-            s = workloads.dsa_sparse(mode=mode, phase=phase)
-            tok, byt, fl = sparse_accounting(s)
-            g = s.to(dev)
-            prm = api.make_sparse_params(g.q, g.cache, g.indices, g.page_table, read_block=s.read_block,
-                                         page_size=s.page_size, seq_len=s.seq_len, sm_scale=s.sm_scale)
-            ws = torch.zeros(api.sparse_mla_workspace_size(prm), dtype=torch.uint8, device=dev)
-            out = torch.empty(s.q.shape[:3] + (512,), dtype=torch.float32, device=dev)
-            ms, kt = time_steps(lambda: api.sparse_mla_forward(g.q, g.cache, g.indices, g.positions, g.page_table,
-                                                               out=out, workspace=ws, **s.options()),
-                                steps if phase == "decode" else max(3, steps // 4), warm, world, timer=True)
-            report(f"dsa_sparse_{phase}_{mode}", tok, byt, fl, ms, kt)
-            del s, g, out, ws
-            torch.cuda.empty_cache()
-    return res
+
+def _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report):
+    s = workloads.dsa_sparse(mode=mode, phase=phase)
+    tok, byt, fl = sparse_accounting(s)
+    g = s.to(dev)
+    prm = api.make_sparse_params(g.q, g.cache, g.indices, g.page_table, read_block=s.read_block,
+                                 page_size=s.page_size, seq_len=s.seq_len, sm_scale=s.sm_scale)
+    ws = torch.zeros(api.sparse_mla_workspace_size(prm), dtype=torch.uint8, device=dev)
+    out = torch.empty(s.q.shape[:3] + (512,), dtype=torch.float32, device=dev)
+    ms, kt = time_steps(lambda: api.sparse_mla_forward(g.q, g.cache, g.indices, g.positions, g.page_table,
+                                                       out=out, workspace=ws, **s.options()),
+                        steps if phase == "decode" else max(3, steps // 4), warm, world, timer=True)
+    report(f"dsa_sparse_{phase}_{mode}", tok, byt, fl, ms, kt)
+    del s, g, out, ws
+    torch.cuda.empty_cache()
 
 
 if __name__ == "__main__":

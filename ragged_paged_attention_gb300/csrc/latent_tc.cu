@@ -105,8 +105,8 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         mbar_init(q_full, 32);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
-        mbar_init(recv_full, 256);
-        mbar_init(peer_done, 256);
+        mbar_init(recv_full, 8);  // one arrive per softmax warp of the peer
+        mbar_init(peer_done, 8);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -373,7 +373,9 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             const int r = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
-            const uint32_t recv_self = smem_u32(smem + kOffRecv) + r * (BK * 4) + half * 128;
+            // exchange layout [half][chunk of 4 scores][row]: a warp's 32 rows of one chunk are
+            // 512 consecutive bytes, so the remote stores and the local reads are conflict free
+            const uint32_t recv_self = smem_u32(smem + kOffRecv) + (half * 8 * 128 + r) * 16;
             const uint32_t recv_peer = mapa_shared(recv_self, peer);
             const uint32_t recv_full_peer = mapa_shared(smem_u32(recv_full), peer);
             const uint32_t peer_done_peer = mapa_shared(smem_u32(peer_done), peer);
@@ -396,24 +398,27 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     break;
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) st_cluster_v4(recv_peer + i * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-                mbar_arrive_cluster(recv_full_peer);
+                for (int i = 0; i < 8; ++i)
+                    st_cluster_v4(recv_peer + i * 128 * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+                __syncwarp();  // the lane-0 release below covers the whole warp's stores
+                if (lane == 0) mbar_arrive_cluster(recv_full_peer);
                 if (!mbar_wait_cluster(recv_full, q & 1, err)) {
                     ok = false;
                     break;
                 }
                 {
-                    const float4* src = reinterpret_cast<const float4*>(smem + kOffRecv + r * (BK * 4) + half * 128);
+                    const float4* src = reinterpret_cast<const float4*>(smem + kOffRecv) + half * 8 * 128 + r;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float4 v = src[i];
+                        const float4 v = src[i * 128];
                         x[4 * i] += v.x;
                         x[4 * i + 1] += v.y;
                         x[4 * i + 2] += v.z;
                         x[4 * i + 3] += v.w;
                     }
                 }
-                mbar_arrive_cluster(peer_done_peer);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(peer_done_peer);
                 // scale, soft cap, key validity
                 if (cap != 0.f) {
 #pragma unroll
