@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     uint64_t* q_full = bars + 14;
     uint64_t* o_full = bars + 15;
     uint64_t* fin = bars + 16;
-    uint64_t* recv_full = bars + 17;  // the peer has written its partial S into recv
+    uint64_t* recv_full = bars + 17;  // the peer's partial S has landed in recv (st.async bytes)
     uint64_t* peer_done = bars + 18;  // the peer has read my partial S out of its recv
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         mbar_init(q_full, 32);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
-        mbar_init(recv_full, 8);  // one arrive per softmax warp of the peer
+        mbar_init(recv_full, 1);  // own thread 0 arms the bytes; the peer's st.async complete them
         mbar_init(peer_done, 8);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -331,39 +331,55 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 const uint32_t q_base = smem_u32(smem);
                 bool ok = mbar_wait(q_full, iph, err);
                 tc_fence_after();
-                auto pv = [&](int i) -> bool {
-                    const uint32_t q = jb + i, sb = q & 1, sp = (q >> 1) & 1;
-                    if (!mbar_wait(&p_full[sb], sp, err)) return false;
-                    tc_fence_after();
-                    const uint32_t p_base = smem_u32(smem + kOffP + sb * kP);
-                    const uint32_t v_base = smem_u32(smem + kOffKV + sb * kStage);
+                // issue QK(next) and PV(next) in whichever order their inputs become ready
+                int nq = 0, np = 0;
+                unsigned long long t0 = 0;
+                while (ok && np < nb) {
+                    bool moved = false;
+                    if (nq < nb) {
+                        const uint32_t q = jb + nq, sb = q & 1, sp = (q >> 1) & 1;
+                        if (mbar_test(&kv_full[sb], sp) && mbar_test(&s_empty[sb], sp ^ 1)) {
+                            tc_fence_after();
+                            const uint32_t k_base = smem_u32(smem + kOffKV + sb * kStage);
+                            for (int p = 0; p < nqp; ++p)
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = umma_desc_sw128(p_base + kk * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, kPanel, 1024);
-                        umma_bf16(tmem + kColO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&p_empty[sb]);
-                    umma_commit(&kv_empty[sb]);
-                    return true;
-                };
-                for (int j = 0; j < nb && ok; ++j) {
-                    const uint32_t q = jb + j, sb = q & 1, sp = (q >> 1) & 1;
-                    ok = mbar_wait(&kv_full[sb], sp, err) && mbar_wait(&s_empty[sb], sp ^ 1, err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t k_base = smem_u32(smem + kOffKV + sb * kStage);
-                    for (int p = 0; p < nqp; ++p)
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ad = umma_desc_sw128(q_base + p * 16384 + ks * 32, 16, 1024);
-                            const uint64_t bd = umma_desc_sw128(k_base + p * kPanel + ks * 32, 16, 1024);
-                            umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, (p > 0 || ks > 0) ? 1u : 0u);
+                                for (int ks = 0; ks < 4; ++ks) {
+                                    const uint64_t ad = umma_desc_sw128(q_base + p * 16384 + ks * 32, 16, 1024);
+                                    const uint64_t bd = umma_desc_sw128(k_base + p * kPanel + ks * 32, 16, 1024);
+                                    umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, (p > 0 || ks > 0) ? 1u : 0u);
+                                }
+                            umma_commit(&s_full[sb]);
+                            ++nq;
+                            moved = true;
                         }
-                    umma_commit(&s_full[sb]);
-                    if (j >= 1) ok = pv(j - 1);
+                    }
+                    if (np < nq) {
+                        const uint32_t q = jb + np, sb = q & 1, sp = (q >> 1) & 1;
+                        if (mbar_test(&p_full[sb], sp)) {
+                            tc_fence_after();
+                            const uint32_t p_base = smem_u32(smem + kOffP + sb * kP);
+                            const uint32_t v_base = smem_u32(smem + kOffKV + sb * kStage);
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                const uint64_t ad = umma_desc_sw128(p_base + kk * 32, 16, 1024);
+                                const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, kPanel, 1024);
+                                umma_bf16(tmem + kColO, ad, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            umma_commit(&p_empty[sb]);
+                            umma_commit(&kv_empty[sb]);
+                            ++np;
+                            moved = true;
+                        }
+                    }
+                    if (moved) {
+                        t0 = 0;
+                    } else if (t0 == 0) {
+                        t0 = global_ns();
+                    } else if (global_ns() - t0 > kWaitLimitNs) {
+                        set_error(err, RPA_DEV_ERR_TIMEOUT);
+                        ok = false;
+                    }
                 }
-                if (ok && nb > 0) ok = pv(nb - 1);
                 umma_commit(o_full);
                 if (!ok) s_abort = 1;
             }
@@ -397,11 +413,12 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     ok = false;
                     break;
                 }
+                // arm this block's phase of my recv barrier (the previous phase has completed:
+                // this thread consumed it), then send my partial with st.async into the peer's
+                if (tid == 0) mbar_arrive_expect_tx(recv_full, kRecv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    st_cluster_v4(recv_peer + i * 128 * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-                __syncwarp();  // the lane-0 release below covers the whole warp's stores
-                if (lane == 0) mbar_arrive_cluster(recv_full_peer);
+                    st_async_v4(recv_peer + i * 128 * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3], recv_full_peer);
                 if (!mbar_wait_cluster(recv_full, q & 1, err)) {
                     ok = false;
                     break;

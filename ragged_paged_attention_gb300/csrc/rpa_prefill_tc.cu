@@ -63,6 +63,48 @@ struct PreTc {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
+// Raw 8-element chunk of a K/V row: 8 bytes of e4m3 or 16 bytes of bf16.
+template <bool FP8>
+struct KvRaw {
+    using type = uint4;
+    __device__ static uint4 zero() { return make_uint4(0, 0, 0, 0); }
+};
+template <>
+struct KvRaw<true> {
+    using type = uint2;
+    __device__ static uint2 zero() { return make_uint2(0, 0); }
+};
+template <bool FP8>
+__device__ __forceinline__ typename KvRaw<FP8>::type kv_load_raw(const uint8_t* row, int c) {
+    if constexpr (FP8)
+        return __ldg(reinterpret_cast<const uint2*>(row + c * 8));
+    else
+        return __ldg(reinterpret_cast<const uint4*>(row + c * 16));
+}
+// Raw chunk -> 16 bytes of bf16: e4m3 (or scaled bf16) values become bf16(float(x) * scale).
+template <bool FP8, bool SCALE>
+__device__ __forceinline__ uint4 kv_convert(typename KvRaw<FP8>::type raw, float sc) {
+    uint32_t w[4];
+    if constexpr (FP8) {
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = e4m3x2_to_float2(h[e]);
+            w[e] = pack_bf16(f.x * sc, f.y * sc);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        if (!SCALE) return raw;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            w[e] = pack_bf16(f.x * sc, f.y * sc);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // 8 source elements of a K/V row -> 16 bytes of bf16 (dequantised when needed).
 template <bool FP8, bool SCALE>
 __device__ __forceinline__ uint4 kv_chunk(const uint8_t* row, int c, float sc) {
@@ -92,7 +134,7 @@ __device__ __forceinline__ uint4 kv_chunk(const uint8_t* row, int c, float sc) {
 }
 
 template <bool TMA>
-constexpr int prefill_warps() { return 8 + (TMA ? 1 : 4) + 1; }  // softmax, producers, MMA
+constexpr int prefill_warps() { return 8 + (TMA ? 2 : 4) + 1; }  // softmax, producers (K, V), MMA
 
 template <int D, bool FP8, bool SCALE, bool TMA>
 __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
@@ -116,7 +158,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint64_t* fin = bars + 4 * NS + 10;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + T::kOffRed);
-    constexpr int kProdW0 = 8, kProdW1 = TMA ? 9 : 12, kMmaW = kProdW1;  // producer warps [8, kProdW1), MMA warp
+    // producer warps [8, kProdW1): the first half streams K, the second half V; then the MMA warp
+    constexpr int kProdW0 = 8, kProdW1 = TMA ? 10 : 12, kMmaW = kProdW1;
     // (no static shared variables: with the 1024-byte aligned dynamic block they would
     // round up to 1 KB and push the kernel past the 227 KB limit)
     WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + T::kOffItem);
@@ -134,9 +177,9 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&k_full[i], TMA ? 32 : 128);
+            mbar_init(&k_full[i], TMA ? 32 : 64);  // the warp(s) streaming K
             mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], TMA ? 32 : 128);
+            mbar_init(&v_full[i], TMA ? 32 : 64);
             mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -145,7 +188,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             mbar_init(&p_full[i], 256);
             mbar_init(&p_empty[i], 1);
         }
-        mbar_init(q_full, TMA ? 32 : 128);
+        mbar_init(q_full, (kProdW1 - kProdW0) * 32);  // every producer thread arrives
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
         s_abort = 0;
@@ -213,138 +256,132 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 mbar_arrive(q_full);
             }
             if (TMA) {
-                if (warp == kProdW0) {
-                    // lane l owns box l (box_rows keys of one page, box_rows >= 8) of every
-                    // block; its page is looked up one block ahead.  Per block the K panels go
-                    // first (their slot frees when QK is done), then the V panels.  Full boxes
-                    // are one TMA per panel; the rows of a partial last box are copied by the
-                    // warp through registers.  Each full barrier takes TMA bytes + 32 arrivals.
-                    const int nbox = BK / box_rows;
-                    const size_t tbl = (size_t)s * a.pages_per_seq;
-                    auto page_of = [&](int j) -> int {
-                        const int key = kb + j * BK + lane * box_rows;
-                        return (lane < nbox && j < nb && key < ke) ? __ldg(a.page_indices + tbl + key / a.page_size) : -1;
-                    };
-                    int page_next = page_of(0);
-                    for (int j = 0; j < nb; ++j) {
-                        const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
-                        const int page = page_next;
-                        page_next = page_of(j + 1);
-                        const int kbx = kb + j * BK + lane * box_rows;
-                        int rows = lane < nbox ? min(box_rows, ke - kbx) : 0;
-                        if (rows < 0) rows = 0;
-                        if (rows > 0 && (unsigned)page >= (unsigned)a.total_num_pages) {
-                            set_error(err, RPA_DEV_ERR_PAGE);
-                            rows = 0;
-                        }
-                        const bool full = rows == box_rows;
-                        uint32_t bytes = full ? (uint32_t)box_rows * T::DP * 128 : 0u;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-                        const int z0 = page * a.page_size + kbx % a.page_size;
-                        const uint32_t pmask = __ballot_sync(0xffffffffu, rows > 0 && !full);
-                        bool go = true;
-#pragma unroll 1
-                        for (int part = 0; part < 2 && go; ++part) {
-                            uint64_t* fb = part ? &v_full[slot] : &k_full[slot];
-                            uint64_t* eb = part ? &v_empty[slot] : &k_empty[slot];
-                            int g = 1;
-                            if (lane == 0) {
-                                g = mbar_wait(eb, par ^ 1, err);
-                                if (g)
-                                    mbar_expect_tx(fb, bytes);
-                                else
-                                    s_abort = 1;
-                            }
-                            go = __shfl_sync(0xffffffffu, g, 0) != 0;
-                            if (!go) break;
-                            uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
-                            if (full) {
-#pragma unroll
-                                for (int p = 0; p < T::DP; ++p)
-                                    tma_load_3d(smem_u32(stage + p * T::kPanel + lane * box_rows * 128), &tm_kv, 64 * p,
-                                                2 * kvh + part, z0, fb);
-                            }
-                            uint32_t pm = pmask;
-                            while (pm) {
-                                const int src_lane = __ffs(pm) - 1;
-                                pm &= pm - 1;
-                                const int prow = __shfl_sync(0xffffffffu, rows, src_lane);
-                                const int pz0 = __shfl_sync(0xffffffffu, z0, src_lane);
-                                for (int i = lane; i < prow * (D / 8); i += 32) {
-                                    const int t = i / (D / 8), c = i % (D / 8);
-                                    const int kk = src_lane * box_rows + t;
-                                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                                        kvp + ((size_t)(pz0 + t) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
-                                    *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 +
-                                                              (((c & 7) ^ (kk & 7)) << 4)) = v;
-                                }
-                            }
-                            fence_proxy_async_smem();
-                            mbar_arrive(fb);
-                        }
-                        if (!go) break;
-                    }
-                }
-            } else {
-                // register path (fp8 / scaled caches): 128 / BK threads per key row, each a
-                // share of the row's chunks; the page of the next block is looked up ahead, and all of
-                // a thread's loads are issued before it converts and stores.
-                constexpr int kRowChunks = D / 8;            // 8-element chunks per K (or V) row
-                constexpr int kTpr = 128 / BK;               // producer threads per key row
-                constexpr int kPer = kRowChunks / kTpr;      // chunks per thread per block
-                static_assert(128 % BK == 0 && kRowChunks % kTpr == 0, "producer split");
-                const int kk = pt / kTpr, hh = pt % kTpr;
+                // warp 8 streams K, warp 9 streams V.  Lane l owns box l (box_rows keys of one
+                // page, box_rows >= 8) of every block; its page is looked up one block ahead.
+                // Full boxes are one TMA per panel; the rows of a partial last box are copied
+                // by the warp through registers.  Each full barrier takes TMA bytes + 32 arrivals.
+                const int part = warp - kProdW0;
+                uint64_t* fbar = part ? v_full : k_full;
+                uint64_t* ebar = part ? v_empty : k_empty;
+                const int nbox = BK / box_rows;
+                const size_t tbl = (size_t)s * a.pages_per_seq;
                 auto page_of = [&](int j) -> int {
-                    const int key = kb + j * BK + kk;
-                    return (j < nb && key < ke) ? __ldg(a.page_indices + (size_t)s * a.pages_per_seq + key / a.page_size)
-                                                : -1;
+                    const int key = kb + j * BK + lane * box_rows;
+                    return (lane < nbox && j < nb && key < ke) ? __ldg(a.page_indices + tbl + key / a.page_size) : -1;
                 };
                 int page_next = page_of(0);
-                bool go = true;
-                for (int j = 0; j < nb && go; ++j) {
+                for (int j = 0; j < nb; ++j) {
                     const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
                     const int page = page_next;
                     page_next = page_of(j + 1);
-                    const int key = kb + j * BK + kk;
-                    bool v = key < ke;
-                    if (v && (unsigned)page >= (unsigned)a.total_num_pages) {
-                        set_error(err, RPA_DEV_ERR_PAGE);
-                        v = false;
+                    const int kbx = kb + j * BK + lane * box_rows;
+                    int rows = lane < nbox ? min(box_rows, ke - kbx) : 0;
+                    if (rows < 0) rows = 0;
+                    if (rows > 0 && (unsigned)page >= (unsigned)a.total_num_pages) {
+                        if (part == 0) set_error(err, RPA_DEV_ERR_PAGE);
+                        rows = 0;
                     }
-#pragma unroll 1
-                    for (int part = 0; part < 2; ++part) {
-                        uint64_t* fb = part ? &v_full[slot] : &k_full[slot];
-                        if (!mbar_wait(part ? &v_empty[slot] : &k_empty[slot], par ^ 1, err)) {
+                    const bool full = rows == box_rows;
+                    uint32_t bytes = full ? (uint32_t)box_rows * T::DP * 128 : 0u;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+                    const int z0 = page * a.page_size + kbx % a.page_size;
+                    const uint32_t pmask = __ballot_sync(0xffffffffu, rows > 0 && !full);
+                    int g = 1;
+                    if (lane == 0) {
+                        g = mbar_wait(&ebar[slot], par ^ 1, err);
+                        if (g)
+                            mbar_expect_tx(&fbar[slot], bytes);
+                        else
                             s_abort = 1;
-                            go = false;
-                            break;
-                        }
-                        uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
-                        const float sc = part ? a.v_scale_or_one : a.k_scale_or_one;
-                        if (v) {
-                            const uint8_t* row = kvp + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * kvh + part) *
-                                                           (size_t)(D * kEsz);
-                            uint4 buf[kPer];
-#pragma unroll
-                            for (int i = 0; i < kPer; ++i) buf[i] = kv_chunk<FP8, SCALE>(row, hh * kPer + i, sc);
-#pragma unroll
-                            for (int i = 0; i < kPer; ++i) {
-                                const int c = hh * kPer + i;
-                                *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
-                                    buf[i];
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < kPer; ++i) {
-                                const int c = hh * kPer + i;
-                                *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
-                                    make_uint4(0, 0, 0, 0);
-                            }
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(fb);
                     }
+                    if (!__shfl_sync(0xffffffffu, g, 0)) break;
+                    uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
+                    if (full) {
+#pragma unroll
+                        for (int p = 0; p < T::DP; ++p)
+                            tma_load_3d(smem_u32(stage + p * T::kPanel + lane * box_rows * 128), &tm_kv, 64 * p,
+                                        2 * kvh + part, z0, &fbar[slot]);
+                    }
+                    uint32_t pm = pmask;
+                    while (pm) {
+                        const int src_lane = __ffs(pm) - 1;
+                        pm &= pm - 1;
+                        const int prow = __shfl_sync(0xffffffffu, rows, src_lane);
+                        const int pz0 = __shfl_sync(0xffffffffu, z0, src_lane);
+                        for (int i = lane; i < prow * (D / 8); i += 32) {
+                            const int t = i / (D / 8), c = i % (D / 8);
+                            const int kk = src_lane * box_rows + t;
+                            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                                kvp + ((size_t)(pz0 + t) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
+                            *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) = v;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&fbar[slot]);
+                }
+            } else {
+                // register path (fp8 / scaled caches): warps 8-9 stream K, warps 10-11 V.  A thread
+                // owns BK / 64 key rows of every block; the next block's pages are looked up
+                // ahead, and all of a row's loads are issued before it is converted and stored.
+                constexpr int kRowChunks = D / 8;  // 8-element chunks per K (or V) row
+                constexpr int kRpt = BK / 64;      // rows per thread
+                const int part = (warp - kProdW0) >> 1;
+                const int gt = pt & 63;
+                uint64_t* fbar = part ? v_full : k_full;
+                uint64_t* ebar = part ? v_empty : k_empty;
+                const float sc = part ? a.v_scale_or_one : a.k_scale_or_one;
+                auto page_of = [&](int j, int i) -> int {
+                    const int key = kb + j * BK + gt + 64 * i;
+                    return (j < nb && key < ke) ? __ldg(a.page_indices + (size_t)s * a.pages_per_seq + key / a.page_size)
+                                                : -1;
+                };
+                int page_next[kRpt];
+#pragma unroll
+                for (int i = 0; i < kRpt; ++i) page_next[i] = page_of(0, i);
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
+                    int page[kRpt];
+#pragma unroll
+                    for (int i = 0; i < kRpt; ++i) {
+                        page[i] = page_next[i];
+                        page_next[i] = page_of(j + 1, i);
+                    }
+                    if (!mbar_wait(&ebar[slot], par ^ 1, err)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
+#pragma unroll 1
+                    for (int i = 0; i < kRpt; ++i) {
+                        const int kk = gt + 64 * i;
+                        const int key = kb + j * BK + kk;
+                        bool v = key < ke;
+                        if (v && (unsigned)page[i] >= (unsigned)a.total_num_pages) {
+                            if (part == 0) set_error(err, RPA_DEV_ERR_PAGE);
+                            v = false;
+                        }
+                        const uint8_t* row =
+                            v ? kvp + (((size_t)page[i] * a.page_size + key % a.page_size) * C + 2 * kvh + part) * (size_t)(D * kEsz)
+                              : nullptr;
+                        // loads in flight per pass: a whole row for fp8 (8-byte chunks), 16 chunks for bf16
+                        constexpr int kGroup = FP8 ? kRowChunks : (kRowChunks < 16 ? kRowChunks : 16);
+#pragma unroll 1
+                        for (int c0 = 0; c0 < kRowChunks; c0 += kGroup) {
+                            // raw loads first (all in flight), then dequantise and store
+                            typename KvRaw<FP8>::type raw[kGroup];
+#pragma unroll
+                            for (int c = 0; c < kGroup; ++c) raw[c] = v ? kv_load_raw<FP8>(row, c0 + c) : KvRaw<FP8>::zero();
+#pragma unroll
+                            for (int c = 0; c < kGroup; ++c) {
+                                const int cc = c0 + c;
+                                *reinterpret_cast<uint4*>(stage + (cc >> 3) * T::kPanel + kk * 128 + (((cc & 7) ^ (kk & 7)) << 4)) =
+                                    kv_convert<FP8, SCALE>(raw[c], sc);
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&fbar[slot]);
                 }
             }
         } else if (warp == kMmaW) {
@@ -355,39 +392,56 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 const uint32_t q_base = smem_u32(smem);
                 bool ok = mbar_wait(q_full, iph, err);
                 tc_fence_after();
-                auto pv = [&](int i) -> bool {
-                    const uint32_t q = jb + i, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
-                    if (!mbar_wait(&p_full[sb], sp, err) || !mbar_wait(&v_full[slot], par, err)) return false;
-                    tc_fence_after();
-                    const uint32_t p_base = smem_u32(smem + T::kOffP + sb * T::kP);
-                    const uint32_t v_base = smem_u32(smem + T::kOffV + slot * T::kStage);
+                // issue QK(next) and PV(next) in whichever order their inputs become ready:
+                // QK needs its K block and a free score buffer, PV its P tile and V block
+                int nq = 0, np = 0;
+                unsigned long long t0 = 0;
+                while (ok && np < nb) {
+                    bool moved = false;
+                    if (nq < nb) {
+                        const uint32_t q = jb + nq, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
+                        if (mbar_test(&k_full[slot], par) && mbar_test(&s_empty[sb], sp ^ 1)) {
+                            tc_fence_after();
+                            const uint32_t k_base = smem_u32(smem + T::kOffK + slot * T::kStage);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = umma_desc_sw128(p_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, T::kPanel, 1024);
-                        umma_bf16(tmem + T::kColO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                                const uint64_t bd = umma_desc_sw128(k_base + (ks >> 2) * T::kPanel + (ks & 3) * 32, 16, 1024);
+                                umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+                            }
+                            umma_commit(&s_full[sb]);
+                            umma_commit(&k_empty[slot]);
+                            ++nq;
+                            moved = true;
+                        }
                     }
-                    umma_commit(&p_empty[sb]);
-                    umma_commit(&v_empty[slot]);
-                    return true;
-                };
-                for (int j = 0; j < nb && ok; ++j) {
-                    const uint32_t q = jb + j, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
-                    ok = mbar_wait(&k_full[slot], par, err) && mbar_wait(&s_empty[sb], sp ^ 1, err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t k_base = smem_u32(smem + T::kOffK + slot * T::kStage);
+                    if (np < nq) {
+                        const uint32_t q = jb + np, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
+                        if (mbar_test(&p_full[sb], sp) && mbar_test(&v_full[slot], par)) {
+                            tc_fence_after();
+                            const uint32_t p_base = smem_u32(smem + T::kOffP + sb * T::kP);
+                            const uint32_t v_base = smem_u32(smem + T::kOffV + slot * T::kStage);
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(k_base + (ks >> 2) * T::kPanel + (ks & 3) * 32, 16, 1024);
-                        umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                const uint64_t ad = umma_desc_sw128(p_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                                const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, T::kPanel, 1024);
+                                umma_bf16(tmem + T::kColO, ad, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            umma_commit(&p_empty[sb]);
+                            umma_commit(&v_empty[slot]);
+                            ++np;
+                            moved = true;
+                        }
                     }
-                    umma_commit(&s_full[sb]);
-                    umma_commit(&k_empty[slot]);
-                    if (j >= 1) ok = pv(j - 1);
+                    if (moved) {
+                        t0 = 0;
+                    } else if (t0 == 0) {
+                        t0 = global_ns();
+                    } else if (global_ns() - t0 > kWaitLimitNs) {
+                        set_error(err, RPA_DEV_ERR_TIMEOUT);
+                        ok = false;
+                    }
                 }
-                if (ok && nb > 0) ok = pv(nb - 1);
                 umma_commit(o_full);
                 if (!ok) s_abort = 1;
             }
