@@ -7,8 +7,9 @@
 // of two CTAs that split the latent dimensions:
 //   rank 0: score dims 0-255 and the 64 rope dims, output dims 0-255;
 //   rank 1: score dims 256-511,                    output dims 256-511.
-// Each CTA keeps its Q slice in shared memory, gathers only its dims of each key row and
-// computes a partial score tile S_r = Q_r K_r^T (tcgen05, 128 x 64 per block).  The two
+// Each CTA keeps its Q slice in tensor memory (the MMA's A operand), gathers only its dims
+// of each key row into a 4-deep shared-memory ring and computes a partial score tile
+// S_r = Q_r K_r^T (tcgen05, 128 x 64 per block).  The two
 // partials are exchanged through distributed shared memory (remote stores + cluster-scope
 // mbarriers), so both CTAs hold the same S = S_0 + S_1, run the same online softmax and
 // write the same P; each then accumulates O_r += P V_r into its own 256 TMEM columns.
@@ -29,23 +30,24 @@ namespace rpa {
 namespace lat {
 constexpr int BK = 64;                        // keys per block
 constexpr int NQP_MAX = 5;                    // score panels of rank 0 (4 latent + 1 rope)
-constexpr int kQ = NQP_MAX * 16384;           // Q slice: panels of [128 rows x 64 dims]
 constexpr int kPanel = BK * 128;              // one key panel: [64 rows x 64 dims]
 constexpr int kStage = NQP_MAX * kPanel;
-constexpr int NS = 2;                         // key stages
+constexpr int NS = 4;                         // key stages
 constexpr int kP = 128 * 128;                 // P tile [128 rows x 64 keys] bf16
 constexpr int kRecv = 128 * BK * 4;           // the peer's partial scores, fp32
-constexpr int kOffKV = kQ;
+constexpr int kOffKV = 0;
 constexpr int kOffP = kOffKV + NS * kStage;
 constexpr int kOffRecv = kOffP + 2 * kP;
 constexpr int kOffBar = kOffRecv + kRecv;
-constexpr int kNumBars = 19;
+constexpr int kNumBars = 3 * NS + 11;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;
 constexpr int kOffVld = kOffRed + 2 * 2 * 128 * 4;
 constexpr int kOffItem = kOffVld + NS * BK;
 constexpr int kSmem = kOffItem + 48;
-constexpr int kColO = 2 * BK;                 // TMEM: S at columns 0 and 64, O half at 128..383
+// TMEM columns: S [128 x 64] fp32 at 0, the Q slice (bf16 pairs, 160 or 128 columns) at 64,
+// the O half [128 x 256] fp32 at 256.
+constexpr int kColS = 0, kColQ = BK, kColO = 256;
 constexpr int kTmemCols = 512;
 constexpr int kWarps = 13;
 constexpr int kProdW0 = 8, kMmaW = 12;
@@ -58,24 +60,23 @@ __device__ __forceinline__ int lat_panel_col(int rank, int p) { return rank == 0
 
 template <bool SPARSE>
 __global__ void __launch_bounds__(lat::kWarps * 32, 1)
-    latent_tc_kernel(LatentArgs a, const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_qb,
-                     const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_kr, int kv_tma,
-                     int box_rows) {
+    latent_tc_kernel(LatentArgs a, const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_kr,
+                     int kv_tma, int box_rows) {
     using namespace lat;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* kv_full = bars + 0;     // [2] this CTA's key panels landed
-    uint64_t* kv_empty = bars + 2;    // [2] PV of that block done
-    uint64_t* vld_full = bars + 4;    // [2] (sparse) key validity written
-    uint64_t* s_full = bars + 6;      // [2] partial S written by QK
-    uint64_t* s_empty = bars + 8;     // [2] partial S read by the softmax
-    uint64_t* p_full = bars + 10;     // [2] P written (and O rescaled)
-    uint64_t* p_empty = bars + 12;    // [2] PV done with that P buffer
-    uint64_t* q_full = bars + 14;
-    uint64_t* o_full = bars + 15;
-    uint64_t* fin = bars + 16;
-    uint64_t* recv_full = bars + 17;  // the peer's partial S has landed in recv (st.async bytes)
-    uint64_t* peer_done = bars + 18;  // the peer has read my partial S out of its recv
+    uint64_t* kv_full = bars + 0;           // [NS] this CTA's key panels landed
+    uint64_t* kv_empty = bars + NS;         // [NS] PV of that block done
+    uint64_t* vld_full = bars + 2 * NS;     // [NS] (sparse) key validity written
+    uint64_t* s_full = bars + 3 * NS;       // partial S written by QK
+    uint64_t* s_empty = bars + 3 * NS + 1;  // partial S read by the softmax
+    uint64_t* p_full = bars + 3 * NS + 2;   // [2] P written (and O rescaled)
+    uint64_t* p_empty = bars + 3 * NS + 4;  // [2] PV done with that P buffer
+    uint64_t* q_full = bars + 3 * NS + 6;   // the Q slice is in TMEM
+    uint64_t* o_full = bars + 3 * NS + 7;
+    uint64_t* fin = bars + 3 * NS + 8;
+    uint64_t* recv_full = bars + 3 * NS + 9;   // the peer's partial S has landed in recv (st.async bytes)
+    uint64_t* peer_done = bars + 3 * NS + 10;  // the peer has read my partial S out of its recv
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     uint8_t* vld = smem + kOffVld;
@@ -93,16 +94,18 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     for (int i = tid * 16; i < kOffP; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&kv_full[i], kv_tma ? 32 : 128);  // TMA: warp 8; registers: all producers
             mbar_init(&kv_empty[i], 1);
             mbar_init(&vld_full[i], 128);
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 256);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&p_full[i], 256);
             mbar_init(&p_empty[i], 1);
         }
-        mbar_init(q_full, 32);
+        mbar_init(s_full, 1);
+        mbar_init(s_empty, 256);
+        mbar_init(q_full, 256);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
         mbar_init(recv_full, 1);  // own thread 0 arms the bytes; the peer's st.async complete them
@@ -169,23 +172,6 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         if (warp >= kProdW0 && warp < kMmaW) {
             // ---------------- producers ----------------
             const int pt = tid - kProdW0 * 32;
-            if (warp == kProdW0) {
-                // Q slice: one 2-D TMA per panel
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(q_full, nqp * 16384);
-                    for (int p = 0; p < nqp; ++p) {
-                        const uint32_t dst = smem_u32(smem + p * 16384);
-                        if (SPARSE)
-                            tma_load_2d(dst, &tm_qa, lat_panel_col(rank, p), qrow0, q_full);
-                        else if (rank == 0 && p == 4)
-                            tma_load_2d(dst, &tm_qb, 0, qrow0, q_full);
-                        else
-                            tma_load_2d(dst, &tm_qa, lat_panel_col(rank, p), qrow0, q_full);
-                    }
-                } else {
-                    mbar_arrive(q_full);
-                }
-            }
             if (!SPARSE && kv_tma) {
                 if (warp == kProdW0) {
                     const int nbox = BK / box_rows;
@@ -196,7 +182,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     };
                     int page_next = page_of(0);
                     for (int j = 0; j < nb; ++j) {
-                        const uint32_t q = jb + j, st = q & 1, par = (q >> 1) & 1;
+                        const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1;
                         const int page = page_next;
                         page_next = page_of(j + 1);
                         const int kbx = kb + j * BK + lane * box_rows;
@@ -286,7 +272,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 bool v_next;
                 const __nv_bfloat16* row_next = resolve(0, v_next);
                 for (int j = 0; j < nb; ++j) {
-                    const uint32_t q = jb + j, st = q & 1, par = (q >> 1) & 1;
+                    const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1;
                     const bool v = v_next;
                     const __nv_bfloat16* row = row_next;
                     row_next = resolve(j + 1, v_next);
@@ -328,7 +314,6 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             if (lane == 0) {
                 constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
                 constexpr uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
-                const uint32_t q_base = smem_u32(smem);
                 bool ok = mbar_wait(q_full, iph, err);
                 tc_fence_after();
                 // issue QK(next) and PV(next) in whichever order their inputs become ready
@@ -337,36 +322,37 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 while (ok && np < nb) {
                     bool moved = false;
                     if (nq < nb) {
-                        const uint32_t q = jb + nq, sb = q & 1, sp = (q >> 1) & 1;
-                        if (mbar_test(&kv_full[sb], sp) && mbar_test(&s_empty[sb], sp ^ 1)) {
+                        // S is single-buffered: QK(q) needs the softmax to have read S(q-1)
+                        const uint32_t q = jb + nq, st = q % NS, par = (q / NS) & 1;
+                        if (mbar_test(&kv_full[st], par) && mbar_test(s_empty, (q & 1) ^ 1)) {
                             tc_fence_after();
-                            const uint32_t k_base = smem_u32(smem + kOffKV + sb * kStage);
+                            const uint32_t k_base = smem_u32(smem + kOffKV + st * kStage);
                             for (int p = 0; p < nqp; ++p)
 #pragma unroll
                                 for (int ks = 0; ks < 4; ++ks) {
-                                    const uint64_t ad = umma_desc_sw128(q_base + p * 16384 + ks * 32, 16, 1024);
                                     const uint64_t bd = umma_desc_sw128(k_base + p * kPanel + ks * 32, 16, 1024);
-                                    umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, (p > 0 || ks > 0) ? 1u : 0u);
+                                    umma_bf16_ta(tmem + kColS, tmem + kColQ + p * 32 + ks * 8, bd, idesc_qk,
+                                                 (p > 0 || ks > 0) ? 1u : 0u);
                                 }
-                            umma_commit(&s_full[sb]);
+                            umma_commit(s_full);
                             ++nq;
                             moved = true;
                         }
                     }
                     if (np < nq) {
-                        const uint32_t q = jb + np, sb = q & 1, sp = (q >> 1) & 1;
-                        if (mbar_test(&p_full[sb], sp)) {
+                        const uint32_t q = jb + np, pb = q & 1, pp = (q >> 1) & 1, st = q % NS;
+                        if (mbar_test(&p_full[pb], pp)) {
                             tc_fence_after();
-                            const uint32_t p_base = smem_u32(smem + kOffP + sb * kP);
-                            const uint32_t v_base = smem_u32(smem + kOffKV + sb * kStage);
+                            const uint32_t p_base = smem_u32(smem + kOffP + pb * kP);
+                            const uint32_t v_base = smem_u32(smem + kOffKV + st * kStage);
 #pragma unroll
                             for (int kk = 0; kk < BK / 16; ++kk) {
                                 const uint64_t ad = umma_desc_sw128(p_base + kk * 32, 16, 1024);
                                 const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, kPanel, 1024);
                                 umma_bf16(tmem + kColO, ad, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
                             }
-                            umma_commit(&p_empty[sb]);
-                            umma_commit(&kv_empty[sb]);
+                            umma_commit(&p_empty[pb]);
+                            umma_commit(&kv_empty[st]);
                             ++np;
                             moved = true;
                         }
@@ -395,19 +381,49 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             const uint32_t recv_peer = mapa_shared(recv_self, peer);
             const uint32_t recv_full_peer = mapa_shared(smem_u32(recv_full), peer);
             const uint32_t peer_done_peer = mapa_shared(smem_u32(peer_done), peer);
+            {
+                // Q slice -> TMEM: this thread's row, half of its 16-byte chunks (8 dims = 4
+                // columns each).  The previous item's MMAs have all completed (o_full).
+                const int nch = nqp * 4, c0 = half * nch;
+                const size_t qrow = (size_t)qrow0 + r;
+                uint4 buf[20];
+#pragma unroll
+                for (int i = 0; i < 20; ++i) {
+                    if (i < nch) {
+                        const int c = c0 + i, p = c >> 3, cc = c & 7;
+                        const __nv_bfloat16* src = SPARSE ? a.q + qrow * kLatDk + lat_panel_col(rank, p) + cc * 8
+                                                   : (rank == 0 && p == 4) ? a.q_pe + qrow * 64 + cc * 8
+                                                                           : a.ql_nope + qrow * kLatDv + lat_panel_col(rank, p) + cc * 8;
+                        buf[i] = __ldg(reinterpret_cast<const uint4*>(src));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 20; i += 4) {
+                    if (i < nch) {
+                        const uint32_t v[16] = {buf[i].x,     buf[i].y,     buf[i].z,     buf[i].w,
+                                                buf[i + 1].x, buf[i + 1].y, buf[i + 1].z, buf[i + 1].w,
+                                                buf[i + 2].x, buf[i + 2].y, buf[i + 2].z, buf[i + 2].w,
+                                                buf[i + 3].x, buf[i + 3].y, buf[i + 3].z, buf[i + 3].w};
+                        tmem_st16_nowait(tmem + lane_off + kColQ + (c0 + i) * 4, v);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(q_full);
+            }
             float m_use = -INFINITY, l_half = 0.f;
             bool ok = true;
             for (int j = 0; j < nb; ++j) {
-                const uint32_t q = jb + j, sb = q & 1, sp = (q >> 1) & 1;
-                if (!mbar_wait(&s_full[sb], sp, err)) {
+                const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1, pb = q & 1, pp = (q >> 1) & 1;
+                if (!mbar_wait(s_full, q & 1, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float x[32];
-                tmem_ld32(tmem + lane_off + sb * BK + half * 32, x);
+                tmem_ld32(tmem + lane_off + kColS + half * 32, x);
                 tc_fence_before();
-                mbar_arrive(&s_empty[sb]);
+                mbar_arrive(s_empty);
                 // exchange partial scores with the peer CTA
                 if (!mbar_wait_cluster(peer_done, (q & 1) ^ 1, err)) {  // the peer has read my previous block
                     ok = false;
@@ -446,11 +462,11 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 }
                 const int key0 = kb + j * BK + half * 32;
                 if (SPARSE) {
-                    if (!mbar_wait(&vld_full[sb], sp, err)) {
+                    if (!mbar_wait(&vld_full[st], par, err)) {
                         ok = false;
                         break;
                     }
-                    const uint8_t* vb = vld + sb * BK + half * 32;
+                    const uint8_t* vb = vld + st * BK + half * 32;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) x[i] = vb[i] ? x[i] : -INFINITY;
                 } else if (!(key0 >= wlo && key0 + 31 < ke)) {
@@ -475,12 +491,12 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     m_use = mx;
                 }
                 const float mu = m_use == -INFINITY ? 0.f : m_use;
-                if (!mbar_wait(&p_empty[sb], sp ^ 1, err)) {
+                if (!mbar_wait(&p_empty[pb], pp ^ 1, err)) {
                     ok = false;
                     break;
                 }
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint8_t* prow = smem + kOffP + sb * kP + r * 128;
+                uint8_t* prow = smem + kOffP + pb * kP + r * 128;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int c = half * 4 + cc;
@@ -515,7 +531,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&p_full[sb]);
+                mbar_arrive(&p_full[pb]);
             }
             // ---- this CTA's output half: 256 columns, 128 per warp of the pair ----
             float l_run = 0.f;
@@ -674,18 +690,11 @@ static bool make_tmap_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint6
 template <bool SPARSE>
 static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream_t stream) {
     using namespace lat;
-    CUtensorMap qa, qb, kc, kr;
-    memset(&qa, 0, sizeof qa);
-    memset(&qb, 0, sizeof qb);
+    CUtensorMap kc, kr;
     memset(&kc, 0, sizeof kc);
     memset(&kr, 0, sizeof kr);
-    int kv_tma = 0, box_rows = 0;
-    bool ok;
-    if (SPARSE) {
-        ok = make_tmap_2d(&qa, a.q, kLatDk, (uint64_t)a.batch * a.num_queries * a.num_heads, kLatDk, 128);
-    } else {
-        ok = make_tmap_2d(&qa, a.ql_nope, 512, (uint64_t)a.max_num_tokens * a.num_heads, 512, 128) &&
-             make_tmap_2d(&qb, a.q_pe, 64, (uint64_t)a.max_num_tokens * a.num_heads, 64, 128);
+    int kv_tma = 0, box_rows = 0;  // without usable key maps the register gather runs
+    if (!SPARSE) {
         const int ps = a.page_size;
         box_rows = ps < BK ? ps : BK;
         if ((ps & (ps - 1)) == 0 && box_rows >= 8) {
@@ -694,7 +703,6 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
                      make_tmap_2d(&kr, a.cache_k_pe, a.r_pad, rows, a.r_pad, box_rows);
         }
     }
-    if (!ok) return cudaErrorInvalidValue;
     auto kern = latent_tc_kernel<SPARSE>;
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg;
@@ -720,7 +728,7 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
     }
     cfg.gridDim = dim3(2 * max_clusters);
     ProfScope ps(SPARSE ? "sparse_attn" : "mla_attn", stream);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, qa, qb, kc, kr, kv_tma, box_rows);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, kc, kr, kv_tma, box_rows);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
