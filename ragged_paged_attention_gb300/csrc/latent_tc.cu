@@ -10,9 +10,13 @@
 // Each CTA keeps its Q slice in tensor memory (the MMA's A operand), gathers only its dims
 // of each key row into a 4-deep shared-memory ring and computes a partial score tile
 // S_r = Q_r K_r^T (tcgen05, 128 x 64 per block).  The two
-// partials are exchanged through distributed shared memory (remote stores + cluster-scope
-// mbarriers), so both CTAs hold the same S = S_0 + S_1, run the same online softmax and
-// write the same P; each then accumulates O_r += P V_r into its own 256 TMEM columns.
+// partials are exchanged through distributed shared memory (st.async into a double-buffered
+// receive area, completing on the receiver's mbarrier), so both CTAs hold the same
+// S = S_0 + S_1, run the same online softmax and write the same P (into TMEM, the A operand
+// of PV); each then accumulates O_r += P V_r into its own 256 TMEM columns.  A receive
+// buffer is reused two blocks later: the peer writes it again only after it has received
+// this CTA's next partial, which is sent after the reads and whose completion is a
+// cluster-scope release, so no separate "buffer free" signal is needed.
 // Warps per CTA: 0-7 softmax (two per TMEM lane quarter, 32 of the 64 columns each),
 // 8-11 producers, 12 MMA issuer.  MLA keys are the causal (windowed) prefix gathered page
 // by page with 2-D TMA boxes (the partial last page through registers); sparse keys are
@@ -33,26 +37,25 @@ constexpr int NQP_MAX = 5;                    // score panels of rank 0 (4 laten
 constexpr int kPanel = BK * 128;              // one key panel: [64 rows x 64 dims]
 constexpr int kStage = NQP_MAX * kPanel;
 constexpr int NS = 4;                         // key stages
-constexpr int kP = 128 * 128;                 // P tile [128 rows x 64 keys] bf16
 constexpr int kRecv = 128 * BK * 4;           // the peer's partial scores, fp32
 constexpr int kOffKV = 0;
-constexpr int kOffP = kOffKV + NS * kStage;
-constexpr int kOffRecv = kOffP + 2 * kP;
-constexpr int kOffBar = kOffRecv + kRecv;
-constexpr int kNumBars = 3 * NS + 11;
+constexpr int kOffRecv = kOffKV + NS * kStage;  // [2] receive buffers
+constexpr int kOffBar = kOffRecv + 2 * kRecv;
+constexpr int kNumBars = 3 * NS + 9;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;
 constexpr int kOffVld = kOffRed + 2 * 2 * 128 * 4;
 constexpr int kOffItem = kOffVld + NS * BK;
 constexpr int kSmem = kOffItem + 48;
 // TMEM columns: S [128 x 64] fp32 at 0, the Q slice (bf16 pairs, 160 or 128 columns) at 64,
-// the O half [128 x 256] fp32 at 256.
-constexpr int kColS = 0, kColQ = BK, kColO = 256;
+// P [128 x 64] bf16 pairs at 224, the O half [128 x 256] fp32 at 256.
+constexpr int kColS = 0, kColQ = BK, kColP = 224, kColO = 256;
 constexpr int kTmemCols = 512;
 constexpr int kWarps = 13;
 constexpr int kProdW0 = 8, kMmaW = 12;
 static_assert(kSmem <= 232448, "shared memory budget");
-static_assert(kOffKV % 1024 == 0 && kOffP % 1024 == 0 && kOffItem % 16 == 0, "alignment");
+static_assert(kOffKV % 1024 == 0 && kOffRecv % 16 == 0 && kOffItem % 16 == 0, "alignment");
+static_assert(kColQ + NQP_MAX * 32 <= kColP && kColP + BK / 2 <= kColO, "TMEM columns");
 }  // namespace lat
 
 // Column (in elements) of latent row data that panel p of CTA `rank` holds.
@@ -70,13 +73,12 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     uint64_t* vld_full = bars + 2 * NS;     // [NS] (sparse) key validity written
     uint64_t* s_full = bars + 3 * NS;       // partial S written by QK
     uint64_t* s_empty = bars + 3 * NS + 1;  // partial S read by the softmax
-    uint64_t* p_full = bars + 3 * NS + 2;   // [2] P written (and O rescaled)
-    uint64_t* p_empty = bars + 3 * NS + 4;  // [2] PV done with that P buffer
-    uint64_t* q_full = bars + 3 * NS + 6;   // the Q slice is in TMEM
-    uint64_t* o_full = bars + 3 * NS + 7;
-    uint64_t* fin = bars + 3 * NS + 8;
-    uint64_t* recv_full = bars + 3 * NS + 9;   // the peer's partial S has landed in recv (st.async bytes)
-    uint64_t* peer_done = bars + 3 * NS + 10;  // the peer has read my partial S out of its recv
+    uint64_t* p_full = bars + 3 * NS + 2;     // P written to TMEM (and O rescaled)
+    uint64_t* p_empty = bars + 3 * NS + 3;    // PV done with P
+    uint64_t* q_full = bars + 3 * NS + 4;     // the Q slice is in TMEM
+    uint64_t* o_full = bars + 3 * NS + 5;
+    uint64_t* fin = bars + 3 * NS + 6;
+    uint64_t* recv_full = bars + 3 * NS + 7;  // [2] the peer's partial S has landed (st.async bytes)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     uint8_t* vld = smem + kOffVld;
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     const int H = a.num_heads;
     const int tiles = H / 128;
 
-    for (int i = tid * 16; i < kOffP; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
+    for (int i = tid * 16; i < kOffRecv; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -99,17 +101,14 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             mbar_init(&kv_empty[i], 1);
             mbar_init(&vld_full[i], 128);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&p_full[i], 256);
-            mbar_init(&p_empty[i], 1);
-        }
+        mbar_init(p_full, 256);
+        mbar_init(p_empty, 1);
         mbar_init(s_full, 1);
         mbar_init(s_empty, 256);
         mbar_init(q_full, 256);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
-        mbar_init(recv_full, 1);  // own thread 0 arms the bytes; the peer's st.async complete them
-        mbar_init(peer_done, 8);
+        for (int i = 0; i < 2; ++i) mbar_init(&recv_full[i], 1);  // own thread 0 arms the bytes; the peer's st.async complete them
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -340,18 +339,16 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         }
                     }
                     if (np < nq) {
-                        const uint32_t q = jb + np, pb = q & 1, pp = (q >> 1) & 1, st = q % NS;
-                        if (mbar_test(&p_full[pb], pp)) {
+                        const uint32_t q = jb + np, st = q % NS;
+                        if (mbar_test(p_full, q & 1)) {
                             tc_fence_after();
-                            const uint32_t p_base = smem_u32(smem + kOffP + pb * kP);
                             const uint32_t v_base = smem_u32(smem + kOffKV + st * kStage);
 #pragma unroll
                             for (int kk = 0; kk < BK / 16; ++kk) {
-                                const uint64_t ad = umma_desc_sw128(p_base + kk * 32, 16, 1024);
                                 const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, kPanel, 1024);
-                                umma_bf16(tmem + kColO, ad, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                                umma_bf16_ta(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
                             }
-                            umma_commit(&p_empty[pb]);
+                            umma_commit(p_empty);
                             umma_commit(&kv_empty[st]);
                             ++np;
                             moved = true;
@@ -380,7 +377,6 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             const uint32_t recv_self = smem_u32(smem + kOffRecv) + (half * 8 * 128 + r) * 16;
             const uint32_t recv_peer = mapa_shared(recv_self, peer);
             const uint32_t recv_full_peer = mapa_shared(smem_u32(recv_full), peer);
-            const uint32_t peer_done_peer = mapa_shared(smem_u32(peer_done), peer);
             {
                 // Q slice -> TMEM: this thread's row, half of its 16-byte chunks (8 dims = 4
                 // columns each).  The previous item's MMAs have all completed (o_full).
@@ -414,7 +410,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             float m_use = -INFINITY, l_half = 0.f;
             bool ok = true;
             for (int j = 0; j < nb; ++j) {
-                const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1, pb = q & 1, pp = (q >> 1) & 1;
+                const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1, rb = q & 1, rp = (q >> 1) & 1;
                 if (!mbar_wait(s_full, q & 1, err)) {
                     ok = false;
                     break;
@@ -424,23 +420,20 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 tmem_ld32(tmem + lane_off + kColS + half * 32, x);
                 tc_fence_before();
                 mbar_arrive(s_empty);
-                // exchange partial scores with the peer CTA
-                if (!mbar_wait_cluster(peer_done, (q & 1) ^ 1, err)) {  // the peer has read my previous block
-                    ok = false;
-                    break;
-                }
-                // arm this block's phase of my recv barrier (the previous phase has completed:
-                // this thread consumed it), then send my partial with st.async into the peer's
-                if (tid == 0) mbar_arrive_expect_tx(recv_full, kRecv);
+                // exchange partial scores with the peer CTA: arm this block's receive barrier
+                // (its previous phase, two blocks ago, was consumed by this thread), then send
+                // my partial into the peer's buffer rb
+                if (tid == 0) mbar_arrive_expect_tx(&recv_full[rb], kRecv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    st_async_v4(recv_peer + i * 128 * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3], recv_full_peer);
-                if (!mbar_wait_cluster(recv_full, q & 1, err)) {
+                    st_async_v4(recv_peer + rb * kRecv + i * 128 * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3],
+                                recv_full_peer + rb * 8);
+                if (!mbar_wait_cluster(&recv_full[rb], rp, err)) {
                     ok = false;
                     break;
                 }
                 {
-                    const float4* src = reinterpret_cast<const float4*>(smem + kOffRecv) + half * 8 * 128 + r;
+                    const float4* src = reinterpret_cast<const float4*>(smem + kOffRecv + rb * kRecv) + half * 8 * 128 + r;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float4 v = src[i * 128];
@@ -450,8 +443,6 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         x[4 * i + 3] += v.w;
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(peer_done_peer);
                 // scale, soft cap, key validity
                 if (cap != 0.f) {
 #pragma unroll
@@ -491,34 +482,24 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     m_use = mx;
                 }
                 const float mu = m_use == -INFINITY ? 0.f : m_use;
-                if (!mbar_wait(&p_empty[pb], pp ^ 1, err)) {
-                    ok = false;
-                    break;
-                }
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint8_t* prow = smem + kOffP + pb * kP + r * 128;
+                uint32_t pk[16];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = half * 4 + cc;
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = fast_exp2(x[cc * 8 + 2 * e] - mu), p1 = fast_exp2(x[cc * 8 + 2 * e + 1] - mu);
-                        sum4[e] += p0 + p1;
-                        w4[e] = pack_bf16(p0, p1);
-                    }
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = fast_exp2(x[2 * e] - mu), p1 = fast_exp2(x[2 * e + 1] - mu);
+                    sum4[e & 3] += p0 + p1;
+                    pk[e] = pack_bf16(p0, p1);
                 }
                 const bool row_rescale = rescale && had;
                 l_half = l_half * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                // PV of the previous block is done with P and has written O
+                if (!mbar_wait(p_empty, (q & 1) ^ 1, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 if (__any_sync(0xffffffffu, row_rescale)) {
                     const float f = row_rescale ? alpha : 1.f;
-                    const uint32_t qp = q - 1, spp = qp & 1, ppp = (qp >> 1) & 1;
-                    if (!mbar_wait(&p_empty[spp], ppp, err)) {  // PV of the previous block has written O
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         float o32[32];
@@ -529,9 +510,10 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         tmem_st32(tmem + lane_off + col, o32);
                     }
                 }
-                fence_proxy_async_smem();
+                tmem_st16_nowait(tmem + lane_off + kColP + half * 16, pk);
+                tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&p_full[pb]);
+                mbar_arrive(p_full);
             }
             // ---- this CTA's output half: 256 columns, 128 per warp of the pair ----
             float l_run = 0.f;
