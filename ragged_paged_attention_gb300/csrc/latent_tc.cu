@@ -64,7 +64,7 @@ __device__ __forceinline__ int lat_panel_col(int rank, int p) { return rank == 0
 template <bool SPARSE>
 __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     latent_tc_kernel(LatentArgs a, const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_kr,
-                     int kv_tma, int box_rows) {
+                     const __grid_constant__ CUtensorMap tm_kc3, int kv_tma, int box_rows) {
     using namespace lat;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -206,7 +206,12 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         if (!__shfl_sync(0xffffffffu, g, 0)) break;
                         uint8_t* stage = smem + kOffKV + st * kStage;
                         const int row0 = page * a.page_size + kbx % a.page_size;
-                        if (full) {
+                        if (full && kv_tma == 2) {
+                            // whole block in one box: the four latent panels of this rank in one
+                            // 3-D copy ([panel][row][64] lands as the stage layout), rope apart
+                            tma_load_3d(smem_u32(stage), &tm_kc3, 0, row0, rank == 0 ? 0 : 4, &kv_full[st]);
+                            if (rank == 0) tma_load_2d(smem_u32(stage + 4 * kPanel), &tm_kr, 0, row0, &kv_full[st]);
+                        } else if (full) {
                             for (int p = 0; p < nqp; ++p) {
                                 const uint32_t dst = smem_u32(stage + p * kPanel + lane * box_rows * 128);
                                 if (rank == 0 && p == 4)
@@ -216,6 +221,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                             }
                         }
                         uint32_t pm = __ballot_sync(0xffffffffu, rows > 0 && !full);
+                        const bool wrote = pm != 0;
                         while (pm) {
                             const int src = __ffs(pm) - 1;
                             pm &= pm - 1;
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                                 *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)) = v;
                             }
                         }
-                        fence_proxy_async_smem();
+                        if (wrote) fence_proxy_async_smem();  // register-written rows, read by the tensor core
                         mbar_arrive(&kv_full[st]);
                     }
                 }
@@ -313,11 +319,16 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             if (lane == 0) {
                 constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
                 constexpr uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
+                // descriptors of stage 0; a byte offset d within shared memory adds d >> 4 to
+                // the start-address field (no carry: every address is below 256 KB)
+                const uint64_t kdesc0 = umma_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
+                const uint64_t vdesc0 = umma_desc_sw128(smem_u32(smem + kOffKV), kPanel, 1024);
                 bool ok = mbar_wait(q_full, iph, err);
                 tc_fence_after();
                 // issue QK(next) and PV(next) in whichever order their inputs become ready
                 int nq = 0, np = 0;
                 unsigned long long t0 = 0;
+                uint32_t idle = 0;
                 while (ok && np < nb) {
                     bool moved = false;
                     if (nq < nb) {
@@ -325,14 +336,17 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         const uint32_t q = jb + nq, st = q % NS, par = (q / NS) & 1;
                         if (mbar_test(&kv_full[st], par) && mbar_test(s_empty, (q & 1) ^ 1)) {
                             tc_fence_after();
-                            const uint32_t k_base = smem_u32(smem + kOffKV + st * kStage);
-                            for (int p = 0; p < nqp; ++p)
+                            const uint64_t bd = kdesc0 + (uint64_t)((st * kStage) >> 4);
+                            const uint32_t sa = tmem + kColS, qa = tmem + kColQ;
 #pragma unroll
-                                for (int ks = 0; ks < 4; ++ks) {
-                                    const uint64_t bd = umma_desc_sw128(k_base + p * kPanel + ks * 32, 16, 1024);
-                                    umma_bf16_ta(tmem + kColS, tmem + kColQ + p * 32 + ks * 8, bd, idesc_qk,
-                                                 (p > 0 || ks > 0) ? 1u : 0u);
+                            for (int p = 0; p < NQP_MAX; ++p) {
+                                if (p < nqp) {
+#pragma unroll
+                                    for (int ks = 0; ks < 4; ++ks)
+                                        umma_bf16_ta(sa, qa + p * 32 + ks * 8, bd + ((p * kPanel + ks * 32) >> 4), idesc_qk,
+                                                     (p > 0 || ks > 0) ? 1u : 0u);
                                 }
+                            }
                             umma_commit(s_full);
                             ++nq;
                             moved = true;
@@ -342,25 +356,29 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         const uint32_t q = jb + np, st = q % NS;
                         if (mbar_test(p_full, q & 1)) {
                             tc_fence_after();
-                            const uint32_t v_base = smem_u32(smem + kOffKV + st * kStage);
+                            const uint64_t bd = vdesc0 + (uint64_t)((st * kStage) >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk) {
-                                const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, kPanel, 1024);
-                                umma_bf16_ta(tmem + kColO, tmem + kColP + kk * 8, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
-                            }
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                umma_bf16_ta(tmem + kColO, tmem + kColP + kk * 8, bd + ((kk * 16 * 128) >> 4), idesc_pv,
+                                             (np > 0 || kk > 0) ? 1u : 0u);
                             umma_commit(p_empty);
                             umma_commit(&kv_empty[st]);
                             ++np;
                             moved = true;
                         }
                     }
+                    // the wait limit is checked every 256 idle polls (the clock read is not free)
                     if (moved) {
                         t0 = 0;
-                    } else if (t0 == 0) {
-                        t0 = global_ns();
-                    } else if (global_ns() - t0 > kWaitLimitNs) {
-                        set_error(err, RPA_DEV_ERR_TIMEOUT);
-                        ok = false;
+                        idle = 0;
+                    } else if (++idle == 256) {
+                        idle = 0;
+                        if (t0 == 0) {
+                            t0 = global_ns();
+                        } else if (global_ns() - t0 > kWaitLimitNs) {
+                            set_error(err, RPA_DEV_ERR_TIMEOUT);
+                            ok = false;
+                        }
                     }
                 }
                 umma_commit(o_full);
@@ -669,12 +687,27 @@ static bool make_tmap_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The latent row [rows][lkv_pad] bf16 viewed as [panel (8)][rows][64]: dims {64, rows, 8},
+// strides {row, 128 bytes}; box {64, 64 rows, 4 panels} lands as four [64 x 64] panels.
+static bool make_tmap_panels(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t stride) {
+    auto enc = lat_tmap_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {64, rows, kLatDv / 64};
+    const cuuint64_t strides[2] = {stride * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)lat::BK, 4};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool SPARSE>
 static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream_t stream) {
     using namespace lat;
-    CUtensorMap kc, kr;
+    CUtensorMap kc, kr, kc3;
     memset(&kc, 0, sizeof kc);
     memset(&kr, 0, sizeof kr);
+    memset(&kc3, 0, sizeof kc3);
     int kv_tma = 0, box_rows = 0;  // without usable key maps the register gather runs
     if (!SPARSE) {
         const int ps = a.page_size;
@@ -683,6 +716,8 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
             const uint64_t rows = (uint64_t)a.total_num_pages * ps;
             kv_tma = make_tmap_2d(&kc, a.cache_kv_c, a.lkv_pad, rows, a.lkv_pad, box_rows) &&
                      make_tmap_2d(&kr, a.cache_k_pe, a.r_pad, rows, a.r_pad, box_rows);
+            // kv_tma 2: a block is one box per panel group (pages of at least a block)
+            if (kv_tma && box_rows == BK && make_tmap_panels(&kc3, a.cache_kv_c, rows, a.lkv_pad)) kv_tma = 2;
         }
     }
     auto kern = latent_tc_kernel<SPARSE>;
@@ -710,7 +745,7 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
     }
     cfg.gridDim = dim3(2 * max_clusters);
     ProfScope ps(SPARSE ? "sparse_attn" : "mla_attn", stream);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, kc, kr, kv_tma, box_rows);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, kc, kr, kc3, kv_tma, box_rows);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
