@@ -9,16 +9,20 @@
 //   rank 1: score dims 256-511,                    output dims 256-511.
 // Each CTA keeps its Q slice in tensor memory (the MMA's A operand), gathers only its dims
 // of each key row into a 4-deep shared-memory ring and computes a partial score tile
-// S_r = Q_r K_r^T (tcgen05, 128 x 64 per block).  The two
-// partials are exchanged through distributed shared memory (st.async into a double-buffered
-// receive area, completing on the receiver's mbarrier), so both CTAs hold the same
-// S = S_0 + S_1, run the same online softmax and write the same P (into TMEM, the A operand
-// of PV); each then accumulates O_r += P V_r into its own 256 TMEM columns.  A receive
-// buffer is reused two blocks later: the peer writes it again only after it has received
-// this CTA's next partial, which is sent after the reads and whose completion is a
-// cluster-scope release, so no separate "buffer free" signal is needed.
-// Warps per CTA: 0-7 softmax (two per TMEM lane quarter, 32 of the 64 columns each),
-// 8-11 producers, 12 MMA issuer.  MLA keys are the causal (windowed) prefix gathered page
+// S_r = Q_r K_r^T (tcgen05, 128 x 64 per block).  The softmax of the 128 rows is split
+// between the two CTAs: rank r owns rows 64r..64r+63.  For the peer's rows, a CTA only
+// sends its partial scores (fp32, through distributed shared memory: st.async into a
+// double-buffered receive area, completing on the receiver's mbarrier) and later receives
+// those rows' P (bf16) and rescale factor; for its own rows it adds the peer's partial,
+// runs the online softmax, keeps P and sends it to the peer.  Both CTAs then accumulate
+// O_r += P V_r into their own 256 TMEM columns (P is the A operand, in TMEM).  This moves
+// 24 KB per block each way instead of 32 (the SM-to-SM link, not the tensor core, bounds
+// a block) and halves the exponentials per CTA.  Receive buffers are reused two blocks
+// later: readers arrive on a local barrier and a signalling warp (with no remote stores of
+// its own in flight) passes that on to the peer with one cluster-scope release arrive.
+// Row statistics (m, l) of the owned rows go to the peer once per item.
+// Warps per CTA: 0-7 softmax (two per TMEM lane quarter, 32 of the 64 columns each; a
+// quarter's warps are owners or helpers), 8-11 producers, 12 MMA issuer, 13 signalling.  MLA keys are the causal (windowed) prefix gathered page
 // by page with 2-D TMA boxes (the partial last page through registers); sparse keys are
 // the selected units' rows, gathered through registers with their validity recorded for
 // the softmax.  Items split long key ranges; partials merge by the log-sum-exp rule.
@@ -37,11 +41,15 @@ constexpr int NQP_MAX = 5;                    // score panels of rank 0 (4 laten
 constexpr int kPanel = BK * 128;              // one key panel: [64 rows x 64 dims]
 constexpr int kStage = NQP_MAX * kPanel;
 constexpr int NS = 4;                         // key stages
-constexpr int kRecv = 128 * BK * 4;           // the peer's partial scores, fp32
+// receive buffers (in the receiving CTA), a warp's 32 rows of one 16-byte chunk contiguous:
+constexpr int kSRecv = 2 * 8 * 64 * 16;       // peer's partial S of my 64 rows: [half][8 chunks][row]
+constexpr int kPRecv = 2 * 4 * 64 * 16 + 64 * 4;  // P of the peer's 64 rows [half][4 chunks][row] + alpha[row]
 constexpr int kOffKV = 0;
-constexpr int kOffRecv = kOffKV + NS * kStage;  // [2] receive buffers
-constexpr int kOffBar = kOffRecv + 2 * kRecv;
-constexpr int kNumBars = 3 * NS + 9;
+constexpr int kOffSRecv = kOffKV + NS * kStage;    // [2]
+constexpr int kOffPRecv = kOffSRecv + 2 * kSRecv;  // [2]
+constexpr int kOffStat = kOffPRecv + 2 * kPRecv;   // (m, l) of the peer's rows
+constexpr int kOffBar = kOffStat + 64 * 8;
+constexpr int kNumBars = 3 * NS + 20;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;
 constexpr int kOffVld = kOffRed + 2 * 2 * 128 * 4;
@@ -51,10 +59,11 @@ constexpr int kSmem = kOffItem + 48;
 // P [128 x 64] bf16 pairs at 224, the O half [128 x 256] fp32 at 256.
 constexpr int kColS = 0, kColQ = BK, kColP = 224, kColO = 256;
 constexpr int kTmemCols = 512;
-constexpr int kWarps = 13;
-constexpr int kProdW0 = 8, kMmaW = 12;
+constexpr int kWarps = 14;
+constexpr int kProdW0 = 8, kMmaW = 12, kSigW = 13;
 static_assert(kSmem <= 232448, "shared memory budget");
-static_assert(kOffKV % 1024 == 0 && kOffRecv % 16 == 0 && kOffItem % 16 == 0, "alignment");
+static_assert(kOffKV % 1024 == 0 && kOffSRecv % 16 == 0 && kOffPRecv % 16 == 0 && kPRecv % 16 == 0 &&
+                  kOffBar % 8 == 0 && kOffItem % 16 == 0, "alignment");
 static_assert(kColQ + NQP_MAX * 32 <= kColP && kColP + BK / 2 <= kColO, "TMEM columns");
 }  // namespace lat
 
@@ -78,7 +87,13 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     uint64_t* q_full = bars + 3 * NS + 4;     // the Q slice is in TMEM
     uint64_t* o_full = bars + 3 * NS + 5;
     uint64_t* fin = bars + 3 * NS + 6;
-    uint64_t* recv_full = bars + 3 * NS + 7;  // [2] the peer's partial S has landed (st.async bytes)
+    uint64_t* srecv_full = bars + 3 * NS + 7;   // [2] the peer's partial S of my rows landed (bytes)
+    uint64_t* srecv_used = bars + 3 * NS + 9;   // [2] my owner threads have read it
+    uint64_t* s_free = bars + 3 * NS + 11;      // [2] the peer has read the S buffer I write next
+    uint64_t* precv_full = bars + 3 * NS + 13;  // [2] P + alpha of the peer's rows landed (bytes)
+    uint64_t* precv_used = bars + 3 * NS + 15;  // [2] my helper threads have read it
+    uint64_t* p_free = bars + 3 * NS + 17;      // [2] the peer has read the P buffer I write next
+    uint64_t* stat_full = bars + 3 * NS + 19;   // (m, l) of the peer's rows landed (bytes)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     uint8_t* vld = smem + kOffVld;
@@ -93,7 +108,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     const int H = a.num_heads;
     const int tiles = H / 128;
 
-    for (int i = tid * 16; i < kOffRecv; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
+    for (int i = tid * 16; i < kOffSRecv; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -108,7 +123,17 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         mbar_init(q_full, 256);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&recv_full[i], 1);  // own thread 0 arms the bytes; the peer's st.async complete them
+        for (int i = 0; i < 2; ++i) {
+            // *_full: one local thread arms the bytes, the peer's st.async complete them;
+            // *_free: the peer's signalling thread arrives
+            mbar_init(&srecv_full[i], 1);
+            mbar_init(&srecv_used[i], 128);
+            mbar_init(&s_free[i], 1);
+            mbar_init(&precv_full[i], 1);
+            mbar_init(&precv_used[i], 128);
+            mbar_init(&p_free[i], 1);
+        }
+        mbar_init(stat_full, 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -127,7 +152,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         sparse_chunk = cdiv(cdiv(slots, a.sparse_splits), BK) * BK;
     }
     const int n_items = SPARSE ? sparse_items : hdr->num_items[2];
-    uint32_t jb = 0, items = 0;
+    uint32_t jb = 0, items = 0, nstat = 0;
     for (int it = (int)cluster_id_x(); it < n_items; it += (int)cluster_count_x()) {
         if (tid == 0) {
             WorkItem w;
@@ -384,17 +409,41 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 umma_commit(o_full);
                 if (!ok) s_abort = 1;
             }
+        } else if (warp == kSigW) {
+            // ---------------- exchange signalling ----------------
+            // once this CTA has read receive buffer rb of block q, tell the peer it may write
+            // it again (block q+2); the release carries the readers' loads (cumulativity)
+            if (lane == 0) {
+                const uint32_t sfree_peer = mapa_shared(smem_u32(s_free), peer);
+                const uint32_t pfree_peer = mapa_shared(smem_u32(p_free), peer);
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t q = jb + j, rb = q & 1, rp = (q >> 1) & 1;
+                    if (!mbar_wait(&srecv_used[rb], rp, err)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_cluster(sfree_peer + rb * 8);
+                    if (!mbar_wait(&precv_used[rb], rp, err)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_cluster(pfree_peer + rb * 8);
+                }
+            }
         } else {
             // ------- softmax: row = TMEM lane, warps w and w+4 take 32 of the 64 columns each -------
             const int quarter = warp & 3, half = warp >> 2;
             const int r = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
-            // exchange layout [half][chunk of 4 scores][row]: a warp's 32 rows of one chunk are
-            // 512 consecutive bytes, so the remote stores and the local reads are conflict free
-            const uint32_t recv_self = smem_u32(smem + kOffRecv) + (half * 8 * 128 + r) * 16;
-            const uint32_t recv_peer = mapa_shared(recv_self, peer);
-            const uint32_t recv_full_peer = mapa_shared(smem_u32(recv_full), peer);
+            // rows 64*rank.. are owned here; `orow` is the row within the owned (or peer-owned) 64
+            const bool owner = (quarter >> 1) == (int)rank;
+            const int orow = (quarter & 1) * 32 + lane;
+            const bool lead = (quarter & 1) == 0 && half == 0 && lane == 0;  // arms this role's receive barriers
+            const uint32_t srecv_peer = mapa_shared(smem_u32(smem + kOffSRecv), peer);
+            const uint32_t precv_peer = mapa_shared(smem_u32(smem + kOffPRecv), peer);
+            const uint32_t srecv_full_peer = mapa_shared(smem_u32(srecv_full), peer);
+            const uint32_t precv_full_peer = mapa_shared(smem_u32(precv_full), peer);
             {
                 // Q slice -> TMEM: this thread's row, half of its 16-byte chunks (8 dims = 4
                 // columns each).  The previous item's MMAs have all completed (o_full).
@@ -427,97 +476,12 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             }
             float m_use = -INFINITY, l_half = 0.f;
             bool ok = true;
-            for (int j = 0; j < nb; ++j) {
-                const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1, rb = q & 1, rp = (q >> 1) & 1;
-                if (!mbar_wait(s_full, q & 1, err)) {
-                    ok = false;
-                    break;
-                }
+            // common tail of a block: once PV of the previous block is done with P and has
+            // written O, rescale this row of O by f and store this row's P
+            auto finish = [&](uint32_t q, const uint32_t (&pk)[16], float f) -> bool {
+                if (!mbar_wait(p_empty, (q & 1) ^ 1, err)) return false;
                 tc_fence_after();
-                float x[32];
-                tmem_ld32(tmem + lane_off + kColS + half * 32, x);
-                tc_fence_before();
-                mbar_arrive(s_empty);
-                // exchange partial scores with the peer CTA: arm this block's receive barrier
-                // (its previous phase, two blocks ago, was consumed by this thread), then send
-                // my partial into the peer's buffer rb
-                if (tid == 0) mbar_arrive_expect_tx(&recv_full[rb], kRecv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    st_async_v4(recv_peer + rb * kRecv + i * 128 * 16, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3],
-                                recv_full_peer + rb * 8);
-                if (!mbar_wait_cluster(&recv_full[rb], rp, err)) {
-                    ok = false;
-                    break;
-                }
-                {
-                    const float4* src = reinterpret_cast<const float4*>(smem + kOffRecv + rb * kRecv) + half * 8 * 128 + r;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 v = src[i * 128];
-                        x[4 * i] += v.x;
-                        x[4 * i + 1] += v.y;
-                        x[4 * i + 2] += v.z;
-                        x[4 * i + 3] += v.w;
-                    }
-                }
-                // scale, soft cap, key validity
-                if (cap != 0.f) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = cap * tanhf(x[i] * scale / cap) * kLog2e;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] *= c_log2;
-                }
-                const int key0 = kb + j * BK + half * 32;
-                if (SPARSE) {
-                    if (!mbar_wait(&vld_full[st], par, err)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint8_t* vb = vld + st * BK + half * 32;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = vb[i] ? x[i] : -INFINITY;
-                } else if (!(key0 >= wlo && key0 + 31 < ke)) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int key = key0 + i;
-                        x[i] = (key < ke && key >= wlo) ? x[i] : -INFINITY;
-                    }
-                }
-                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
-                float* red_j = red + (q & 1) * 256;
-                red_j[half * 128 + r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-                const float mx = fmaxf(red_j[r], red_j[128 + r]);
-                float alpha = 1.f;
-                const bool had = m_use > -INFINITY;
-                const bool rescale = mx > m_use + 8.f;
-                if (rescale) {
-                    alpha = fast_exp2(m_use - mx);
-                    m_use = mx;
-                }
-                const float mu = m_use == -INFINITY ? 0.f : m_use;
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(x[2 * e] - mu), p1 = fast_exp2(x[2 * e + 1] - mu);
-                    sum4[e & 3] += p0 + p1;
-                    pk[e] = pack_bf16(p0, p1);
-                }
-                const bool row_rescale = rescale && had;
-                l_half = l_half * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-                // PV of the previous block is done with P and has written O
-                if (!mbar_wait(p_empty, (q & 1) ^ 1, err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, row_rescale)) {
-                    const float f = row_rescale ? alpha : 1.f;
+                if (__any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         float o32[32];
@@ -532,15 +496,175 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(p_full);
+                return true;
+            };
+            if (!owner) {
+                // ---- helper rows (owned by the peer): send my partial S as soon as it exists,
+                // then take the row's P and rescale factor back; block q+1's partial goes out
+                // before block q's P is awaited, so neither CTA waits on a round trip ----
+                auto send_s = [&](uint32_t q) -> bool {
+                    const uint32_t rb = q & 1, rp = (q >> 1) & 1;
+                    if (!mbar_wait(s_full, q & 1, err)) return false;
+                    tc_fence_after();
+                    float x[32];
+                    tmem_ld32(tmem + lane_off + kColS + half * 32, x);
+                    tc_fence_before();
+                    mbar_arrive(s_empty);
+                    if (!mbar_wait_cluster(&s_free[rb], rp ^ 1, err)) return false;  // the peer has read block q-2
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        st_async_v4(srecv_peer + rb * kSRecv + ((half * 8 + i) * 64 + orow) * 16, x[4 * i], x[4 * i + 1],
+                                    x[4 * i + 2], x[4 * i + 3], srecv_full_peer + rb * 8);
+                    return true;
+                };
+                if (nb > 0 && !send_s(jb)) ok = false;
+                for (int j = 0; j < nb && ok; ++j) {
+                    const uint32_t q = jb + j, rb = q & 1, rp = (q >> 1) & 1;
+                    if (j + 1 < nb && !send_s(q + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lead) mbar_arrive_expect_tx(&precv_full[rb], kPRecv);  // phase of block q-2 consumed here
+                    if (!mbar_wait_cluster(&precv_full[rb], rp, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* pr = smem + kOffPRecv + rb * kPRecv;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(pr + ((half * 4 + i) * 64 + orow) * 16);
+                        pk[4 * i] = v.x;
+                        pk[4 * i + 1] = v.y;
+                        pk[4 * i + 2] = v.z;
+                        pk[4 * i + 3] = v.w;
+                    }
+                    const float f = reinterpret_cast<const float*>(pr + 2 * 4 * 64 * 16)[orow];
+                    mbar_arrive(&precv_used[rb]);
+                    if (!finish(q, pk, f)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            } else {
+                // ---- owned rows: add the peer's partial, online softmax, P to the peer ----
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1, rb = q & 1, rp = (q >> 1) & 1;
+                    if (!mbar_wait(s_full, q & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float x[32];
+                    tmem_ld32(tmem + lane_off + kColS + half * 32, x);
+                    tc_fence_before();
+                    mbar_arrive(s_empty);
+                    if (lead) mbar_arrive_expect_tx(&srecv_full[rb], kSRecv);  // phase of block q-2 consumed here
+                    if (!mbar_wait_cluster(&srecv_full[rb], rp, err)) {
+                        ok = false;
+                        break;
+                    }
+                    {
+                        const uint8_t* sr = smem + kOffSRecv + rb * kSRecv;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 v = *reinterpret_cast<const float4*>(sr + ((half * 8 + i) * 64 + orow) * 16);
+                            x[4 * i] += v.x;
+                            x[4 * i + 1] += v.y;
+                            x[4 * i + 2] += v.z;
+                            x[4 * i + 3] += v.w;
+                        }
+                    }
+                    mbar_arrive(&srecv_used[rb]);
+                    // scale, soft cap, key validity
+                    if (cap != 0.f) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] = cap * tanhf(x[i] * scale / cap) * kLog2e;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] *= c_log2;
+                    }
+                    const int key0 = kb + j * BK + half * 32;
+                    if (SPARSE) {
+                        if (!mbar_wait(&vld_full[st], par, err)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint8_t* vb = vld + st * BK + half * 32;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] = vb[i] ? x[i] : -INFINITY;
+                    } else if (!(key0 >= wlo && key0 + 31 < ke)) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int key = key0 + i;
+                            x[i] = (key < ke && key >= wlo) ? x[i] : -INFINITY;
+                        }
+                    }
+                    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
+                    float* red_j = red + (q & 1) * 256;
+                    red_j[half * 128 + r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                    const float mx = fmaxf(red_j[r], red_j[128 + r]);
+                    float alpha = 1.f;
+                    const bool had = m_use > -INFINITY;
+                    const bool rescale = mx > m_use + 8.f;
+                    if (rescale) {
+                        alpha = fast_exp2(m_use - mx);
+                        m_use = mx;
+                    }
+                    const float mu = m_use == -INFINITY ? 0.f : m_use;
+                    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = fast_exp2(x[2 * e] - mu), p1 = fast_exp2(x[2 * e + 1] - mu);
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    const float f = (rescale && had) ? alpha : 1.f;
+                    l_half = l_half * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                    if (!mbar_wait_cluster(&p_free[rb], rp ^ 1, err)) {  // the peer has read block q-2 out of it
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t pdst = precv_peer + rb * kPRecv;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_async_u4(pdst + ((half * 4 + i) * 64 + orow) * 16,
+                                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]),
+                                    precv_full_peer + rb * 8);
+                    if (half == 0) st_async_f32(pdst + 2 * 4 * 64 * 16 + orow * 4, f, precv_full_peer + rb * 8);
+                    if (!finish(q, pk, f)) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
-            // ---- this CTA's output half: 256 columns, 128 per warp of the pair ----
+            // ---- row statistics: owners reduce l over the pair and send (m, l) to the peer ----
             float l_run = 0.f;
-            if (ok) {
-                float* red_l = red + ((jb + nb) & 1) * 256;
-                red_l[half * 128 + r] = l_half;
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-                l_run = red_l[r] + red_l[128 + r];
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+            if (ok && nb > 0) {
+                const uint32_t sph = nstat & 1;
+                if (owner) {
+                    float* red_l = red + ((jb + nb) & 1) * 256;
+                    red_l[half * 128 + r] = l_half;
+                    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                    l_run = red_l[r] + red_l[128 + r];
+                    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                    if (half == 0)
+                        st_async_v2(mapa_shared(smem_u32(smem + kOffStat + orow * 8), peer), m_use, l_run,
+                                    mapa_shared(smem_u32(stat_full), peer));
+                } else {
+                    if (lead) mbar_arrive_expect_tx(stat_full, 64 * 8);
+                    if (mbar_wait_cluster(stat_full, sph, err)) {
+                        const float2 ml = *reinterpret_cast<const float2*>(smem + kOffStat + orow * 8);
+                        m_use = ml.x;
+                        l_run = ml.y;
+                    } else {
+                        ok = false;
+                    }
+                }
             }
             if (ok && mbar_wait(o_full, iph, err)) {
                 tc_fence_after();
@@ -593,6 +717,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         }
         jb += nb;
         ++items;
+        if (nb > 0) ++nstat;
         __syncthreads();
         tc_fence_after();
         if (w.num_splits > 1 && !s_abort) {
