@@ -105,6 +105,64 @@ def load_peaks():
         return dict(FALLBACK), "fallback"
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's libnvidia-ml, read-only
+    queries) every ~0.5 ms by a thread, so a timed region of a few milliseconds is covered."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, local_rank):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ident = vis.split(",")[local_rank].strip() if vis else str(local_rank)
+        self.h = ctypes.c_void_p()
+        if ident.startswith("GPU-") or ident.startswith("MIG-"):
+            rc = self.lib.nvmlDeviceGetHandleByUUID(ident.encode(), ctypes.byref(self.h))
+        else:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(int(ident), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError(f"nvml handle: {rc}")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+        self.sm, self.bits, self.stop_flag = [], 0, False
+
+    def _poll(self):
+        ct = self.ct
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) == 0:
+                self.sm.append(float(mhz.value))
+            if self.reasons_fn(self.h, ct.byref(rs)) == 0:
+                self.bits |= rs.value
+            time.sleep(0.0005)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        return self
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join(timeout=2)
+        return {"sm_mhz": statistics.median(self.sm) if self.sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.bits & b), "samples": len(self.sm),
+                "source": "nvml, ~0.5 ms polling during the timed region"}
+
+
+def clock_sampler(local_rank):
+    try:
+        return NvmlSampler(local_rank)
+    except Exception:
+        return ClockSampler(local_rank)
+
+
 class ClockSampler:
     """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
 
@@ -370,7 +428,7 @@ def main():
         api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, workspace=ws,
                         **opts)
 
-    clocks = ClockSampler(local).start()
+    clocks = clock_sampler(local).start()
     ms, ktimes = time_steps(step, args.steps, args.warmup, world, timer=True)
     clk = clocks.stop()
     assert api.check_device_status(ws) == 0 and api.check_device_status(ws_u) == 0
