@@ -87,7 +87,7 @@ RpaLayout rpa_layout(const rpa_params* p) {
     const int G = p->num_q_heads / hkv;
     const int dh = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
     const int groups = cdiv(hkv, dh);
-    L.max_dec = kDecodeTargetCtas + groups * p->max_num_seqs;
+    L.max_dec = kDecodeTargetCtas + 2 * groups * p->max_num_seqs;  // up to two 8-row halves per sequence
     L.max_pre = hkv * (int)((long long)p->max_num_tokens * G / kPrefillRows + p->max_num_seqs + 1);
     size_t off = kWsHeaderBytes;
     L.items_dec = off;

@@ -13,6 +13,7 @@ struct WsHeader;
 // Tiling constants of the RPA kernels.
 constexpr int kMaxDecodeHeads = 4;      // most KV heads a decode CTA covers (one warp each)
 constexpr int kDecodeBK = 16;           // keys per decode pipeline stage
+constexpr int kDecodeRows = 8;          // query rows (q_len x G) per decode item (mma N)
 constexpr int kPrefillRows = 128;       // (token, q-head) rows per prefill item (one TMEM tile)
 constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
 constexpr int kDecodeTargetCtas = 1024; // split so decode work spreads over about this many CTAs

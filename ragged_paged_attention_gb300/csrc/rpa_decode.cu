@@ -8,10 +8,15 @@
 //     segment of HG KV heads of that token (HG * 2 * D elements) lands in a padded
 //     shared-memory row (padding keeps ldmatrix conflict free); a full/empty mbarrier
 //     pair per stage orders producer and consumers;
-//   * HG consumer warps, one per KV head, hold their query rows (G heads x q_len
-//     tokens, <= 16) as tensor-core A fragments in registers and run QK^T and PV on
-//     m16n8k16 tiles with an online softmax; fp8 (or scaled bf16) K/V are first
-//     dequantised by the warp into its own bf16 rows as bf16(float(x) * scale);
+//   * HG consumer warps, one per KV head, run the contractions transposed so that the
+//     16 keys of a stage fill the M side of the m16n8k16 tile and the item's <= 8 query
+//     rows (G heads x q_len tokens) its N side: S^T = K Q^T with Q^T held as B fragments
+//     in registers, then O^T += V^T P^T with V^T loaded by a transposing ldmatrix and
+//     P^T moved into B-fragment layout by movmatrix; the online softmax runs per column
+//     (a query row) across the 8 lanes that share it.  Half the tensor-core work and
+//     half the accumulator registers of rows-on-M tiles, whose 16 rows would be mostly
+//     padding; fp8 (or scaled bf16) K/V are first dequantised by the warp into its own
+//     bf16 rows as bf16(float(x) * scale);
 //   * slots past kv_len are never copied: the stage memory is zeroed once at start, so
 //     a skipped row holds finite data whose probability is exactly zero.
 // Items split the keys of a sequence (flash-decoding); split partials (m, l, O) are
@@ -162,34 +167,37 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
             }
         } else {
             // ---------------- consumer warp: KV head h0 + warp ----------------
+            // C-fragment columns of this thread: rows rb + 2*q4 + {0,1}; B-fragment column: row rb + g8
             const bool head_ok = warp < seg_heads;
             const int head = h0 + warp;
             const int g8 = lane >> 2, q4 = lane & 3;
+            const int rb = w.row_begin;
             int qpos[2], wlo[2];
             bool rv[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int R = g8 + e * 8;
-                rv[e] = head_ok && R < n_rows;
-                qpos[e] = rv[e] ? kv_len - q_len + R / G : -1;
-                wlo[e] = a.sliding_window > 0 ? qpos[e] - a.sliding_window + 1 : 0;
+            for (int j = 0; j < 2; ++j) {
+                const int R = rb + 2 * q4 + j;
+                rv[j] = head_ok && R < n_rows;
+                qpos[j] = rv[j] ? kv_len - q_len + R / G : -1;
+                wlo[j] = a.sliding_window > 0 ? qpos[j] - a.sliding_window + 1 : 0;
             }
-            // query rows as A fragments (row g8 / g8+8, columns 2*q4.. of each 16-wide k-step)
-            uint32_t qa[D / 16][4];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int R = g8 + e * 8;
+            const int Rb = rb + g8;
+            const bool rvb = head_ok && Rb < n_rows;
+            // Q^T as B fragments: column g8, k = dims 2*q4.. and 2*q4+8.. of each 16-wide step
+            uint32_t qb[D / 16][2];
+            {
                 const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                    a.q + ((size_t)(q_start + (rv[e] ? R / G : 0)) * a.num_q_heads + head * G + (rv[e] ? R % G : 0)) * D);
+                    a.q + ((size_t)(q_start + (rvb ? Rb / G : 0)) * a.num_q_heads + head * G + (rvb ? Rb % G : 0)) * D);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    qa[ks][e] = rv[e] ? __ldg(qrow + ks * 8 + q4) : 0u;
-                    qa[ks][e + 2] = rv[e] ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;
+                    qb[ks][0] = rvb ? __ldg(qrow + ks * 8 + q4) : 0u;
+                    qb[ks][1] = rvb ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;
                 }
             }
-            float o[D / 8][4];
+            // O^T tiles: rows (dims) 16*dm + g8 and +8, columns (query rows) 2*q4, 2*q4+1
+            float o[D / 16][4];
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
             const float scale = a.sm_scale, cap = a.soft_cap;
 
@@ -206,6 +214,7 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     uint8_t* cb = conv + warp * BK * T::kConvRow;
                     if (head_ok) {
                         constexpr int kChunks = 2 * D / 8;  // 8-element chunks of K|V per key
+#pragma unroll 4
                         for (int i = lane; i < BK * kChunks; i += 32) {
                             const int kk = i / kChunks, c = i % kChunks;
                             const float sc = c < D / 8 ? a.k_scale_or_one : a.v_scale_or_one;
@@ -224,72 +233,63 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                 vbase = kbase + D * 2;
                 if (head_ok) {
                     const int key0 = kb + blk * BK;
-                    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    // S^T [16 keys x 8 rows] = K Q^T; A = K rows (ldmatrix: keys 0-7 / 8-15, dims 0-7 / 8-15)
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
                     {
-                        const uint32_t ka = kbase + (((lane >> 4) << 3) + (lane & 7)) * rowb + ((lane >> 3) & 1) * 16;
+                        const uint32_t ka = kbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * rowb + (lane >> 4) * 16;
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(ka + ks * 32, b0, b1, b2, b3);
-                            mma_bf16(sc[0], qa[ks], b0, b1);
-                            mma_bf16(sc[1], qa[ks], b2, b3);
+                            uint32_t ka4[4];
+                            ldsm_x4(ka + ks * 32, ka4[0], ka4[1], ka4[2], ka4[3]);
+                            mma_bf16(sc, ka4, qb[ks][0], qb[ks][1]);
                         }
                     }
+                    // sc[e]: key g8 + 8*(e>>1), row 2*q4 + (e&1)
                     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int r = e >> 1;
-                            const int key = key0 + nt * 8 + 2 * q4 + (e & 1);
-                            float x = sc[nt][e] * scale;
-                            if (cap != 0.f) x = cap * tanhf(x / cap);
-                            x *= kLog2e;
-                            const bool ok = key <= qpos[r] && key >= wlo[r] && key < ke;
-                            x = ok ? x : -INFINITY;
-                            sc[nt][e] = x;
-                            mx[r] = fmaxf(mx[r], x);
-                        }
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = e & 1;
+                        const int key = key0 + g8 + (e >> 1) * 8;
+                        float x = sc[e] * scale;
+                        if (cap != 0.f) x = cap * tanhf(x / cap);
+                        x *= kLog2e;
+                        const bool ok = key <= qpos[j] && key >= wlo[j] && key < ke;
+                        x = ok ? x : -INFINITY;
+                        sc[e] = x;
+                        mx[j] = fmaxf(mx[j], x);
                     }
                     float alpha[2], muse[2];
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                        const float mn = fmaxf(m_run[r], mx[r]);
-                        muse[r] = mn == -INFINITY ? 0.f : mn;
-                        alpha[r] = fast_exp2(m_run[r] - muse[r]);
-                        m_run[r] = mn;
-                        l_run[r] *= alpha[r];
+                    for (int j = 0; j < 2; ++j) {
+                        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+                        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+                        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+                        const float mn = fmaxf(m_run[j], mx[j]);
+                        muse[j] = mn == -INFINITY ? 0.f : mn;
+                        alpha[j] = fast_exp2(m_run[j] - muse[j]);
+                        m_run[j] = mn;
+                        l_run[j] *= alpha[j];
                     }
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
+                    for (int e = 0; e < 4; ++e) {
+                        const float p = fast_exp2(sc[e] - muse[e & 1]);
+                        sc[e] = p;
+                        l_run[e & 1] += p;
+                    }
+                    // P^T as B fragments (k = keys 2*q4.., n = row g8): transpose the 8x8 blocks
+                    const uint32_t pb0 = movmatrix_t(pack_bf16(sc[0], sc[1]));
+                    const uint32_t pb1 = movmatrix_t(pack_bf16(sc[2], sc[3]));
+                    // O^T [16 dims x 8 rows] += V^T P^T; A = V^T by a transposing ldmatrix of V rows
+                    const uint32_t va = vbase + ((lane & 7) + ((lane >> 4) << 3)) * rowb + ((lane >> 3) & 1) * 16;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float p = fast_exp2(sc[nt][e] - muse[e >> 1]);
-                            sc[nt][e] = p;
-                            l_run[e >> 1] += p;
-                        }
-                    uint32_t pf[4];
-                    pf[0] = pack_bf16(sc[0][0], sc[0][1]);
-                    pf[1] = pack_bf16(sc[0][2], sc[0][3]);
-                    pf[2] = pack_bf16(sc[1][0], sc[1][1]);
-                    pf[3] = pack_bf16(sc[1][2], sc[1][3]);
-                    const uint32_t va = vbase + ((lane & 7) + (((lane >> 3) & 1) << 3)) * rowb + (lane >> 4) * 16;
-#pragma unroll
-                    for (int dp = 0; dp < D / 16; ++dp) {
-                        o[2 * dp][0] *= alpha[0];
-                        o[2 * dp][1] *= alpha[0];
-                        o[2 * dp][2] *= alpha[1];
-                        o[2 * dp][3] *= alpha[1];
-                        o[2 * dp + 1][0] *= alpha[0];
-                        o[2 * dp + 1][1] *= alpha[0];
-                        o[2 * dp + 1][2] *= alpha[1];
-                        o[2 * dp + 1][3] *= alpha[1];
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(va + dp * 32, b0, b1, b2, b3);
-                        mma_bf16(o[2 * dp], pf, b0, b1);
-                        mma_bf16(o[2 * dp + 1], pf, b2, b3);
+                    for (int dm = 0; dm < D / 16; ++dm) {
+                        o[dm][0] *= alpha[0];
+                        o[dm][1] *= alpha[1];
+                        o[dm][2] *= alpha[0];
+                        o[dm][3] *= alpha[1];
+                        uint32_t va4[4];
+                        ldsm_x4_t(va + dm * 32, va4[0], va4[1], va4[2], va4[3]);
+                        mma_bf16(o[dm], va4, pb0, pb1);
                     }
                 }
                 if (!CONV) {
@@ -299,38 +299,44 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
             }
             // ---- results of this warp's rows ----
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-                l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+            for (int j = 0; j < 2; ++j) {
+                l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+                l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+                l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
             }
-            if (!s_abort) {
+            // (warp-uniform: the movmatrix below is warp-collective)
+            if (!__any_sync(0xffffffffu, s_abort != 0) && head_ok) {
                 if (w.num_splits == 1) {
+                    // normalise per column, transpose each 8x8 block back to rows: thread then
+                    // holds row rb + g8, dims 2*q4, 2*q4+1 of the block (32-bit stores)
+                    const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
+                    const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
+                    __nv_bfloat16* dst = a.out + ((size_t)(q_start + (rvb ? Rb / G : 0)) * a.num_q_heads + head * G +
+                                                  (rvb ? Rb % G : 0)) * D;
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if (!rv[e]) continue;
-                        const int R = g8 + e * 8;
-                        const float inv = l_run[e] > 0.f ? 1.f / l_run[e] : 0.f;
-                        __nv_bfloat16* dst =
-                            a.out + ((size_t)(q_start + R / G) * a.num_q_heads + head * G + R % G) * D;
-#pragma unroll
-                        for (int dt = 0; dt < D / 8; ++dt)
-                            *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * q4) =
-                                pack_bf16(o[dt][2 * e] * inv, o[dt][2 * e + 1] * inv);
+                    for (int dm = 0; dm < D / 16; ++dm) {
+                        const uint32_t t0 = movmatrix_t(pack_bf16(o[dm][0] * inv0, o[dm][1] * inv1));
+                        const uint32_t t1 = movmatrix_t(pack_bf16(o[dm][2] * inv0, o[dm][3] * inv1));
+                        if (rvb) {
+                            *reinterpret_cast<uint32_t*>(dst + dm * 16 + 2 * q4) = t0;
+                            *reinterpret_cast<uint32_t*>(dst + dm * 16 + 8 + 2 * q4) = t1;
+                        }
                     }
                 } else {
                     float* po = a.partial_o + (size_t)self * (a.decode_heads * 16 * D);
                     float* pml = a.partial_ml + (size_t)self * (a.decode_heads * 16 * 2);
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if (!rv[e]) continue;
-                        const int r = warp * 16 + g8 + e * 8;
+                    for (int j = 0; j < 2; ++j) {
+                        if (!rv[j]) continue;
+                        const int r = warp * 16 + rb + 2 * q4 + j;
 #pragma unroll
-                        for (int dt = 0; dt < D / 8; ++dt)
-                            *reinterpret_cast<float2*>(po + (size_t)r * D + dt * 8 + 2 * q4) =
-                                make_float2(o[dt][2 * e], o[dt][2 * e + 1]);
-                        if (q4 == 0) {
-                            pml[r * 2] = m_run[e];
-                            pml[r * 2 + 1] = l_run[e];
+                        for (int dm = 0; dm < D / 16; ++dm) {
+                            po[(size_t)r * D + dm * 16 + g8] = o[dm][j];
+                            po[(size_t)r * D + dm * 16 + 8 + g8] = o[dm][2 + j];
+                        }
+                        if (g8 == 0) {
+                            pml[r * 2] = m_run[j];
+                            pml[r * 2 + 1] = l_run[j];
                         }
                     }
                 }
@@ -349,7 +355,7 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
         __threadfence();
         if (!producer && warp < seg_heads) {
             const int head = h0 + warp;
-            for (int R = 0; R < min(n_rows, 16); ++R) {
+            for (int R = w.row_begin; R < min(n_rows, w.row_begin + kDecodeRows); ++R) {
                 const int row = warp * 16 + R;
                 float M = -INFINITY;
                 for (int sp = 0; sp < w.num_splits; ++sp)

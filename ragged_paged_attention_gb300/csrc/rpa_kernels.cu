@@ -4,7 +4,8 @@
 // One rpa_forward call = plan kernel + attention kernel(s), all on the caller's stream:
 //   * rpa_plan_kernel reads the device metadata (num_seqs, cu_q_lens, kv_lens),
 //     validates it, and writes two work lists into the workspace: "decode" items
-//     (sequences whose q_len * G rows fit one 16-row tile, split along the keys) and
+//     (sequences whose q_len * G rows fit one 16-row tile, split along the keys and, past
+//     8 rows, into two 8-row halves) and
 //     "prefill" items (128-row tiles of one KV head over the whole causal key range)
 //     (prefill items are 128 rows of one KV head: kPrefillRows).
 //   * the prefill items run on tcgen05/TMEM (rpa_prefill_tc.cu), the decode items on
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
         int ql, kl, klo;
         if (seq_shape(a, s, ql, kl) && ql >= 1 && ql * G <= 16) {
             klo = decode_key_begin(a, ql, kl);
-            dec_keys += (long long)(kl - klo) * n_groups;
+            dec_keys += (long long)(kl - klo) * n_groups * cdiv(ql * G, kDecodeRows);
         }
     }
     for (int o = 16; o > 0; o >>= 1) dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
@@ -67,13 +68,14 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     int dec_base = 0, pre_base = 0;
     for (int s0 = 0; s0 < num; s0 += blockDim.x) {
         const int s = s0 + tid;
-        int ql = 0, kl = 0, nd = 0, np = 0, klo = 0, nsplit = 0;
+        int ql = 0, kl = 0, nd = 0, np = 0, klo = 0, nsplit = 0, nrh = 0;
         bool ok = s < num && seq_shape(a, s, ql, kl);
         if (ok && ql >= 1) {
             if (ql * G <= 16) {
                 klo = decode_key_begin(a, ql, kl);
                 nsplit = cdiv(kl - klo, chunk);
-                nd = nsplit * n_groups;
+                nrh = cdiv(ql * G, kDecodeRows);
+                nd = nsplit * n_groups * nrh;
             } else {
                 np = cdiv(ql * G, kPrefillRows) * a.num_kv_heads;
             }
@@ -81,19 +83,20 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
         int tot_d, tot_p;
         const int od = block_exclusive_scan(nd, scan_scratch, &tot_d) + dec_base;
         const int op = block_exclusive_scan(np, scan_scratch, &tot_p) + pre_base;
-        for (int g = 0; g < n_groups && nd; ++g) {
+        for (int gh = 0; gh < n_groups * nrh && nd; ++gh) {
+            const int g = gh / nrh, rh = gh % nrh;
             for (int i = 0; i < nsplit; ++i) {
-                const int it = od + g * nsplit + i;
+                const int it = od + gh * nsplit + i;
                 if (it >= a.max_dec_items) break;  // cannot happen: the host bound covers it
                 WorkItem w;
                 w.seq = s;
                 w.head = g * a.decode_heads;
                 w.key_begin = klo + i * chunk;
                 w.key_end = min(kl, klo + (i + 1) * chunk);
-                w.first_item = od + g * nsplit;
+                w.first_item = od + gh * nsplit;
                 w.num_splits = nsplit;
                 w.split = i;
-                w.row_begin = 0;
+                w.row_begin = rh * kDecodeRows;
                 a.dec_items[it] = w;
                 a.tickets[it] = 0;
             }
