@@ -15,8 +15,8 @@
 //     P^T moved into B-fragment layout by movmatrix; the online softmax runs per column
 //     (a query row) across the 8 lanes that share it.  Half the tensor-core work and
 //     half the accumulator registers of rows-on-M tiles, whose 16 rows would be mostly
-//     padding; fp8 (or scaled bf16) K/V are first dequantised by the warp into its own
-//     bf16 rows as bf16(float(x) * scale);
+//     padding; fp8 (or scaled bf16) K/V are dequantised by the warp into its own bf16
+//     rows as bf16(float(x) * scale): K first, then (after QK) V into the same rows;
 //   * slots past kv_len are never copied: the stage memory is zeroed once at start, so
 //     a skipped row holds finite data whose probability is exactly zero.
 // Items split the keys of a sequence (flash-decoding); split partials (m, l, O) are
@@ -33,9 +33,12 @@ struct DecTile {
     static constexpr int kSeg = HG * 2 * D * ESZ;        // bytes of one token's segment
     static constexpr int kRow = kSeg + 16;               // padded shared-memory row
     static constexpr int kStage = BK * kRow;
-    static constexpr int kConvRow = 2 * D * 2 + 16;      // one head's K|V in bf16, padded
+    static constexpr int kConvRow = D * 2 + 16;          // one head's K (then V) in bf16, padded
     static constexpr int kConv = CONV ? HG * BK * kConvRow : 0;
-    static constexpr int kBudget = 104 * 1024;           // two CTAs per SM
+    // shared memory per CTA: two stages and (fp8) the conversion rows fit four fp8 or three
+    // bf16 CTAs on an SM (with ~150 / ~95 registers a thread); measured on the Gemma-2 and
+    // Llama decode batches, occupancy beats deeper rings here
+    static constexpr int kBudget = CONV ? 56 * 1024 : 72 * 1024;
     static constexpr int kFit = (kBudget - kConv) / kStage;
     static constexpr int STAGES = kFit < 2 ? 2 : (kFit > 4 ? 4 : kFit);
     static constexpr int kBarOff = STAGES * kStage + kConv;
@@ -210,27 +213,28 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                 const uint8_t* stg = stages + st * T::kStage;
                 uint32_t kbase, vbase;
                 int rowb;
-                if (CONV) {
-                    uint8_t* cb = conv + warp * BK * T::kConvRow;
-                    if (head_ok) {
-                        constexpr int kChunks = 2 * D / 8;  // 8-element chunks of K|V per key
+                uint8_t* cb = conv + warp * BK * T::kConvRow;
+                // CONV: dequantise 16 rows of K (part 0) or V (part 1) of this warp's head into cb
+                auto convert = [&](int part) {
+                    constexpr int kChunks = D / 8;  // 8-element chunks of K or V per key
+                    const float sc = part == 0 ? a.k_scale_or_one : a.v_scale_or_one;
 #pragma unroll 4
-                        for (int i = lane; i < BK * kChunks; i += 32) {
-                            const int kk = i / kChunks, c = i % kChunks;
-                            const float sc = c < D / 8 ? a.k_scale_or_one : a.v_scale_or_one;
-                            *reinterpret_cast<uint4*>(cb + kk * T::kConvRow + c * 16) =
-                                dequant8<ESZ>(stg + kk * T::kRow + (warp * 2 * D + c * 8) * ESZ, sc);
-                        }
+                    for (int i = lane; i < BK * kChunks; i += 32) {
+                        const int kk = i / kChunks, c = i % kChunks;
+                        *reinterpret_cast<uint4*>(cb + kk * T::kConvRow + c * 16) =
+                            dequant8<ESZ>(stg + kk * T::kRow + (warp * 2 * D + part * D + c * 8) * ESZ, sc);
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);  // the stage is free once converted
-                    kbase = smem_u32(cb);
+                };
+                if (CONV) {
+                    if (head_ok) convert(0);
+                    kbase = vbase = smem_u32(cb);
                     rowb = T::kConvRow;
                 } else {
                     kbase = smem_u32(stg) + warp * 2 * D * 2;
+                    vbase = kbase + D * 2;
                     rowb = T::kRow;
                 }
-                vbase = kbase + D * 2;
                 if (head_ok) {
                     const int key0 = kb + blk * BK;
                     // S^T [16 keys x 8 rows] = K Q^T; A = K rows (ldmatrix: keys 0-7 / 8-15, dims 0-7 / 8-15)
@@ -243,6 +247,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                             ldsm_x4(ka + ks * 32, ka4[0], ka4[1], ka4[2], ka4[3]);
                             mma_bf16(sc, ka4, qb[ks][0], qb[ks][1]);
                         }
+                    }
+                    if (CONV) {
+                        __syncwarp();  // every lane is done reading K out of cb
+                        convert(1);
                     }
                     // sc[e]: key g8 + 8*(e>>1), row 2*q4 + (e&1)
                     float mx[2] = {-INFINITY, -INFINITY};
@@ -292,10 +300,8 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         mma_bf16(o[dm], va4, pb0, pb1);
                     }
                 }
-                if (!CONV) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);  // (CONV: free once V was converted)
             }
             // ---- results of this warp's rows ----
 #pragma unroll
