@@ -389,26 +389,30 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             if (lane == 0) {
                 constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
                 constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, false, true);
-                const uint32_t q_base = smem_u32(smem);
+                // descriptors of the operand bases; a byte offset d within shared memory adds
+                // d >> 4 to the start-address field (no carry: every address is below 256 KB)
+                const uint64_t qdesc = umma_desc_sw128(smem_u32(smem), 16, 1024);
+                const uint64_t kdesc = umma_desc_sw128(smem_u32(smem + T::kOffK), 16, 1024);
+                const uint64_t pdesc = umma_desc_sw128(smem_u32(smem + T::kOffP), 16, 1024);
+                const uint64_t vdesc = umma_desc_sw128(smem_u32(smem + T::kOffV), T::kPanel, 1024);
                 bool ok = mbar_wait(q_full, iph, err);
                 tc_fence_after();
                 // issue QK(next) and PV(next) in whichever order their inputs become ready:
                 // QK needs its K block and a free score buffer, PV its P tile and V block
                 int nq = 0, np = 0;
                 unsigned long long t0 = 0;
+                uint32_t idle = 0;
                 while (ok && np < nb) {
                     bool moved = false;
                     if (nq < nb) {
                         const uint32_t q = jb + nq, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
                         if (mbar_test(&k_full[slot], par) && mbar_test(&s_empty[sb], sp ^ 1)) {
                             tc_fence_after();
-                            const uint32_t k_base = smem_u32(smem + T::kOffK + slot * T::kStage);
+                            const uint64_t kb0 = kdesc + (uint64_t)((slot * T::kStage) >> 4);
 #pragma unroll
-                            for (int ks = 0; ks < D / 16; ++ks) {
-                                const uint64_t ad = umma_desc_sw128(q_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                                const uint64_t bd = umma_desc_sw128(k_base + (ks >> 2) * T::kPanel + (ks & 3) * 32, 16, 1024);
-                                umma_bf16(tmem + sb * BK, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
-                            }
+                            for (int ks = 0; ks < D / 16; ++ks)
+                                umma_bf16(tmem + sb * BK, qdesc + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                          kb0 + (((ks >> 2) * T::kPanel + (ks & 3) * 32) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
                             umma_commit(&s_full[sb]);
                             umma_commit(&k_empty[slot]);
                             ++nq;
@@ -419,27 +423,30 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                         const uint32_t q = jb + np, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
                         if (mbar_test(&p_full[sb], sp) && mbar_test(&v_full[slot], par)) {
                             tc_fence_after();
-                            const uint32_t p_base = smem_u32(smem + T::kOffP + sb * T::kP);
-                            const uint32_t v_base = smem_u32(smem + T::kOffV + slot * T::kStage);
+                            const uint64_t pb0 = pdesc + (uint64_t)((sb * T::kP) >> 4);
+                            const uint64_t vb0 = vdesc + (uint64_t)((slot * T::kStage) >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk) {
-                                const uint64_t ad = umma_desc_sw128(p_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                                const uint64_t bd = umma_desc_sw128(v_base + kk * 16 * 128, T::kPanel, 1024);
-                                umma_bf16(tmem + T::kColO, ad, bd, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
-                            }
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                umma_bf16(tmem + T::kColO, pb0 + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                                          vb0 + ((kk * 16 * 128) >> 4), idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
                             umma_commit(&p_empty[sb]);
                             umma_commit(&v_empty[slot]);
                             ++np;
                             moved = true;
                         }
                     }
+                    // the wait limit is checked every 256 idle polls (the clock read is not free)
                     if (moved) {
                         t0 = 0;
-                    } else if (t0 == 0) {
-                        t0 = global_ns();
-                    } else if (global_ns() - t0 > kWaitLimitNs) {
-                        set_error(err, RPA_DEV_ERR_TIMEOUT);
-                        ok = false;
+                        idle = 0;
+                    } else if (++idle == 256) {
+                        idle = 0;
+                        if (t0 == 0) {
+                            t0 = global_ns();
+                        } else if (global_ns() - t0 > kWaitLimitNs) {
+                            set_error(err, RPA_DEV_ERR_TIMEOUT);
+                            ok = false;
+                        }
                     }
                 }
                 umma_commit(o_full);
