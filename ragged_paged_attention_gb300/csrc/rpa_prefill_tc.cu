@@ -7,8 +7,8 @@
 //   * producers gather the item's Q rows and, per key block, the K
 //     and V rows of that KV head page by page into 128-byte-swizzled K-major panels.
 //     bf16 caches go by TMA (one 3-D tensor copy per page-sized box and 64-wide panel,
-//     issued by the lanes of warp 4, pages looked up one block ahead; the partial last
-//     page is copied by that warp through registers); fp8 / scaled
+//     issued by the lanes of two warps per operand, pages looked up one block ahead; the
+//     partial last page is copied by those warps through registers); fp8 / scaled
 //     caches go through registers in warps 4-7 and are dequantised there as
 //     bf16(float(x) * scale).  Rows past the key range are never copied: the stage
 //     memory is zeroed at start, so such rows hold finite data with zero probability;
@@ -134,7 +134,7 @@ __device__ __forceinline__ uint4 kv_chunk(const uint8_t* row, int c, float sc) {
 }
 
 template <bool TMA>
-constexpr int prefill_warps() { return 8 + (TMA ? 2 : 4) + 1; }  // softmax, producers (K, V), MMA
+constexpr int prefill_warps() { return 8 + 4 + 1; }  // softmax, producers (2 for K, 2 for V), MMA
 
 template <int D, bool FP8, bool SCALE, bool TMA>
 __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint64_t* fin = bars + 4 * NS + 10;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + T::kOffRed);
-    // producer warps [8, kProdW1): the first half streams K, the second half V; then the MMA warp
-    constexpr int kProdW0 = 8, kProdW1 = TMA ? 10 : 12, kMmaW = kProdW1;
+    // producer warps [8, 12): warps 8-9 stream K, 10-11 V; then the MMA warp
+    constexpr int kProdW0 = 8, kProdW1 = 12, kMmaW = kProdW1;
     // (no static shared variables: with the 1024-byte aligned dynamic block they would
     // round up to 1 KB and push the kernel past the 227 KB limit)
     WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + T::kOffItem);
@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&k_full[i], TMA ? 32 : 64);  // the warp(s) streaming K
+            mbar_init(&k_full[i], 64);  // the two warps streaming K
             mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], TMA ? 32 : 64);
+            mbar_init(&v_full[i], 64);
             mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -256,11 +256,15 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 mbar_arrive(q_full);
             }
             if (TMA) {
-                // warp 8 streams K, warp 9 streams V.  Lane l owns box l (box_rows keys of one
-                // page, box_rows >= 8) of every block; its page is looked up one block ahead.
-                // Full boxes are one TMA per panel; the rows of a partial last box are copied
-                // by the warp through registers.  Each full barrier takes TMA bytes + 32 arrivals.
-                const int part = warp - kProdW0;
+                // warps 8-9 stream K, 10-11 V, each warp half of the 64-wide panels (a TMA
+                // issue costs ~65 cycles and is serial within a warp, so small page boxes need
+                // several issuing warps).  Lane l owns box l (box_rows keys of one page,
+                // box_rows >= 8) of every block; its page is looked up one block ahead.  Full
+                // boxes are one TMA per panel; the rows of a partial last box are copied by the
+                // warp through registers.  Each full barrier takes TMA bytes + 64 arrivals.
+                const int part = (warp - kProdW0) >> 1, pw = (warp - kProdW0) & 1;
+                constexpr int kPW = (T::DP + 1) / 2;  // panels per warp
+                const int p0 = pw * kPW, p1 = min(T::DP, p0 + kPW);
                 uint64_t* fbar = part ? v_full : k_full;
                 uint64_t* ebar = part ? v_empty : k_empty;
                 const int nbox = BK / box_rows;
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                         rows = 0;
                     }
                     const bool full = rows == box_rows;
-                    uint32_t bytes = full ? (uint32_t)box_rows * T::DP * 128 : 0u;
+                    uint32_t bytes = full ? (uint32_t)box_rows * (p1 - p0) * 128 : 0u;
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
                     const int z0 = page * a.page_size + kbx % a.page_size;
@@ -298,26 +302,28 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     if (!__shfl_sync(0xffffffffu, g, 0)) break;
                     uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
                     if (full) {
-#pragma unroll
-                        for (int p = 0; p < T::DP; ++p)
+                        for (int p = p0; p < p1; ++p)
                             tma_load_3d(smem_u32(stage + p * T::kPanel + lane * box_rows * 128), &tm_kv, 64 * p,
                                         2 * kvh + part, z0, &fbar[slot]);
                     }
-                    uint32_t pm = pmask;
+                    uint32_t pm = p1 > p0 ? pmask : 0u;
+                    const bool wrote = pm != 0;
                     while (pm) {
                         const int src_lane = __ffs(pm) - 1;
                         pm &= pm - 1;
                         const int prow = __shfl_sync(0xffffffffu, rows, src_lane);
                         const int pz0 = __shfl_sync(0xffffffffu, z0, src_lane);
-                        for (int i = lane; i < prow * (D / 8); i += 32) {
-                            const int t = i / (D / 8), c = i % (D / 8);
+                        constexpr int kCh = kPW * 8;  // this warp's 16-byte chunks of a row
+                        for (int i = lane; i < prow * kCh; i += 32) {
+                            const int t = i / kCh, c = p0 * 8 + i % kCh;
+                            if (c >= D / 8) continue;
                             const int kk = src_lane * box_rows + t;
                             const uint4 v = __ldg(reinterpret_cast<const uint4*>(
                                 kvp + ((size_t)(pz0 + t) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
                             *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) = v;
                         }
                     }
-                    fence_proxy_async_smem();
+                    if (wrote) fence_proxy_async_smem();  // register-written rows, read by the tensor core
                     mbar_arrive(&fbar[slot]);
                 }
             } else {
