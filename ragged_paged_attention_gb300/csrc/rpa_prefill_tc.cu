@@ -19,11 +19,13 @@
 //     shared memory): scale, soft cap, mask (only on blocks that cross a row's causal or
 //     window limit), online softmax in the log2 domain with lazy rescaling (the running
 //     max only moves when it grows by more than 2^8, and then O is rescaled in TMEM),
-//     P written as bf16 panels; at the end they read O, divide by l, store bf16 rows.
+//     P written as bf16 pairs into TMEM over the first half of the block's score buffer
+//     (PV reads its A operand from TMEM, so shared memory holds only Q and the K/V rings);
+//     at the end they read O, divide by l, store bf16 rows.
 // Barriers: k_full/k_empty and v_full/v_empty (producers <-> MMA; separate K and V rings
-// of NS stages, so a K slot frees as soon as its QK is done), s_full/s_empty (MMA <->
-// softmax, per score buffer), p_full/p_empty (softmax <-> MMA, per P buffer), q_full,
-// o_full.  Blocks are 128 keys (64 for D = 256); producers run up to two blocks ahead.
+// of NS stages, so a K slot frees as soon as its QK is done), s_full (MMA -> softmax, per
+// score buffer), p_full/p_empty (softmax <-> MMA per buffer; a buffer takes the next QK
+// once PV has read its P), q_full, o_full.  Blocks are 128 keys (64 for D = 256).
 // Every wait is bounded (common.cuh); on a timeout the CTA records an error and stops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -38,24 +40,25 @@ template <int D>
 struct PreTc {
     static constexpr int BK = D >= 256 ? 64 : 128;       // keys per block
     static constexpr int DP = D / 64;                    // 64-wide panels of the head dim
-    static constexpr int KP = BK / 64;                   // 64-wide panels of the key dim (P tile)
-    static constexpr int NS = 2;                         // stages of the K ring and of the V ring
     static constexpr int kQ = DP * 128 * 128;            // Q tile: DP panels of [128 rows x 128 B]
     static constexpr int kPanel = BK * 128;              // one K or V panel: [BK rows x 128 B]
     static constexpr int kStage = DP * kPanel;           // K (or V) of one block
-    static constexpr int kP = KP * 128 * 128;            // P tile: KP panels of [128 rows x 64 keys]
+    // stages of the K ring and of the V ring: as many as fit (P lives in TMEM)
+    static constexpr int kFitNS = (232448 - kQ - 2560) / (2 * kStage);  // 2.5 KB: barriers, scratch
+    static constexpr int NS = kFitNS > 4 ? 4 : kFitNS;
     static constexpr int kOffK = kQ;
     static constexpr int kOffV = kOffK + NS * kStage;
-    static constexpr int kOffP = kOffV + NS * kStage;
-    static constexpr int kOffBar = kOffP + 2 * kP;
-    static constexpr int kNumBars = 4 * NS + 11;
+    static constexpr int kOffBar = kOffV + NS * kStage;
+    static constexpr int kNumBars = 4 * NS + 9;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
     static constexpr int kOffItem = kOffRed + 2 * 2 * 128 * 4;            // WorkItem (16-byte aligned) + abort flag
     static constexpr int kSmem = kOffItem + 48;
     static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
-    static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle-atom alignment");
-    static constexpr int kColO = 2 * BK;                 // TMEM: S buffers at 0 and BK, O after
+    static_assert(NS >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
+    // TMEM: S buffers at 0 and BK (P, bf16 pairs, over the first BK/2 columns of its block's
+    // buffer once the softmax has read it), O after
+    static constexpr int kColO = 2 * BK;
     static constexpr int kTmemCols = kColO + D <= 256 ? 256 : 512;
     static constexpr int kSoftWarps = 8;                 // two per TMEM lane quarter (column halves)
     static constexpr int kHalf = BK / 2;                 // score columns per softmax warp
@@ -149,13 +152,12 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint64_t* k_empty = bars + NS;        // [NS]  QK of that block done
     uint64_t* v_full = bars + 2 * NS;     // [NS]  V block landed
     uint64_t* v_empty = bars + 3 * NS;    // [NS]  PV of that block done
-    uint64_t* s_full = bars + 4 * NS;     // [2]   S buffer written by QK
-    uint64_t* s_empty = bars + 4 * NS + 2;  // [2] S buffer read by the softmax
-    uint64_t* p_full = bars + 4 * NS + 4;   // [2] P buffer written (and O rescaled)
-    uint64_t* p_empty = bars + 4 * NS + 6;  // [2] PV of that P buffer done
-    uint64_t* q_full = bars + 4 * NS + 8;
-    uint64_t* o_full = bars + 4 * NS + 9;
-    uint64_t* fin = bars + 4 * NS + 10;
+    uint64_t* s_full = bars + 4 * NS;       // [2] S buffer written by QK
+    uint64_t* p_full = bars + 4 * NS + 2;   // [2] P written over that buffer (and O rescaled)
+    uint64_t* p_empty = bars + 4 * NS + 4;  // [2] PV of that buffer's P done (buffer free again)
+    uint64_t* q_full = bars + 4 * NS + 6;
+    uint64_t* o_full = bars + 4 * NS + 7;
+    uint64_t* fin = bars + 4 * NS + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + T::kOffRed);
     // producer warps [8, 12): warps 8-9 stream K, 10-11 V; then the MMA warp
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     const uint8_t* kvp = static_cast<const uint8_t*>(a.kv_pages);
 
     // zero Q and the K/V stages once: rows no copy ever writes stay finite
-    for (int i = tid * 16; i < T::kOffP; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
+    for (int i = tid * 16; i < T::kOffBar; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -184,7 +186,6 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 256);
             mbar_init(&p_full[i], 256);
             mbar_init(&p_empty[i], 1);
         }
@@ -399,7 +400,6 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 // d >> 4 to the start-address field (no carry: every address is below 256 KB)
                 const uint64_t qdesc = umma_desc_sw128(smem_u32(smem), 16, 1024);
                 const uint64_t kdesc = umma_desc_sw128(smem_u32(smem + T::kOffK), 16, 1024);
-                const uint64_t pdesc = umma_desc_sw128(smem_u32(smem + T::kOffP), 16, 1024);
                 const uint64_t vdesc = umma_desc_sw128(smem_u32(smem + T::kOffV), T::kPanel, 1024);
                 bool ok = mbar_wait(q_full, iph, err);
                 tc_fence_after();
@@ -412,7 +412,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     bool moved = false;
                     if (nq < nb) {
                         const uint32_t q = jb + nq, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
-                        if (mbar_test(&k_full[slot], par) && mbar_test(&s_empty[sb], sp ^ 1)) {
+                        // the score buffer is free once PV two blocks back has read its P
+                        if (mbar_test(&k_full[slot], par) && mbar_test(&p_empty[sb], sp ^ 1)) {
                             tc_fence_after();
                             const uint64_t kb0 = kdesc + (uint64_t)((slot * T::kStage) >> 4);
 #pragma unroll
@@ -429,12 +430,11 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                         const uint32_t q = jb + np, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
                         if (mbar_test(&p_full[sb], sp) && mbar_test(&v_full[slot], par)) {
                             tc_fence_after();
-                            const uint64_t pb0 = pdesc + (uint64_t)((sb * T::kP) >> 4);
                             const uint64_t vb0 = vdesc + (uint64_t)((slot * T::kStage) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < BK / 16; ++kk)
-                                umma_bf16(tmem + T::kColO, pb0 + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
-                                          vb0 + ((kk * 16 * 128) >> 4), idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                                umma_bf16_ta(tmem + T::kColO, tmem + sb * BK + kk * 8, vb0 + ((kk * 16 * 128) >> 4), idesc_pv,
+                                             (np > 0 || kk > 0) ? 1u : 0u);
                             umma_commit(&p_empty[sb]);
                             umma_commit(&v_empty[slot]);
                             ++np;
@@ -487,7 +487,6 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     for (int i = 0; i < 32; ++i) x[c * 32 + i] = t32[i];
                 }
                 tc_fence_before();
-                mbar_arrive(&s_empty[slot]);
                 const int key0 = kb + j * BK + half * HB;
                 if (cap != 0.f) {
 #pragma unroll
@@ -510,7 +509,9 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 for (int i = 0; i < HB; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
                 float* red_j = red + (q & 1) * 256;
                 red_j[half * 128 + r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                // the pair barrier also orders both halves' S reads before either writes P over them
                 asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                tc_fence_after();
                 const float mx = fmaxf(red_j[r], red_j[128 + r]);
                 float alpha = 1.f;
                 const bool had = m_use > -INFINITY;  // O already holds earlier blocks of this row
@@ -520,25 +521,19 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     m_use = mx;
                 }
                 const float mu = m_use == -INFINITY ? 0.f : m_use;
-                // the P buffer of this slot is free once PV two blocks back has finished
-                if (!mbar_wait(&p_empty[slot], par ^ 1, err)) {
-                    ok = false;
-                    break;
-                }
+                // P (bf16 pairs) over the first half of this block's score buffer: this warp's
+                // HB keys are TMEM columns slot * BK + half * HB / 2 ..
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint8_t* prow = smem + T::kOffP + slot * T::kP + r * 128;
 #pragma unroll
-                for (int cc = 0; cc < HB / 8; ++cc) {
-                    const int c = half * (HB / 8) + cc;  // 16-byte chunk of the row's BK keys
-                    uint32_t w4[4];
+                for (int c16 = 0; c16 < HB / 32; ++c16) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = fast_exp2(x[cc * 8 + 2 * e] - mu), p1 = fast_exp2(x[cc * 8 + 2 * e + 1] - mu);
-                        sum4[e] += p0 + p1;
-                        w4[e] = pack_bf16(p0, p1);
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = fast_exp2(x[c16 * 32 + 2 * e] - mu), p1 = fast_exp2(x[c16 * 32 + 2 * e + 1] - mu);
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
                     }
-                    *reinterpret_cast<uint4*>(prow + (c >> 3) * 16384 + (((c & 7) ^ (r & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    tmem_st16_nowait(tmem + lane_off + slot * BK + half * (HB / 2) + c16 * 16, pk);
                 }
                 // O already holds this row's earlier blocks when l was positive before
                 const bool row_rescale = rescale && had;
@@ -563,7 +558,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                         tmem_st32(tmem + lane_off + col, o32);
                     }
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[slot]);
             }
