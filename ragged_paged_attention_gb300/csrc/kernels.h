@@ -14,6 +14,7 @@ struct WsHeader;
 constexpr int kMaxDecodeHeads = 4;      // most KV heads a decode CTA covers (one warp each)
 constexpr int kDecodeBK = 16;           // keys per decode pipeline stage
 constexpr int kDecodeRows = 8;          // query rows (q_len x G) per decode item (mma N)
+constexpr int kCuCache = 4096;          // cu_q_lens entries the cache-write kernels stage in shared memory
 constexpr int kPrefillRows = 128;       // (token, q-head) rows per prefill item (one TMEM tile)
 constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
 constexpr int kDecodeTargetCtas = 1024; // split so decode work spreads over about this many CTAs
@@ -172,6 +173,17 @@ __device__ __forceinline__ bool seq_shape(const RpaArgs& a, int s, int& ql, int&
         return false;
     }
     return true;
+}
+
+// Sequence of token t: the last s in [0, num) with cu[s] <= t (cu = cu_q_lens, in global or
+// shared memory; callers check that t really lies in [cu[s], cu[s+1])).
+__device__ __forceinline__ int seq_of_token(const int32_t* cu, int num, int t) {
+    int lo = 0, hi = num - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 // First key any query of a decode-class sequence can see (aligned down to a stage).

@@ -24,6 +24,7 @@ namespace rpa {
 // MLA cache update: one warp per token, 16-byte copies, rope pad written as zeros
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) {
+    extern __shared__ int s_cu[];  // cu_q_lens[0..num] when it fits (kCuCache entries)
     __shared__ int s_num;
     if (threadIdx.x == 0) {
         int n = a.distribution[2];
@@ -37,18 +38,19 @@ __global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) {
     __syncthreads();
     const int num = s_num;
     if (num == 0) return;
-    const int total = a.cu_q_lens[num];
+    // one global round trip for the metadata the per-token search reads
+    const bool cached = num + 1 <= kCuCache;
+    if (cached)
+        for (int i = threadIdx.x; i <= num; i += blockDim.x) s_cu[i] = a.cu_q_lens[i];
+    __syncthreads();
+    const int32_t* cu = cached ? s_cu : a.cu_q_lens;
+    const int total = cu[num];
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int kv_chunks = a.lkv_pad / 8, pe_chunks = a.r_pad / 8;
     for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < min(total, a.max_num_tokens); t += gridDim.x * warps) {
-        int lo = 0, hi = num - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.cu_q_lens[mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        const int s = lo;
-        const int q_start = a.cu_q_lens[s], q_len = a.cu_q_lens[s + 1] - q_start, kv_len = a.kv_lens[s];
+        const int s = seq_of_token(cu, num, t);
+        const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = a.kv_lens[s];
         if (t < q_start || t >= q_start + q_len) continue;
         if (q_len > kv_len) {
             if (lane == 0) set_error(a.err, RPA_DEV_ERR_Q_LEN);
@@ -65,17 +67,27 @@ __global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) {
             continue;
         }
         const size_t slot = (size_t)page * a.page_size + pos % a.page_size;
-        for (int c = lane; c < kv_chunks + pe_chunks; c += 32) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (c < kv_chunks) {
-                if (c * 8 < a.lkv_dim)
-                    v = __ldg(reinterpret_cast<const uint4*>(a.new_kv_c + (size_t)t * a.lkv_dim + c * 8));
-                *reinterpret_cast<uint4*>(a.cache_kv_c + slot * a.lkv_pad + c * 8) = v;
-            } else {
-                const int cc = c - kv_chunks;
-                if (cc * 8 < a.r_dim)
-                    v = __ldg(reinterpret_cast<const uint4*>(a.new_k_pe + (size_t)t * a.r_dim + cc * 8));
-                *reinterpret_cast<uint4*>(a.cache_k_pe + slot * a.r_pad + cc * 8) = v;
+        // up to 4 chunks per lane in flight: all loads of a batch before its stores
+        for (int c0 = lane; c0 < kv_chunks + pe_chunks; c0 += 32 * 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + 32 * j;
+                v[j] = make_uint4(0, 0, 0, 0);
+                if (c < kv_chunks) {
+                    if (c * 8 < a.lkv_dim) v[j] = __ldg(reinterpret_cast<const uint4*>(a.new_kv_c + (size_t)t * a.lkv_dim + c * 8));
+                } else if (c < kv_chunks + pe_chunks) {
+                    const int cc = c - kv_chunks;
+                    if (cc * 8 < a.r_dim) v[j] = __ldg(reinterpret_cast<const uint4*>(a.new_k_pe + (size_t)t * a.r_dim + cc * 8));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + 32 * j;
+                if (c < kv_chunks)
+                    *reinterpret_cast<uint4*>(a.cache_kv_c + slot * a.lkv_pad + c * 8) = v[j];
+                else if (c < kv_chunks + pe_chunks)
+                    *reinterpret_cast<uint4*>(a.cache_k_pe + slot * a.r_pad + (c - kv_chunks) * 8) = v[j];
             }
         }
     }
@@ -196,8 +208,9 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(LatentArgs a) {
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream) {
     const int grid = min(cdiv(a.max_num_tokens, 8), num_sms * 8);
     if (grid <= 0) return cudaSuccess;
+    const int smem = min(a.max_num_seqs + 1, kCuCache) * (int)sizeof(int);
     ProfScope ps("mla_update", stream);
-    mla_update_kernel<<<grid, 256, 0, stream>>>(a);
+    mla_update_kernel<<<grid, 256, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

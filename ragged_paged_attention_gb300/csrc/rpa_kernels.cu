@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     __shared__ long long red[32];
     __shared__ int s_num;
     __shared__ int s_chunk;
+    // per sequence of the current group of blockDim.x: item end offsets and decode shape
+    __shared__ int e_dend[1024], e_pend[1024], e_klo[1024], e_kl[1024], e_ns[1024], e_nrh[1024];
     WsHeader* hdr = a.hdr;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -81,43 +83,66 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
             }
         }
         int tot_d, tot_p;
-        const int od = block_exclusive_scan(nd, scan_scratch, &tot_d) + dec_base;
-        const int op = block_exclusive_scan(np, scan_scratch, &tot_p) + pre_base;
-        for (int gh = 0; gh < n_groups * nrh && nd; ++gh) {
-            const int g = gh / nrh, rh = gh % nrh;
-            for (int i = 0; i < nsplit; ++i) {
-                const int it = od + gh * nsplit + i;
-                if (it >= a.max_dec_items) break;  // cannot happen: the host bound covers it
-                WorkItem w;
-                w.seq = s;
-                w.head = g * a.decode_heads;
-                w.key_begin = klo + i * chunk;
-                w.key_end = min(kl, klo + (i + 1) * chunk);
-                w.first_item = od + gh * nsplit;
-                w.num_splits = nsplit;
-                w.split = i;
-                w.row_begin = rh * kDecodeRows;
-                a.dec_items[it] = w;
-                a.tickets[it] = 0;
+        const int od = block_exclusive_scan(nd, scan_scratch, &tot_d);
+        const int op = block_exclusive_scan(np, scan_scratch, &tot_p);
+        // every thread then emits items: a thread per item, not per sequence (a long prefill
+        // sequence has hundreds); item idx belongs to the first sequence whose end offset
+        // (exclusive prefix + count) exceeds it
+        e_dend[tid] = od + nd;
+        e_pend[tid] = op + np;
+        e_klo[tid] = klo;
+        e_kl[tid] = kl;
+        e_ns[tid] = nsplit;
+        e_nrh[tid] = nrh;
+        __syncthreads();
+        const int nseq = min((int)blockDim.x, num - s0);
+        auto owner = [&](const int* ends, int idx) {
+            int lo = 0, hi = nseq - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (ends[mid] > idx) hi = mid; else lo = mid + 1;
             }
+            return lo;
+        };
+        for (int idx = tid; idx < tot_d; idx += blockDim.x) {
+            const int it = dec_base + idx;
+            if (it >= a.max_dec_items) break;  // cannot happen: the host bound covers it
+            const int k = owner(e_dend, idx);
+            const int ns = e_ns[k], nh = e_nrh[k];
+            const int beg = e_dend[k] - ns * n_groups * nh;
+            const int rel = idx - beg, gh = rel / ns, i = rel - gh * ns;
+            const int g = gh / nh, rh = gh - g * nh;
+            WorkItem w;
+            w.seq = s0 + k;
+            w.head = g * a.decode_heads;
+            w.key_begin = e_klo[k] + i * chunk;
+            w.key_end = min(e_kl[k], e_klo[k] + (i + 1) * chunk);
+            w.first_item = dec_base + beg + gh * ns;
+            w.num_splits = ns;
+            w.split = i;
+            w.row_begin = rh * kDecodeRows;
+            a.dec_items[it] = w;
+            a.tickets[it] = 0;
         }
-        const int tiles = np ? np / a.num_kv_heads : 0;
-        for (int h = 0; h < a.num_kv_heads && np; ++h) {
-            for (int r = 0; r < tiles; ++r) {
-                const int it = op + h * tiles + r;
-                if (it >= a.max_pre_items) break;
-                WorkItem w;
-                w.seq = s;
-                w.head = h;
-                w.row_begin = r * kPrefillRows;
-                w.key_begin = 0;
-                w.key_end = kl;
-                w.first_item = it;
-                w.num_splits = 1;
-                w.split = 0;
-                a.pre_items[it] = w;
-            }
+        for (int idx = tid; idx < tot_p; idx += blockDim.x) {
+            const int it = pre_base + idx;
+            if (it >= a.max_pre_items) break;
+            const int k = owner(e_pend, idx);
+            const int kprev = k > 0 ? e_pend[k - 1] : 0;  // this sequence's items start here
+            const int tiles = (e_pend[k] - kprev) / a.num_kv_heads;
+            const int rel = idx - kprev, h = rel / tiles, r = rel - h * tiles;
+            WorkItem w;
+            w.seq = s0 + k;
+            w.head = h;
+            w.row_begin = r * kPrefillRows;
+            w.key_begin = 0;
+            w.key_end = e_kl[k];
+            w.first_item = it;
+            w.num_splits = 1;
+            w.split = 0;
+            a.pre_items[it] = w;
         }
+        __syncthreads();  // the next group of sequences reuses the e_* arrays
         dec_base += tot_d;
         pre_base += tot_p;
     }
@@ -133,6 +158,7 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
 // Cache write: new K/V rows -> their page slots (16-byte copies, bit exact)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
+    extern __shared__ int s_cu[];  // cu_q_lens[0..num] when it fits (kCuCache entries)
     __shared__ int s_num;
     if (threadIdx.x == 0) {
         int n = a.num_seqs[0];
@@ -145,44 +171,58 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
     __syncthreads();
     const int num = s_num;
     if (num == 0) return;
-    const int total = a.cu_q_lens[num];
+    // one global round trip for the metadata the per-token search reads
+    const bool cached = num + 1 <= kCuCache;
+    if (cached)
+        for (int i = threadIdx.x; i <= num; i += blockDim.x) s_cu[i] = a.cu_q_lens[i];
+    __syncthreads();
+    const int32_t* cu = cached ? s_cu : a.cu_q_lens;
+    const int total = cu[num];
+    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
     const int Hkv = a.num_kv_heads, C = 2 * Hkv;
     const int row_chunks = a.head_dim * a.esz / 16;  // 16-byte chunks per head row
     const int chunks = Hkv * 2 * row_chunks;
-    for (int t = blockIdx.x; t < min(total, a.max_num_tokens); t += gridDim.x) {
-        // sequence of token t: last s with cu_q_lens[s] <= t
-        int lo = 0, hi = num - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.cu_q_lens[mid] <= t) lo = mid; else hi = mid - 1;
-        }
-        const int s = lo;
-        const int q_start = a.cu_q_lens[s], q_len = a.cu_q_lens[s + 1] - q_start, kv_len = a.kv_lens[s];
+    // one warp per token
+    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < min(total, a.max_num_tokens); t += gridDim.x * warps) {
+        const int s = seq_of_token(cu, num, t);
+        const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = a.kv_lens[s];
         if (t < q_start || t >= q_start + q_len) continue;
         if (q_len > kv_len) {
-            if (threadIdx.x == 0) set_error(a.err, RPA_DEV_ERR_Q_LEN);
+            if (lane == 0) set_error(a.err, RPA_DEV_ERR_Q_LEN);
             continue;
         }
         const int pos = kv_len - q_len + (t - q_start);
         if (pos / a.page_size >= a.pages_per_seq) {
-            if (threadIdx.x == 0) set_error(a.err, RPA_DEV_ERR_KV_LEN);
+            if (lane == 0) set_error(a.err, RPA_DEV_ERR_KV_LEN);
             continue;
         }
         const int page = a.page_indices[(size_t)s * a.pages_per_seq + pos / a.page_size];
         if ((unsigned)page >= (unsigned)a.total_num_pages) {
-            if (threadIdx.x == 0) set_error(a.err, RPA_DEV_ERR_PAGE);
+            if (lane == 0) set_error(a.err, RPA_DEV_ERR_PAGE);
             continue;
         }
         uint8_t* slot = static_cast<uint8_t*>(a.kv_pages) +
                         ((size_t)page * a.page_size + pos % a.page_size) * C * a.head_dim * a.esz;
-        for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
-            const int head = i / (2 * row_chunks);
-            const int part = (i / row_chunks) & 1;
-            const int c = i % row_chunks;
-            const uint8_t* src = static_cast<const uint8_t*>(part ? a.new_v : a.new_k) +
-                                 (((size_t)t * Hkv + head) * a.head_dim * a.esz) + c * 16;
-            *reinterpret_cast<uint4*>(slot + ((size_t)(2 * head + part) * a.head_dim * a.esz) + c * 16) =
-                __ldg(reinterpret_cast<const uint4*>(src));
+        // up to 8 chunks per lane in flight: all loads of a batch before its stores
+        for (int i0 = lane; i0 < chunks; i0 += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + 32 * j;
+                if (i < chunks) {
+                    const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
+                    v[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(part ? a.new_v : a.new_k) +
+                                                                 (((size_t)t * Hkv + head) * a.head_dim * a.esz) + c * 16));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + 32 * j;
+                if (i < chunks) {
+                    const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
+                    *reinterpret_cast<uint4*>(slot + ((size_t)(2 * head + part) * a.head_dim * a.esz) + c * 16) = v[j];
+                }
+            }
         }
     }
 }
@@ -204,10 +244,11 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
 }
 
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream) {
-    const int grid = min(a.max_num_tokens, num_sms * 8);
+    const int grid = min(cdiv(a.max_num_tokens, 8), num_sms * 8);
     if (grid <= 0) return cudaSuccess;
+    const int smem = min(a.max_num_seqs + 1, kCuCache) * (int)sizeof(int);
     ProfScope ps("rpa_update", stream);
-    rpa_update_kernel<<<grid, 256, 0, stream>>>(a);
+    rpa_update_kernel<<<grid, 256, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
