@@ -78,6 +78,11 @@ constexpr int kLatDk = 576;       // 512 latent + 64 rope
 constexpr int kLatDv = 512;
 constexpr int kLatMinChunk = 512;
 constexpr int kLatTargetCtas = 512;
+// sparse MLA splits a query's selected keys only down to about this many items in all (half
+// the two-CTA clusters): its per-item cost (Q slice, pipeline fill, fp32 partial and merge)
+// outweighs the extra parallelism on decode-sized batches (64 single-query sequences: 127 us
+// unsplit, 197 us in two splits, 361 us in four; measured)
+constexpr int kSparseTargetCtas = 38;
 
 struct LatentArgs {
     int sparse;                     // 0 = MLA (paged, causal), 1 = DSA sparse
@@ -143,7 +148,7 @@ cudaError_t launch_sparse_attention(const LatentArgs& a, int num_sms, cudaStream
 inline int sparse_num_splits(int batch, int num_queries, int heads, int slots) {
     long long tiles = (long long)batch * num_queries * (heads / kLatRows);
     long long total = tiles * slots;
-    long long chunk = (total + kLatTargetCtas - 1) / kLatTargetCtas;
+    long long chunk = (total + kSparseTargetCtas - 1) / kSparseTargetCtas;
     if (chunk < kLatMinChunk) chunk = kLatMinChunk;
     chunk = (chunk + kLatBK - 1) / kLatBK * kLatBK;
     long long n = (slots + chunk - 1) / chunk;

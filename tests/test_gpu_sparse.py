@@ -60,3 +60,13 @@ def test_sparse_prefill_full_size_sampled(mode):
 def test_sparse_decode_full_size_sampled(mode):
     s = workloads.dsa_sparse(mode=mode, phase="decode")
     run_and_check(s, queries=list(range(0, 64, 5)))
+
+
+def test_sparse_split_merge():
+    # two queries x 4096 selected tokens: far above one item per two-CTA cluster, so each
+    # query's keys are split (8 ways) and the partials merged by the log-sum-exp rule
+    pos = np.array([[8191, 5000]], dtype=np.int32)
+    s = workloads.make_sparse(batch=1, num_queries=2, seq_len=8192, positions=pos, topk=4096, read_block=1, seed=33)
+    # the library's rule: chunk = max(512, ceil(2 * 4096 / 38)) rounded to 64 keys -> 8 splits
+    assert s.indices.shape[-1] * s.read_block > 512
+    run_and_check(s)
