@@ -267,10 +267,9 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     }
                 }
             } else {
-                // register gather: two threads per key row, each half of the row's panels.
-                // The row of the next block is resolved (index -> token -> page) while this
-                // block's slot is still busy; then all of a thread's chunk loads are issued
-                // before any store, so one block costs one memory latency per thread.
+                // row gather: two threads per key row, each half of the row's panels.  The row
+                // of the next block is resolved (index -> token -> page) while this block's slot
+                // is still busy.
                 const int kk = pt >> 1, hh = pt & 1;
                 const int nch = nqp * 4;  // chunks of this thread (20 or 16)
                 auto resolve = [&](int j, bool& v) -> const __nv_bfloat16* {
@@ -301,6 +300,10 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 };
                 bool v_next;
                 const __nv_bfloat16* row_next = resolve(0, v_next);
+                // copies go by cp.async (no register staging): a thread keeps one block's copies
+                // in flight while it issues the next, and publishes a block (proxy fence, arrive)
+                // once that block's copies have landed
+                int prev_st = -1;
                 for (int j = 0; j < nb; ++j) {
                     const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1;
                     const bool v = v_next;
@@ -315,28 +318,32 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         // MLA rope panel (rank 0, panel 4) comes from the k_pe cache row
                         const __nv_bfloat16* pe_row =
                             SPARSE ? nullptr : a.cache_k_pe + (size_t)((row - a.cache_kv_c) / a.lkv_pad) * a.r_pad;
-                        uint4 buf[20];
 #pragma unroll
                         for (int i = 0; i < 20; ++i) {
                             if (i < nch) {
                                 const int c = hh * nch + i, p = c >> 3, cc = c & 7;
                                 const __nv_bfloat16* src = (!SPARSE && rank == 0 && p == 4) ? pe_row + cc * 8
                                                                                            : row + lat_panel_col(rank, p) + cc * 8;
-                                buf[i] = __ldg(reinterpret_cast<const uint4*>(src));
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 20; ++i) {
-                            if (i < nch) {
-                                const int c = hh * nch + i, p = c >> 3, cc = c & 7;
-                                *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((cc ^ (kk & 7)) << 4)) = buf[i];
+                                cp_async16(smem_u32(stage + p * kPanel + kk * 128 + ((cc ^ (kk & 7)) << 4)), src, true);
                             }
                         }
                     }
-                    if (SPARSE && hh == 0) vld[st * BK + kk] = v ? 1 : 0;
+                    cp_async_commit();
+                    if (SPARSE) {
+                        if (hh == 0) vld[st * BK + kk] = v ? 1 : 0;
+                        mbar_arrive(&vld_full[st]);  // (read by the softmax through plain loads)
+                    }
+                    if (prev_st >= 0) {
+                        cp_async_wait<1>();  // the previous block's copies have landed
+                        fence_proxy_async_smem();
+                        mbar_arrive(&kv_full[prev_st]);
+                    }
+                    prev_st = (int)st;
+                }
+                cp_async_wait<0>();
+                if (prev_st >= 0 && !s_abort) {
                     fence_proxy_async_smem();
-                    if (SPARSE) mbar_arrive(&vld_full[st]);
-                    mbar_arrive(&kv_full[st]);
+                    mbar_arrive(&kv_full[prev_st]);
                 }
             }
         } else if (warp == kMmaW) {
