@@ -443,6 +443,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             const int r = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
+            const float cap_k2 = cap != 0.f ? 2.f * kLog2e / cap : 0.f;
             // rows 64*rank.. are owned here; `orow` is the row within the owned (or peer-owned) 64
             const bool owner = (quarter >> 1) == (int)rank;
             const int orow = (quarter & 1) * 32 + lane;
@@ -586,7 +587,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     // scale, soft cap, key validity
                     if (cap != 0.f) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) x[i] = cap * tanhf(x[i] * scale / cap) * kLog2e;
+                        for (int i = 0; i < 32; ++i) x[i] = soft_cap(x[i] * scale, cap, cap_k2) * kLog2e;
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) x[i] *= c_log2;

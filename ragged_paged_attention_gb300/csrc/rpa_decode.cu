@@ -71,9 +71,21 @@ __device__ __forceinline__ uint4 dequant8(const uint8_t* src, float sc) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int D, int HG, int ESZ, bool CONV>
+// 8 e4m3 elements -> 8 f16 (exact, unscaled), packed in a uint4.
+__device__ __forceinline__ uint4 fp8x8_to_f16(const uint8_t* src) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+    return make_uint4(e4m3x2_to_f16x2(h[0]), e4m3x2_to_f16x2(h[1]), e4m3x2_to_f16x2(h[2]), e4m3x2_to_f16x2(h[3]));
+}
+
+// F16 (fp8 caches whose k_scale and v_scale are powers of two): bf16(float(x) * scale) is then
+// exactly x * scale, so K and V go to the tensor cores as exact f16 values (one convert per
+// pair) and the scales are applied to S and O instead; each query row is brought into f16
+// range by a power of two (undone on its scores), which keeps its bf16 values exact.
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
 __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decode_kernel(RpaArgs a) {
     using T = DecTile<D, HG, ESZ, CONV>;
+    static_assert(!F16 || (CONV && ESZ == 1), "the f16 path takes fp8 caches");
     constexpr int BK = T::BK, STAGES = T::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
@@ -197,12 +209,42 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     qb[ks][1] = rvb ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;
                 }
             }
+            // F16: the row's power-of-two range factor (its 4 lanes hold its D values), the
+            // fragments re-packed as f16, and each C column's factor back on its scores
+            float colmul[2] = {1.f, 1.f};
+            if (F16) {
+                float mabs = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qb[ks][h]));
+                        mabs = fmaxf(mabs, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                mabs = fmaxf(mabs, __shfl_xor_sync(0xffffffffu, mabs, 1));
+                mabs = fmaxf(mabs, __shfl_xor_sync(0xffffffffu, mabs, 2));
+                int ex = 0;
+                frexpf(mabs, &ex);                               // mabs < 2^ex
+                const int k = max(-30, min(100, ex - 15));       // mabs * 2^-k in [2^14, 2^15)
+                const float qs = ldexpf(1.f, -k);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qb[ks][h]));
+                        qb[ks][h] = pack_f16(f.x * qs, f.y * qs);
+                    }
+                const float rowmul = ldexpf(1.f, k);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) colmul[j] = __shfl_sync(0xffffffffu, rowmul, (2 * q4 + j) * 4) * a.k_scale_or_one;
+            }
             // O^T tiles: rows (dims) 16*dm + g8 and +8, columns (query rows) 2*q4, 2*q4+1
             float o[D / 16][4];
 #pragma unroll
             for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
             const float scale = a.sm_scale, cap = a.soft_cap;
+            const float cap_k2 = cap != 0.f ? 2.f * kLog2e / cap : 0.f;
 
             for (int blk = 0; blk < n_blocks; ++blk) {
                 const uint32_t qn = pipe + blk, st = qn % STAGES, ph = (qn / STAGES) & 1;
@@ -221,8 +263,9 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
 #pragma unroll 4
                     for (int i = lane; i < BK * kChunks; i += 32) {
                         const int kk = i / kChunks, c = i % kChunks;
+                        const uint8_t* src = stg + kk * T::kRow + (warp * 2 * D + part * D + c * 8) * ESZ;
                         *reinterpret_cast<uint4*>(cb + kk * T::kConvRow + c * 16) =
-                            dequant8<ESZ>(stg + kk * T::kRow + (warp * 2 * D + part * D + c * 8) * ESZ, sc);
+                            F16 ? fp8x8_to_f16(src) : dequant8<ESZ>(src, sc);
                     }
                     __syncwarp();
                 };
@@ -245,7 +288,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         for (int ks = 0; ks < D / 16; ++ks) {
                             uint32_t ka4[4];
                             ldsm_x4(ka + ks * 32, ka4[0], ka4[1], ka4[2], ka4[3]);
-                            mma_bf16(sc, ka4, qb[ks][0], qb[ks][1]);
+                            if (F16)
+                                mma_f16(sc, ka4, qb[ks][0], qb[ks][1]);
+                            else
+                                mma_bf16(sc, ka4, qb[ks][0], qb[ks][1]);
                         }
                     }
                     if (CONV) {
@@ -258,8 +304,8 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     for (int e = 0; e < 4; ++e) {
                         const int j = e & 1;
                         const int key = key0 + g8 + (e >> 1) * 8;
-                        float x = sc[e] * scale;
-                        if (cap != 0.f) x = cap * tanhf(x / cap);
+                        float x = sc[e] * (F16 ? scale * colmul[j] : scale);
+                        if (cap != 0.f) x = soft_cap(x, cap, cap_k2);
                         x *= kLog2e;
                         const bool ok = key <= qpos[j] && key >= wlo[j] && key < ke;
                         x = ok ? x : -INFINITY;
@@ -285,8 +331,8 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         l_run[e & 1] += p;
                     }
                     // P^T as B fragments (k = keys 2*q4.., n = row g8): transpose the 8x8 blocks
-                    const uint32_t pb0 = movmatrix_t(pack_bf16(sc[0], sc[1]));
-                    const uint32_t pb1 = movmatrix_t(pack_bf16(sc[2], sc[3]));
+                    const uint32_t pb0 = movmatrix_t(F16 ? pack_f16(sc[0], sc[1]) : pack_bf16(sc[0], sc[1]));
+                    const uint32_t pb1 = movmatrix_t(F16 ? pack_f16(sc[2], sc[3]) : pack_bf16(sc[2], sc[3]));
                     // O^T [16 dims x 8 rows] += V^T P^T; A = V^T by a transposing ldmatrix of V rows
                     const uint32_t va = vbase + ((lane & 7) + ((lane >> 4) << 3)) * rowb + ((lane >> 3) & 1) * 16;
 #pragma unroll
@@ -297,7 +343,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         o[dm][3] *= alpha[1];
                         uint32_t va4[4];
                         ldsm_x4_t(va + dm * 32, va4[0], va4[1], va4[2], va4[3]);
-                        mma_bf16(o[dm], va4, pb0, pb1);
+                        if (F16)
+                            mma_f16(o[dm], va4, pb0, pb1);
+                        else
+                            mma_bf16(o[dm], va4, pb0, pb1);
                     }
                 }
                 __syncwarp();
@@ -315,8 +364,9 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                 if (w.num_splits == 1) {
                     // normalise per column, transpose each 8x8 block back to rows: thread then
                     // holds row rb + g8, dims 2*q4, 2*q4+1 of the block (32-bit stores)
-                    const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
-                    const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
+                    const float vs = F16 ? a.v_scale_or_one : 1.f;  // (F16: V went in unscaled)
+                    const float inv0 = l_run[0] > 0.f ? vs / l_run[0] : 0.f;
+                    const float inv1 = l_run[1] > 0.f ? vs / l_run[1] : 0.f;
                     __nv_bfloat16* dst = a.out + ((size_t)(q_start + (rvb ? Rb / G : 0)) * a.num_q_heads + head * G +
                                                   (rvb ? Rb % G : 0)) * D;
 #pragma unroll
@@ -336,9 +386,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         if (!rv[j]) continue;
                         const int r = warp * 16 + rb + 2 * q4 + j;
 #pragma unroll
+                        const float vs = F16 ? a.v_scale_or_one : 1.f;
                         for (int dm = 0; dm < D / 16; ++dm) {
-                            po[(size_t)r * D + dm * 16 + g8] = o[dm][j];
-                            po[(size_t)r * D + dm * 16 + 8 + g8] = o[dm][2 + j];
+                            po[(size_t)r * D + dm * 16 + g8] = o[dm][j] * vs;
+                            po[(size_t)r * D + dm * 16 + 8 + g8] = o[dm][2 + j] * vs;
                         }
                         if (g8 == 0) {
                             pml[r * 2] = m_run[j];
@@ -396,10 +447,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
     }
 }
 
-template <int D, int HG, int ESZ, bool CONV>
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
 static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream) {
     using T = DecTile<D, HG, ESZ, CONV>;
-    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV>;
+    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16>;
     static int per_sm = 0;
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -414,6 +465,13 @@ static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t str
     return cudaGetLastError();
 }
 
+// A scale the f16 path may take: a power of two with e4m3 * scale inside bf16's normal range.
+static bool pow2_scale(float s) {
+    int e = 0;
+    const float m = frexpf(s, &e);
+    return s > 0.f && m == 0.5f && e >= -40 && e <= 40;
+}
+
 int decode_heads_for(int head_dim, bool fp8) {
     (void)fp8;
     return head_dim >= 256 ? 2 : 4;
@@ -422,6 +480,8 @@ int decode_heads_for(int head_dim, bool fp8) {
 template <int D>
 static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
     constexpr int HG = D >= 256 ? 2 : 4;
+    if (a.kv_fp8 && pow2_scale(a.k_scale_or_one) && pow2_scale(a.v_scale_or_one))
+        return launch_decode<D, HG, 1, true, true>(a, num_sms, stream);
     if (a.kv_fp8) return launch_decode<D, HG, 1, true>(a, num_sms, stream);
     if (a.has_scale) return launch_decode<D, HG, 2, true>(a, num_sms, stream);
     return launch_decode<D, HG, 2, false>(a, num_sms, stream);

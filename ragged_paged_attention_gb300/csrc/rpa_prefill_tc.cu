@@ -468,6 +468,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             const int wlo = a.sliding_window > 0 ? qpos - a.sliding_window + 1 : INT_MIN;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
+            const float cap_k2 = cap != 0.f ? 2.f * kLog2e / cap : 0.f;
             constexpr int HB = T::kHalf;
             float m_use = -INFINITY, l_half = 0.f;
             bool ok = true;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 const int key0 = kb + j * BK + half * HB;
                 if (cap != 0.f) {
 #pragma unroll
-                    for (int i = 0; i < HB; ++i) x[i] = cap * tanhf(x[i] * scale / cap) * kLog2e;
+                    for (int i = 0; i < HB; ++i) x[i] = soft_cap(x[i] * scale, cap, cap_k2) * kLog2e;
                 } else {
 #pragma unroll
                     for (int i = 0; i < HB; ++i) x[i] *= c_log2;
