@@ -285,7 +285,11 @@ def roof_time(byt, fl, peaks, sustained=False):
 # ---------------------------------------------------------------------------
 # timing helpers
 # ---------------------------------------------------------------------------
-def time_steps(fn, steps, warmup, world, timer=False):
+def time_steps(fn, steps, warmup, world, timer=False, launches=False):
+    """ms per step over `steps` timed steps (CUDA events on the current stream). timer=True
+    also brackets every library launch with events (per-kernel times; the library then
+    serialises launches it would otherwise overlap); launches=True also returns how many
+    library kernels the timed steps launched."""
     from ragged_paged_attention_gb300 import api
     for _ in range(warmup):
         fn()
@@ -296,15 +300,19 @@ def time_steps(fn, steps, warmup, world, timer=False):
     kt = api.KernelTimer() if timer else None
     if kt:
         kt.__enter__()
+    n0 = api.launch_count()
     e0.record(st)
     for _ in range(steps):
         fn()
     e1.record(st)
+    n1 = api.launch_count()
     torch.cuda.synchronize()
     if kt:
         kt.__exit__(None, None, None)
     barrier(world)
     ms = e0.elapsed_time(e1) / steps
+    if launches:
+        return ms, (kt.result if kt else {}), n1 - n0
     return ms, (kt.result if kt else {})
 
 
@@ -429,8 +437,11 @@ def main():
                         **opts)
 
     clocks = clock_sampler(local).start()
-    ms, ktimes = time_steps(step, args.steps, args.warmup, world, timer=True)
+    ms, _, n_launch = time_steps(step, args.steps, args.warmup, world, launches=True)
     clk = clocks.stop()
+    # per-kernel durations: a second pass with every launch bracketed by CUDA events (the
+    # library runs its kernels one after another while they are timed)
+    _, ktimes = time_steps(step, args.steps, 1, world, timer=True)
     assert api.check_device_status(ws) == 0 and api.check_device_status(ws_u) == 0
     ms = max_over_ranks(ms, world)
     T = b.num_tokens
@@ -508,7 +519,9 @@ def main():
                               "tflops": step_flops / (ms * 1e-3) / 1e12},
             "roofline": roof,
             "kernels": kernels,
-            "gpu_launches": int(sum(v[0] for v in ktimes.values())),
+            "gpu_launches": int(n_launch),
+            "kernel_timing": "kernels/roofline: separate pass of the same steps with each launch bracketed by "
+                             "CUDA events (kernels serialised); value/ms_per_step: unbracketed steps",
             "clocks": clk,
             "e2e": None if ms_e2e is None else {
                 "value": T * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -557,8 +570,12 @@ def _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report):
     ws = torch.zeros(api.rpa_workspace_size(api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty_like(g.q)
-    ms, kt = time_steps(lambda: api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs,
-                                                out=out, workspace=ws, **opts), steps, warm, world, timer=True)
+    def fwd():
+        api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, workspace=ws,
+                        **opts)
+
+    ms, _ = time_steps(fwd, steps, warm, world)
+    _, kt = time_steps(fwd, steps, 1, world, timer=True)  # per-kernel pass (serialised)
     dec_us = 1e3 * kt["rpa_decode_attn"][1] / kt["rpa_decode_attn"][0]
     report("gemma2_fp8_sw_cap", b.num_tokens, acc["decode"][1] + acc["prefill"][1],
            acc["decode"][2] + acc["prefill"][2], ms, kt,

@@ -298,6 +298,10 @@ RPA_API int rpa_profile_enable(int on);
 RPA_API int rpa_profile_reset(void);
 RPA_API int rpa_profile_read(rpa_kernel_time* out, int max_entries, int* n_entries);
 
+/* Number of kernels the library has launched since it was loaded, counted whether or not
+ * timing is enabled (a host-side counter; no synchronisation). */
+RPA_API int64_t rpa_launch_count(void);
+
 /* Thread-local description of the last failed call ("" if none). */
 RPA_API const char* rpa_last_error(void);
 

@@ -27,7 +27,7 @@ STATUS = {0: "RPA_OK", -1: "RPA_ERR_NULL", -2: "RPA_ERR_SHAPE", -3: "RPA_ERR_DTY
 EXPORTS = ("rpa_workspace_size", "rpa_forward", "rpa_update_kv_cache", "mla_workspace_size",
            "mla_update_kv_cache", "mla_rpa_forward", "sparse_mla_workspace_size", "sparse_mla_forward",
            "rpa_check_device_status", "rpa_last_error", "rpa_version", "rpa_profile_enable",
-           "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc")
+           "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc", "rpa_launch_count")
 
 
 class RpaError(RuntimeError):
@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH):
         lib.rpa_profile_enable.argtypes = [ctypes.c_int]
         lib.rpa_profile_reset.argtypes = []
         lib.rpa_profile_read.argtypes = [ctypes.POINTER(rpa_kernel_time), ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+        lib.rpa_launch_count.argtypes = []
+        lib.rpa_launch_count.restype = ctypes.c_int64
         for name in EXPORTS:
             if name not in ("rpa_last_error",):
                 getattr(lib, name).restype = ctypes.c_int
@@ -381,6 +383,11 @@ def check_device_status(workspace: torch.Tensor) -> int:
     if rc not in (0, -7):
         _check(rc)
     return bits.value
+
+
+def launch_count() -> int:
+    """Kernels the library has launched since it was loaded (``rpa_launch_count``)."""
+    return int(load_library().rpa_launch_count())
 
 
 class KernelTimer:

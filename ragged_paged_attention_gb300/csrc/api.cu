@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "profile.h"
 
 using namespace rpa;
 
@@ -52,7 +53,7 @@ float resolve_mask(float m) { return isnan(m) ? -0.7f * 3.402823466e38f : m; }
 
 // ---------------------------- RPA ----------------------------------------
 struct RpaLayout {
-    size_t items_dec, items_pre, tickets, pml, po, total;
+    size_t items_dec, items_pre, tickets, cta_first, pml, po, total;
     int max_dec, max_pre;
 };
 
@@ -87,7 +88,9 @@ RpaLayout rpa_layout(const rpa_params* p) {
     const int G = p->num_q_heads / hkv;
     const int dh = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
     const int groups = cdiv(hkv, dh);
-    L.max_dec = kDecodeTargetCtas + 2 * groups * p->max_num_seqs;  // up to two 8-row halves per sequence
+    // pieces: one per CTA share plus one more per group a share boundary cuts (groups: up to two
+    // 8-row halves per sequence and KV-head group)
+    L.max_dec = kMaxDecodeCtas + 2 * groups * p->max_num_seqs;
     L.max_pre = hkv * (int)((long long)p->max_num_tokens * G / kPrefillRows + p->max_num_seqs + 1);
     size_t off = kWsHeaderBytes;
     L.items_dec = off;
@@ -96,10 +99,12 @@ RpaLayout rpa_layout(const rpa_params* p) {
     off = align_up(off + sizeof(WorkItem) * (size_t)L.max_pre);
     L.tickets = off;
     off = align_up(off + sizeof(int) * (size_t)L.max_dec);
+    L.cta_first = off;
+    off = align_up(off + sizeof(int) * (size_t)(kMaxDecodeCtas + 1));
     L.pml = off;
-    off = align_up(off + sizeof(float) * 2 * dh * 16 * (size_t)L.max_dec);
+    off = align_up(off + sizeof(float) * 2 * dh * kDecodeRows * (size_t)L.max_dec);
     L.po = off;
-    off = align_up(off + sizeof(float) * (size_t)p->head_dim * dh * 16 * (size_t)L.max_dec);
+    off = align_up(off + sizeof(float) * (size_t)p->head_dim * dh * kDecodeRows * (size_t)L.max_dec);
     L.total = off;
     return L;
 }
@@ -247,12 +252,17 @@ int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const 
     a.has_scale = p->k_scale != 0.f || p->v_scale != 0.f;
     a.k_scale_or_one = p->k_scale != 0.f ? p->k_scale : 1.f;
     a.v_scale_or_one = p->v_scale != 0.f ? p->v_scale : 1.f;
-    a.decode_target_ctas = kDecodeTargetCtas;
     a.decode_heads = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
+    a.num_sms = sms;
+    a.overlap = prof_enabled() ? 0 : 1;
+    rpa_rates(p->head_dim, a.kv_fp8 != 0, a.has_scale != 0, &a.pre_flops_per_ns_sm, &a.dec_bytes_per_ns_sm);
+    a.decode_per_sm = rpa_decode_ctas_per_sm(a);
+    if (a.decode_per_sm <= 0) return fail(RPA_ERR_CUDA, "decode kernel occupancy query failed");
     a.hdr = reinterpret_cast<WsHeader*>(ws);
     a.dec_items = reinterpret_cast<WorkItem*>(ws + L.items_dec);
     a.pre_items = reinterpret_cast<WorkItem*>(ws + L.items_pre);
     a.tickets = reinterpret_cast<int*>(ws + L.tickets);
+    a.cta_first = reinterpret_cast<int*>(ws + L.cta_first);
     a.partial_ml = reinterpret_cast<float*>(ws + L.pml);
     a.partial_o = reinterpret_cast<float*>(ws + L.po);
     a.max_dec_items = L.max_dec;

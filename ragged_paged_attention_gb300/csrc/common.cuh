@@ -19,9 +19,18 @@ struct WsHeader {
     int32_t next_item[4];    // work-stealing counters, reset by the plan kernel
     int32_t num_items[4];    // items written by the plan kernel, per work list
     int32_t chunk_keys;      // split-KV chunk chosen by the plan kernel
-    int32_t pad[54];
+    int32_t prefill_ctas;    // prefill CTAs that run beside the decode kernel (plan kernel)
+    int32_t dec_ctas;        // static decode shares, one per decode CTA (plan kernel)
+    int32_t dec_shares;      // static + pooled decode shares (plan kernel)
+    int32_t pad[51];
 };
 static_assert(sizeof(WsHeader) == kWsHeaderBytes, "header size");
+
+// Programmatic dependent launch: a grid lets the next launch of its stream (made with
+// programmatic stream serialization) start once all of its CTAs have signalled; that grid
+// waits for its predecessor's completion (and memory) only where it asks to.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
@@ -147,28 +156,29 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Exclusive scan over a block (blockDim.x a multiple of 32, <= 1024); returns the
 // thread's exclusive prefix and writes the block total to *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total) {
+template <typename I>
+__device__ __forceinline__ I block_exclusive_scan(I v, I* scratch /* >= 33 entries */, I* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int x = v;
+    I x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
+        I y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) scratch[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = lane < nw ? scratch[lane] : 0;
+        I w = lane < nw ? scratch[lane] : I(0);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, w, o);
+            I y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
         scratch[lane] = w;  // inclusive per-warp totals
     }
     __syncthreads();
-    const int warp_off = warp ? scratch[warp - 1] : 0;
-    const int tot = scratch[nw - 1];
+    const I warp_off = warp ? scratch[warp - 1] : I(0);
+    const I tot = scratch[nw - 1];
     __syncthreads();
     *total = tot;
     return warp_off + x - v;

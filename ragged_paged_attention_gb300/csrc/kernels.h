@@ -17,7 +17,29 @@ constexpr int kDecodeRows = 8;          // query rows (q_len x G) per decode ite
 constexpr int kCuCache = 4096;          // cu_q_lens entries the cache-write kernels stage in shared memory
 constexpr int kPrefillRows = 128;       // (token, q-head) rows per prefill item (one TMEM tile)
 constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
-constexpr int kDecodeTargetCtas = 1024; // split so decode work spreads over about this many CTAs
+constexpr int kMaxDecodeCtas = 2048;    // most decode shares (static, one per CTA, and pooled)
+// Pool: the part of the line left after the static shares (here only their rounding
+// remainder: measured on the Llama-3 and Gemma-2 batches, pooled shares of 64-256 keys cost
+// more in per-item start-up than they recover in balance)
+constexpr int kPoolPercent = 0;         // share of the decode work left to the pool
+constexpr int kMinPoolChunk = 64;       // smallest pooled decode share (keys)
+constexpr int kPoolPerCta = 3;          // pooled shares per decode CTA (about)
+
+// Prefill beside decode: the prefill items are tensor-core bound and the decode items HBM
+// bound, so the plan kernel gives prefill the share of the SMs that makes both lists end
+// together, from the batch's prefill FLOPs and decode bytes and these measured rates
+// (a mis-estimate costs a short tail: prefill left over when decode ends runs on every SM).
+constexpr float kDecHbmBytesPerNs = 5800.f;   // decode kernel with HBM saturated
+
+// Per-SM rates of the two kernels by head size and cache type: prefill FLOPs per ns per SM,
+// decode bytes per ns per SM while the SMs (not HBM) limit it. Measured on GB300 for head_dim
+// 128 bf16 (Llama-3 batch) and 256 fp8 (Gemma-2 batch); the other entries are scaled from
+// those. Only the SM split depends on them, never a result.
+inline void rpa_rates(int head_dim, bool fp8, bool scale, float* pre, float* dec) {
+    const bool conv = fp8 || scale;
+    *pre = conv ? (head_dim >= 256 ? 1800.f : 2200.f) : (head_dim >= 256 ? 3000.f : head_dim >= 128 ? 3800.f : 2400.f);
+    *dec = conv ? 26.f : 60.f;
+}
 
 // One unit of work for a persistent attention CTA (32 bytes).
 struct __align__(16) WorkItem {
@@ -46,13 +68,18 @@ struct RpaArgs {
     int sliding_window;
     int has_scale;              // k_scale or v_scale given
     float k_scale_or_one, v_scale_or_one;
-    int decode_target_ctas;
+    int decode_per_sm;          // decode CTAs resident per SM (occupancy of the chosen kernel)
     int decode_heads;           // KV heads per decode item (decode_heads_for)
+    int num_sms;
+    int overlap;                // run prefill beside decode (off while kernels are timed one by one)
+    float pre_flops_per_ns_sm;  // prefill kernel rate per SM (this head size and cache type)
+    float dec_bytes_per_ns_sm;  // decode kernel rate per SM while SMs, not HBM, limit it
     // workspace
     WsHeader* hdr;
     WorkItem* dec_items;
     WorkItem* pre_items;
     int* tickets;
+    int* cta_first;             // [kMaxDecodeCtas + 1] first decode item of each decode share
     float* partial_ml;
     float* partial_o;
     int max_dec_items, max_pre_items;
@@ -135,7 +162,8 @@ struct MlaUpdateArgs {
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_rpa_decode(const RpaArgs& a, int num_sms, cudaStream_t stream);
-cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream);
+int rpa_decode_ctas_per_sm(const RpaArgs& a);  // resident CTAs per SM of the kernel launch_rpa_decode picks
+cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream, int tail);
 int decode_heads_for(int head_dim, bool fp8);
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);

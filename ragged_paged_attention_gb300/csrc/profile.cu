@@ -14,6 +14,7 @@
 namespace rpa {
 namespace {
 std::atomic<int> g_on{0};
+std::atomic<long long> g_launches{0};
 struct Rec {
     const char* name;
     cudaEvent_t a, b;
@@ -35,7 +36,10 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
+bool prof_enabled() { return g_on.load(std::memory_order_relaxed) != 0; }
+
 ProfScope::ProfScope(const char* name, cudaStream_t s) : name_(name), stream_(s), a_(nullptr), b_(nullptr) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_on.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lk(g_mu);
     a_ = take_event();
@@ -55,6 +59,8 @@ ProfScope::~ProfScope() {
 using namespace rpa;
 
 extern "C" {
+
+int64_t rpa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int rpa_profile_enable(int on) {
     g_on.store(on ? 1 : 0);

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 
 namespace rpa {
+bool prof_enabled();  // per-kernel timing on: launches are bracketed, so nothing may overlap
+
 class ProfScope {
    public:
     ProfScope(const char* name, cudaStream_t s);

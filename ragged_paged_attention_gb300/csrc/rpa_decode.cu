@@ -120,12 +120,33 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
     uint32_t pipe = 0;            // blocks this CTA has pushed through the ring so far
     uint32_t issued_phase[4] = {0, 0, 0, 0};  // producer: last phase issued per stage (+1)
 
+    // prefill first (the plan gave it every SM): start once it has ended, so that the CTAs
+    // begin their equal shares together (no-op on an ordinary launch)
+    if (hdr->prefill_ctas >= a.num_sms && hdr->num_items[1] > 0) pdl_wait();
+    // shares are runs of consecutive items laid out by the plan kernel: this CTA's own (the
+    // first dec_ctas CTAs have one), then shares taken from the pool (thread 0 keeps the run)
+    const int n_items = hdr->num_items[0], n_static = hdr->dec_ctas, n_shares = hdr->dec_shares;
+    int my_it = 0, my_end = 0;
+    bool pool_left = true;
+    if (tid == 0 && (int)blockIdx.x < n_static) {
+        my_it = min(max(a.cta_first[blockIdx.x], 0), n_items);
+        my_end = min(max(a.cta_first[blockIdx.x + 1], my_it), n_items);
+    }
     while (true) {
         if (tid == 0) {
-            const int it = atomicAdd(&hdr->next_item[0], 1);
+            while (my_it >= my_end && pool_left) {
+                const int c = n_static + atomicAdd(&hdr->next_item[2], 1);
+                if (c >= n_shares) {
+                    pool_left = false;
+                } else {
+                    my_it = min(max(a.cta_first[c], 0), n_items);
+                    my_end = min(max(a.cta_first[c + 1], my_it), n_items);
+                }
+            }
+            const int it = my_it < my_end ? my_it++ : -1;
             s_item.seq = -1;
             s_item_idx = it;
-            if (it < hdr->num_items[0]) s_item = a.dec_items[it];
+            if (it >= 0) s_item = a.dec_items[it];
         }
         __syncthreads();
         const WorkItem w = s_item;
@@ -379,14 +400,15 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         }
                     }
                 } else {
-                    float* po = a.partial_o + (size_t)self * (a.decode_heads * 16 * D);
-                    float* pml = a.partial_ml + (size_t)self * (a.decode_heads * 16 * 2);
+                    // partials: kDecodeRows rows per KV head, numbered from the item's first row
+                    float* po = a.partial_o + (size_t)self * (a.decode_heads * kDecodeRows * D);
+                    float* pml = a.partial_ml + (size_t)self * (a.decode_heads * kDecodeRows * 2);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         if (!rv[j]) continue;
-                        const int r = warp * 16 + rb + 2 * q4 + j;
-#pragma unroll
+                        const int r = warp * kDecodeRows + 2 * q4 + j;
                         const float vs = F16 ? a.v_scale_or_one : 1.f;
+#pragma unroll
                         for (int dm = 0; dm < D / 16; ++dm) {
                             po[(size_t)r * D + dm * 16 + g8] = o[dm][j] * vs;
                             po[(size_t)r * D + dm * 16 + 8 + g8] = o[dm][2 + j] * vs;
@@ -413,10 +435,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
         if (!producer && warp < seg_heads) {
             const int head = h0 + warp;
             for (int R = w.row_begin; R < min(n_rows, w.row_begin + kDecodeRows); ++R) {
-                const int row = warp * 16 + R;
+                const int row = warp * kDecodeRows + (R - w.row_begin);
                 float M = -INFINITY;
                 for (int sp = 0; sp < w.num_splits; ++sp)
-                    M = fmaxf(M, __ldcg(a.partial_ml + (size_t)(w.first_item + sp) * (a.decode_heads * 32) + row * 2));
+                    M = fmaxf(M, __ldcg(a.partial_ml + (size_t)(w.first_item + sp) * (a.decode_heads * kDecodeRows * 2) + row * 2));
                 const float Mu = M == -INFINITY ? 0.f : M;
                 float L = 0.f;
                 float acc[D / 32];
@@ -424,11 +446,11 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                 for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
                 for (int sp = 0; sp < w.num_splits; ++sp) {
                     const size_t it = (size_t)(w.first_item + sp);
-                    const float m = __ldcg(a.partial_ml + it * (a.decode_heads * 32) + row * 2);
-                    const float l = __ldcg(a.partial_ml + it * (a.decode_heads * 32) + row * 2 + 1);
+                    const float m = __ldcg(a.partial_ml + it * (a.decode_heads * kDecodeRows * 2) + row * 2);
+                    const float l = __ldcg(a.partial_ml + it * (a.decode_heads * kDecodeRows * 2) + row * 2 + 1);
                     const float f = fast_exp2(m - Mu);
                     L += f * l;
-                    const float* src = a.partial_o + it * (a.decode_heads * 16 * D) + (size_t)row * D;
+                    const float* src = a.partial_o + it * (a.decode_heads * kDecodeRows * D) + (size_t)row * D;
 #pragma unroll
                     for (int i = 0; i < D / 32; ++i) acc[i] += f * __ldcg(src + i * 32 + lane);
                 }
@@ -445,10 +467,16 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
         for (int st = 0; st < STAGES; ++st)
             if (issued_phase[st]) mbar_wait(&full[st], issued_phase[st] - 1, err);
     }
+    // a CTA with a share is out of decode work (the prefill grid's signal when there is no pool)
+    if (tid == 0 && (int)blockIdx.x < n_static) atomicAdd(&hdr->next_item[0], 1);
+    // started early beside the prefill grid: end after it, so that the stream order seen by
+    // later launches is the plain one (no-op on an ordinary launch)
+    if (tid == 0) pdl_wait();
 }
 
+// per_sm_out != nullptr: only report the kernel's resident CTAs per SM (no launch)
 template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
-static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     using T = DecTile<D, HG, ESZ, CONV>;
     auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16>;
     static int per_sm = 0;
@@ -460,9 +488,22 @@ static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t str
         if (e != cudaSuccess) return e;
         per_sm = n > 0 ? n : 1;
     }
+    if (per_sm_out) {
+        *per_sm_out = per_sm;
+        return cudaSuccess;
+    }
     ProfScope ps("rpa_decode_attn", stream);
-    kern<<<num_sms * per_sm, T::kThreads, T::kSmem, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms * per_sm);
+    cfg.blockDim = dim3(T::kThreads);
+    cfg.dynamicSmemBytes = T::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // A scale the f16 path may take: a power of two with e4m3 * scale inside bf16's normal range.
@@ -478,22 +519,31 @@ int decode_heads_for(int head_dim, bool fp8) {
 }
 
 template <int D>
-static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     constexpr int HG = D >= 256 ? 2 : 4;
     if (a.kv_fp8 && pow2_scale(a.k_scale_or_one) && pow2_scale(a.v_scale_or_one))
-        return launch_decode<D, HG, 1, true, true>(a, num_sms, stream);
-    if (a.kv_fp8) return launch_decode<D, HG, 1, true>(a, num_sms, stream);
-    if (a.has_scale) return launch_decode<D, HG, 2, true>(a, num_sms, stream);
-    return launch_decode<D, HG, 2, false>(a, num_sms, stream);
+        return launch_decode<D, HG, 1, true, true>(a, num_sms, stream, per_sm_out);
+    if (a.kv_fp8) return launch_decode<D, HG, 1, true>(a, num_sms, stream, per_sm_out);
+    if (a.has_scale) return launch_decode<D, HG, 2, true>(a, num_sms, stream, per_sm_out);
+    return launch_decode<D, HG, 2, false>(a, num_sms, stream, per_sm_out);
+}
+
+static cudaError_t decode_dispatch(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
+    switch (a.head_dim) {
+        case 64: return launch_decode_d<64>(a, num_sms, stream, per_sm_out);
+        case 128: return launch_decode_d<128>(a, num_sms, stream, per_sm_out);
+        case 256: return launch_decode_d<256>(a, num_sms, stream, per_sm_out);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_rpa_decode(const RpaArgs& a, int num_sms, cudaStream_t stream) {
-    switch (a.head_dim) {
-        case 64: return launch_decode_d<64>(a, num_sms, stream);
-        case 128: return launch_decode_d<128>(a, num_sms, stream);
-        case 256: return launch_decode_d<256>(a, num_sms, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return decode_dispatch(a, num_sms, stream, nullptr);
+}
+
+int rpa_decode_ctas_per_sm(const RpaArgs& a) {
+    int n = 0;
+    return decode_dispatch(a, 0, nullptr, &n) == cudaSuccess ? n : 0;
 }
 
 }  // namespace rpa

@@ -20,13 +20,26 @@ namespace rpa {
 // ---------------------------------------------------------------------------
 // Plan
 // ---------------------------------------------------------------------------
+// Decode work is cut into shares of one line: every decode group (sequence x KV-head group x
+// 8-row half) is a stream of its keys rounded up to 16, and the streams lie end to end. The
+// first three quarters of the line are R equal shares, one per decode CTA resident at once;
+// the rest is cut into small shares that CTAs take from a pool once their own is done. The
+// pieces of a group that fall to different shares are its splits (merged by whichever
+// finishes last). Equal shares remove the tail a queue of long items leaves (a few CTAs
+// finishing while the rest of the GPU idles); the pool evens out CTAs that stream faster
+// than others.
 __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     __shared__ int scan_scratch[40];
+    __shared__ long long scan_ll[40];
     __shared__ long long red[32];
+    __shared__ float red_f[32];
     __shared__ int s_num;
-    __shared__ int s_chunk;
-    // per sequence of the current group of blockDim.x: item end offsets and decode shape
-    __shared__ int e_dend[1024], e_pend[1024], e_klo[1024], e_kl[1024], e_ns[1024], e_nrh[1024];
+    __shared__ long long s_q1, s_q2, s_ls;  // static share size, pooled share size, static part
+    __shared__ int s_r;                     // static shares
+    // per sequence of the current group of blockDim.x: item end offsets, decode shape and the
+    // line position of its first decode group
+    __shared__ int e_dend[1024], e_pend[1024], e_klo[1024], e_kl[1024], e_nrh[1024];
+    __shared__ long long e_pos[1024];
     WsHeader* hdr = a.hdr;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -41,45 +54,120 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     const int num = s_num;
     const int G = a.num_q_heads / a.num_kv_heads;
     const int n_groups = cdiv(a.num_kv_heads, a.decode_heads);
+    auto round_bk = [](int keys) { return (long long)cdiv(keys, kDecodeBK) * kDecodeBK; };
 
-    // pass 1: total decode work (keys x head groups)
-    long long dec_keys = 0;
+    // pass 1: decode work (line length) and the prefill (query, key) pairs
+    long long work = 0;
+    float pre_pairs = 0.f;
     for (int s = tid; s < num; s += blockDim.x) {
-        int ql, kl, klo;
-        if (seq_shape(a, s, ql, kl) && ql >= 1 && ql * G <= 16) {
-            klo = decode_key_begin(a, ql, kl);
-            dec_keys += (long long)(kl - klo) * n_groups * cdiv(ql * G, kDecodeRows);
+        int ql, kl;
+        if (seq_shape(a, s, ql, kl) && ql >= 1) {
+            if (ql * G <= 16) {
+                const int klo = decode_key_begin(a, ql, kl);
+                work += round_bk(kl - klo) * n_groups * cdiv(ql * G, kDecodeRows);
+            } else {
+                // causal: query i of the chunk sees kl - ql + i + 1 keys (at most the window)
+                float seen = (float)kl - 0.5f * (float)(ql - 1);
+                if (a.sliding_window > 0) seen = fminf(seen, (float)a.sliding_window);
+                pre_pairs += (float)ql * seen;
+            }
         }
     }
-    for (int o = 16; o > 0; o >>= 1) dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
-    if ((tid & 31) == 0) red[tid >> 5] = dec_keys;
-    __syncthreads();
-    if (tid == 0) {
-        long long t = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-        long long c = (t + a.decode_target_ctas - 1) / a.decode_target_ctas;
-        if (c < kMinChunk) c = kMinChunk;
-        c = (c + kDecodeBK - 1) / kDecodeBK * kDecodeBK;
-        s_chunk = (int)c;
-        hdr->chunk_keys = (int)c;
+    for (int o = 16; o > 0; o >>= 1) {
+        work += __shfl_xor_sync(0xffffffffu, work, o);
+        pre_pairs += __shfl_xor_sync(0xffffffffu, pre_pairs, o);
+    }
+    if ((tid & 31) == 0) {
+        red[tid >> 5] = work;
+        red_f[tid >> 5] = pre_pairs;
     }
     __syncthreads();
-    const int chunk = s_chunk;
-
+    if (tid == 0) {
+        long long W = 0;
+        float pp = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            W += red[w];
+            pp += red_f[w];
+        }
+        // SMs for the prefill kernel beside decode: the n minimising max(prefill time on n SMs,
+        // decode time on the rest); all of them (prefill first) unless that beats it by 10%
+        const int S = a.num_sms;
+        const float pre_flops = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
+        const float dec_bytes = (float)W * (float)a.decode_heads * 2.f * (float)a.head_dim * (a.kv_fp8 ? 1.f : 2.f);
+        int n_pre = S;
+        if (pre_flops <= 0.f) {
+            n_pre = 0;
+        } else if (a.overlap && dec_bytes > 0.f && S > 1) {
+            const float serial = pre_flops / (a.pre_flops_per_ns_sm * (float)S) +
+                                 dec_bytes / fminf(kDecHbmBytesPerNs, a.dec_bytes_per_ns_sm * (float)S);
+            float best = 0.9f * serial;
+            for (int n = 1; n < S; ++n) {
+                const float tp = pre_flops / (a.pre_flops_per_ns_sm * (float)n);
+                const float td = dec_bytes / fminf(kDecHbmBytesPerNs, a.dec_bytes_per_ns_sm * (float)(S - n));
+                const float tt = fmaxf(tp, td);
+                if (tt < best) {
+                    best = tt;
+                    n_pre = n;
+                }
+            }
+        }
+        hdr->prefill_ctas = n_pre;
+        // decode CTAs resident at once: beside the prefill share, or every slot
+        int ctas = (n_pre > 0 && n_pre < S ? S - n_pre : S) * a.decode_per_sm;
+        ctas = max(1, min(ctas, kMaxDecodeCtas / 2));
+        // static shares: all but the pool's part of the line, none under kMinChunk keys
+        const long long w_static = W * (100 - kPoolPercent) / 100;
+        long long q1 = w_static / ctas / kDecodeBK * kDecodeBK;
+        int r = ctas;
+        if (q1 < kMinChunk) {
+            q1 = kMinChunk;
+            r = (int)min((long long)ctas, w_static / kMinChunk);
+        }
+        const long long ls = (long long)r * q1;
+        // pooled shares: about kPoolPerCta per CTA, at least kMinPoolChunk keys, within the bound
+        const long long rest = W - ls;
+        long long q2 = rest / ((long long)kPoolPerCta * ctas);
+        q2 = max(q2, (rest + (kMaxDecodeCtas - r) - 1) / (kMaxDecodeCtas - r));
+        q2 = max((long long)kMinPoolChunk, (q2 + kDecodeBK - 1) / kDecodeBK * kDecodeBK);
+        s_q1 = q1;
+        s_q2 = q2;
+        s_ls = ls;
+        s_r = r;
+        hdr->chunk_keys = (int)min(q1, (long long)0x7fffffff);
+        hdr->dec_ctas = r;
+        hdr->dec_shares = r + (int)((rest + q2 - 1) / q2);
+    }
+    __syncthreads();
+    const long long q1 = s_q1, q2 = s_q2, ls = s_ls;
+    const int n_static = s_r;
+    // share holding line position p, and where share c starts
+    auto share_of = [&](long long p) { return p < ls ? p / q1 : n_static + (p - ls) / q2; };
+    auto share_start = [&](long long c) { return c < n_static ? c * q1 : ls + (c - n_static) * q2; };
     // pass 2: item counts, scan, emit
     int dec_base = 0, pre_base = 0;
+    long long pos_base = 0;  // line position of the current group of sequences
     for (int s0 = 0; s0 < num; s0 += blockDim.x) {
         const int s = s0 + tid;
-        int ql = 0, kl = 0, nd = 0, np = 0, klo = 0, nsplit = 0, nrh = 0;
+        int ql = 0, kl = 0, nd = 0, np = 0, klo = 0, nrh = 0;
+        long long wk = 0;  // this sequence's decode work (all its groups)
         bool ok = s < num && seq_shape(a, s, ql, kl);
         if (ok && ql >= 1) {
             if (ql * G <= 16) {
                 klo = decode_key_begin(a, ql, kl);
-                nsplit = cdiv(kl - klo, chunk);
                 nrh = cdiv(ql * G, kDecodeRows);
-                nd = nsplit * n_groups * nrh;
+                wk = round_bk(kl - klo) * n_groups * nrh;
             } else {
                 np = cdiv(ql * G, kPrefillRows) * a.num_kv_heads;
+            }
+        }
+        long long tot_w;
+        const long long pos = pos_base + block_exclusive_scan(wk, scan_ll, &tot_w);
+        // splits of each group: the number of CTA shares its stretch of the line meets
+        if (wk > 0) {
+            const long long len = round_bk(kl - klo);
+            for (int j = 0; j < n_groups * nrh; ++j) {
+                const long long p0 = pos + j * len;
+                nd += (int)(share_of(p0 + len - 1) - share_of(p0) + 1);
             }
         }
         int tot_d, tot_p;
@@ -92,8 +180,8 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
         e_pend[tid] = op + np;
         e_klo[tid] = klo;
         e_kl[tid] = kl;
-        e_ns[tid] = nsplit;
         e_nrh[tid] = nrh;
+        e_pos[tid] = pos;
         __syncthreads();
         const int nseq = min((int)blockDim.x, num - s0);
         auto owner = [&](const int* ends, int idx) {
@@ -108,21 +196,35 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
             const int it = dec_base + idx;
             if (it >= a.max_dec_items) break;  // cannot happen: the host bound covers it
             const int k = owner(e_dend, idx);
-            const int ns = e_ns[k], nh = e_nrh[k];
-            const int beg = e_dend[k] - ns * n_groups * nh;
-            const int rel = idx - beg, gh = rel / ns, i = rel - gh * ns;
-            const int g = gh / nh, rh = gh - g * nh;
+            const int nh = e_nrh[k], kl_k = e_kl[k], klo_k = e_klo[k];
+            const long long len = round_bk(kl_k - klo_k);
+            const int seq_first = k > 0 ? e_dend[k - 1] : 0;
+            // the group j of this sequence holding the item, and the item's split in it
+            int rel = idx - seq_first, first = dec_base + seq_first, j = 0;
+            long long p0 = e_pos[k];
+            int ns = (int)(share_of(p0 + len - 1) - share_of(p0) + 1);
+            while (rel >= ns) {
+                rel -= ns;
+                first += ns;
+                ++j;
+                p0 += len;
+                ns = (int)(share_of(p0 + len - 1) - share_of(p0) + 1);
+            }
+            const long long c = share_of(p0) + rel;  // the share holding this piece
+            const long long c_lo = share_start(c);
+            const long long b0 = max(p0, c_lo) - p0, b1 = min(p0 + len, share_start(c + 1)) - p0;
             WorkItem w;
             w.seq = s0 + k;
-            w.head = g * a.decode_heads;
-            w.key_begin = e_klo[k] + i * chunk;
-            w.key_end = min(e_kl[k], e_klo[k] + (i + 1) * chunk);
-            w.first_item = dec_base + beg + gh * ns;
+            w.head = (j / nh) * a.decode_heads;
+            w.row_begin = (j % nh) * kDecodeRows;
+            w.key_begin = klo_k + (int)b0;
+            w.key_end = min(kl_k, klo_k + (int)b1);
+            w.first_item = first;
             w.num_splits = ns;
-            w.split = i;
-            w.row_begin = rh * kDecodeRows;
+            w.split = rel;
             a.dec_items[it] = w;
             a.tickets[it] = 0;
+            if (p0 + b0 == c_lo) a.cta_first[c] = it;  // the piece that opens share c
         }
         for (int idx = tid; idx < tot_p; idx += blockDim.x) {
             const int it = pre_base + idx;
@@ -145,12 +247,15 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
         __syncthreads();  // the next group of sequences reuses the e_* arrays
         dec_base += tot_d;
         pre_base += tot_p;
+        pos_base += tot_w;
     }
     if (tid == 0) {
         hdr->num_items[0] = min(dec_base, a.max_dec_items);
         hdr->num_items[1] = min(pre_base, a.max_pre_items);
+        a.cta_first[hdr->dec_shares] = hdr->num_items[0];
         hdr->next_item[0] = 0;
-        hdr->next_item[1] = 0;
+        hdr->next_item[1] = 0;  // prefill queue
+        hdr->next_item[2] = 0;  // pooled decode shares taken
     }
 }
 
@@ -238,9 +343,14 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    e = launch_rpa_prefill(a, num_sms, stream);
+    // overlap: prefill on the plan's share of the SMs, decode started early (programmatic
+    // launch) on the rest and finishing after that prefill grid, then the prefill items still
+    // queued when decode ran dry, on every SM; otherwise prefill then decode
+    e = launch_rpa_prefill(a, num_sms, stream, 0);
     if (e != cudaSuccess) return e;
-    return launch_rpa_decode(a, num_sms, stream);
+    e = launch_rpa_decode(a, num_sms, stream);
+    if (e != cudaSuccess || !a.overlap) return e;
+    return launch_rpa_prefill(a, num_sms, stream, 1);
 }
 
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream) {

@@ -142,9 +142,17 @@ constexpr int prefill_warps() { return 8 + 4 + 1; }  // softmax, producers (2 fo
 template <int D, bool FP8, bool SCALE, bool TMA>
 __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
-                          int box_rows, int q_tma) {
+                          int box_rows, int q_tma, int tail) {
     using T = PreTc<D>;
     constexpr int BK = T::BK;
+    // first launch (tail == 0): the decode grid behind may start once every CTA got here; only
+    // the plan's share of the CTAs works. Either launch leaves at once when the list is empty.
+    if (!tail) pdl_launch_dependents();
+    {
+        const WsHeader* h = a.hdr;
+        if ((!tail && (int)blockIdx.x >= h->prefill_ctas) || *(volatile const int*)&h->next_item[1] >= h->num_items[1])
+            return;
+    }
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
     constexpr int NS = T::NS;
@@ -205,9 +213,18 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint32_t items = 0;  // items this CTA has processed (q_full / o_full phases)
     while (true) {
         if (tid == 0) {
-            const int it = atomicAdd(&hdr->next_item[1], 1);
             s_item.seq = -1;
-            if (it < hdr->num_items[1]) s_item = a.pre_items[it];
+            // beside decode, take no new item once decode is ending (its pool is empty, or half
+            // of its CTAs are out of work): what is left goes to the launch after decode, on
+            // every SM
+            const int n_pool = hdr->dec_shares - hdr->dec_ctas;
+            const bool stop = !tail && a.overlap && hdr->dec_shares > 0 &&
+                              (n_pool > 0 ? *(volatile const int*)&hdr->next_item[2] >= n_pool
+                                          : *(volatile const int*)&hdr->next_item[0] >= max(1, hdr->dec_ctas / 2));
+            if (!stop) {
+                const int it = atomicAdd(&hdr->next_item[1], 1);
+                if (it < hdr->num_items[1]) s_item = a.pre_items[it];
+            }
         }
         __syncthreads();
         const WorkItem w = s_item;
@@ -645,7 +662,7 @@ static bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t d0, uint6
 
 template <int D, bool FP8, bool SCALE, bool TMA>
 static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
-                              const CUtensorMap& tq, int box_rows, int q_tma) {
+                              const CUtensorMap& tq, int box_rows, int q_tma, int tail) {
     using T = PreTc<D>;
     auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA>;
     static bool configured = false;
@@ -654,13 +671,13 @@ static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    ProfScope ps("rpa_prefill_attn", stream);
-    kern<<<num_sms, prefill_warps<TMA>() * 32, T::kSmem, stream>>>(a, tkv, tq, box_rows, q_tma);
+    ProfScope ps(tail ? "rpa_prefill_tail" : "rpa_prefill_attn", stream);
+    kern<<<num_sms, prefill_warps<TMA>() * 32, T::kSmem, stream>>>(a, tkv, tq, box_rows, q_tma, tail);
     return cudaGetLastError();
 }
 
 template <int D>
-static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stream, int tail) {
     constexpr int BK = PreTc<D>::BK;
     CUtensorMap tkv, tq;
     memset(&tkv, 0, sizeof tkv);
@@ -676,17 +693,17 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     int q_tma = 0;
     if (tma && 128 % G == 0)
         q_tma = make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
-    if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma);
-    if (a.kv_fp8) return launch_pre<D, true, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0);
-    if (a.has_scale) return launch_pre<D, false, true, false>(a, num_sms, stream, tkv, tq, box_rows, 0);
-    return launch_pre<D, false, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0);
+    if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma, tail);
+    if (a.kv_fp8) return launch_pre<D, true, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
+    if (a.has_scale) return launch_pre<D, false, true, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
+    return launch_pre<D, false, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
 }
 
-cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream, int tail) {
     switch (a.head_dim) {
-        case 64: return launch_pre_d<64>(a, num_sms, stream);
-        case 128: return launch_pre_d<128>(a, num_sms, stream);
-        case 256: return launch_pre_d<256>(a, num_sms, stream);
+        case 64: return launch_pre_d<64>(a, num_sms, stream, tail);
+        case 128: return launch_pre_d<128>(a, num_sms, stream, tail);
+        case 256: return launch_pre_d<256>(a, num_sms, stream, tail);
         default: return cudaErrorInvalidValue;
     }
 }
