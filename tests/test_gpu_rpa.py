@@ -96,6 +96,30 @@ def test_fp8_scales_and_query_magnitudes(ks, vs):
     check(b, TOL_FP8 * vs)
 
 
+@pytest.mark.parametrize("q_lens,kv_lens,hq,hkv", [
+    ([1, 1] + [256] * 4, [40, 70] + [1024] * 4, 16, 4),        # prefill-heavy: decode ends first
+    ([1] * 60 + [40], [3000] * 60 + [300], 16, 4),             # decode-heavy, one small prefill
+    ([1] * 30, list(range(100, 3100, 100)), 16, 4),            # decode only
+    ([200, 300], [900, 300], 16, 4),                           # prefill only
+    ([1, 1, 1, 1, 24], [5000, 17, 2000, 1, 600], 32, 2),       # 16 query rows: two 8-row halves
+])
+def test_prefill_beside_decode_regimes(q_lens, kv_lens, hq, hkv):
+    # the SM split between the two kernels, the prefill left for the launch after decode and
+    # the equal decode shares depend on the batch's mix of work
+    b = workloads.make_rpa(q_lens, kv_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=128, page_size=16,
+                           seed=sum(kv_lens) % 1000)
+    check(b, TOL_BF16, tokens=sample_tokens(b.q_lens))
+
+
+def test_serialised_launches():
+    # with per-kernel timing on, the kernels run one after another (prefill on every SM,
+    # decode after it): the same results within tolerance
+    b = workloads.llama_mixed(scale=1 / 8)
+    with api.KernelTimer() as kt:
+        check(b, TOL_BF16)
+    assert {"rpa_plan", "rpa_prefill_attn", "rpa_decode_attn"} <= set(kt.result)
+
+
 def test_empty_batch_and_zero_length_sequences():
     b = workloads.make_rpa([0, 2, 0], [5, 2, 0], num_q_heads=4, num_kv_heads=2, head_dim=128, page_size=16, seed=14,
                            max_num_tokens=8)
