@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace rpa {
 
 struct WsHeader;
@@ -30,6 +32,9 @@ constexpr int kPoolPerCta = 3;          // pooled shares per decode CTA (about)
 // together, from the batch's prefill FLOPs and decode bytes and these measured rates
 // (a mis-estimate costs a short tail: prefill left over when decode ends runs on every SM).
 constexpr float kDecHbmBytesPerNs = 5800.f;   // decode kernel with HBM saturated
+// the prefill grid beside decode takes no new item once this share of the decode CTAs with a
+// share are out of work (equal shares end within a few percent of one another)
+constexpr int kPrefillStopPercent = 90;
 
 // Per-SM rates of the two kernels by head size and cache type: prefill FLOPs per ns per SM,
 // decode bytes per ns per SM while the SMs (not HBM) limit it. Measured on GB300 for head_dim
@@ -161,6 +166,24 @@ struct MlaUpdateArgs {
 };
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
+// Launch with programmatic stream serialization when pdl (the kernel may start before the
+// previous launch of the stream ends; it orders itself with griddepcontrol), else plainly.
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                       A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
+
 cudaError_t launch_rpa_decode(const RpaArgs& a, int num_sms, cudaStream_t stream);
 int rpa_decode_ctas_per_sm(const RpaArgs& a);  // resident CTAs per SM of the kernel launch_rpa_decode picks
 cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream, int tail);

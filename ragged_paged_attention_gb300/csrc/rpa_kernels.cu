@@ -36,12 +36,16 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     __shared__ int s_num;
     __shared__ long long s_q1, s_q2, s_ls;  // static share size, pooled share size, static part
     __shared__ int s_r;                     // static shares
+    __shared__ float s_pf, s_db, best_t[32];
+    __shared__ int best_n[32];
     // per sequence of the current group of blockDim.x: item end offsets, decode shape and the
     // line position of its first decode group
     __shared__ int e_dend[1024], e_pend[1024], e_klo[1024], e_kl[1024], e_nrh[1024];
     __shared__ long long e_pos[1024];
     WsHeader* hdr = a.hdr;
     const int tid = threadIdx.x;
+    // the prefill grid behind may become resident now; it waits for this grid's end
+    pdl_launch_dependents();
     if (tid == 0) {
         int n = a.num_seqs[0];
         if (n < 0 || n > a.max_num_seqs) {
@@ -89,27 +93,56 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
             W += red[w];
             pp += red_f[w];
         }
-        // SMs for the prefill kernel beside decode: the n minimising max(prefill time on n SMs,
-        // decode time on the rest); all of them (prefill first) unless that beats it by 10%
-        const int S = a.num_sms;
-        const float pre_flops = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
-        const float dec_bytes = (float)W * (float)a.decode_heads * 2.f * (float)a.head_dim * (a.kv_fp8 ? 1.f : 2.f);
+        red[0] = W;
+        s_pf = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
+        s_db = (float)W * (float)a.decode_heads * 2.f * (float)a.head_dim * (a.kv_fp8 ? 1.f : 2.f);
+    }
+    __syncthreads();
+    // SMs for the prefill kernel beside decode: the n minimising max(prefill time on n SMs,
+    // decode time on the rest), one candidate n = tid + 1 per thread
+    const int S = a.num_sms;
+    {
+        const float pre_flops = s_pf, dec_bytes = s_db;
+        float tt = INFINITY;
+        int nn = S;
+        if (a.overlap && pre_flops > 0.f && dec_bytes > 0.f && tid + 1 < S) {
+            nn = tid + 1;
+            const float tp = pre_flops / (a.pre_flops_per_ns_sm * (float)nn);
+            const float td = dec_bytes / fminf(kDecHbmBytesPerNs, a.dec_bytes_per_ns_sm * (float)(S - nn));
+            tt = fmaxf(tp, td);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float t2 = __shfl_xor_sync(0xffffffffu, tt, o);
+            const int n2 = __shfl_xor_sync(0xffffffffu, nn, o);
+            if (t2 < tt || (t2 == tt && n2 < nn)) {
+                tt = t2;
+                nn = n2;
+            }
+        }
+        if ((tid & 31) == 0) {
+            best_t[tid >> 5] = tt;
+            best_n[tid >> 5] = nn;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const long long W = red[0];
+        const float pre_flops = s_pf, dec_bytes = s_db;
+        float bt = INFINITY;
+        int bn = S;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+            if (best_t[w] < bt || (best_t[w] == bt && best_n[w] < bn)) {
+                bt = best_t[w];
+                bn = best_n[w];
+            }
+        // all SMs to prefill first unless the split beats the serial order by 10%
         int n_pre = S;
         if (pre_flops <= 0.f) {
             n_pre = 0;
         } else if (a.overlap && dec_bytes > 0.f && S > 1) {
             const float serial = pre_flops / (a.pre_flops_per_ns_sm * (float)S) +
                                  dec_bytes / fminf(kDecHbmBytesPerNs, a.dec_bytes_per_ns_sm * (float)S);
-            float best = 0.9f * serial;
-            for (int n = 1; n < S; ++n) {
-                const float tp = pre_flops / (a.pre_flops_per_ns_sm * (float)n);
-                const float td = dec_bytes / fminf(kDecHbmBytesPerNs, a.dec_bytes_per_ns_sm * (float)(S - n));
-                const float tt = fmaxf(tp, td);
-                if (tt < best) {
-                    best = tt;
-                    n_pre = n;
-                }
-            }
+            if (bt < 0.9f * serial) n_pre = bn;
         }
         hdr->prefill_ctas = n_pre;
         // decode CTAs resident at once: beside the prefill share, or every slot
@@ -256,6 +289,9 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
         hdr->next_item[0] = 0;
         hdr->next_item[1] = 0;  // prefill queue
         hdr->next_item[2] = 0;  // pooled decode shares taken
+        // started beside the cache write (programmatic launch): end after it, so that the
+        // attention grids behind see the new rows (no-op on an ordinary launch)
+        pdl_wait();
     }
 }
 
@@ -265,6 +301,9 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
 __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
     extern __shared__ int s_cu[];  // cu_q_lens[0..num] when it fits (kCuCache entries)
     __shared__ int s_num;
+    // an rpa_forward plan kernel behind may start now: it reads only metadata this kernel does
+    // not write, and it ends after this grid has
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         int n = a.num_seqs[0];
         if (n < 0 || n > a.max_num_seqs) {
@@ -339,8 +378,7 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
     cudaError_t e;
     {
         ProfScope ps("rpa_plan", stream);
-        rpa_plan_kernel<<<1, 1024, 0, stream>>>(a);
-        e = cudaGetLastError();
+        e = launch_pdl(rpa_plan_kernel, dim3(1), dim3(1024), 0, stream, a.overlap != 0, a);
     }
     if (e != cudaSuccess) return e;
     // overlap: prefill on the plan's share of the SMs, decode started early (programmatic

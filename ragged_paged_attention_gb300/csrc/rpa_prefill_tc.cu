@@ -145,9 +145,13 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                           int box_rows, int q_tma, int tail) {
     using T = PreTc<D>;
     constexpr int BK = T::BK;
-    // first launch (tail == 0): the decode grid behind may start once every CTA got here; only
-    // the plan's share of the CTAs works. Either launch leaves at once when the list is empty.
-    if (!tail) pdl_launch_dependents();
+    // first launch (tail == 0): started early behind the plan kernel, it waits for it, then lets
+    // the decode grid behind start; only the plan's share of its CTAs works. Either launch
+    // leaves at once when the list is empty.
+    if (!tail) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     {
         const WsHeader* h = a.hdr;
         if ((!tail && (int)blockIdx.x >= h->prefill_ctas) || *(volatile const int*)&h->next_item[1] >= h->num_items[1])
@@ -214,13 +218,11 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     while (true) {
         if (tid == 0) {
             s_item.seq = -1;
-            // beside decode, take no new item once decode is ending (its pool is empty, or half
-            // of its CTAs are out of work): what is left goes to the launch after decode, on
-            // every SM
-            const int n_pool = hdr->dec_shares - hdr->dec_ctas;
-            const bool stop = !tail && a.overlap && hdr->dec_shares > 0 &&
-                              (n_pool > 0 ? *(volatile const int*)&hdr->next_item[2] >= n_pool
-                                          : *(volatile const int*)&hdr->next_item[0] >= max(1, hdr->dec_ctas / 2));
+            // beside decode, take no new item once most decode CTAs with a share are out of
+            // work (decode is ending): what is left goes to the launch after decode, on every SM
+            const bool stop = !tail && a.overlap && hdr->dec_ctas > 0 &&
+                              *(volatile const int*)&hdr->next_item[0] >=
+                                  max(1, hdr->dec_ctas * kPrefillStopPercent / 100);
             if (!stop) {
                 const int it = atomicAdd(&hdr->next_item[1], 1);
                 if (it < hdr->num_items[1]) s_item = a.pre_items[it];
@@ -672,8 +674,8 @@ static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream
         configured = true;
     }
     ProfScope ps(tail ? "rpa_prefill_tail" : "rpa_prefill_attn", stream);
-    kern<<<num_sms, prefill_warps<TMA>() * 32, T::kSmem, stream>>>(a, tkv, tq, box_rows, q_tma, tail);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(prefill_warps<TMA>() * 32), T::kSmem, stream, a.overlap && !tail, a,
+                      tkv, tq, box_rows, q_tma, tail);
 }
 
 template <int D>
