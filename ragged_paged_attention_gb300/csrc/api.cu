@@ -256,6 +256,7 @@ int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const 
     a.num_sms = sms;
     a.overlap = prof_enabled() ? 0 : 1;
     rpa_rates(p->head_dim, a.kv_fp8 != 0, a.has_scale != 0, &a.pre_flops_per_ns_sm, &a.dec_bytes_per_ns_sm);
+    a.item_cost_keys = rpa_item_cost_keys(a.kv_fp8 || a.has_scale);
     a.decode_per_sm = rpa_decode_ctas_per_sm(a);
     if (a.decode_per_sm <= 0) return fail(RPA_ERR_CUDA, "decode kernel occupancy query failed");
     a.hdr = reinterpret_cast<WsHeader*>(ws);

@@ -26,6 +26,13 @@ constexpr int kMaxDecodeCtas = 2048;    // most decode shares (static, one per C
 constexpr int kPoolPercent = 0;         // share of the decode work left to the pool
 constexpr int kMinPoolChunk = 64;       // smallest pooled decode share (keys)
 constexpr int kPoolPerCta = 3;          // pooled shares per decode CTA (about)
+// Each decode group also costs its items a fixed start (descriptor, metadata, Q and the first
+// stage's latency) and, when split, a fence, ticket and merge. Counted in keys, that cost is laid
+// on the line ahead of the group's keys, so shares that cross more groups get fewer keys and all
+// shares still end together. Measured on GB300: 128 keys takes the Llama-3 bf16 decode kernel from
+// 190.7 to 182.3 us; the converting (fp8 or scaled) kernel, slower per key, ends best at 0
+// (Gemma-2 fp8: 204 us, 210 us at 128).
+inline int rpa_item_cost_keys(bool converting) { return converting ? 0 : 128; }
 
 // Prefill beside decode: the prefill items are tensor-core bound and the decode items HBM
 // bound, so the plan kernel gives prefill the share of the SMs that makes both lists end
@@ -79,6 +86,7 @@ struct RpaArgs {
     int overlap;                // run prefill beside decode (off while kernels are timed one by one)
     float pre_flops_per_ns_sm;  // prefill kernel rate per SM (this head size and cache type)
     float dec_bytes_per_ns_sm;  // decode kernel rate per SM while SMs, not HBM, limit it
+    int item_cost_keys;         // per-group cost on the decode line (a multiple of 16 keys)
     // workspace
     WsHeader* hdr;
     WorkItem* dec_items;

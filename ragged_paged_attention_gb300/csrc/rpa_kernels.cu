@@ -31,7 +31,7 @@ namespace rpa {
 __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     __shared__ int scan_scratch[40];
     __shared__ long long scan_ll[40];
-    __shared__ long long red[32];
+    __shared__ long long red[32], red_g[32];
     __shared__ float red_f[32];
     __shared__ int s_num;
     __shared__ long long s_q1, s_q2, s_ls;  // static share size, pooled share size, static part
@@ -60,15 +60,18 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     const int n_groups = cdiv(a.num_kv_heads, a.decode_heads);
     auto round_bk = [](int keys) { return (long long)cdiv(keys, kDecodeBK) * kDecodeBK; };
 
-    // pass 1: decode work (line length) and the prefill (query, key) pairs
-    long long work = 0;
+    // pass 1: decode work (line length: keys and per-group cost), decode groups and the prefill
+    // (query, key) pairs
+    long long work = 0, ngrp = 0;
     float pre_pairs = 0.f;
     for (int s = tid; s < num; s += blockDim.x) {
         int ql, kl;
         if (seq_shape(a, s, ql, kl) && ql >= 1) {
             if (ql * G <= 16) {
                 const int klo = decode_key_begin(a, ql, kl);
-                work += round_bk(kl - klo) * n_groups * cdiv(ql * G, kDecodeRows);
+                const long long g = (long long)n_groups * cdiv(ql * G, kDecodeRows);
+                work += (round_bk(kl - klo) + a.item_cost_keys) * g;
+                ngrp += g;
             } else {
                 // causal: query i of the chunk sees kl - ql + i + 1 keys (at most the window)
                 float seen = (float)kl - 0.5f * (float)(ql - 1);
@@ -79,23 +82,27 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     }
     for (int o = 16; o > 0; o >>= 1) {
         work += __shfl_xor_sync(0xffffffffu, work, o);
+        ngrp += __shfl_xor_sync(0xffffffffu, ngrp, o);
         pre_pairs += __shfl_xor_sync(0xffffffffu, pre_pairs, o);
     }
     if ((tid & 31) == 0) {
         red[tid >> 5] = work;
+        red_g[tid >> 5] = ngrp;
         red_f[tid >> 5] = pre_pairs;
     }
     __syncthreads();
     if (tid == 0) {
-        long long W = 0;
+        long long W = 0, NG = 0;
         float pp = 0.f;
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
             W += red[w];
+            NG += red_g[w];
             pp += red_f[w];
         }
         red[0] = W;
         s_pf = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
-        s_db = (float)W * (float)a.decode_heads * 2.f * (float)a.head_dim * (a.kv_fp8 ? 1.f : 2.f);
+        s_db = (float)(W - NG * a.item_cost_keys) * (float)a.decode_heads * 2.f * (float)a.head_dim *
+               (a.kv_fp8 ? 1.f : 2.f);
     }
     __syncthreads();
     // SMs for the prefill kernel beside decode: the n minimising max(prefill time on n SMs,
@@ -162,6 +169,8 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
         long long q2 = rest / ((long long)kPoolPerCta * ctas);
         q2 = max(q2, (rest + (kMaxDecodeCtas - r) - 1) / (kMaxDecodeCtas - r));
         q2 = max((long long)kMinPoolChunk, (q2 + kDecodeBK - 1) / kDecodeBK * kDecodeBK);
+        // (every share longer than a group's cost holds at least one key)
+        q2 = max(q2, (long long)(a.item_cost_keys + kDecodeBK));
         s_q1 = q1;
         s_q2 = q2;
         s_ls = ls;
@@ -188,19 +197,20 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
             if (ql * G <= 16) {
                 klo = decode_key_begin(a, ql, kl);
                 nrh = cdiv(ql * G, kDecodeRows);
-                wk = round_bk(kl - klo) * n_groups * nrh;
+                wk = (round_bk(kl - klo) + a.item_cost_keys) * n_groups * nrh;
             } else {
                 np = cdiv(ql * G, kPrefillRows) * a.num_kv_heads;
             }
         }
         long long tot_w;
         const long long pos = pos_base + block_exclusive_scan(wk, scan_ll, &tot_w);
-        // splits of each group: the number of CTA shares its stretch of the line meets
+        // splits of each group: the number of shares its keys' stretch of the line meets (a group
+        // spans its cost, then its keys)
         if (wk > 0) {
             const long long len = round_bk(kl - klo);
             for (int j = 0; j < n_groups * nrh; ++j) {
-                const long long p0 = pos + j * len;
-                nd += (int)(share_of(p0 + len - 1) - share_of(p0) + 1);
+                const long long kr0 = pos + j * (len + a.item_cost_keys) + a.item_cost_keys;
+                nd += (int)(share_of(kr0 + len - 1) - share_of(kr0) + 1);
             }
         }
         int tot_d, tot_p;
@@ -234,18 +244,19 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
             const int seq_first = k > 0 ? e_dend[k - 1] : 0;
             // the group j of this sequence holding the item, and the item's split in it
             int rel = idx - seq_first, first = dec_base + seq_first, j = 0;
-            long long p0 = e_pos[k];
-            int ns = (int)(share_of(p0 + len - 1) - share_of(p0) + 1);
+            long long p0 = e_pos[k], kr0 = p0 + a.item_cost_keys;  // group start, its keys' start
+            int ns = (int)(share_of(kr0 + len - 1) - share_of(kr0) + 1);
             while (rel >= ns) {
                 rel -= ns;
                 first += ns;
                 ++j;
-                p0 += len;
-                ns = (int)(share_of(p0 + len - 1) - share_of(p0) + 1);
+                p0 += len + a.item_cost_keys;
+                kr0 = p0 + a.item_cost_keys;
+                ns = (int)(share_of(kr0 + len - 1) - share_of(kr0) + 1);
             }
-            const long long c = share_of(p0) + rel;  // the share holding this piece
+            const long long c = share_of(kr0) + rel;  // the share holding this piece
             const long long c_lo = share_start(c);
-            const long long b0 = max(p0, c_lo) - p0, b1 = min(p0 + len, share_start(c + 1)) - p0;
+            const long long b0 = max(kr0, c_lo) - kr0, b1 = min(kr0 + len, share_start(c + 1)) - kr0;
             WorkItem w;
             w.seq = s0 + k;
             w.head = (j / nh) * a.decode_heads;
@@ -257,7 +268,9 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
             w.split = rel;
             a.dec_items[it] = w;
             a.tickets[it] = 0;
-            if (p0 + b0 == c_lo) a.cta_first[c] = it;  // the piece that opens share c
+            // the piece that opens share c: a later piece of a group, or its first when the share
+            // began within this group's stretch
+            if (rel > 0 || c_lo >= p0) a.cta_first[c] = it;
         }
         for (int idx = tid; idx < tot_p; idx += blockDim.x) {
             const int it = pre_base + idx;
