@@ -317,6 +317,28 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
     // an rpa_forward plan kernel behind may start now: it reads only metadata this kernel does
     // not write, and it ends after this grid has
     pdl_launch_dependents();
+    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    const int Hkv = a.num_kv_heads, C = 2 * Hkv;
+    const int row_chunks = a.head_dim * a.esz / 16;  // 16-byte chunks per head row
+    const int chunks = Hkv * 2 * row_chunks;
+    // one warp per token; each lane moves up to kBatch 16-byte chunks of the token's rows at a
+    // time, loaded before the sequence and page lookups (they depend on the token index only)
+    constexpr int kBatch = 8;
+    auto load_batch = [&](int t, int i0, uint4 (&v)[kBatch]) {
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = i0 + 32 * j;
+            if (i < chunks) {
+                const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
+                v[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(part ? a.new_v : a.new_k) +
+                                                             (((size_t)t * Hkv + head) * a.head_dim * a.esz) + c * 16));
+            }
+        }
+    };
+    // the first token's rows are in flight while the metadata arrives
+    const int t_first = blockIdx.x * warps + (threadIdx.x >> 5);
+    uint4 v[kBatch];
+    if (t_first < a.max_num_tokens) load_batch(t_first, lane, v);
     if (threadIdx.x == 0) {
         int n = a.num_seqs[0];
         if (n < 0 || n > a.max_num_seqs) {
@@ -335,12 +357,8 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
     __syncthreads();
     const int32_t* cu = cached ? s_cu : a.cu_q_lens;
     const int total = cu[num];
-    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
-    const int Hkv = a.num_kv_heads, C = 2 * Hkv;
-    const int row_chunks = a.head_dim * a.esz / 16;  // 16-byte chunks per head row
-    const int chunks = Hkv * 2 * row_chunks;
-    // one warp per token
-    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < min(total, a.max_num_tokens); t += gridDim.x * warps) {
+    for (int t = t_first; t < min(total, a.max_num_tokens); t += gridDim.x * warps) {
+        if (t != t_first) load_batch(t, lane, v);
         const int s = seq_of_token(cu, num, t);
         const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = a.kv_lens[s];
         if (t < q_start || t >= q_start + q_len) continue;
@@ -360,20 +378,10 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
         }
         uint8_t* slot = static_cast<uint8_t*>(a.kv_pages) +
                         ((size_t)page * a.page_size + pos % a.page_size) * C * a.head_dim * a.esz;
-        // up to 8 chunks per lane in flight: all loads of a batch before its stores
-        for (int i0 = lane; i0 < chunks; i0 += 32 * 8) {
-            uint4 v[8];
+        for (int i0 = lane; i0 < chunks; i0 += 32 * kBatch) {
+            if (i0 != lane) load_batch(t, i0, v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + 32 * j;
-                if (i < chunks) {
-                    const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
-                    v[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(part ? a.new_v : a.new_k) +
-                                                                 (((size_t)t * Hkv + head) * a.head_dim * a.esz) + c * 16));
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
                 const int i = i0 + 32 * j;
                 if (i < chunks) {
                     const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
