@@ -10,8 +10,9 @@ U[512, 2048]): the batch's new K/V rows are written into their pages
 Printed as one JSON line:
   value      query tokens/s over the whole job, inputs resident in HBM (CUDA events)
   e2e        the same through the public API from pinned host buffers, with the
-             host->device copy of the step's inputs and the device->host read of
-             its output inside the timed region
+             host->device copy of every step's inputs and the device->host read of
+             its output inside the timed region (double-buffered on two copy
+             streams, so the copies of neighbouring steps run under the compute)
   roofline   the dominant kernel's algorithmic bytes (or flops) per launch over its
              CUDA-event duration, against the measured HBM / bf16 peak
   cpu_baseline  the float64 oracle on a bounded sample of the same batch, host cores
@@ -472,28 +473,66 @@ def main():
     step_flops = acc["decode"][2] + acc["prefill"][2]
     t_roof = roof_time(step_bytes, step_flops, peaks)
 
-    # end to end: pinned host inputs -> device, update + attention, output -> host
+    # end to end: pinned host inputs -> device, update + attention, output -> host, every
+    # step. Served the way a serving loop would: inputs and outputs double-buffered on the
+    # device, the host-to-device copies on one copy stream and the device-to-host copy on
+    # another, so step i+1's inputs and step i-1's output move while step i computes.
     host = {k: v.pin_memory() for k, v in
             dict(q=b.q, new_k=b.new_k, new_v=b.new_v, kv_lens=b.kv_lens, page_indices=b.page_indices,
                  cu_q_lens=b.cu_q_lens, num_seqs=b.num_seqs).items()}
-    dq = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dq = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    outs_h = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in_free", "in_ready", "out_ready", "out_free")}
 
-    def e2e_step():
-        for k, v in host.items():
-            dq[k].copy_(v, non_blocking=True)
-        api.rpa_update_kv_cache(dq["new_k"], dq["new_v"], g.kv_pages, dq["kv_lens"], dq["page_indices"],
-                                dq["cu_q_lens"], dq["num_seqs"], workspace=ws_u)
-        api.rpa_forward(dq["q"], g.kv_pages, dq["kv_lens"], dq["page_indices"], dq["cu_q_lens"], dq["num_seqs"],
-                        out=out, workspace=ws, **opts)
-        out_h.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        s_in.wait_event(ev["in_free"][k])  # step i-2 is done with these device inputs
+        with torch.cuda.stream(s_in):
+            for name, v in host.items():
+                dq[k][name].copy_(v, non_blocking=True)
+        ev["in_ready"][k].record(s_in)
+        comp.wait_event(ev["in_ready"][k])
+        comp.wait_event(ev["out_free"][k])  # step i-2's output has reached the host
+        d = dq[k]
+        api.rpa_update_kv_cache(d["new_k"], d["new_v"], g.kv_pages, d["kv_lens"], d["page_indices"],
+                                d["cu_q_lens"], d["num_seqs"], workspace=ws_u)
+        api.rpa_forward(d["q"], g.kv_pages, d["kv_lens"], d["page_indices"], d["cu_q_lens"], d["num_seqs"],
+                        out=outs[k], workspace=ws, **opts)
+        ev["in_free"][k].record(comp)
+        ev["out_ready"][k].record(comp)
+        s_out.wait_event(ev["out_ready"][k])
+        with torch.cuda.stream(s_out):
+            outs_h[k].copy_(outs[k], non_blocking=True)
+        ev["out_free"][k].record(s_out)
+
+    def time_e2e(steps, warmup):
+        for i in range(warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(comp)
+        for i in range(warmup, warmup + steps):
+            e2e_step(i)
+        comp.wait_event(ev["out_free"][(warmup + steps - 1) % 2])  # the last output is on the host
+        e1.record(comp)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / steps
 
     ms_e2e = None
     if not args.no_e2e:
-        ms_e2e, _ = time_steps(e2e_step, args.steps, args.warmup, world)
-        ms_e2e = max_over_ranks(ms_e2e, world)
+        ms_e2e = max_over_ranks(time_e2e(args.steps, args.warmup), world)
+        # the host copy of the last output is the device result of the same inputs (one more
+        # resident step in the same launch mode: the decode shares depend on the SM split)
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(outs_h[(args.warmup + args.steps - 1) % 2][:b.num_tokens].to(dev), out[:b.num_tokens])
 
     # same-run variants (decode/prefill sub-launches are in `kernels`)
     variants = {}
@@ -525,7 +564,9 @@ def main():
             "clocks": clk,
             "e2e": None if ms_e2e is None else {
                 "value": T * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "copies": "pinned host buffers; inputs and outputs double-buffered on the device, "
+                          "host-to-device and device-to-host copies on their own streams beside the compute"},
             "cpu_baseline": cpu,
             "variants": variants,
         }
