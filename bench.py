@@ -5,7 +5,8 @@ One step = one pass of the hot path over one mixed prefill+decode batch shaped l
 Llama-3-8B serving (32 q / 8 kv heads, head_dim 128, page_size 16, 128 decode
 sequences with kv_len U[512, 4096] and 4 prefill chunks of 512 queries with kv_len
 U[512, 2048]): the batch's new K/V rows are written into their pages
-(rpa_update_kv_cache) and attention runs over the whole batch (rpa_forward).
+and attention runs over the whole batch, in one call (rpa_forward_update: the cache write
+of rpa_update_kv_cache shares a launch with rpa_forward's plan).
 
 Printed as one JSON line:
   value      query tokens/s over the whole job, inputs resident in HBM (CUDA events)
@@ -428,14 +429,12 @@ def main():
     opts = b.options()
     prm = api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)
     ws = torch.zeros(api.rpa_workspace_size(prm), dtype=torch.uint8, device=dev)
-    ws_u = torch.zeros(256, dtype=torch.uint8, device=dev)
     out = torch.empty_like(g.q)
 
     def step():
-        api.rpa_update_kv_cache(g.new_k, g.new_v, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs,
-                                workspace=ws_u)
-        api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, workspace=ws,
-                        **opts)
+        # the batch's new K/V rows into the cache, then attention: one call (rpa_forward_update)
+        api.rpa_forward_update(g.q, g.new_k, g.new_v, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens,
+                               g.num_seqs, out=out, workspace=ws, **opts)
 
     clocks = clock_sampler(local).start()
     ms, _, n_launch = time_steps(step, args.steps, args.warmup, world, launches=True)
@@ -443,7 +442,7 @@ def main():
     # per-kernel durations: a second pass with every launch bracketed by CUDA events (the
     # library runs its kernels one after another while they are timed)
     _, ktimes = time_steps(step, args.steps, 1, world, timer=True)
-    assert api.check_device_status(ws) == 0 and api.check_device_status(ws_u) == 0
+    assert api.check_device_status(ws) == 0
     ms = max_over_ranks(ms, world)
     T = b.num_tokens
     value = T * world / (ms * 1e-3)
@@ -499,10 +498,8 @@ def main():
         comp.wait_event(ev["in_ready"][k])
         comp.wait_event(ev["out_free"][k])  # step i-2's output has reached the host
         d = dq[k]
-        api.rpa_update_kv_cache(d["new_k"], d["new_v"], g.kv_pages, d["kv_lens"], d["page_indices"],
-                                d["cu_q_lens"], d["num_seqs"], workspace=ws_u)
-        api.rpa_forward(d["q"], g.kv_pages, d["kv_lens"], d["page_indices"], d["cu_q_lens"], d["num_seqs"],
-                        out=outs[k], workspace=ws, **opts)
+        api.rpa_forward_update(d["q"], d["new_k"], d["new_v"], g.kv_pages, d["kv_lens"], d["page_indices"],
+                               d["cu_q_lens"], d["num_seqs"], out=outs[k], workspace=ws, **opts)
         ev["in_free"][k].record(comp)
         ev["out_ready"][k].record(comp)
         s_out.wait_event(ev["out_ready"][k])
@@ -551,7 +548,7 @@ def main():
             "config": {"workload": "llama3_8b_mixed_batch", "num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128,
                        "page_size": 16, "decode_seqs": 128, "prefill_chunks": "4 x 512", "query_tokens": T,
                        "kv_cache_bytes": g.kv_pages.numel() * g.kv_pages.element_size(),
-                       "step": "rpa_update_kv_cache + rpa_forward",
+                       "step": "rpa_forward_update (cache write of the new K/V rows + attention)",
                        "l2": "inputs larger than L2 (KV cache >1 GB read each step)", "parallelism": "replicas"},
             "step_roofline": {"bytes": step_bytes, "flops": step_flops, "roofline_us": t_roof * 1e6,
                               "frac": t_roof / (ms * 1e-3), "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,

@@ -176,6 +176,18 @@ RPA_API int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const vo
                         const int32_t* num_seqs, void* workspace, size_t workspace_bytes,
                         rpa_stream_t stream);
 
+/* rpa_update_kv_cache followed by rpa_forward, in one call with one launch fewer: the cache
+ * write of the batch's new K/V rows (exactly as rpa_update_kv_cache: bit-exact, in place)
+ * runs in the same launch as the work-list plan, and the attention launches read the cache
+ * only after both have ended, so the new tokens attend to themselves. The tpu-inference RPA
+ * v2 wrapper leaves this write inside the attention call as a TODO; this is that fused form.
+ * Arguments as in the two calls; `workspace` is rpa_forward's (its error word also records the
+ * cache write's metadata errors). `out` must not alias q, kv_pages, new_k or new_v. */
+RPA_API int rpa_forward_update(const rpa_params* p, const void* q, const void* new_k, const void* new_v,
+                               void* kv_pages, const int32_t* kv_lens, const int32_t* page_indices,
+                               const int32_t* cu_q_lens, const int32_t* num_seqs, void* out, void* workspace,
+                               size_t workspace_bytes, rpa_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* MLA latent ragged paged attention                                       */
 /* ---------------------------------------------------------------------- */

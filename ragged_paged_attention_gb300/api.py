@@ -27,7 +27,8 @@ STATUS = {0: "RPA_OK", -1: "RPA_ERR_NULL", -2: "RPA_ERR_SHAPE", -3: "RPA_ERR_DTY
 EXPORTS = ("rpa_workspace_size", "rpa_forward", "rpa_update_kv_cache", "mla_workspace_size",
            "mla_update_kv_cache", "mla_rpa_forward", "sparse_mla_workspace_size", "sparse_mla_forward",
            "rpa_check_device_status", "rpa_last_error", "rpa_version", "rpa_profile_enable",
-           "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc", "rpa_launch_count")
+           "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc", "rpa_launch_count",
+           "rpa_forward_update")
 
 
 class RpaError(RuntimeError):
@@ -90,6 +91,7 @@ def load_library(path: str = LIB_PATH):
         lib.rpa_forward.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P, sz, P]
         lib.rpa_forward_noalloc.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P]
         lib.rpa_update_kv_cache.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P, sz, P]
+        lib.rpa_forward_update.argtypes = [ctypes.POINTER(rpa_params), P, P, P, P, P, P, P, P, P, P, sz, P]
         lib.mla_workspace_size.argtypes = [ctypes.POINTER(mla_params), szp]
         lib.mla_update_kv_cache.argtypes = [ctypes.POINTER(mla_params), P, P, P, P, P, P, P, P, P, sz, P]
         lib.mla_rpa_forward.argtypes = [ctypes.POINTER(mla_params), P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
@@ -257,6 +259,39 @@ def rpa_update_kv_cache(new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens
                                    _ptr(page_indices), _ptr(cu_q_lens), _ptr(num_seqs), _ptr(workspace),
                                    workspace.numel(), _stream()))
     return kv_pages
+
+
+def rpa_forward_update(q, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_scale=1.0,
+                       sliding_window=None, soft_cap=None, mask_value=None, k_scale=None, v_scale=None, out=None,
+                       workspace=None):
+    """rpa_update_kv_cache then rpa_forward in one call (the cache write shares the plan's
+    launch); writes ``kv_pages`` in place and returns ``out``."""
+    lib = load_library()
+    _dev(q, "q", torch.bfloat16)
+    _dev(kv_pages, "kv_pages")
+    _dev(new_k, "new_k", kv_pages.dtype)
+    _dev(new_v, "new_v", kv_pages.dtype)
+    for n, t in (("kv_lens", kv_lens), ("page_indices", page_indices), ("cu_q_lens", cu_q_lens),
+                 ("num_seqs", num_seqs)):
+        _dev(t, n, torch.int32)
+    prm = make_rpa_params(q, kv_pages, page_indices, sm_scale=sm_scale, sliding_window=sliding_window,
+                          soft_cap=soft_cap, mask_value=mask_value, k_scale=k_scale, v_scale=v_scale)
+    if kv_lens.numel() != prm.max_num_seqs or cu_q_lens.numel() != prm.max_num_seqs + 1 or num_seqs.numel() != 1:
+        raise ValueError("kv_lens must be [max_num_seqs], cu_q_lens [max_num_seqs + 1], num_seqs [1]")
+    if kv_pages.shape[-1] != q.shape[-1]:
+        raise ValueError("q and kv_pages head_dim differ")
+    if (new_k.shape != new_v.shape or new_k.shape[0] != q.shape[0] or new_k.shape[1] * 2 != kv_pages.shape[2]
+            or new_k.shape[2] != kv_pages.shape[3]):
+        raise ValueError("new_k/new_v must be [max_num_tokens, num_kv_heads, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.bfloat16)
+    if workspace is None:
+        workspace = Workspace.get(rpa_workspace_size(prm), q.device, "rpa")
+    _check(lib.rpa_forward_update(ctypes.byref(prm), _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(kv_pages),
+                                  _ptr(kv_lens), _ptr(page_indices), _ptr(cu_q_lens), _ptr(num_seqs), _ptr(out),
+                                  _ptr(workspace), workspace.numel(), _stream()))
+    return out
 
 
 def make_mla_params(ql_nope, q_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, *, sm_scale=1.0,

@@ -213,9 +213,10 @@ int rpa_workspace_size(const rpa_params* p, size_t* bytes) {
     return RPA_OK;
 }
 
-int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
-                const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs, void* out,
-                void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+// Validates an rpa_forward call and fills the kernels' argument block.
+static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                       const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs, void* out,
+                       void* workspace, size_t workspace_bytes, RpaArgs& a, int& sms) {
     int rc = check_rpa_params(p);
     if (rc) return rc;
     if (!q || !kv_pages || !kv_lens || !page_indices || !cu_q_lens || !num_seqs || !out)
@@ -225,10 +226,9 @@ int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const 
     const RpaLayout L = rpa_layout(p);
     rc = check_workspace(workspace, workspace_bytes, L.total);
     if (rc) return rc;
-    const int sms = num_sms_current();
+    sms = num_sms_current();
     if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    RpaArgs a;
     memset(&a, 0, sizeof a);
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.kv_pages = kv_pages;
@@ -268,24 +268,20 @@ int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const 
     a.partial_o = reinterpret_cast<float*>(ws + L.po);
     a.max_dec_items = L.max_dec;
     a.max_pre_items = L.max_pre;
-    cudaError_t e = launch_rpa_forward(a, sms, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "rpa_forward launch");
     return RPA_OK;
 }
 
-int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const void* new_v, void* kv_pages,
-                        const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
-                        const int32_t* num_seqs, void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+// Validates an rpa_update_kv_cache call (the workspace is checked by the caller) and fills the
+// cache-write kernel's argument block.
+static int rpa_update_prepare(const rpa_params* p, const void* new_k, const void* new_v, void* kv_pages,
+                              const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
+                              const int32_t* num_seqs, uint32_t* err, RpaUpdateArgs& a) {
     int rc = check_rpa_params(p);
     if (rc) return rc;
     if (!new_k || !new_v || !kv_pages || !kv_lens || !page_indices || !cu_q_lens || !num_seqs)
         return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
     if (!aligned16(new_k) || !aligned16(new_v) || !aligned16(kv_pages))
         return fail(RPA_ERR_VALUE, "new_k, new_v and kv_pages must be 16-byte aligned");
-    if (workspace && workspace_bytes < (size_t)kWsHeaderBytes) return fail(RPA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
-    const int sms = num_sms_current();
-    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
-    RpaUpdateArgs a;
     a.new_k = new_k;
     a.new_v = new_v;
     a.kv_pages = kv_pages;
@@ -293,7 +289,7 @@ int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const void* new_
     a.page_indices = page_indices;
     a.cu_q_lens = cu_q_lens;
     a.num_seqs = num_seqs;
-    a.err = workspace ? &reinterpret_cast<WsHeader*>(workspace)->error_bits : nullptr;
+    a.err = err;
     a.max_num_tokens = p->max_num_tokens;
     a.num_kv_heads = p->num_combined_kv_heads / 2;
     a.head_dim = p->head_dim;
@@ -302,8 +298,53 @@ int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const void* new_
     a.page_size = p->page_size;
     a.max_num_seqs = p->max_num_seqs;
     a.pages_per_seq = p->pages_per_seq;
+    return RPA_OK;
+}
+
+int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* num_seqs, void* out,
+                void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+    RpaArgs a;
+    int sms = 0;
+    const int rc = rpa_prepare(p, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, out, workspace,
+                               workspace_bytes, a, sms);
+    if (rc) return rc;
+    cudaError_t e = launch_rpa_forward(a, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_forward launch");
+    return RPA_OK;
+}
+
+int rpa_update_kv_cache(const rpa_params* p, const void* new_k, const void* new_v, void* kv_pages,
+                        const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
+                        const int32_t* num_seqs, void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+    if (workspace && workspace_bytes < (size_t)kWsHeaderBytes) return fail(RPA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    RpaUpdateArgs a;
+    const int rc = rpa_update_prepare(p, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs,
+                                      workspace ? &reinterpret_cast<WsHeader*>(workspace)->error_bits : nullptr, a);
+    if (rc) return rc;
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
     cudaError_t e = launch_rpa_update(a, sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "rpa_update_kv_cache launch");
+    return RPA_OK;
+}
+
+int rpa_forward_update(const rpa_params* p, const void* q, const void* new_k, const void* new_v, void* kv_pages,
+                       const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
+                       const int32_t* num_seqs, void* out, void* workspace, size_t workspace_bytes,
+                       rpa_stream_t stream) {
+    RpaArgs a;
+    int sms = 0;
+    int rc = rpa_prepare(p, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, out, workspace, workspace_bytes,
+                         a, sms);
+    if (rc) return rc;
+    if (out == new_k || out == new_v) return fail(RPA_ERR_VALUE, "out must not alias new_k or new_v");
+    RpaUpdateArgs u;
+    rc = rpa_update_prepare(p, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs,
+                            &a.hdr->error_bits, u);
+    if (rc) return rc;
+    cudaError_t e = launch_rpa_forward_update(a, u, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_forward_update launch");
     return RPA_OK;
 }
 

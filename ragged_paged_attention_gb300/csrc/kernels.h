@@ -174,6 +174,7 @@ struct MlaUpdateArgs {
 };
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_rpa_forward_update(const RpaArgs& a, const RpaUpdateArgs& u, int num_sms, cudaStream_t stream);
 // Launch with programmatic stream serialization when pdl (the kernel may start before the
 // previous launch of the stream ends; it orders itself with griddepcontrol), else plainly.
 template <typename... P, typename... A>

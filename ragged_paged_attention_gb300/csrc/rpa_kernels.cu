@@ -28,7 +28,7 @@ namespace rpa {
 // finishes last). Equal shares remove the tail a queue of long items leaves (a few CTAs
 // finishing while the rest of the GPU idles); the pool evens out CTAs that stream faster
 // than others.
-__global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
+__device__ __forceinline__ void plan_body(const RpaArgs& a) {
     __shared__ int scan_scratch[40];
     __shared__ long long scan_ll[40];
     __shared__ long long red[32], red_g[32];
@@ -308,10 +308,12 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) {
     }
 }
 
+__global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) { plan_body(a); }
+
 // ---------------------------------------------------------------------------
 // Cache write: new K/V rows -> their page slots (16-byte copies, bit exact)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
+__device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, int nblocks) {
     extern __shared__ int s_cu[];  // cu_q_lens[0..num] when it fits (kCuCache entries)
     __shared__ int s_num;
     // an rpa_forward plan kernel behind may start now: it reads only metadata this kernel does
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
         }
     };
     // the first token's rows are in flight while the metadata arrives
-    const int t_first = blockIdx.x * warps + (threadIdx.x >> 5);
+    const int t_first = block * warps + (threadIdx.x >> 5);
     uint4 v[kBatch];
     if (t_first < a.max_num_tokens) load_batch(t_first, lane, v);
     if (threadIdx.x == 0) {
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
     __syncthreads();
     const int32_t* cu = cached ? s_cu : a.cu_q_lens;
     const int total = cu[num];
-    for (int t = t_first; t < min(total, a.max_num_tokens); t += gridDim.x * warps) {
+    for (int t = t_first; t < min(total, a.max_num_tokens); t += nblocks * warps) {
         if (t != t_first) load_batch(t, lane, v);
         const int s = seq_of_token(cu, num, t);
         const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = a.kv_lens[s];
@@ -392,9 +394,33 @@ __global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) {
     }
 }
 
+__global__ void __launch_bounds__(256) rpa_update_kernel(RpaUpdateArgs a) { update_body(a, blockIdx.x, gridDim.x); }
+
+// The cache write and the plan in one launch (rpa_forward_update): block 0 plans, the others
+// write the batch's new K/V rows. The attention grids behind start reading only once this whole
+// grid has ended, so they see the new rows.
+__global__ void __launch_bounds__(1024) rpa_plan_update_kernel(RpaArgs a, RpaUpdateArgs u) {
+    if (blockIdx.x == 0)
+        plan_body(a);
+    else
+        update_body(u, blockIdx.x - 1, gridDim.x - 1);
+}
+
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
+// the attention launches behind the plan: with overlap, prefill on the plan's share of the SMs,
+// decode started early (programmatic launch) on the rest and finishing after that prefill grid,
+// then the prefill items still queued when decode ran dry, on every SM; otherwise prefill then
+// decode
+static cudaError_t launch_attention(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    cudaError_t e = launch_rpa_prefill(a, num_sms, stream, 0);
+    if (e != cudaSuccess) return e;
+    e = launch_rpa_decode(a, num_sms, stream);
+    if (e != cudaSuccess || !a.overlap) return e;
+    return launch_rpa_prefill(a, num_sms, stream, 1);
+}
+
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream) {
     cudaError_t e;
     {
@@ -402,14 +428,20 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
         e = launch_pdl(rpa_plan_kernel, dim3(1), dim3(1024), 0, stream, a.overlap != 0, a);
     }
     if (e != cudaSuccess) return e;
-    // overlap: prefill on the plan's share of the SMs, decode started early (programmatic
-    // launch) on the rest and finishing after that prefill grid, then the prefill items still
-    // queued when decode ran dry, on every SM; otherwise prefill then decode
-    e = launch_rpa_prefill(a, num_sms, stream, 0);
-    if (e != cudaSuccess) return e;
-    e = launch_rpa_decode(a, num_sms, stream);
-    if (e != cudaSuccess || !a.overlap) return e;
-    return launch_rpa_prefill(a, num_sms, stream, 1);
+    return launch_attention(a, num_sms, stream);
+}
+
+cudaError_t launch_rpa_forward_update(const RpaArgs& a, const RpaUpdateArgs& u, int num_sms, cudaStream_t stream) {
+    // one warp per new token in 1024-thread blocks, behind the plan's block
+    const int ublocks = max(1, min(cdiv(u.max_num_tokens, 32), num_sms * 2));
+    const int smem = min(u.max_num_seqs + 1, kCuCache) * (int)sizeof(int);
+    {
+        ProfScope ps("rpa_plan_update", stream);
+        rpa_plan_update_kernel<<<1 + ublocks, 1024, smem, stream>>>(a, u);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return launch_attention(a, num_sms, stream);
 }
 
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream) {

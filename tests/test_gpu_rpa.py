@@ -192,3 +192,37 @@ def test_update_then_attend_full_size():
     ref = oracle.rpa(b.q, ref_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=toks,
                      **b.options())
     assert max_abs(out[toks], ref[toks]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("make", [
+    lambda: workloads.llama_mixed(scale=1 / 8),
+    lambda: workloads.gemma_options(scale=1 / 8),
+    lambda: workloads.make_rpa([1, 1, 6, 19, 1], [33, 1, 6, 40, 300], num_q_heads=8, num_kv_heads=4, head_dim=64,
+                               page_size=8, seed=19, kv_dtype=torch.float8_e4m3fn, k_scale=0.37, v_scale=1.7,
+                               max_num_seqs=7, max_num_tokens=40, extra_pages=4),
+], ids=["llama", "gemma_fp8", "fp8_scaled_d64"])
+def test_forward_update_matches_update_then_forward(make):
+    # the fused call writes the same cache bytes as rpa_update_kv_cache and attends over them
+    b = make()
+    n = len(b.q_lens)
+    ref_pages = oracle.rpa_update_kv_cache(b.new_k[:b.num_tokens].contiguous(), b.new_v[:b.num_tokens].contiguous(),
+                                           b.kv_pages, b.kv_lens[:n], b.page_indices[:n], b.cu_q_lens[:n + 1], n)
+    g1, g2 = b.to("cuda"), b.to("cuda")
+    opts = b.options()
+    api.rpa_update_kv_cache(g1.new_k, g1.new_v, g1.kv_pages, g1.kv_lens, g1.page_indices, g1.cu_q_lens, g1.num_seqs)
+    out1 = api.rpa_forward(g1.q, g1.kv_pages, g1.kv_lens, g1.page_indices, g1.cu_q_lens, g1.num_seqs, **opts)
+    ws = torch.zeros(api.rpa_workspace_size(api.make_rpa_params(g2.q, g2.kv_pages, g2.page_indices, **opts)),
+                     dtype=torch.uint8, device="cuda")
+    out2 = torch.full_like(g2.q, 7.0)
+    api.rpa_forward_update(g2.q, g2.new_k, g2.new_v, g2.kv_pages, g2.kv_lens, g2.page_indices, g2.cu_q_lens,
+                           g2.num_seqs, out=out2, workspace=ws, **opts)
+    assert api.check_device_status(ws) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(g2.kv_pages.cpu().view(torch.uint8), ref_pages.view(torch.uint8))
+    T = b.num_tokens
+    assert torch.equal(out2[:T], out1[:T])  # same plan, same kernels: the same bits
+    assert (out2[T:].float() == 7.0).all()
+    tokens = sample_tokens(b.q_lens)
+    ref = oracle.rpa(b.q, ref_pages, b.kv_lens, b.page_indices, b.cu_q_lens, n, tokens=tokens, **opts)
+    tol = TOL_FP8 * (opts["v_scale"] or 1.0) if b.kv_pages.dtype == torch.float8_e4m3fn else TOL_BF16
+    assert max_abs(out2[tokens], ref[tokens]) <= tol
