@@ -239,7 +239,9 @@ RPA_API int mla_update_kv_cache(const mla_params* p, const void* new_kv_c, const
                         size_t workspace_bytes, rpa_stream_t stream);
 
 /* mla_update_kv_cache followed by attention of every query token over the updated
- * caches (the caches are modified in place). */
+ * caches (the caches are modified in place).  The cache write runs in the same launch as
+ * the work-list plan (the MLA v1 page leaves fusing it as a TODO); attention starts once
+ * both have ended. */
 RPA_API int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, const void* new_kv_c,
                     const void* new_k_pe, void* cache_kv_c, void* cache_k_pe, const int32_t* kv_lens,
                     const int32_t* page_indices, const int32_t* cu_q_lens, const int32_t* distribution,

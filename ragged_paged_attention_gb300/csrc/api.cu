@@ -356,11 +356,9 @@ int mla_workspace_size(const mla_params* p, size_t* bytes) {
     return RPA_OK;
 }
 
-static int mla_update_impl(const mla_params* p, const void* new_kv_c, const void* new_k_pe, void* cache_kv_c,
-                           void* cache_k_pe, const int32_t* kv_lens, const int32_t* page_indices,
-                           const int32_t* cu_q_lens, const int32_t* distribution, uint32_t* err, int sms,
-                           cudaStream_t stream) {
-    MlaUpdateArgs a;
+static void mla_update_args(const mla_params* p, const void* new_kv_c, const void* new_k_pe, void* cache_kv_c,
+                            void* cache_k_pe, const int32_t* kv_lens, const int32_t* page_indices,
+                            const int32_t* cu_q_lens, const int32_t* distribution, uint32_t* err, MlaUpdateArgs& a) {
     a.new_kv_c = static_cast<const __nv_bfloat16*>(new_kv_c);
     a.new_k_pe = static_cast<const __nv_bfloat16*>(new_k_pe);
     a.cache_kv_c = static_cast<__nv_bfloat16*>(cache_kv_c);
@@ -379,9 +377,6 @@ static int mla_update_impl(const mla_params* p, const void* new_kv_c, const void
     a.page_size = p->page_size;
     a.max_num_seqs = p->max_num_seqs;
     a.pages_per_seq = p->pages_per_seq;
-    cudaError_t e = launch_mla_update(a, sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "mla_update_kv_cache launch");
-    return RPA_OK;
 }
 
 int mla_update_kv_cache(const mla_params* p, const void* new_kv_c, const void* new_k_pe, void* cache_kv_c,
@@ -398,9 +393,12 @@ int mla_update_kv_cache(const mla_params* p, const void* new_kv_c, const void* n
     if (workspace && workspace_bytes < (size_t)kWsHeaderBytes) return fail(RPA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
     const int sms = num_sms_current();
     if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
-    return mla_update_impl(p, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
-                           distribution, workspace ? &reinterpret_cast<WsHeader*>(workspace)->error_bits : nullptr,
-                           sms, reinterpret_cast<cudaStream_t>(stream));
+    MlaUpdateArgs a;
+    mla_update_args(p, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens, distribution,
+                    workspace ? &reinterpret_cast<WsHeader*>(workspace)->error_bits : nullptr, a);
+    cudaError_t e = launch_mla_update(a, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "mla_update_kv_cache launch");
+    return RPA_OK;
 }
 
 int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, const void* new_kv_c,
@@ -425,9 +423,9 @@ int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, 
     if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = mla_update_impl(p, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
-                         distribution, &reinterpret_cast<WsHeader*>(ws)->error_bits, sms, st);
-    if (rc) return rc;
+    MlaUpdateArgs u;
+    mla_update_args(p, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens, distribution,
+                    &reinterpret_cast<WsHeader*>(ws)->error_bits, u);
     LatentArgs a;
     memset(&a, 0, sizeof a);
     a.sparse = 0;
@@ -457,7 +455,8 @@ int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, 
     a.partial_ml = reinterpret_cast<float*>(ws + L.pml);
     a.partial_o = reinterpret_cast<float*>(ws + L.po);
     a.max_items = L.max_items;
-    cudaError_t e = launch_mla_forward(a, sms, st);
+    // the cache write shares the plan's launch; attention starts once both have ended
+    cudaError_t e = launch_mla_forward_update(a, u, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "mla_rpa_forward launch");
     return RPA_OK;
 }

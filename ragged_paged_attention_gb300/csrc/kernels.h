@@ -175,6 +175,7 @@ struct MlaUpdateArgs {
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_rpa_forward_update(const RpaArgs& a, const RpaUpdateArgs& u, int num_sms, cudaStream_t stream);
+cudaError_t launch_mla_forward_update(const LatentArgs& a, const MlaUpdateArgs& u, int num_sms, cudaStream_t stream);
 // Launch with programmatic stream serialization when pdl (the kernel may start before the
 // previous launch of the stream ends; it orders itself with griddepcontrol), else plainly.
 template <typename... P, typename... A>
@@ -198,7 +199,6 @@ int rpa_decode_ctas_per_sm(const RpaArgs& a);  // resident CTAs per SM of the ke
 cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream, int tail);
 int decode_heads_for(int head_dim, bool fp8);
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream);
-cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_sparse_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_attention(const LatentArgs& a, int num_sms, cudaStream_t stream);

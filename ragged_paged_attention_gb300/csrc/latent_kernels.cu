@@ -23,7 +23,7 @@ namespace rpa {
 // ---------------------------------------------------------------------------
 // MLA cache update: one warp per token, 16-byte copies, rope pad written as zeros
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) {
+__device__ __forceinline__ void mla_update_body(const MlaUpdateArgs& a, int block, int nblocks) {
     extern __shared__ int s_cu[];  // cu_q_lens[0..num] when it fits (kCuCache entries)
     __shared__ int s_num;
     if (threadIdx.x == 0) {
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) {
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const int kv_chunks = a.lkv_pad / 8, pe_chunks = a.r_pad / 8;
-    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < min(total, a.max_num_tokens); t += gridDim.x * warps) {
+    for (int t = block * warps + (threadIdx.x >> 5); t < min(total, a.max_num_tokens); t += nblocks * warps) {
         const int s = seq_of_token(cu, num, t);
         const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = a.kv_lens[s];
         if (t < q_start || t >= q_start + q_len) continue;
@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) {
     }
 }
 
+__global__ void __launch_bounds__(256) mla_update_kernel(MlaUpdateArgs a) { mla_update_body(a, blockIdx.x, gridDim.x); }
+
 // ---------------------------------------------------------------------------
 // MLA plan: one item per (token, 64-head tile, key chunk)
 // ---------------------------------------------------------------------------
@@ -120,7 +122,7 @@ __device__ __forceinline__ bool mla_token(const LatentArgs& a, int num, int t, i
     return true;
 }
 
-__global__ void __launch_bounds__(1024) mla_plan_kernel(LatentArgs a) {
+__device__ __forceinline__ void mla_plan_body(const LatentArgs& a) {
     __shared__ int scan_scratch[40];
     __shared__ long long red[32];
     __shared__ int s_num, s_total, s_chunk, s_bad;
@@ -205,6 +207,15 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(LatentArgs a) {
     }
 }
 
+// The cache write and the plan in one launch (mla_rpa_forward): block 0 plans, the others write
+// the batch's new latent rows; the attention launch behind starts once this whole grid has ended.
+__global__ void __launch_bounds__(1024) mla_plan_update_kernel(LatentArgs a, MlaUpdateArgs u) {
+    if (blockIdx.x == 0)
+        mla_plan_body(a);
+    else
+        mla_update_body(u, blockIdx.x - 1, gridDim.x - 1);
+}
+
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream) {
     const int grid = min(cdiv(a.max_num_tokens, 8), num_sms * 8);
     if (grid <= 0) return cudaSuccess;
@@ -214,14 +225,16 @@ cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_mla_forward(const LatentArgs& a, int num_sms, cudaStream_t stream) {
-    cudaError_t e;
+cudaError_t launch_mla_forward_update(const LatentArgs& a, const MlaUpdateArgs& u, int num_sms, cudaStream_t stream) {
+    // one warp per new token in 1024-thread blocks, behind the plan's block
+    const int ublocks = max(1, min(cdiv(u.max_num_tokens, 32), num_sms * 2));
+    const int smem = min(u.max_num_seqs + 1, kCuCache) * (int)sizeof(int);
     {
-        ProfScope ps("mla_plan", stream);
-        mla_plan_kernel<<<1, 1024, 0, stream>>>(a);
-        e = cudaGetLastError();
+        ProfScope ps("mla_plan_update", stream);
+        mla_plan_update_kernel<<<1 + ublocks, 1024, smem, stream>>>(a, u);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    if (e != cudaSuccess) return e;
     return launch_mla_attention(a, num_sms, stream);
 }
 
