@@ -9,6 +9,7 @@
  *   rpa_update_kv_cache  scatter of the batch's new K/V tokens into their pages
  *                        (no counterpart on the pages beyond the v2 wrapper's TODO for a
  *                        cache-write kernel; defined like the MLA update_kv_cache).
+ *                        rpa_forward_update does both in one call.
  *   mla_rpa_forward      MLA latent attention with its cache update
  *                        (tpu-inference "mla/v1/kernel.py", update_kv_cache and
  *                        mla_ragged_paged_attention / ref_mla_ragged_paged_attention).
