@@ -103,6 +103,23 @@ class SparseParams(ctypes.Structure):
     ]
 
 
+class RaggedParams(ctypes.Structure):
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32),
+        ("num_seqs", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("dv", ctypes.c_int32),
+        ("rope", ctypes.c_int32),
+        ("row_stride", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("read_block", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_page_ids", ctypes.c_int32),
+        ("total_num_pages", ctypes.c_int32),
+        ("sm_scale", ctypes.c_double),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile ``rpa_oracle.c`` into ``_build/liboracle.so`` (gcc, OpenMP)."""
     with _lock:
@@ -131,6 +148,9 @@ def _load():
                                    ctypes.c_int]
         lib.oracle_sparse_mla.argtypes = [ctypes.POINTER(SparseParams), P, P, P, P, P, P, i32, P,
                                           ctypes.c_int]
+        lib.oracle_sparse_ragged_write.argtypes = [ctypes.POINTER(RaggedParams), P, P, P, P]
+        lib.oracle_sparse_mla_ragged.argtypes = [ctypes.POINTER(RaggedParams), P, P, P, P, P, P, P, P, P, P, i32,
+                                                 P, ctypes.c_int]
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
@@ -138,7 +158,7 @@ def _load():
         lib.oracle_round_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_round_f32_to_bf16.restype = ctypes.c_double
         for f in ("oracle_rpa", "oracle_rpa_update_kv_cache", "oracle_mla_update_kv_cache",
-                  "oracle_mla", "oracle_sparse_mla"):
+                  "oracle_mla", "oracle_sparse_mla", "oracle_sparse_ragged_write", "oracle_sparse_mla_ragged"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -304,6 +324,49 @@ def sparse_mla(q, cache, indices, positions, page_table, *, read_block, page_siz
                                _ptr(_i32(indices)), _ptr(_i32(positions)), _ptr(_i32(page_table)), _ptr(qs),
                                0 if qs is None else qs.numel(), _ptr(out), _nthreads(nthreads))
     _check(rc, "oracle_sparse_mla")
+    return out
+
+
+def _ragged_params(ql, qpe, cache, topk, seq_lens, page_indices, *, read_block, page_size, sm_scale):
+    T, H, dv = ql.shape
+    row_stride = cache.shape[-1]
+    return RaggedParams(num_tokens=T, num_seqs=seq_lens.numel(), num_heads=H, dv=dv, rope=qpe.shape[-1],
+                        row_stride=row_stride, topk=topk.shape[-1], read_block=read_block, page_size=page_size,
+                        num_page_ids=page_indices.numel(),
+                        total_num_pages=cache.numel() // (page_size * row_stride), sm_scale=float(sm_scale))
+
+
+def sparse_ragged_write(kvc, kpe, cache, loc, *, page_size) -> torch.Tensor:
+    """The packed-ragged self-write; returns a written copy of ``cache`` (any shape whose
+    row-major bytes are ``[P * page_size, row_stride]``)."""
+    lib = _load()
+    T, dv = kvc.shape
+    row_stride = cache.shape[-1]
+    prm = RaggedParams(num_tokens=T, num_seqs=1, num_heads=1, dv=dv, rope=kpe.shape[-1], row_stride=row_stride,
+                       topk=1, read_block=1, page_size=page_size, num_page_ids=1,
+                       total_num_pages=cache.numel() // (page_size * row_stride), sm_scale=1.0)
+    out = cache.contiguous().clone()
+    _check(lib.oracle_sparse_ragged_write(ctypes.byref(prm), _ptr(kvc.contiguous()), _ptr(kpe.contiguous()),
+                                          _ptr(out), _ptr(_i32(loc))), "oracle_sparse_ragged_write")
+    return out
+
+
+def sparse_mla_ragged(ql, qpe, cache, topk, positions, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *,
+                      read_block, page_size, sm_scale, queries=None, nthreads=None) -> torch.Tensor:
+    """DSA sparse MLA in the packed-ragged mode over an already written cache; returns
+    float64 ``[T, H, dv]`` (rows of unlisted tokens are NaN)."""
+    lib = _load()
+    prm = _ragged_params(ql, qpe, cache, topk, seq_lens, page_indices, read_block=read_block, page_size=page_size,
+                         sm_scale=sm_scale)
+    T, H, dv = ql.shape
+    out = torch.full((T, H, dv), math.nan, dtype=torch.float64)
+    qs = None if queries is None else _i32(queries)
+    rc = lib.oracle_sparse_mla_ragged(ctypes.byref(prm), _ptr(ql.contiguous()), _ptr(qpe.contiguous()),
+                                      _ptr(cache.contiguous()), _ptr(_i32(topk)), _ptr(_i32(positions)),
+                                      _ptr(_i32(seq_lens)), _ptr(_i32(cu_q_lens)), _ptr(_i32(cu_kv_lens)),
+                                      _ptr(_i32(page_indices)), _ptr(qs), 0 if qs is None else qs.numel(), _ptr(out),
+                                      _nthreads(nthreads))
+    _check(rc, "oracle_sparse_mla_ragged")
     return out
 
 

@@ -20,6 +20,10 @@
  *   - oracle_sparse_mla           : sglang-jax "dsa/sparse_mla_prefill.py",
  *                                   _sparse_mla_kernel_chunked_hminor (validity rule,
  *                                   -inf-safe softmax) and units_to_token_ids.
+ *   - oracle_sparse_ragged_write,   same page, prefill_write_and_attend_ragged (the
+ *     oracle_sparse_mla_ragged      self-write, the request of each token, its causal
+ *                                   bound and page base) and the ragged branch of
+ *                                   sparse_mla_attention.
  *
  * Arithmetic is IEEE binary64 except where the pages fix a precision: the RPA
  * reference dequantises K and V as float32(k) * k_scale rounded to the query
@@ -485,6 +489,141 @@ int oracle_sparse_mla(const oracle_sparse_params* p, const uint16_t* q, const ui
         }
         free(x);
         free(keys);
+        free(rows);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------ */
+/* DSA sparse MLA, packed-ragged mode with the self-write              */
+/* (sglang-jax "dsa/sparse_mla_prefill.py", prefill_write_and_attend_  */
+/* ragged and the ragged branch of sparse_mla_attention).              */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t num_tokens;   /* T: queries packed along one axis */
+    int32_t num_seqs;     /* S: requests (length of seq_lens) */
+    int32_t num_heads;    /* H */
+    int32_t dv;           /* 512: kv_lora_rank, the value width */
+    int32_t rope;         /* 64: k_rope width; dk = dv + rope */
+    int32_t row_stride;   /* stored row width of the cache (>= dv + rope) */
+    int32_t topk;         /* K unit slots per query */
+    int32_t read_block;   /* RB tokens per unit */
+    int32_t page_size;
+    int32_t num_page_ids; /* PTW: length of the packed page_indices list */
+    int32_t total_num_pages;
+    double sm_scale;
+} oracle_ragged_params;
+
+/* Self-write: token t's row [kvc[t] (dv) | kpe[t] (rope) | zeros] goes to flat cache row
+ * loc[t]; a slot outside [0, P * page_size) (the -1 padding included) is dropped and the
+ * cache is left as it was there. */
+int oracle_sparse_ragged_write(const oracle_ragged_params* p, const uint16_t* kvc, const uint16_t* kpe,
+                               uint16_t* cache, const int32_t* loc) {
+    if (!p || !kvc || !kpe || !cache || !loc) return ORACLE_ERR_ARG;
+    const long slots = (long)p->total_num_pages * p->page_size;
+    for (int t = 0; t < p->num_tokens; ++t) {
+        const long slot = loc[t];
+        if (slot < 0 || slot >= slots) continue;
+        uint16_t* row = cache + (size_t)slot * p->row_stride;
+        for (int d = 0; d < p->row_stride; ++d) row[d] = 0;
+        for (int d = 0; d < p->dv; ++d) row[d] = kvc[(size_t)t * p->dv + d];
+        for (int d = 0; d < p->rope; ++d) row[p->dv + d] = kpe[(size_t)t * p->rope + d];
+    }
+    return ORACLE_OK;
+}
+
+/* Request of token t: the number of cu_q_lens[1..S] entries <= t (searchsorted, right
+ * side, over cu_q_lens[1:]), clipped to [0, S - 1]. */
+static int ragged_request(const int32_t* cu_q_lens, int S, int t) {
+    int n = 0;
+    for (int i = 1; i <= S; ++i)
+        if (cu_q_lens[i] <= t) ++n;
+    return n < 0 ? 0 : (n > S - 1 ? S - 1 : n);
+}
+
+/* ql bf16 [T, H, dv], qpe bf16 [T, H, rope] (the query is their concatenation); cache bf16
+ * [P * page_size, row_stride] (already written); topk [T, K] request-local unit ids (-1 =
+ * none); positions [T]; seq_lens [S]; cu_q_lens [S + 1]; cu_kv_lens [S + 1] (page-aligned
+ * key offsets); page_indices [PTW].  Token t of request r = request(t) attends to key kp =
+ * u * RB + j of each selected unit u when kp <= positions[t] and kp < seq_lens[r]; the key's
+ * page is page_indices[min(cu_kv_lens[r] / page_size + kp / page_size, PTW - 1)].
+ * out float64 [T, H, dv] for the listed tokens (all when queries == NULL). */
+int oracle_sparse_mla_ragged(const oracle_ragged_params* p, const uint16_t* ql, const uint16_t* qpe,
+                             const uint16_t* cache, const int32_t* topk, const int32_t* positions,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                             const int32_t* page_indices, const int32_t* queries, int32_t n_queries, double* out,
+                             int nthreads) {
+    if (!p || !ql || !qpe || !cache || !topk || !positions || !seq_lens || !cu_q_lens || !cu_kv_lens ||
+        !page_indices || !out || p->num_seqs < 1 || p->num_page_ids < 1)
+        return ORACLE_ERR_ARG;
+    const int T = p->num_tokens, H = p->num_heads, K = p->topk, RB = p->read_block, ps = p->page_size;
+    const int dk = p->dv + p->rope;
+    const int n = queries ? n_queries : T;
+    int err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(default_threads(nthreads))
+    for (int it = 0; it < n; ++it) {
+        const int t = queries ? queries[it] : it;
+        if (t < 0 || t >= T) {
+#pragma omp atomic write
+            err = ORACLE_ERR_ARG;
+            continue;
+        }
+        const int r = ragged_request(cu_q_lens, p->num_seqs, t);
+        const long bound = seq_lens[r];
+        const long base = cu_kv_lens[r] / ps;
+        const int qpos = positions[t];
+        size_t* rows = (size_t*)malloc(sizeof(size_t) * (size_t)K * RB + 8);
+        int nk = 0, bad = 0;
+        for (int i = 0; i < K; ++i) {
+            const int u = topk[(size_t)t * K + i];
+            if (u < 0) continue;
+            for (int j = 0; j < RB; ++j) {
+                const long kp = (long)u * RB + j;
+                if (!(kp <= qpos && kp < bound)) continue;
+                long pidx = base + kp / ps;
+                if (pidx > p->num_page_ids - 1) pidx = p->num_page_ids - 1;
+                if (pidx < 0) {
+                    bad = 1;
+                    continue;
+                }
+                const int32_t page = page_indices[pidx];
+                if (page < 0 || page >= p->total_num_pages) {
+                    bad = 1;
+                    continue;
+                }
+                rows[nk++] = (size_t)page * ps + (size_t)(kp % ps);
+            }
+        }
+        if (bad) {
+#pragma omp atomic write
+            err = ORACLE_ERR_PAGE;
+            free(rows);
+            continue;
+        }
+        double* x = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+        for (int h = 0; h < H; ++h) {
+            const uint16_t* qn = ql + ((size_t)t * H + h) * p->dv;
+            const uint16_t* qr = qpe + ((size_t)t * H + h) * p->rope;
+            for (int i = 0; i < nk; ++i) {
+                const uint16_t* row = cache + rows[i] * p->row_stride;
+                double dot = 0.0;
+                for (int d = 0; d < dk; ++d)
+                    dot += (double)bf16_bits_to_f32(d < p->dv ? qn[d] : qr[d - p->dv]) * bf16_bits_to_f32(row[d]);
+                x[i] = p->sm_scale * dot;
+            }
+            double l;
+            softmax_weights(x, nk, &l);
+            double* o = out + ((size_t)t * H + h) * p->dv;
+            for (int d = 0; d < p->dv; ++d) o[d] = 0.0;
+            for (int i = 0; i < nk; ++i) {
+                const uint16_t* row = cache + rows[i] * p->row_stride;
+                for (int d = 0; d < p->dv; ++d) o[d] += x[i] * bf16_bits_to_f32(row[d]);
+            }
+            const double inv = l > 0.0 ? 1.0 / l : 0.0;
+            for (int d = 0; d < p->dv; ++d) o[d] *= inv;
+        }
+        free(x);
         free(rows);
     }
     return err;
