@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="llama_mixed",
                     choices=["llama_mixed", "gemma2_fp8_sw_cap", "mla_deepseek_v3", "dsa_sparse_prefill_token",
-                             "dsa_sparse_prefill_page", "dsa_sparse_decode_token", "dsa_sparse_decode_page"],
+                             "dsa_sparse_prefill_page", "dsa_sparse_decode_token", "dsa_sparse_decode_page",
+                             "dsa_sparse_ragged_token", "dsa_sparse_ragged_page"],
                     help="the headline step is llama_mixed; the others time one variant alone (profiling runs)")
     return ap.parse_args()
 
@@ -277,6 +278,27 @@ def sparse_accounting(s):
     byt = rows * 576 * 2 + B * S * H * (576 * 2 + 512 * 4)
     fl = pairs * 2 * H * (576 + 512)
     return B * S, byt, fl
+
+
+def sparse_ragged_accounting(s):
+    """Tokens, bytes (the distinct selected rows, Q, the written rows, fp32 O) and flops of one
+    packed-ragged call."""
+    T, H, _ = s.ql.shape
+    RB, ps = s.read_block, s.page_size
+    cu_q = s.cu_q_lens.numpy()
+    rid = np.clip(np.searchsorted(cu_q[1:], np.arange(T), side="right"), 0, len(s.seq_lens) - 1)
+    bound = s.seq_lens.numpy().astype(np.int64)[rid]
+    base = s.cu_kv_lens.numpy().astype(np.int64)[rid] // ps
+    idx = s.topk.numpy().astype(np.int64)
+    pos = s.positions.numpy().astype(np.int64)
+    units = idx[..., None] * RB + np.arange(RB)  # [T, K, RB] request-local keys
+    valid = (idx[..., None] >= 0) & (units <= pos[:, None, None]) & (units < bound[:, None, None])
+    pages = s.page_indices.numpy().astype(np.int64)
+    slot = pages[np.minimum(base[:, None, None] + units // ps, len(pages) - 1)] * ps + units % ps
+    rows = np.unique(slot[valid]).size
+    byt = rows * 576 * 2 + T * H * (576 * 2 + 512 * 4) + T * 640 * 2
+    fl = int(valid.sum()) * 2 * H * (576 + 512)
+    return T, byt, fl
 
 
 def roof_time(byt, fl, peaks, sustained=False):
@@ -597,6 +619,9 @@ def run_variants(dev, peaks, args, world, only=None):
         for mode in ("token", "page"):
             if want(f"dsa_sparse_{phase}_{mode}"):
                 _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report)
+    for mode in ("token", "page"):
+        if want(f"dsa_sparse_ragged_{mode}"):
+            _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report)
     return res
 
 
@@ -638,6 +663,25 @@ def _variant_mla(dev, peaks, api, workloads, steps, warm, world, report):
     report("mla_deepseek_v3", tok, byt, fl, ms, kt,
            {"attn_tensor_frac": fl / (att_us * 1e-6) / 1e12 / peaks["bf16_tflops"]})
     del m, g, out, ws
+    torch.cuda.empty_cache()
+
+
+def _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report):
+    s = workloads.dsa_sparse_ragged(mode=mode)
+    tok, byt, fl = sparse_ragged_accounting(s)
+    g = s.to(dev)
+    prm = api.make_sparse_ragged_params(g.ql, g.qpe, g.cache, g.topk, g.seq_lens, g.page_indices, **s.options())
+    ws = torch.zeros(api.sparse_mla_ragged_workspace_size(prm), dtype=torch.uint8, device=dev)
+    out = torch.empty(s.ql.shape[:2] + (512,), dtype=torch.float32, device=dev)
+
+    def call():
+        api.sparse_mla_write_and_attend_ragged(g.ql, g.qpe, g.kvc, g.kpe, g.cache, g.topk, g.positions, g.loc,
+                                               g.seq_lens, g.cu_q_lens, g.cu_kv_lens, g.page_indices, out=out,
+                                               workspace=ws, **s.options())
+
+    ms, kt = time_steps(call, max(3, steps // 2), warm, world, timer=True)
+    report(f"dsa_sparse_ragged_{mode}", tok, byt, fl, ms, kt)
+    del s, g, out, ws
     torch.cuda.empty_cache()
 
 

@@ -289,6 +289,55 @@ RPA_API int sparse_mla_forward(const sparse_params* p, const void* q, const void
                        const int32_t* positions, const int32_t* page_table, float* out, void* workspace,
                        size_t workspace_bytes, rpa_stream_t stream);
 
+/* Packed-ragged mode with the self-write (sglang-jax "dsa/sparse_mla_prefill.py",
+ * prefill_write_and_attend_ragged and the ragged branch of sparse_mla_attention): several
+ * requests' tokens packed along one axis.
+ *   ql         [num_tokens, num_heads, dv]      bf16 absorbed latent query (dv = 512)
+ *   qpe        [num_tokens, num_heads, rope]    bf16 rope query (rope = 64); the query is
+ *              their concatenation (dk = dv + rope = 576)
+ *   kvc, kpe   [num_tokens, dv], [num_tokens, rope]  bf16 new latent rows (both NULL: no write)
+ *   cache      [total_num_pages * page_size, row_stride]  bf16, written in place
+ *   topk       int32 [num_tokens, topk]   request-local unit ids, -1 = empty slot
+ *   positions  int32 [num_tokens]         absolute query positions
+ *   loc        int32 [num_tokens]         flat cache row of each token's new row (-1 = none;
+ *              NULL with kvc/kpe NULL)
+ *   seq_lens   int32 [num_seqs]           each request's key length (causal bound)
+ *   cu_q_lens  int32 [num_seqs + 1]       request r owns tokens [cu_q_lens[r], cu_q_lens[r+1])
+ *   cu_kv_lens int32 [num_seqs + 1]       page-aligned key offsets into page_indices' runs
+ *   page_indices int32 [num_page_ids]     packed physical page ids
+ *   out        [num_tokens, num_heads, dv]  float32
+ * First every token's row [kvc | kpe | zeros] is written to cache row loc[t] (rows outside
+ * the cache are dropped; two tokens naming one row leave either's). Then token t attends as
+ * in sparse_mla_forward, where its request r is the number of cu_q_lens[1..num_seqs]
+ * entries <= t (clipped to num_seqs - 1), the causal bound is seq_lens[r], and key kp sits
+ * in page page_indices[min(cu_kv_lens[r] / page_size + kp / page_size, num_page_ids - 1)].
+ * read_block must divide page_size. */
+typedef struct {
+    uint32_t struct_size;        /* sizeof(sparse_ragged_params) */
+    uint32_t version;            /* RPA_ABI_VERSION */
+    int32_t num_tokens;
+    int32_t num_seqs;
+    int32_t num_heads;           /* multiple of 128 */
+    int32_t dv;                  /* 512 */
+    int32_t rope;                /* 64 */
+    int32_t row_stride;          /* elements per cache row (>= dv + rope, multiple of 8) */
+    int32_t topk;
+    int32_t read_block;
+    int32_t page_size;
+    int32_t num_page_ids;
+    int32_t total_num_pages;
+    float sm_scale;              /* required, > 0 */
+} sparse_ragged_params;
+
+RPA_API int sparse_mla_ragged_workspace_size(const sparse_ragged_params* p, size_t* bytes);
+
+RPA_API int sparse_mla_write_and_attend_ragged(const sparse_ragged_params* p, const void* ql, const void* qpe,
+                                               const void* kvc, const void* kpe, void* cache, const int32_t* topk,
+                                               const int32_t* positions, const int32_t* loc,
+                                               const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                               const int32_t* cu_kv_lens, const int32_t* page_indices, float* out,
+                                               void* workspace, size_t workspace_bytes, rpa_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Status and diagnostics                                                   */
 /* ---------------------------------------------------------------------- */

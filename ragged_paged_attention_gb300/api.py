@@ -28,7 +28,7 @@ EXPORTS = ("rpa_workspace_size", "rpa_forward", "rpa_update_kv_cache", "mla_work
            "mla_update_kv_cache", "mla_rpa_forward", "sparse_mla_workspace_size", "sparse_mla_forward",
            "rpa_check_device_status", "rpa_last_error", "rpa_version", "rpa_profile_enable",
            "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc", "rpa_launch_count",
-           "rpa_forward_update")
+           "rpa_forward_update", "sparse_mla_ragged_workspace_size", "sparse_mla_write_and_attend_ragged")
 
 
 class RpaError(RuntimeError):
@@ -70,6 +70,14 @@ class sparse_params(ctypes.Structure):
                 ("total_num_pages", ctypes.c_int32), ("seq_len", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
 
 
+class sparse_ragged_params(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_uint32), ("version", ctypes.c_uint32), ("num_tokens", ctypes.c_int32),
+                ("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("rope", ctypes.c_int32), ("row_stride", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("read_block", ctypes.c_int32), ("page_size", ctypes.c_int32), ("num_page_ids", ctypes.c_int32),
+                ("total_num_pages", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -97,6 +105,8 @@ def load_library(path: str = LIB_PATH):
         lib.mla_rpa_forward.argtypes = [ctypes.POINTER(mla_params), P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
         lib.sparse_mla_workspace_size.argtypes = [ctypes.POINTER(sparse_params), szp]
         lib.sparse_mla_forward.argtypes = [ctypes.POINTER(sparse_params), P, P, P, P, P, P, P, sz, P]
+        lib.sparse_mla_ragged_workspace_size.argtypes = [ctypes.POINTER(sparse_ragged_params), szp]
+        lib.sparse_mla_write_and_attend_ragged.argtypes = [ctypes.POINTER(sparse_ragged_params)] + [P] * 14 + [sz, P]
         lib.rpa_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
         lib.rpa_profile_enable.argtypes = [ctypes.c_int]
         lib.rpa_profile_reset.argtypes = []
@@ -407,6 +417,64 @@ def sparse_mla_forward(q, cache, indices, positions, page_table, *, read_block, 
         workspace = Workspace.get(sparse_mla_workspace_size(prm), q.device, "sparse")
     _check(lib.sparse_mla_forward(ctypes.byref(prm), _ptr(q), _ptr(cache), _ptr(indices), _ptr(positions),
                                   _ptr(page_table), _ptr(out), _ptr(workspace), workspace.numel(), _stream()))
+    return out
+
+
+def make_sparse_ragged_params(ql, qpe, cache, topk, seq_lens, page_indices, *, read_block, page_size,
+                              sm_scale) -> sparse_ragged_params:
+    T, H, dv = ql.shape
+    row_stride = cache.shape[-1]
+    return sparse_ragged_params(
+        struct_size=ctypes.sizeof(sparse_ragged_params), version=ABI_VERSION, num_tokens=T, num_seqs=seq_lens.numel(),
+        num_heads=H, dv=dv, rope=qpe.shape[-1], row_stride=row_stride, topk=topk.shape[-1], read_block=read_block,
+        page_size=page_size, num_page_ids=page_indices.numel(),
+        total_num_pages=cache.numel() // (page_size * row_stride), sm_scale=float(sm_scale))
+
+
+def sparse_mla_ragged_workspace_size(params: sparse_ragged_params) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    _check(lib.sparse_mla_ragged_workspace_size(ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def sparse_mla_write_and_attend_ragged(ql, qpe, kvc, kpe, cache, topk, positions, loc, seq_lens, cu_q_lens,
+                                       cu_kv_lens, page_indices, *, read_block, page_size, sm_scale, out=None,
+                                       workspace=None):
+    """Packed-ragged sparse MLA with the self-write: writes ``kvc``/``kpe`` rows (may be None,
+    with ``loc``) into ``cache`` in place, then attends; returns ``out`` [T, H, dv] float32."""
+    lib = load_library()
+    for n, t in (("ql", ql), ("qpe", qpe), ("cache", cache)):
+        _dev(t, n, torch.bfloat16)
+    for n, t in (("topk", topk), ("positions", positions), ("seq_lens", seq_lens), ("cu_q_lens", cu_q_lens),
+                 ("cu_kv_lens", cu_kv_lens), ("page_indices", page_indices)):
+        _dev(t, n, torch.int32)
+    T, H, dv = ql.shape
+    if qpe.shape[:2] != (T, H) or topk.shape[0] != T or positions.numel() != T:
+        raise ValueError("qpe [T, H, rope], topk [T, K] and positions [T] must match ql [T, H, dv]")
+    if cu_q_lens.numel() != seq_lens.numel() + 1 or cu_kv_lens.numel() != seq_lens.numel() + 1:
+        raise ValueError("cu_q_lens and cu_kv_lens must have num_seqs + 1 entries")
+    if (kvc is None) != (kpe is None) or (kvc is None) != (loc is None):
+        raise ValueError("kvc, kpe and loc go together")
+    if kvc is not None:
+        _dev(kvc, "kvc", torch.bfloat16)
+        _dev(kpe, "kpe", torch.bfloat16)
+        _dev(loc, "loc", torch.int32)
+        if kvc.shape != (T, dv) or kpe.shape != (T, qpe.shape[-1]) or loc.numel() != T:
+            raise ValueError("kvc [T, dv], kpe [T, rope] and loc [T] must match ql")
+    if sm_scale is None:
+        raise ValueError("sm_scale is required")
+    prm = make_sparse_ragged_params(ql, qpe, cache, topk, seq_lens, page_indices, read_block=read_block,
+                                    page_size=page_size, sm_scale=sm_scale)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.float32, device=ql.device)
+    _dev(out, "out", torch.float32)
+    if workspace is None:
+        workspace = Workspace.get(sparse_mla_ragged_workspace_size(prm), ql.device, "sparse_ragged")
+    _check(lib.sparse_mla_write_and_attend_ragged(
+        ctypes.byref(prm), _ptr(ql), _ptr(qpe), _ptr(kvc), _ptr(kpe), _ptr(cache), _ptr(topk), _ptr(positions),
+        _ptr(loc), _ptr(seq_lens), _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream()))
     return out
 
 

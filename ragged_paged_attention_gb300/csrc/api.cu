@@ -197,6 +197,50 @@ LatLayout sparse_layout(const sparse_params* p, int* splits) {
     return lat_layout(sp > 1 ? items : 0);
 }
 
+// The packed-ragged mode as a sparse problem of one batch entry and num_tokens queries
+// (checked by check_sparse_params), plus its own checks.
+int ragged_as_sparse(const sparse_ragged_params* p, sparse_params& sp) {
+    if (!p) return fail(RPA_ERR_NULL, "params is NULL");
+    if (p->struct_size < sizeof(sparse_ragged_params)) return fail(RPA_ERR_VALUE, "sparse_ragged_params.struct_size too small");
+    if (p->version != RPA_ABI_VERSION) return fail(RPA_ERR_VALUE, "sparse_ragged_params.version %u != %d", p->version, RPA_ABI_VERSION);
+    if (p->num_seqs <= 0 || p->num_page_ids <= 0) return fail(RPA_ERR_SHAPE, "all sizes must be positive");
+    if (p->dv % 8 || p->rope % 8) return fail(RPA_ERR_SHAPE, "dv and rope must be multiples of 8");
+    memset(&sp, 0, sizeof sp);
+    sp.struct_size = sizeof(sparse_params);
+    sp.version = RPA_ABI_VERSION;
+    sp.batch = 1;
+    sp.num_queries = p->num_tokens;
+    sp.num_heads = p->num_heads;
+    sp.dk = p->dv + p->rope;
+    sp.dv = p->dv;
+    sp.row_stride = p->row_stride;
+    sp.topk = p->topk;
+    sp.read_block = p->read_block;
+    sp.page_size = p->page_size;
+    sp.max_pages = p->num_page_ids;
+    sp.total_num_pages = p->total_num_pages;
+    sp.seq_len = 0;
+    sp.sm_scale = p->sm_scale;
+    return check_sparse_params(&sp);
+}
+
+struct RaggedLayout {
+    LatLayout lat;
+    size_t q_bound, q_base, total;
+};
+
+RaggedLayout ragged_layout(const sparse_params& sp, int* splits) {
+    RaggedLayout L;
+    L.lat = sparse_layout(&sp, splits);
+    size_t off = align_up(L.lat.total);
+    L.q_bound = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)sp.num_queries);
+    L.q_base = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)sp.num_queries);
+    L.total = off;
+    return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -512,6 +556,92 @@ int sparse_mla_forward(const sparse_params* p, const void* q, const void* cache,
     a.max_items = L.max_items;
     cudaError_t e = launch_sparse_forward(a, sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_forward launch");
+    return RPA_OK;
+}
+
+int sparse_mla_ragged_workspace_size(const sparse_ragged_params* p, size_t* bytes) {
+    sparse_params sp;
+    int rc = ragged_as_sparse(p, sp);
+    if (rc) return rc;
+    if (!bytes) return fail(RPA_ERR_NULL, "bytes is NULL");
+    *bytes = ragged_layout(sp, nullptr).total;
+    return RPA_OK;
+}
+
+int sparse_mla_write_and_attend_ragged(const sparse_ragged_params* p, const void* ql, const void* qpe,
+                                       const void* kvc, const void* kpe, void* cache, const int32_t* topk,
+                                       const int32_t* positions, const int32_t* loc, const int32_t* seq_lens,
+                                       const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                       const int32_t* page_indices, float* out, void* workspace,
+                                       size_t workspace_bytes, rpa_stream_t stream) {
+    sparse_params sp;
+    int rc = ragged_as_sparse(p, sp);
+    if (rc) return rc;
+    if (!ql || !qpe || !cache || !topk || !positions || !seq_lens || !cu_q_lens || !cu_kv_lens || !page_indices ||
+        !out)
+        return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
+    const bool write = kvc || kpe;
+    if (write && (!kvc || !kpe || !loc)) return fail(RPA_ERR_NULL, "kvc, kpe and loc go together");
+    if (!aligned16(ql) || !aligned16(qpe) || !aligned16(cache) || !aligned16(out) ||
+        (write && (!aligned16(kvc) || !aligned16(kpe))))
+        return fail(RPA_ERR_VALUE, "ql, qpe, kvc, kpe, cache and out must be 16-byte aligned");
+    int splits = 1;
+    const RaggedLayout L = ragged_layout(sp, &splits);
+    rc = check_workspace(workspace, workspace_bytes, L.total);
+    if (rc) return rc;
+    const int sms = num_sms_current();
+    if (!sms) return fail(RPA_ERR_CUDA, "no CUDA device");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    SparseRaggedPrepArgs pa;
+    pa.kvc = write ? static_cast<const __nv_bfloat16*>(kvc) : nullptr;
+    pa.kpe = static_cast<const __nv_bfloat16*>(kpe);
+    pa.cache = static_cast<__nv_bfloat16*>(cache);
+    pa.loc = loc;
+    pa.seq_lens = seq_lens;
+    pa.cu_q_lens = cu_q_lens;
+    pa.cu_kv_lens = cu_kv_lens;
+    pa.q_bound = reinterpret_cast<int32_t*>(ws + L.q_bound);
+    pa.q_base = reinterpret_cast<int32_t*>(ws + L.q_base);
+    pa.num_tokens = p->num_tokens;
+    pa.num_seqs = p->num_seqs;
+    pa.dv = p->dv;
+    pa.rope = p->rope;
+    pa.row_stride = p->row_stride;
+    pa.page_size = p->page_size;
+    pa.total_num_pages = p->total_num_pages;
+    LatentArgs a;
+    memset(&a, 0, sizeof a);
+    a.sparse = 1;
+    a.num_heads = p->num_heads;
+    a.sm_scale = p->sm_scale;
+    a.q = nullptr;  // split query: ql_nope and q_pe
+    a.ql_nope = static_cast<const __nv_bfloat16*>(ql);
+    a.q_pe = static_cast<const __nv_bfloat16*>(qpe);
+    a.cache = static_cast<const __nv_bfloat16*>(cache);
+    a.indices = topk;
+    a.positions = positions;
+    a.page_table = page_indices;
+    a.q_bound = pa.q_bound;
+    a.q_base = pa.q_base;
+    a.batch = 1;
+    a.num_queries = p->num_tokens;
+    a.topk = p->topk;
+    a.read_block = p->read_block;
+    a.max_pages = p->num_page_ids;
+    a.seq_len = 0;
+    a.row_stride = p->row_stride;
+    a.sparse_splits = splits;
+    a.out_f32 = out;
+    a.total_num_pages = p->total_num_pages;
+    a.page_size = p->page_size;
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.items = nullptr;
+    a.tickets = reinterpret_cast<int*>(ws + L.lat.tickets);
+    a.partial_ml = reinterpret_cast<float*>(ws + L.lat.pml);
+    a.partial_o = reinterpret_cast<float*>(ws + L.lat.po);
+    a.max_items = L.lat.max_items;
+    cudaError_t e = launch_sparse_ragged(pa, a, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_write_and_attend_ragged launch");
     return RPA_OK;
 }
 

@@ -147,6 +147,11 @@ struct LatentArgs {
     const int32_t* positions;       // [B, S]
     const int32_t* page_table;      // [B, max_pages]
     int batch, num_queries, topk, read_block, max_pages, seq_len, row_stride, sparse_splits;
+    // sparse, packed-ragged mode (q_base != nullptr): B = 1, S = tokens; query s's causal bound
+    // and its base in the packed page list (page_table, max_pages entries) come from these
+    // (written by the prep kernel); Q comes from ql_nope and q_pe when q is null
+    const int32_t* q_bound;
+    const int32_t* q_base;
     float* out_f32;                 // [B, S, H, 512]
     // common
     int total_num_pages, page_size;
@@ -157,6 +162,21 @@ struct LatentArgs {
     float* partial_ml;
     float* partial_o;
     int max_items;
+};
+
+// Packed-ragged sparse MLA: each token's request, causal bound and page base, and the
+// self-write of its latent row.
+struct SparseRaggedPrepArgs {
+    const __nv_bfloat16* kvc;       // [T, dv] (null: no self-write)
+    const __nv_bfloat16* kpe;       // [T, rope]
+    __nv_bfloat16* cache;           // rows of row_stride
+    const int32_t* loc;             // [T] flat slot per token (-1: none)
+    const int32_t* seq_lens;        // [S]
+    const int32_t* cu_q_lens;       // [S + 1]
+    const int32_t* cu_kv_lens;      // [S + 1]
+    int32_t* q_bound;               // [T] out
+    int32_t* q_base;                // [T] out
+    int num_tokens, num_seqs, dv, rope, row_stride, page_size, total_num_pages;
 };
 
 struct MlaUpdateArgs {
@@ -201,6 +221,8 @@ int decode_heads_for(int head_dim, bool fp8);
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_sparse_forward(const LatentArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_sparse_ragged(const SparseRaggedPrepArgs& pa, const LatentArgs& a, int num_sms,
+                                 cudaStream_t stream);
 cudaError_t launch_mla_attention(const LatentArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_sparse_attention(const LatentArgs& a, int num_sms, cudaStream_t stream);
 

@@ -238,6 +238,58 @@ cudaError_t launch_mla_forward_update(const LatentArgs& a, const MlaUpdateArgs& 
     return launch_mla_attention(a, num_sms, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Packed-ragged sparse MLA (sglang-jax "dsa/sparse_mla_prefill.py",
+// prefill_write_and_attend_ragged): one warp per token finds its request (the number of
+// cu_q_lens[1..S] entries <= t, as searchsorted, clipped to the last request), records that
+// request's causal bound (seq_lens) and page base (cu_kv_lens / page_size), and writes the
+// token's latent row [c_kv | k_rope | zeros] into cache slot loc[t] (a slot outside the cache,
+// the -1 padding included, is dropped).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) sparse_ragged_prep_kernel(SparseRaggedPrepArgs a) {
+    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    const long long slots = (long long)a.total_num_pages * a.page_size;
+    const int chunks = a.row_stride / 8;  // 16-byte chunks of a row
+    for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < a.num_tokens; t += gridDim.x * warps) {
+        if (lane == 0) {
+            int lo = 1, hi = a.num_seqs + 1;  // first i in [1, S] with cu_q_lens[i] > t (S + 1: none)
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (a.cu_q_lens[mid] > t) hi = mid; else lo = mid + 1;
+            }
+            const int r = min(lo - 1, a.num_seqs - 1);
+            a.q_bound[t] = a.seq_lens[r];
+            const int kvo = a.cu_kv_lens[r];
+            a.q_base[t] = kvo >= 0 ? kvo / a.page_size : -1;
+        }
+        if (!a.kvc) continue;
+        const long long slot = a.loc[t];
+        if (slot < 0 || slot >= slots) continue;
+        uint4* row = reinterpret_cast<uint4*>(a.cache + slot * a.row_stride);
+        for (int c = lane; c < chunks; c += 32) {
+            const int e = c * 8;  // dv and rope are multiples of 8: no chunk straddles two parts
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (e < a.dv)
+                v = __ldg(reinterpret_cast<const uint4*>(a.kvc + (size_t)t * a.dv + e));
+            else if (e < a.dv + a.rope)
+                v = __ldg(reinterpret_cast<const uint4*>(a.kpe + (size_t)t * a.rope + (e - a.dv)));
+            row[c] = v;
+        }
+    }
+}
+
+cudaError_t launch_sparse_ragged(const SparseRaggedPrepArgs& pa, const LatentArgs& a, int num_sms,
+                                 cudaStream_t stream) {
+    {
+        ProfScope ps("sparse_ragged_prep", stream);
+        const int grid = max(1, min(cdiv(pa.num_tokens, 8), num_sms * 8));
+        sparse_ragged_prep_kernel<<<grid, 256, 0, stream>>>(pa);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return launch_sparse_attention(a, num_sms, stream);
+}
+
 cudaError_t launch_sparse_forward(const LatentArgs& a, int num_sms, cudaStream_t stream) {
     return launch_sparse_attention(a, num_sms, stream);
 }

@@ -178,9 +178,12 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         if (s_abort) break;
         const int h0 = w.head;
         int qpos, b = 0, seq = 0, t = 0, wlo = INT_MIN, q_start = 0;
+        int kbound = 0, kbase = 0;  // sparse: the query's causal bound and packed page base
         if (SPARSE) {
             b = w.seq / a.num_queries;
             qpos = a.positions[w.seq];
+            kbound = a.q_bound ? a.q_bound[w.seq] : a.seq_len;
+            kbase = a.q_base ? a.q_base[w.seq] : 0;
         } else {
             seq = w.seq;
             t = w.row_begin;
@@ -279,10 +282,16 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     if (SPARSE) {
                         const int u = __ldg(a.indices + (size_t)w.seq * a.topk + key / a.read_block);
                         const long long kp = (long long)u * a.read_block + key % a.read_block;
-                        v = u >= 0 && kp <= qpos && kp < a.seq_len;
+                        v = u >= 0 && kp <= qpos && kp < kbound;
                         if (!v) return nullptr;
                         const int lp = (int)(kp / a.page_size);
-                        const int page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
+                        int page;
+                        if (a.q_base) {  // packed list: the request's run, clamped to the list's end
+                            const long long pidx = min((long long)kbase + lp, (long long)a.max_pages - 1);
+                            page = pidx >= 0 ? __ldg(a.page_table + pidx) : -1;
+                        } else {
+                            page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
+                        }
                         if ((unsigned)page >= (unsigned)a.total_num_pages) {
                             set_error(err, RPA_DEV_ERR_PAGE);
                             v = false;
@@ -462,7 +471,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 for (int i = 0; i < 20; ++i) {
                     if (i < nch) {
                         const int c = c0 + i, p = c >> 3, cc = c & 7;
-                        const __nv_bfloat16* src = SPARSE ? a.q + qrow * kLatDk + lat_panel_col(rank, p) + cc * 8
+                        const __nv_bfloat16* src = (SPARSE && a.q) ? a.q + qrow * kLatDk + lat_panel_col(rank, p) + cc * 8
                                                    : (rank == 0 && p == 4) ? a.q_pe + qrow * 64 + cc * 8
                                                                            : a.ql_nope + qrow * kLatDv + lat_panel_col(rank, p) + cc * 8;
                         buf[i] = __ldg(reinterpret_cast<const uint4*>(src));

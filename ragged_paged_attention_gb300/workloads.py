@@ -326,6 +326,96 @@ def make_sparse(*, batch, num_queries, seq_len, positions, topk, read_block, see
         sm_scale=(1.0 / math.sqrt(192.0)) if sm_scale is None else float(sm_scale), dv=dv)
 
 
+@dataclasses.dataclass
+class SparseRaggedInputs:
+    """One packed-ragged batch for ``sparse_mla_write_and_attend_ragged``."""
+    ql: torch.Tensor           # [T, H, 512] bf16
+    qpe: torch.Tensor          # [T, H, 64] bf16
+    kvc: torch.Tensor          # [T, 512] bf16 new latent rows
+    kpe: torch.Tensor          # [T, 64] bf16
+    cache: torch.Tensor        # [P, ps/2, 2, 640] bf16 (cols 576.. zero; rows to be written: NaN)
+    topk: torch.Tensor         # [T, K] int32 request-local unit ids, -1 padded
+    positions: torch.Tensor    # [T] int32
+    loc: torch.Tensor          # [T] int32 flat cache row of each token's new row (-1: padding)
+    seq_lens: torch.Tensor     # [S] int32
+    cu_q_lens: torch.Tensor    # [S + 1] int32
+    cu_kv_lens: torch.Tensor   # [S + 1] int32 page-aligned
+    page_indices: torch.Tensor  # [sum of pages] int32
+    read_block: int
+    page_size: int
+    sm_scale: float
+    q_lens: list
+
+    def options(self) -> dict:
+        return dict(read_block=self.read_block, page_size=self.page_size, sm_scale=self.sm_scale)
+
+    def to(self, device) -> "SparseRaggedInputs":
+        kw = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in dataclasses.asdict(self).items()}
+        return SparseRaggedInputs(**kw)
+
+
+def make_sparse_ragged(q_lens, seq_lens, *, topk, read_block, seed, num_heads=128, dv=512, rope=64, page_size=64,
+                       kv_packing=2, row_stride=640, extra_pages=0, pad_tokens=0, sm_scale=None) -> SparseRaggedInputs:
+    """Requests extending their sequences: request r's q_lens[r] new tokens sit at the end of its
+    seq_lens[r] keys; its pages are a random run of the packed page list starting at
+    cu_kv_lens[r] / page_size; each token writes its new row to the slot of its own position
+    (those rows hold NaN until written) and selects ``topk`` units drawn causally within its
+    request. ``pad_tokens`` padding tokens follow with loc = -1."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    S = len(q_lens)
+    pages = [-(-int(L) // page_size) for L in seq_lens]
+    cu_kv = np.concatenate([[0], np.cumsum([n * page_size for n in pages])]).astype(np.int32)
+    n_ids = int(sum(pages))
+    P = n_ids + extra_pages
+    perm = rng.permutation(P).astype(np.int32)
+    page_ids = perm[:n_ids].copy()
+    cache = torch.zeros((P, page_size, row_stride), dtype=torch.bfloat16)
+    cache[..., :dv + rope] = _randn(rng, (P, page_size, dv + rope), torch.bfloat16)
+    for p in perm[n_ids:]:
+        _fill_nan(cache[int(p)])
+    flat = cache.view(P * page_size, row_stride)
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(cu_q[-1]) + pad_tokens
+    positions = np.zeros(T, np.int32)
+    loc = np.full(T, -1, np.int32)
+    for r in range(S):
+        L, base = int(seq_lens[r]), int(cu_kv[r]) // page_size
+        if L % page_size:  # slots past the request's keys in its last page
+            _fill_nan(cache[int(page_ids[base + pages[r] - 1]), L % page_size:])
+        for j, t in enumerate(range(cu_q[r], cu_q[r + 1])):
+            pos = L - q_lens[r] + j
+            positions[t] = pos
+            loc[t] = int(page_ids[base + pos // page_size]) * page_size + pos % page_size
+            _fill_nan(flat[int(loc[t])])
+    topk_ids = np.full((T, topk), -1, np.int32)
+    for r in range(S):
+        toks = np.arange(cu_q[r], cu_q[r + 1])
+        if len(toks):
+            topk_ids[toks] = sorted_causal_subsets(rng, positions[toks], topk, read_block)
+    for t in range(int(cu_q[-1]), T):
+        positions[t] = int(seq_lens[-1]) - 1
+        topk_ids[t, 0] = 0
+    return SparseRaggedInputs(
+        ql=_randn(rng, (T, num_heads, dv), torch.bfloat16), qpe=_randn(rng, (T, num_heads, rope), torch.bfloat16),
+        kvc=_randn(rng, (T, dv), torch.bfloat16), kpe=_randn(rng, (T, rope), torch.bfloat16),
+        cache=cache.reshape(P, page_size // kv_packing, kv_packing, row_stride),
+        topk=torch.from_numpy(topk_ids), positions=torch.from_numpy(positions), loc=torch.from_numpy(loc),
+        seq_lens=torch.tensor(list(seq_lens), dtype=torch.int32), cu_q_lens=torch.from_numpy(cu_q),
+        cu_kv_lens=torch.from_numpy(cu_kv), page_indices=torch.from_numpy(page_ids), read_block=read_block,
+        page_size=page_size, sm_scale=(1.0 / math.sqrt(192.0)) if sm_scale is None else float(sm_scale),
+        q_lens=list(q_lens))
+
+
+def dsa_sparse_ragged(*, mode="token", scale=1.0, seed=1005) -> SparseRaggedInputs:
+    """DSA multi-request extend, packed: 4 requests of 256 new tokens each at the end of
+    seq_lens U[2048, 8192]; token mode RB 1, K 2048; page mode RB 64, K 32."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    ql = max(1, int(256 * scale))
+    seq = rng.integers(max(ql, int(2048 * scale)), max(ql, int(8192 * scale)) + 1, size=4)
+    RB, K = (1, max(16, int(2048 * scale))) if mode == "token" else (64, max(2, int(32 * scale)))
+    return make_sparse_ragged([ql] * 4, list(seq), topk=K, read_block=RB, seed=seed)
+
+
 # ---------------------------------------------------------------------------
 # The five named workloads.  ``scale`` < 1 shrinks lengths and counts for
 # parity runs the oracle finishes in seconds; 1.0 is the benchmark size.

@@ -70,3 +70,52 @@ def test_sparse_split_merge():
     # the library's rule: chunk = max(512, ceil(2 * 4096 / 38)) rounded to 64 keys -> 8 splits
     assert s.indices.shape[-1] * s.read_block > 512
     run_and_check(s)
+
+
+# ---------------------------------------------------------------------------
+# packed-ragged mode with the self-write
+# ---------------------------------------------------------------------------
+def run_ragged(s, *, write=True, tokens=None):
+    """GPU call against the oracle: cache bytes after the self-write (bit exact) and the
+    output rows of ``tokens`` (all by default) within the bf16 tolerance."""
+    flat = s.cache.reshape(-1, s.cache.shape[-1])
+    ref_cache = oracle.sparse_ragged_write(s.kvc, s.kpe, flat, s.loc, page_size=s.page_size)
+    ref = oracle.sparse_mla_ragged(s.ql, s.qpe, ref_cache, s.topk, s.positions, s.seq_lens, s.cu_q_lens,
+                                   s.cu_kv_lens, s.page_indices, queries=tokens, **s.options())
+    g = s.to("cuda")
+    if not write:  # attend only, over a cache already holding the rows
+        g.cache.copy_(ref_cache.reshape(g.cache.shape).to("cuda"))
+    prm = api.make_sparse_ragged_params(g.ql, g.qpe, g.cache, g.topk, g.seq_lens, g.page_indices, **s.options())
+    ws = torch.zeros(api.sparse_mla_ragged_workspace_size(prm), dtype=torch.uint8, device="cuda")
+    out = api.sparse_mla_write_and_attend_ragged(
+        g.ql, g.qpe, g.kvc if write else None, g.kpe if write else None, g.cache, g.topk, g.positions,
+        g.loc if write else None, g.seq_lens, g.cu_q_lens, g.cu_kv_lens, g.page_indices, workspace=ws, **s.options())
+    assert api.check_device_status(ws) == 0
+    torch.cuda.synchronize()
+    got_cache = g.cache.reshape(-1, g.cache.shape[-1]).cpu()
+    assert torch.equal(got_cache.view(torch.int16), ref_cache.view(torch.int16))
+    rows = list(range(s.ql.shape[0])) if tokens is None else list(tokens)
+    err = max_abs(out[rows], ref[rows])
+    assert err <= TOL_BF16, f"max-abs {err}"
+    return out
+
+
+@pytest.mark.parametrize("rb,k", [(1, 24), (16, 6), (64, 3)])
+def test_sparse_ragged_small(rb, k):
+    # three requests (one a single decode token), padding tokens with loc -1, spare pages
+    s = workloads.make_sparse_ragged([3, 5, 1], [200, 333, 90], topk=k, read_block=rb, seed=40 + rb, extra_pages=3,
+                                     pad_tokens=2)
+    run_ragged(s)
+
+
+def test_sparse_ragged_attend_only():
+    s = workloads.make_sparse_ragged([4, 2], [150, 70], topk=16, read_block=1, seed=47, extra_pages=1)
+    run_ragged(s, write=False)
+
+
+def test_sparse_ragged_full_size_sampled():
+    for mode in ("token", "page"):
+        s = workloads.dsa_sparse_ragged(mode=mode)
+        rng = np.random.default_rng(3)
+        tokens = sorted(rng.choice(s.ql.shape[0], size=24, replace=False).tolist())
+        run_ragged(s, tokens=tokens)
