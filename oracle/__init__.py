@@ -45,6 +45,7 @@ _lib = None
 
 BF16 = 1
 E4M3 = 2
+INT8 = 3
 DEFAULT_MASK_VALUE = -0.7 * 3.4028234663852886e38  # -0.7 * float32 max
 
 
@@ -155,6 +156,8 @@ def _load():
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
+        lib.oracle_decode_int8.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_int8.restype = ctypes.c_double
         lib.oracle_round_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_round_f32_to_bf16.restype = ctypes.c_double
         for f in ("oracle_rpa", "oracle_rpa_update_kv_cache", "oracle_mla_update_kv_cache",
@@ -190,6 +193,8 @@ def _kv_code(dtype: torch.dtype) -> int:
         return BF16
     if dtype == torch.float8_e4m3fn:
         return E4M3
+    if dtype == torch.int8:
+        return INT8
     raise ValueError(f"unsupported kv dtype {dtype}")
 
 
@@ -376,6 +381,10 @@ def decode_bf16(bits: int) -> float:
 
 def decode_e4m3(bits: int) -> float:
     return _load().oracle_decode_e4m3(bits)
+
+
+def decode_int8(bits: int) -> float:
+    return _load().oracle_decode_int8(bits)
 
 
 def round_f32_to_bf16(x: float) -> float:

@@ -47,6 +47,7 @@
 /* dtype codes understood by the oracle */
 #define ORACLE_BF16 1
 #define ORACLE_E4M3 2
+#define ORACLE_INT8 3
 
 /* ------------------------------------------------------------------ */
 /* Number formats, decoded from their definitions.                     */
@@ -89,8 +90,13 @@ static float f32_round_to_bf16(float f) {
     return r;
 }
 
+/* int8: a two's-complement byte; the RPA reference promotes it exactly (it is a bfloat16
+ * value) or, with a scale, multiplies float32(x) by it like any other KV dtype. */
+static float int8_to_f32(uint8_t b) { return (float)(b < 128 ? (int)b : (int)b - 256); }
+
 static float load_elem(const void* base, size_t idx, int dtype) {
     if (dtype == ORACLE_E4M3) return e4m3_bits_to_f32(((const uint8_t*)base)[idx]);
+    if (dtype == ORACLE_INT8) return int8_to_f32(((const uint8_t*)base)[idx]);
     return bf16_bits_to_f32(((const uint16_t*)base)[idx]);
 }
 
@@ -108,6 +114,7 @@ static double rpa_kv_value(const void* base, size_t idx, int dtype, float scale)
 /* Exported for the pin tests: decode / round a single value. */
 double oracle_decode_bf16(uint16_t bits) { return (double)bf16_bits_to_f32(bits); }
 double oracle_decode_e4m3(uint8_t bits) { return (double)e4m3_bits_to_f32(bits); }
+double oracle_decode_int8(uint8_t bits) { return (double)int8_to_f32(bits); }
 double oracle_round_f32_to_bf16(float f) { return (double)f32_round_to_bf16(f); }
 
 /* ------------------------------------------------------------------ */
@@ -166,7 +173,7 @@ typedef struct {
     int32_t page_size;
     int32_t max_num_seqs;
     int32_t pages_per_seq;
-    int32_t kv_dtype;       /* ORACLE_BF16 or ORACLE_E4M3 */
+    int32_t kv_dtype;       /* ORACLE_BF16, ORACLE_E4M3 or ORACLE_INT8 */
     double sm_scale;
     int32_t sliding_window; /* 0 = none */
     double soft_cap;        /* 0 = none */
@@ -256,7 +263,7 @@ int oracle_rpa_update_kv_cache(const oracle_rpa_params* p, const void* new_k, co
                                const int32_t* cu_q_lens, int32_t num_seqs) {
     if (!p || !new_k || !new_v || !kv_pages) return ORACLE_ERR_ARG;
     const int C = p->num_combined_kv_heads, Hkv = C / 2, D = p->head_dim, ps = p->page_size;
-    const size_t esz = p->kv_dtype == ORACLE_E4M3 ? 1 : 2;
+    const size_t esz = p->kv_dtype == ORACLE_BF16 ? 2 : 1;
     for (int i = 0; i < num_seqs; ++i) {
         const int q_start = cu_q_lens[i], q_len = cu_q_lens[i + 1] - cu_q_lens[i];
         const int kv_len = kv_lens[i];

@@ -76,8 +76,12 @@ def rand_bf16(rng, shape):
 
 def ragged_case(rng, q_lens, kv_lens, Hq, Hkv, D, ps, sm_scale=None, sw=None, soft_cap=None,
                 dtype=torch.bfloat16, scale=None, mask_value=MASK):
-    K_list = [rand_bf16(rng, (k, Hkv, D)).to(dtype) for k in kv_lens]
-    V_list = [rand_bf16(rng, (k, Hkv, D)).to(dtype) for k in kv_lens]
+    if dtype == torch.int8:  # the full two's-complement range
+        K_list = [torch.from_numpy(rng.integers(-128, 128, size=(k, Hkv, D)).astype(np.int8)) for k in kv_lens]
+        V_list = [torch.from_numpy(rng.integers(-128, 128, size=(k, Hkv, D)).astype(np.int8)) for k in kv_lens]
+    else:
+        K_list = [rand_bf16(rng, (k, Hkv, D)).to(dtype) for k in kv_lens]
+        V_list = [rand_bf16(rng, (k, Hkv, D)).to(dtype) for k in kv_lens]
     T = sum(q_lens)
     q = rand_bf16(rng, (T, Hq, D))
     pages, table = page_rpa(K_list, V_list, ps, rng, dtype=dtype)
@@ -172,6 +176,20 @@ def test_rpa_window_softcap_bruteforce():
     rng = np.random.default_rng(7)
     out, exp, _ = ragged_case(rng, [1, 6, 4], [30, 25, 9], 4, 2, 16, 4, sw=5, soft_cap=0.7)
     np.testing.assert_allclose(out, exp, rtol=0, atol=1e-12)
+
+
+def test_int8_decode_all_codes():
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.int8).to(torch.float64).numpy()
+    got = np.array([oracle.decode_int8(c) for c in range(256)])
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("scale,sm_scale", [(None, 0.002), (1 / 64, None), (0.0123, None)])
+def test_rpa_int8_bruteforce(scale, sm_scale):
+    # int8 K/V: promoted exactly without a scale, else bf16(float32(x) * scale) (torch's casts)
+    rng = np.random.default_rng(21)
+    out, exp, _ = ragged_case(rng, [1, 3], [20, 11], 4, 2, 16, 8, dtype=torch.int8, scale=scale, sm_scale=sm_scale)
+    np.testing.assert_allclose(out, exp, rtol=0, atol=1e-10)
 
 
 def test_rpa_fp8_scaled_bruteforce():
