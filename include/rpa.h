@@ -78,7 +78,8 @@ typedef enum {
 typedef enum {
     RPA_DTYPE_BF16 = 1,
     RPA_DTYPE_FP8_E4M3 = 2,
-    RPA_DTYPE_F32 = 3
+    RPA_DTYPE_F32 = 3,
+    RPA_DTYPE_INT8 = 4           /* two's-complement bytes (RPA K/V only) */
 } rpa_dtype;
 
 /* Bits of the device error word (OR-ed together). */
@@ -112,7 +113,10 @@ typedef struct CUstream_st* rpa_stream_t;
  * k <= q_pos and (sliding_window == 0 or k > q_pos - sliding_window).  Q head h reads
  * KV head h / (num_q_heads / num_kv_heads).  Logits: sm_scale * q.k, then
  * soft_cap * tanh(x / soft_cap) when soft_cap != 0.  When k_scale (v_scale) != 0 the
- * keys (values) are dequantised as bf16(float(k) * k_scale) before the dot products. */
+ * keys (values) are dequantised as bf16(float(k) * k_scale) before the dot products.
+ * kv_dtype int8 (the v2 kernel's packed integer KV): the bytes are two's-complement
+ * integers, read as their exact value without a scale and dequantised like any other
+ * dtype with one. */
 typedef struct {
     uint32_t struct_size;        /* sizeof(rpa_params) */
     uint32_t version;            /* RPA_ABI_VERSION */
@@ -125,7 +129,7 @@ typedef struct {
     int32_t max_num_seqs;
     int32_t pages_per_seq;
     int32_t q_dtype;             /* RPA_DTYPE_BF16 */
-    int32_t kv_dtype;            /* RPA_DTYPE_BF16 or RPA_DTYPE_FP8_E4M3 */
+    int32_t kv_dtype;            /* RPA_DTYPE_BF16, RPA_DTYPE_FP8_E4M3 or RPA_DTYPE_INT8 */
     float sm_scale;
     int32_t sliding_window;      /* 0 = none */
     float soft_cap;              /* 0 = none */

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librpa_gb300.so")
 ABI_VERSION = 1
 
-BF16, FP8_E4M3, F32 = 1, 2, 3
+BF16, FP8_E4M3, F32, INT8 = 1, 2, 3, 4
 
 STATUS = {0: "RPA_OK", -1: "RPA_ERR_NULL", -2: "RPA_ERR_SHAPE", -3: "RPA_ERR_DTYPE", -4: "RPA_ERR_VALUE",
           -5: "RPA_ERR_UNSUPPORTED", -6: "RPA_ERR_CUDA", -7: "RPA_ERR_DEVICE_CHECK", -8: "RPA_ERR_WORKSPACE"}
@@ -172,6 +172,8 @@ def _kv_code(dtype) -> int:
         return BF16
     if dtype == torch.float8_e4m3fn:
         return FP8_E4M3
+    if dtype == torch.int8:
+        return INT8
     raise ValueError(f"unsupported KV dtype {dtype}")
 
 

@@ -70,8 +70,8 @@ int check_rpa_params(const rpa_params* p) {
     if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
         return fail(RPA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", p->head_dim);
     if (p->q_dtype != RPA_DTYPE_BF16) return fail(RPA_ERR_DTYPE, "q_dtype must be bf16");
-    if (p->kv_dtype != RPA_DTYPE_BF16 && p->kv_dtype != RPA_DTYPE_FP8_E4M3)
-        return fail(RPA_ERR_DTYPE, "kv_dtype must be bf16 or fp8 e4m3");
+    if (p->kv_dtype != RPA_DTYPE_BF16 && p->kv_dtype != RPA_DTYPE_FP8_E4M3 && p->kv_dtype != RPA_DTYPE_INT8)
+        return fail(RPA_ERR_DTYPE, "kv_dtype must be bf16, fp8 e4m3 or int8");
     if (!isfinite(p->sm_scale)) return fail(RPA_ERR_VALUE, "sm_scale must be finite");
     if (p->sliding_window < 0) return fail(RPA_ERR_VALUE, "sliding_window must be positive (0 = none)");
     if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
@@ -86,7 +86,7 @@ RpaLayout rpa_layout(const rpa_params* p) {
     RpaLayout L;
     const int hkv = p->num_combined_kv_heads / 2;
     const int G = p->num_q_heads / hkv;
-    const int dh = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
+    const int dh = decode_heads_for(p->head_dim, p->kv_dtype != RPA_DTYPE_BF16);
     const int groups = cdiv(hkv, dh);
     // pieces: one per CTA share plus one more per group a share boundary cuts (groups: up to two
     // 8-row halves per sequence and KV-head group)
@@ -289,18 +289,19 @@ static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages,
     a.page_size = p->page_size;
     a.max_num_seqs = p->max_num_seqs;
     a.pages_per_seq = p->pages_per_seq;
-    a.kv_fp8 = p->kv_dtype == RPA_DTYPE_FP8_E4M3;
+    a.kv_byte = p->kv_dtype != RPA_DTYPE_BF16;
+    a.kv_int8 = p->kv_dtype == RPA_DTYPE_INT8;
     a.sm_scale = p->sm_scale;
     a.soft_cap = p->soft_cap;
     a.sliding_window = p->sliding_window;
     a.has_scale = p->k_scale != 0.f || p->v_scale != 0.f;
     a.k_scale_or_one = p->k_scale != 0.f ? p->k_scale : 1.f;
     a.v_scale_or_one = p->v_scale != 0.f ? p->v_scale : 1.f;
-    a.decode_heads = decode_heads_for(p->head_dim, p->kv_dtype == RPA_DTYPE_FP8_E4M3);
+    a.decode_heads = decode_heads_for(p->head_dim, p->kv_dtype != RPA_DTYPE_BF16);
     a.num_sms = sms;
     a.overlap = prof_enabled() ? 0 : 1;
-    rpa_rates(p->head_dim, a.kv_fp8 != 0, a.has_scale != 0, &a.pre_flops_per_ns_sm, &a.dec_bytes_per_ns_sm);
-    a.item_cost_keys = rpa_item_cost_keys(a.kv_fp8 || a.has_scale);
+    rpa_rates(p->head_dim, a.kv_byte != 0, a.has_scale != 0, &a.pre_flops_per_ns_sm, &a.dec_bytes_per_ns_sm);
+    a.item_cost_keys = rpa_item_cost_keys(a.kv_byte || a.has_scale);
     a.decode_per_sm = rpa_decode_ctas_per_sm(a);
     if (a.decode_per_sm <= 0) return fail(RPA_ERR_CUDA, "decode kernel occupancy query failed");
     a.hdr = reinterpret_cast<WsHeader*>(ws);
@@ -337,7 +338,7 @@ static int rpa_update_prepare(const rpa_params* p, const void* new_k, const void
     a.max_num_tokens = p->max_num_tokens;
     a.num_kv_heads = p->num_combined_kv_heads / 2;
     a.head_dim = p->head_dim;
-    a.esz = p->kv_dtype == RPA_DTYPE_FP8_E4M3 ? 1 : 2;
+    a.esz = p->kv_dtype == RPA_DTYPE_BF16 ? 2 : 1;
     a.total_num_pages = p->total_num_pages;
     a.page_size = p->page_size;
     a.max_num_seqs = p->max_num_seqs;

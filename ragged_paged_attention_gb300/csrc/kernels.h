@@ -75,7 +75,8 @@ struct RpaArgs {
     __nv_bfloat16* out;
     int max_num_tokens, num_q_heads, num_kv_heads, head_dim;
     int total_num_pages, page_size, max_num_seqs, pages_per_seq;
-    int kv_fp8;
+    int kv_byte;                // one-byte K/V elements: e4m3, or int8 when kv_int8
+    int kv_int8;
     float sm_scale, soft_cap;
     int sliding_window;
     int has_scale;              // k_scale or v_scale given

@@ -15,8 +15,8 @@
 //     P^T moved into B-fragment layout by movmatrix; the online softmax runs per column
 //     (a query row) across the 8 lanes that share it.  Half the tensor-core work and
 //     half the accumulator registers of rows-on-M tiles, whose 16 rows would be mostly
-//     padding; fp8 (or scaled bf16) K/V are dequantised by the warp into its own bf16
-//     rows as bf16(float(x) * scale): K first, then (after QK) V into the same rows;
+//     padding; fp8 or int8 (or scaled bf16) K/V are dequantised by the warp into its own
+//     bf16 rows as bf16(float(x) * scale): K first, then (after QK) V into the same rows;
 //   * slots past kv_len are never copied: the stage memory is zeroed once at start, so
 //     a skipped row holds finite data whose probability is exactly zero.
 // Items split the keys of a sequence (flash-decoding); split partials (m, l, O) are
@@ -47,11 +47,17 @@ struct DecTile {
     static_assert(kSeg % 16 == 0, "bulk copies move 16-byte multiples");
 };
 
-// 8 elements (K or V of one head) -> 8 bf16 of bf16(float(x) * scale), packed in a uint4.
-template <int ESZ>
+// 8 elements (K or V of one head) -> 8 bf16 of bf16(float(x) * scale), packed in a uint4
+// (one-byte elements: e4m3, or int8 when I8).
+template <int ESZ, bool I8 = false>
 __device__ __forceinline__ uint4 dequant8(const uint8_t* src, float sc) {
     uint32_t w[4];
-    if (ESZ == 1) {
+    if (ESZ == 1 && I8) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+        const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16((float)b[2 * e] * sc, (float)b[2 * e + 1] * sc);
+    } else if (ESZ == 1) {
         const uint2 raw = *reinterpret_cast<const uint2*>(src);
         const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
 #pragma unroll
@@ -71,21 +77,36 @@ __device__ __forceinline__ uint4 dequant8(const uint8_t* src, float sc) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// 8 e4m3 elements -> 8 f16 (exact, unscaled), packed in a uint4.
-__device__ __forceinline__ uint4 fp8x8_to_f16(const uint8_t* src) {
+// Two int8 -> an f16 pair, exactly: with the exponent field of 1024 (0x6400) an f16's
+// 10-bit mantissa counts units, so 0x6400 | (x + 128) is 1024 + x + 128; subtracting 1152
+// leaves x (every intermediate is an integer below 2048: exact).
+__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t v) {
+    const uint32_t u = (v & 0xFFu) | ((uint32_t)(v & 0xFF00u) << 8);  // bytes to the two halves
+    uint32_t h = (u ^ 0x00800080u) | 0x64006400u;
+    const uint32_t bias = 0x64806480u;                                 // 1152 in both halves
+    asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(h) : "r"(bias));
+    return h;
+}
+
+// 8 one-byte elements (e4m3, or int8 when I8) -> 8 f16 (exact, unscaled), packed in a uint4.
+template <bool I8>
+__device__ __forceinline__ uint4 byte8_to_f16(const uint8_t* src) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src);
     const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+    if (I8) return make_uint4(s8x2_to_f16x2(h[0]), s8x2_to_f16x2(h[1]), s8x2_to_f16x2(h[2]), s8x2_to_f16x2(h[3]));
     return make_uint4(e4m3x2_to_f16x2(h[0]), e4m3x2_to_f16x2(h[1]), e4m3x2_to_f16x2(h[2]), e4m3x2_to_f16x2(h[3]));
 }
 
-// F16 (fp8 caches whose k_scale and v_scale are powers of two): bf16(float(x) * scale) is then
-// exactly x * scale, so K and V go to the tensor cores as exact f16 values (one convert per
-// pair) and the scales are applied to S and O instead; each query row is brought into f16
-// range by a power of two (undone on its scores), which keeps its bf16 values exact.
-template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
+// F16 (fp8 or int8 caches whose k_scale and v_scale are powers of two): bf16(float(x) * scale)
+// is then exactly x * scale, so K and V go to the tensor cores as exact f16 values and the
+// scales are applied to S and O instead; each query row is brought into f16 range by a power
+// of two (undone on its scores), which keeps its bf16 values exact. I8: the one-byte elements
+// are int8.
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false>
 __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decode_kernel(RpaArgs a) {
     using T = DecTile<D, HG, ESZ, CONV>;
-    static_assert(!F16 || (CONV && ESZ == 1), "the f16 path takes fp8 caches");
+    static_assert(!F16 || (CONV && ESZ == 1), "the f16 path takes one-byte caches");
+    static_assert(!I8 || (CONV && ESZ == 1), "int8 caches take the converting path");
     constexpr int BK = T::BK, STAGES = T::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
@@ -286,7 +307,7 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         const int kk = i / kChunks, c = i % kChunks;
                         const uint8_t* src = stg + kk * T::kRow + (warp * 2 * D + part * D + c * 8) * ESZ;
                         *reinterpret_cast<uint4*>(cb + kk * T::kConvRow + c * 16) =
-                            F16 ? fp8x8_to_f16(src) : dequant8<ESZ>(src, sc);
+                            F16 ? byte8_to_f16<I8>(src) : dequant8<ESZ, I8>(src, sc);
                     }
                     __syncwarp();
                 };
@@ -475,10 +496,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
 }
 
 // per_sm_out != nullptr: only report the kernel's resident CTAs per SM (no launch)
-template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false>
 static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     using T = DecTile<D, HG, ESZ, CONV>;
-    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16>;
+    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16, I8>;
     static int per_sm = 0;
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -521,9 +542,11 @@ int decode_heads_for(int head_dim, bool fp8) {
 template <int D>
 static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     constexpr int HG = D >= 256 ? 2 : 4;
-    if (a.kv_fp8 && pow2_scale(a.k_scale_or_one) && pow2_scale(a.v_scale_or_one))
-        return launch_decode<D, HG, 1, true, true>(a, num_sms, stream, per_sm_out);
-    if (a.kv_fp8) return launch_decode<D, HG, 1, true>(a, num_sms, stream, per_sm_out);
+    const bool pow2 = pow2_scale(a.k_scale_or_one) && pow2_scale(a.v_scale_or_one);
+    if (a.kv_int8 && pow2) return launch_decode<D, HG, 1, true, true, true>(a, num_sms, stream, per_sm_out);
+    if (a.kv_int8) return launch_decode<D, HG, 1, true, false, true>(a, num_sms, stream, per_sm_out);
+    if (a.kv_byte && pow2) return launch_decode<D, HG, 1, true, true>(a, num_sms, stream, per_sm_out);
+    if (a.kv_byte) return launch_decode<D, HG, 1, true>(a, num_sms, stream, per_sm_out);
     if (a.has_scale) return launch_decode<D, HG, 2, true>(a, num_sms, stream, per_sm_out);
     return launch_decode<D, HG, 2, false>(a, num_sms, stream, per_sm_out);
 }

@@ -102,7 +102,7 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         red[0] = W;
         s_pf = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
         s_db = (float)(W - NG * a.item_cost_keys) * (float)a.decode_heads * 2.f * (float)a.head_dim *
-               (a.kv_fp8 ? 1.f : 2.f);
+               (a.kv_byte ? 1.f : 2.f);
     }
     __syncthreads();
     // SMs for the prefill kernel beside decode: the n minimising max(prefill time on n SMs,

@@ -84,11 +84,17 @@ __device__ __forceinline__ typename KvRaw<FP8>::type kv_load_raw(const uint8_t* 
     else
         return __ldg(reinterpret_cast<const uint4*>(row + c * 16));
 }
-// Raw chunk -> 16 bytes of bf16: e4m3 (or scaled bf16) values become bf16(float(x) * scale).
-template <bool FP8, bool SCALE>
+// Raw chunk -> 16 bytes of bf16: e4m3 or int8 (I8) (or scaled bf16) values become
+// bf16(float(x) * scale).
+template <bool FP8, bool SCALE, bool I8 = false>
 __device__ __forceinline__ uint4 kv_convert(typename KvRaw<FP8>::type raw, float sc) {
     uint32_t w[4];
-    if constexpr (FP8) {
+    if constexpr (FP8 && I8) {
+        const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16((float)b[2 * e] * sc, (float)b[2 * e + 1] * sc);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (FP8) {
         const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -108,38 +114,10 @@ __device__ __forceinline__ uint4 kv_convert(typename KvRaw<FP8>::type raw, float
     }
 }
 
-// 8 source elements of a K/V row -> 16 bytes of bf16 (dequantised when needed).
-template <bool FP8, bool SCALE>
-__device__ __forceinline__ uint4 kv_chunk(const uint8_t* row, int c, float sc) {
-    if (FP8) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row + c * 8));
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = e4m3x2_to_float2(h[e]);
-            w[e] = pack_bf16(f.x * sc, f.y * sc);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    uint4 v = __ldg(reinterpret_cast<const uint4*>(row + c * 16));
-    if (SCALE) {
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h[e]);
-            w[e] = pack_bf16(f.x * sc, f.y * sc);
-        }
-        v = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    return v;
-}
-
 template <bool TMA>
 constexpr int prefill_warps() { return 8 + 4 + 1; }  // softmax, producers (2 for K, 2 for V), MMA
 
-template <int D, bool FP8, bool SCALE, bool TMA>
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false>
 __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                           int box_rows, int q_tma, int tail) {
@@ -402,7 +380,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                             for (int c = 0; c < kGroup; ++c) {
                                 const int cc = c0 + c;
                                 *reinterpret_cast<uint4*>(stage + (cc >> 3) * T::kPanel + kk * 128 + (((cc & 7) ^ (kk & 7)) << 4)) =
-                                    kv_convert<FP8, SCALE>(raw[c], sc);
+                                    kv_convert<FP8, SCALE, I8>(raw[c], sc);
                             }
                         }
                     }
@@ -662,11 +640,11 @@ static bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t d0, uint6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FP8, bool SCALE, bool TMA>
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false>
 static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
                               const CUtensorMap& tq, int box_rows, int q_tma, int tail) {
     using T = PreTc<D>;
-    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA>;
+    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -689,14 +667,15 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     // the block, or boxes too small for one lane each, take the register path
     const int box_rows = ps < BK ? ps : BK;
     // (boxes of >= 8 rows keep every TMA destination on a 1024-byte swizzle-atom boundary)
-    bool tma = !a.kv_fp8 && !a.has_scale && (ps & (ps - 1)) == 0 && box_rows >= 8 && BK / box_rows <= 32;
+    bool tma = !a.kv_byte && !a.has_scale && (ps & (ps - 1)) == 0 && box_rows >= 8 && BK / box_rows <= 32;
     const uint64_t tokens = (uint64_t)a.total_num_pages * ps;
     if (tma) tma = make_tmap_bf16(&tkv, a.kv_pages, D, C, tokens, 1, box_rows);
     int q_tma = 0;
     if (tma && 128 % G == 0)
         q_tma = make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
     if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma, tail);
-    if (a.kv_fp8) return launch_pre<D, true, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
+    if (a.kv_int8) return launch_pre<D, true, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
+    if (a.kv_byte) return launch_pre<D, true, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     if (a.has_scale) return launch_pre<D, false, true, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     return launch_pre<D, false, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
 }

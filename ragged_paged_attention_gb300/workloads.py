@@ -39,6 +39,8 @@ def _randn(rng: np.random.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
     """N(0, 1) float32 values rounded to ``dtype``.  Large draws are split into fixed
     blocks, each from its own PCG64 stream spawned from one seed taken from ``rng``,
     and filled by a thread pool."""
+    if dtype == torch.int8:  # integer caches: uniform over the whole byte
+        return torch.from_numpy(rng.integers(-128, 128, size=tuple(shape)).astype(np.int8))
     n = int(np.prod(shape))
     if n <= _CHUNK:
         x = rng.standard_normal(size=n, dtype=np.float32)
@@ -63,6 +65,8 @@ def _fill_nan(t: torch.Tensor) -> None:
         t.view(torch.int16).fill_(BF16_NAN)
     elif t.dtype == torch.float8_e4m3fn:
         t.view(torch.uint8).fill_(E4M3_NAN)
+    elif t.dtype == torch.int8:  # no NaN: the extreme value, which would show in any output
+        t.fill_(127)
     else:
         t.fill_(float("nan"))
 

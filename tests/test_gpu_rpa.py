@@ -167,7 +167,7 @@ def test_bad_page_index_sets_device_error():
     assert bits & 0x04
 
 
-@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn])
+@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn, torch.int8])
 def test_update_kv_cache_bit_exact(kv_dtype):
     b = workloads.make_rpa([1, 1, 6, 19], [33, 1, 6, 40], num_q_heads=8, num_kv_heads=4, head_dim=128, page_size=16,
                            seed=18, kv_dtype=kv_dtype, max_num_seqs=6, max_num_tokens=32, extra_pages=4)
@@ -226,3 +226,21 @@ def test_forward_update_matches_update_then_forward(make):
     ref = oracle.rpa(b.q, ref_pages, b.kv_lens, b.page_indices, b.cu_q_lens, n, tokens=tokens, **opts)
     tol = TOL_FP8 * (opts["v_scale"] or 1.0) if b.kv_pages.dtype == torch.float8_e4m3fn else TOL_BF16
     assert max_abs(out2[tokens], ref[tokens]) <= tol
+
+
+@pytest.mark.parametrize("ks,vs", [(None, None), (1 / 32, 1 / 64), (0.0123, 0.021)],
+                         ids=["exact", "pow2_f16", "scaled_bf16"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_int8_kv(ks, vs, d):
+    # int8 caches: exact integers without scales and with power-of-two scales (the f16
+    # tensor-core path), bf16(float(x) * scale) otherwise; decode and prefill sequences
+    hq, hkv = (8, 2) if d < 256 else (4, 2)
+    b = workloads.make_rpa([1, 9, 1, 40], [77, 30, 300, 200], num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                           page_size=16, seed=60 + d, kv_dtype=torch.int8, k_scale=ks, v_scale=vs,
+                           sm_scale=2.0 / (74.0 * (ks or 1.0) * math.sqrt(d)))  # logits' spread ~2
+    out, bits, _ = run_gpu(b)
+    assert bits == 0
+    ref = oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), **b.options())
+    T = b.num_tokens
+    scale = float(ref[:T].abs().max())
+    assert max_abs(out[:T], ref[:T]) <= 2e-2 * scale
