@@ -350,6 +350,13 @@ RPA_API int sparse_mla_write_and_attend_ragged(const sparse_ragged_params* p, co
  * NULL) and clears it.  Returns RPA_ERR_DEVICE_CHECK when any bit was set. */
 RPA_API int rpa_check_device_status(void* workspace, uint32_t* bits, rpa_stream_t stream);
 
+/* Failure-path check (diagnostics): launches one thread that waits, through the same bounded
+ * wait every pipeline of the library uses, on a barrier nothing arrives on.  The wait gives up
+ * after its limit (2 s), sets RPA_DEV_ERR_TIMEOUT in the workspace's error word and the kernel
+ * returns: rpa_check_device_status then reports it, and the context stays usable.
+ * `workspace` needs at least 256 bytes. */
+RPA_API int rpa_selftest_bounded_wait(void* workspace, size_t workspace_bytes, rpa_stream_t stream);
+
 /* Per-kernel timing (diagnostics).  While enabled, every kernel the library launches
  * is bracketed by two CUDA events on its launch stream (a GPU-side timestamp pair; no
  * host synchronisation).  rpa_profile_read synchronises on the recorded events and

@@ -28,7 +28,8 @@ EXPORTS = ("rpa_workspace_size", "rpa_forward", "rpa_update_kv_cache", "mla_work
            "mla_update_kv_cache", "mla_rpa_forward", "sparse_mla_workspace_size", "sparse_mla_forward",
            "rpa_check_device_status", "rpa_last_error", "rpa_version", "rpa_profile_enable",
            "rpa_profile_reset", "rpa_profile_read", "rpa_forward_noalloc", "rpa_launch_count",
-           "rpa_forward_update", "sparse_mla_ragged_workspace_size", "sparse_mla_write_and_attend_ragged")
+           "rpa_forward_update", "sparse_mla_ragged_workspace_size", "sparse_mla_write_and_attend_ragged",
+           "rpa_selftest_bounded_wait")
 
 
 class RpaError(RuntimeError):
@@ -108,6 +109,7 @@ def load_library(path: str = LIB_PATH):
         lib.sparse_mla_ragged_workspace_size.argtypes = [ctypes.POINTER(sparse_ragged_params), szp]
         lib.sparse_mla_write_and_attend_ragged.argtypes = [ctypes.POINTER(sparse_ragged_params)] + [P] * 14 + [sz, P]
         lib.rpa_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+        lib.rpa_selftest_bounded_wait.argtypes = [P, sz, P]
         lib.rpa_profile_enable.argtypes = [ctypes.c_int]
         lib.rpa_profile_reset.argtypes = []
         lib.rpa_profile_read.argtypes = [ctypes.POINTER(rpa_kernel_time), ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
@@ -478,6 +480,12 @@ def sparse_mla_write_and_attend_ragged(ql, qpe, kvc, kpe, cache, topk, positions
         _ptr(loc), _ptr(seq_lens), _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream()))
     return out
+
+
+def selftest_bounded_wait(workspace: torch.Tensor) -> None:
+    """Launch the failure-path check (a bounded wait that runs out after 2 s and records
+    RPA_DEV_ERR_TIMEOUT in ``workspace``'s error word)."""
+    _check(load_library().rpa_selftest_bounded_wait(_ptr(workspace), workspace.numel(), _stream()))
 
 
 def check_device_status(workspace: torch.Tensor) -> int:

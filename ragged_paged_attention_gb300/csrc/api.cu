@@ -646,6 +646,15 @@ int sparse_mla_write_and_attend_ragged(const sparse_ragged_params* p, const void
     return RPA_OK;
 }
 
+int rpa_selftest_bounded_wait(void* workspace, size_t workspace_bytes, rpa_stream_t stream) {
+    if (!workspace) return fail(RPA_ERR_NULL, "workspace is NULL");
+    if (workspace_bytes < (size_t)kWsHeaderBytes) return fail(RPA_ERR_WORKSPACE, "workspace smaller than 256 bytes");
+    cudaError_t e = launch_wait_selftest(&reinterpret_cast<WsHeader*>(workspace)->error_bits,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rpa_selftest_bounded_wait launch");
+    return RPA_OK;
+}
+
 int rpa_check_device_status(void* workspace, uint32_t* bits, rpa_stream_t stream) {
     if (!workspace) return fail(RPA_ERR_NULL, "workspace is NULL");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -195,6 +195,7 @@ struct MlaUpdateArgs {
 };
 
 cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t stream);
 cudaError_t launch_rpa_forward_update(const RpaArgs& a, const RpaUpdateArgs& u, int num_sms, cudaStream_t stream);
 cudaError_t launch_mla_forward_update(const LatentArgs& a, const MlaUpdateArgs& u, int num_sms, cudaStream_t stream);
 // Launch with programmatic stream serialization when pdl (the kernel may start before the

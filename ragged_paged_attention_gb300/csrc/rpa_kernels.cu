@@ -407,6 +407,26 @@ __global__ void __launch_bounds__(1024) rpa_plan_update_kernel(RpaArgs a, RpaUpd
 }
 
 // ---------------------------------------------------------------------------
+// Failure path check: one thread waits, through the bounded wait every pipeline uses, on an
+// mbarrier nothing ever arrives on; the wait gives up after its limit, records
+// RPA_DEV_ERR_TIMEOUT and the kernel returns (no fault, the context stays usable).
+// ---------------------------------------------------------------------------
+__global__ void rpa_wait_selftest_kernel(uint32_t* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t stream) {
+    rpa_wait_selftest_kernel<<<1, 32, 0, stream>>>(err);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
 // the attention launches behind the plan: with overlap, prefill on the plan's share of the SMs,
