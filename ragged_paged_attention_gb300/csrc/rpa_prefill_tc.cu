@@ -12,20 +12,22 @@
 //     caches go through registers in warps 4-7 and are dequantised there as
 //     bf16(float(x) * scale).  Rows past the key range are never copied: the stage
 //     memory is zeroed at start, so such rows hold finite data with zero probability;
-//   * the last warp issues tcgen05.mma: S = Q K^T into one of two TMEM score buffers, then
-//     O += P V into the TMEM output accumulator (V read MN-major from the same panels);
+//   * warp 12 issues tcgen05.mma S = Q K^T into one of two TMEM score buffers, warp 13
+//     O += P V into the TMEM output accumulator (V read MN-major from the same panels, P
+//     the A operand from one of two TMEM P buffers);
 //   * warps 0-7 turn S into P, two warps per TMEM lane quarter (one thread per row, each
 //     warp of the pair half of the row's columns; the row max is exchanged through
-//     shared memory): scale, soft cap, mask (only on blocks that cross a row's causal or
-//     window limit), online softmax in the log2 domain with lazy rescaling (the running
-//     max only moves when it grows by more than 2^8, and then O is rescaled in TMEM),
-//     P written as bf16 pairs into TMEM over the first half of the block's score buffer
-//     (PV reads its A operand from TMEM, so shared memory holds only Q and the K/V rings);
-//     at the end they read O, divide by l, store bf16 rows.
+//     shared memory): scale (folded into the exponent's FFMA when there is no soft cap),
+//     soft cap, mask (only on blocks that cross a row's causal or window limit), online
+//     softmax in the log2 domain with lazy rescaling (the running max only moves when it
+//     grows by more than 2^8, and then O is rescaled in TMEM), P written as bf16 pairs into
+//     the block's P buffer (shared memory holds only Q and the K/V rings); at the end they
+//     read O, divide by l, store bf16 rows.
 // Barriers: k_full/k_empty and v_full/v_empty (producers <-> MMA; separate K and V rings
-// of NS stages, so a K slot frees as soon as its QK is done), s_full (MMA -> softmax, per
-// score buffer), p_full/p_empty (softmax <-> MMA per buffer; a buffer takes the next QK
-// once PV has read its P), q_full, o_full.  Blocks are 128 keys (64 for D = 256).
+// of NSK / NSV stages, so a K slot frees as soon as its QK is done); per score buffer s_full
+// (QK -> softmax) and s_free (the softmax has loaded the scores: the next QK into that buffer
+// may start while the softmax is still computing); per P buffer p_full (softmax -> PV) and
+// p_empty (PV has read P); q_full, o_full.  Blocks are 128 keys (64 for D = 256).
 // Every wait is bounded (common.cuh); on a timeout the CTA records an error and stops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -43,22 +45,28 @@ struct PreTc {
     static constexpr int kQ = DP * 128 * 128;            // Q tile: DP panels of [128 rows x 128 B]
     static constexpr int kPanel = BK * 128;              // one K or V panel: [BK rows x 128 B]
     static constexpr int kStage = DP * kPanel;           // K (or V) of one block
-    // stages of the K ring and of the V ring: as many as fit (P lives in TMEM)
-    static constexpr int kFitNS = (232448 - kQ - 2560) / (2 * kStage);  // 2.5 KB: barriers, scratch
-    static constexpr int NS = kFitNS > 4 ? 4 : kFitNS;
+    // stages of the K ring and of the V ring: as many as fit (P lives in TMEM), V's ring the
+    // deeper one when the count is odd (a V slot is held from its load until PV, K's only until QK)
+    static constexpr int kFitS = (232448 - kQ - 2560) / kStage;  // 2.5 KB: barriers, scratch
+    static constexpr int kTotS = kFitS > 8 ? 8 : kFitS;
+    static constexpr int NSK = kTotS / 2;
+    static constexpr int NSV = kTotS - NSK;
     static constexpr int kOffK = kQ;
-    static constexpr int kOffV = kOffK + NS * kStage;
-    static constexpr int kOffBar = kOffV + NS * kStage;
-    static constexpr int kNumBars = 4 * NS + 9;
+    static constexpr int kOffV = kOffK + NSK * kStage;
+    static constexpr int kOffBar = kOffV + NSV * kStage;
+    static constexpr int kNumBars = 2 * (NSK + NSV) + 4 * 2 + 3;  // rings, S/P barriers (kSB = 2), q, o, fin
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
     static constexpr int kOffItem = kOffRed + 2 * 2 * 128 * 4;            // WorkItem (16-byte aligned) + abort flag
     static constexpr int kSmem = kOffItem + 48;
     static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
-    static_assert(NS >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
-    // TMEM: S buffers at 0 and BK (P, bf16 pairs, over the first BK/2 columns of its block's
-    // buffer once the softmax has read it), O after
-    static constexpr int kColO = 2 * BK;
+    static_assert(NSK >= 2 && NSV >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
+    // TMEM: kSB score buffers of BK columns, kSB P buffers of BK/2 columns (bf16 pairs), O.
+    // S and P live apart, so QK of block j+2 may overwrite S as soon as the softmax has loaded
+    // block j's scores, while PV of block j still reads P(j) from its own buffer.
+    static constexpr int kSB = 2;
+    static constexpr int kColP = kSB * BK;
+    static constexpr int kColO = kColP + kSB * (BK / 2);
     static constexpr int kTmemCols = kColO + D <= 256 ? 256 : 512;
     static constexpr int kSoftWarps = 8;                 // two per TMEM lane quarter (column halves)
     static constexpr int kHalf = BK / 2;                 // score columns per softmax warp
@@ -115,7 +123,7 @@ __device__ __forceinline__ uint4 kv_convert(typename KvRaw<FP8>::type raw, float
 }
 
 template <bool TMA>
-constexpr int prefill_warps() { return 8 + 4 + 1; }  // softmax, producers (2 for K, 2 for V), MMA
+constexpr int prefill_warps() { return 8 + 4 + 2; }  // softmax, producers (2 for K, 2 for V), QK and PV issuers
 
 template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false>
 __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
@@ -137,21 +145,28 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     }
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
-    constexpr int NS = T::NS;
-    uint64_t* k_full = bars;              // [NS]  K block landed
-    uint64_t* k_empty = bars + NS;        // [NS]  QK of that block done
-    uint64_t* v_full = bars + 2 * NS;     // [NS]  V block landed
-    uint64_t* v_empty = bars + 3 * NS;    // [NS]  PV of that block done
-    uint64_t* s_full = bars + 4 * NS;       // [2] S buffer written by QK
-    uint64_t* p_full = bars + 4 * NS + 2;   // [2] P written over that buffer (and O rescaled)
-    uint64_t* p_empty = bars + 4 * NS + 4;  // [2] PV of that buffer's P done (buffer free again)
-    uint64_t* q_full = bars + 4 * NS + 6;
-    uint64_t* o_full = bars + 4 * NS + 7;
-    uint64_t* fin = bars + 4 * NS + 8;
+    constexpr int NSK = T::NSK, NSV = T::NSV;
+    uint64_t* k_full = bars;                       // [NSK] K block landed
+    uint64_t* k_empty = bars + NSK;                // [NSK] QK of that block done
+    uint64_t* v_full = bars + 2 * NSK;             // [NSV] V block landed
+    uint64_t* v_empty = bars + 2 * NSK + NSV;      // [NSV] PV of that block done
+    uint64_t* const bars_s = bars + 2 * (NSK + NSV);
+    constexpr int SB = T::kSB;
+    static_assert(T::kSB == 2, "barrier layout");
+    uint64_t* s_full = bars_s;            // [SB] S buffer written by QK
+    uint64_t* s_free = bars_s + SB;       // [SB] the softmax has loaded that buffer's scores
+    uint64_t* p_full = bars_s + 2 * SB;   // [SB] P buffer written (and O rescaled)
+    uint64_t* p_empty = bars_s + 3 * SB;  // [SB] PV of that buffer's P done (buffer free again)
+    uint64_t* q_full = bars_s + 4 * SB;
+    uint64_t* o_full = q_full + 1;
+    uint64_t* fin = q_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + T::kOffRed);
     // producer warps [8, 12): warps 8-9 stream K, 10-11 V; then the MMA warp
-    constexpr int kProdW0 = 8, kProdW1 = 12, kMmaW = kProdW1;
+    // warp 12 issues the QK MMAs (and owns the TMEM allocation), warp 13 the PV MMAs: two issuing
+    // threads, so neither stream waits behind the other's inputs (an MMA issue blocks while the
+    // tensor pipe's short queue is full)
+    constexpr int kProdW0 = 8, kProdW1 = 12, kMmaW = kProdW1, kPvW = kProdW1 + 1;
     // (no static shared variables: with the 1024-byte aligned dynamic block they would
     // round up to 1 KB and push the kernel past the 227 KB limit)
     WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + T::kOffItem);
@@ -168,20 +183,23 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     for (int i = tid * 16; i < T::kOffBar; i += blockDim.x * 16) *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NSK; ++i) {
             mbar_init(&k_full[i], 64);  // the two warps streaming K
             mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], 64);
+        }
+        for (int i = 0; i < NSV; ++i) {
+            mbar_init(&v_full[i], 64);  // the two warps streaming V
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 256);
+            mbar_init(&s_free[i], T::kSoftWarps * 32);
+            mbar_init(&p_full[i], T::kSoftWarps * 32);
             mbar_init(&p_empty[i], 1);
         }
         mbar_init(q_full, (kProdW1 - kProdW0) * 32);  // every producer thread arrives
         mbar_init(o_full, 1);
-        mbar_init(fin, 1);
+        mbar_init(fin, 2);  // both issuing threads
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -265,59 +283,57 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 const int p0 = pw * kPW, p1 = min(T::DP, p0 + kPW);
                 uint64_t* fbar = part ? v_full : k_full;
                 uint64_t* ebar = part ? v_empty : k_empty;
+                // box_rows and page_size are powers of two (the host's condition for this path) and
+                // a box never crosses a page, so the per-block bookkeeping is shifts and one compare
+                // per lane: the number of full boxes is the same on every lane (no shuffles)
                 const int nbox = BK / box_rows;
-                const size_t tbl = (size_t)s * a.pages_per_seq;
+                const int lbr = __ffs(box_rows) - 1, lps = __ffs(a.page_size) - 1, pmask_ps = a.page_size - 1;
+                const uint32_t box_bytes = (uint32_t)box_rows * (p1 - p0) * 128;
+                const int* tbl = a.page_indices + (size_t)s * a.pages_per_seq;
                 auto page_of = [&](int j) -> int {
                     const int key = kb + j * BK + lane * box_rows;
-                    return (lane < nbox && j < nb && key < ke) ? __ldg(a.page_indices + tbl + key / a.page_size) : -1;
+                    return (lane < nbox && j < nb && key < ke) ? __ldg(tbl + (key >> lps)) : 0;
                 };
                 int page_next = page_of(0);
                 for (int j = 0; j < nb; ++j) {
-                    const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
-                    const int page = page_next;
+                    const uint32_t q = jb + j, slot = part ? q % NSV : q % NSK, par = (part ? q / NSV : q / NSK) & 1;
+                    int page = page_next;
                     page_next = page_of(j + 1);
-                    const int kbx = kb + j * BK + lane * box_rows;
-                    int rows = lane < nbox ? min(box_rows, ke - kbx) : 0;
-                    if (rows < 0) rows = 0;
-                    if (rows > 0 && (unsigned)page >= (unsigned)a.total_num_pages) {
+                    const int kbj = kb + j * BK, avail = ke - kbj;  // avail >= 1
+                    const int nfull = min(nbox, avail >> lbr);
+                    const int prow = nfull < nbox ? avail - (nfull << lbr) : 0;  // rows of a partial box
+                    if (lane <= nfull && lane < nbox && (unsigned)page >= (unsigned)a.total_num_pages) {
                         if (part == 0) set_error(err, RPA_DEV_ERR_PAGE);
-                        rows = 0;
+                        page = 0;  // an in-bounds page keeps the barrier's byte count; the error is recorded
                     }
-                    const bool full = rows == box_rows;
-                    uint32_t bytes = full ? (uint32_t)box_rows * (p1 - p0) * 128 : 0u;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-                    const int z0 = page * a.page_size + kbx % a.page_size;
-                    const uint32_t pmask = __ballot_sync(0xffffffffu, rows > 0 && !full);
+                    const int kbx = kbj + lane * box_rows;
+                    const int z0 = (page << lps) + (kbx & pmask_ps);
                     int g = 1;
                     if (lane == 0) {
                         g = mbar_wait(&ebar[slot], par ^ 1, err);
                         if (g)
-                            mbar_expect_tx(&fbar[slot], bytes);
+                            mbar_expect_tx(&fbar[slot], (uint32_t)nfull * box_bytes);
                         else
                             s_abort = 1;
                     }
                     if (!__shfl_sync(0xffffffffu, g, 0)) break;
                     uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage;
-                    if (full) {
+                    if (lane < nfull) {
                         for (int p = p0; p < p1; ++p)
                             tma_load_3d(smem_u32(stage + p * T::kPanel + lane * box_rows * 128), &tm_kv, 64 * p,
                                         2 * kvh + part, z0, &fbar[slot]);
                     }
-                    uint32_t pm = p1 > p0 ? pmask : 0u;
-                    const bool wrote = pm != 0;
-                    while (pm) {
-                        const int src_lane = __ffs(pm) - 1;
-                        pm &= pm - 1;
-                        const int prow = __shfl_sync(0xffffffffu, rows, src_lane);
-                        const int pz0 = __shfl_sync(0xffffffffu, z0, src_lane);
+                    const bool wrote = prow > 0 && p1 > p0;
+                    if (wrote) {
+                        // the partial last box: its rows through registers, by the whole warp
+                        const int pz0 = __shfl_sync(0xffffffffu, z0, nfull);
                         constexpr int kCh = kPW * 8;  // this warp's 16-byte chunks of a row
                         for (int i = lane; i < prow * kCh; i += 32) {
-                            const int t = i / kCh, c = p0 * 8 + i % kCh;
+                            const int tr = i / kCh, c = p0 * 8 + i % kCh;
                             if (c >= D / 8) continue;
-                            const int kk = src_lane * box_rows + t;
+                            const int kk = nfull * box_rows + tr;
                             const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                                kvp + ((size_t)(pz0 + t) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
+                                kvp + ((size_t)(pz0 + tr) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
                             *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) = v;
                         }
                     }
@@ -344,7 +360,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
 #pragma unroll
                 for (int i = 0; i < kRpt; ++i) page_next[i] = page_of(0, i);
                 for (int j = 0; j < nb; ++j) {
-                    const uint32_t q = jb + j, slot = q % NS, par = (q / NS) & 1;
+                    const uint32_t q = jb + j, slot = part ? q % NSV : q % NSK, par = (part ? q / NSV : q / NSK) & 1;
                     int page[kRpt];
 #pragma unroll
                     for (int i = 0; i < kRpt; ++i) {
@@ -389,68 +405,48 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 }
             }
         } else if (warp == kMmaW) {
-            // ---------------- MMA issuer ----------------
+            // ---------------- QK issuer ----------------
             if (lane == 0) {
                 constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
-                constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, false, true);
                 // descriptors of the operand bases; a byte offset d within shared memory adds
                 // d >> 4 to the start-address field (no carry: every address is below 256 KB)
                 const uint64_t qdesc = umma_desc_sw128(smem_u32(smem), 16, 1024);
                 const uint64_t kdesc = umma_desc_sw128(smem_u32(smem + T::kOffK), 16, 1024);
-                const uint64_t vdesc = umma_desc_sw128(smem_u32(smem + T::kOffV), T::kPanel, 1024);
                 bool ok = mbar_wait(q_full, iph, err);
-                tc_fence_after();
-                // issue QK(next) and PV(next) in whichever order their inputs become ready:
-                // QK needs its K block and a free score buffer, PV its P tile and V block
-                int nq = 0, np = 0;
-                unsigned long long t0 = 0;
-                uint32_t idle = 0;
-                while (ok && np < nb) {
-                    bool moved = false;
-                    if (nq < nb) {
-                        const uint32_t q = jb + nq, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
-                        // the score buffer is free once PV two blocks back has read its P
-                        if (mbar_test(&k_full[slot], par) && mbar_test(&p_empty[sb], sp ^ 1)) {
-                            tc_fence_after();
-                            const uint64_t kb0 = kdesc + (uint64_t)((slot * T::kStage) >> 4);
+                for (int j = 0; ok && j < nb; ++j) {
+                    const uint32_t q = jb + j, sb = q % SB, sp = (q / SB) & 1, slot = q % NSK, par = (q / NSK) & 1;
+                    // K landed, and the score buffer's previous scores (block q - SB) loaded by the softmax
+                    ok = mbar_wait(&k_full[slot], par, err) && mbar_wait(&s_free[sb], sp ^ 1, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t kb0 = kdesc + (uint64_t)((slot * T::kStage) >> 4);
 #pragma unroll
-                            for (int ks = 0; ks < D / 16; ++ks)
-                                umma_bf16(tmem + sb * BK, qdesc + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                                          kb0 + (((ks >> 2) * T::kPanel + (ks & 3) * 32) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
-                            umma_commit(&s_full[sb]);
-                            umma_commit(&k_empty[slot]);
-                            ++nq;
-                            moved = true;
-                        }
-                    }
-                    if (np < nq) {
-                        const uint32_t q = jb + np, sb = q & 1, sp = (q >> 1) & 1, slot = q % NS, par = (q / NS) & 1;
-                        if (mbar_test(&p_full[sb], sp) && mbar_test(&v_full[slot], par)) {
-                            tc_fence_after();
-                            const uint64_t vb0 = vdesc + (uint64_t)((slot * T::kStage) >> 4);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_bf16(tmem + sb * BK, qdesc + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                  kb0 + (((ks >> 2) * T::kPanel + (ks & 3) * 32) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+                    umma_commit(&s_full[sb]);
+                    umma_commit(&k_empty[slot]);
+                }
+                if (!ok) s_abort = 1;
+            }
+        } else if (warp == kPvW) {
+            // ---------------- PV issuer ----------------
+            if (lane == 0) {
+                constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, false, true);
+                const uint64_t vdesc = umma_desc_sw128(smem_u32(smem + T::kOffV), T::kPanel, 1024);
+                bool ok = true;
+                for (int j = 0; ok && j < nb; ++j) {
+                    const uint32_t q = jb + j, pb = q % SB, pp = (q / SB) & 1, slot = q % NSV, par = (q / NSV) & 1;
+                    ok = mbar_wait(&p_full[pb], pp, err) && mbar_wait(&v_full[slot], par, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t vb0 = vdesc + (uint64_t)((slot * T::kStage) >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk)
-                                umma_bf16_ta(tmem + T::kColO, tmem + sb * BK + kk * 8, vb0 + ((kk * 16 * 128) >> 4), idesc_pv,
-                                             (np > 0 || kk > 0) ? 1u : 0u);
-                            umma_commit(&p_empty[sb]);
-                            umma_commit(&v_empty[slot]);
-                            ++np;
-                            moved = true;
-                        }
-                    }
-                    // the wait limit is checked every 256 idle polls (the clock read is not free)
-                    if (moved) {
-                        t0 = 0;
-                        idle = 0;
-                    } else if (++idle == 256) {
-                        idle = 0;
-                        if (t0 == 0) {
-                            t0 = global_ns();
-                        } else if (global_ns() - t0 > kWaitLimitNs) {
-                            set_error(err, RPA_DEV_ERR_TIMEOUT);
-                            ok = false;
-                        }
-                    }
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_ta(tmem + T::kColO, tmem + T::kColP + pb * (BK / 2) + kk * 8, vb0 + ((kk * 16 * 128) >> 4),
+                                     idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&p_empty[pb]);
+                    umma_commit(&v_empty[slot]);
                 }
                 umma_commit(o_full);
                 if (!ok) s_abort = 1;
@@ -466,11 +462,15 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
             const float cap_k2 = cap != 0.f ? 2.f * kLog2e / cap : 0.f;
+            // without a soft cap (and with a positive scale) the row max is taken on the raw
+            // scores and the scale goes into the exponent's one FFMA: 2^(s * c - m)
+            const bool fold = cap == 0.f && c_log2 > 0.f;
+            const float cs = fold ? c_log2 : 1.f;
             constexpr int HB = T::kHalf;
             float m_use = -INFINITY, l_half = 0.f;
             bool ok = true;
-            for (int j = 0; j < nb; ++j) {
-                const uint32_t q = jb + j, slot = q & 1, par = (q >> 1) & 1;  // S / P double buffers
+            for (int j = 0; ok && j < nb; ++j) {
+                const uint32_t q = jb + j, slot = q % SB, par = (q / SB) & 1;  // S and P buffers
                 if (!mbar_wait(&s_full[slot], par, err)) {
                     ok = false;
                     break;
@@ -485,11 +485,12 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     for (int i = 0; i < 32; ++i) x[c * 32 + i] = t32[i];
                 }
                 tc_fence_before();
+                mbar_arrive(&s_free[slot]);  // QK of block q + SB may overwrite these scores
                 const int key0 = kb + j * BK + half * HB;
                 if (cap != 0.f) {
 #pragma unroll
                     for (int i = 0; i < HB; ++i) x[i] = soft_cap(x[i] * scale, cap, cap_k2) * kLog2e;
-                } else {
+                } else if (!fold) {
 #pragma unroll
                     for (int i = 0; i < HB; ++i) x[i] *= c_log2;
                 }
@@ -504,13 +505,12 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 }
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < HB; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], x[i]);
+                for (int i = 0; i < HB; i += 2) mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], x[i], x[i + 1]);
                 float* red_j = red + (q & 1) * 256;
                 red_j[half * 128 + r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                // the pair barrier also orders both halves' S reads before either writes P over them
                 asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
                 tc_fence_after();
-                const float mx = fmaxf(red_j[r], red_j[128 + r]);
+                const float mx = fmaxf(red_j[r], red_j[128 + r]) * cs;  // log2 units
                 float alpha = 1.f;
                 const bool had = m_use > -INFINITY;  // O already holds earlier blocks of this row
                 const bool rescale = mx > m_use + 8.f;
@@ -518,29 +518,37 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     alpha = fast_exp2(m_use - mx);
                     m_use = mx;
                 }
-                const float mu = m_use == -INFINITY ? 0.f : m_use;
-                // P (bf16 pairs) over the first half of this block's score buffer: this warp's
-                // HB keys are TMEM columns slot * BK + half * HB / 2 ..
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                const float nmu = m_use == -INFINITY ? 0.f : -m_use;
+                // P (bf16 pairs) into this block's P buffer once PV of block q - SB has read it:
+                // this warp's HB keys are its columns half * HB / 2 ..
+                if (!mbar_wait(&p_empty[slot], par ^ 1, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 cs2 = make_float2(cs, cs), nmu2 = make_float2(nmu, nmu);
 #pragma unroll
                 for (int c16 = 0; c16 < HB / 32; ++c16) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = fast_exp2(x[c16 * 32 + 2 * e] - mu), p1 = fast_exp2(x[c16 * 32 + 2 * e + 1] - mu);
-                        sum4[e & 3] += p0 + p1;
-                        pk[e] = pack_bf16(p0, p1);
+                        float2 a2 = ffma2(make_float2(x[c16 * 32 + 2 * e], x[c16 * 32 + 2 * e + 1]), cs2, nmu2);
+                        a2.x = fast_exp2(a2.x);
+                        a2.y = fast_exp2(a2.y);
+                        sum2[e & 1] = fadd2(sum2[e & 1], a2);
+                        pk[e] = pack_bf16(a2.x, a2.y);
                     }
-                    tmem_st16_nowait(tmem + lane_off + slot * BK + half * (HB / 2) + c16 * 16, pk);
+                    tmem_st16_nowait(tmem + lane_off + T::kColP + slot * (BK / 2) + half * (HB / 2) + c16 * 16, pk);
                 }
                 // O already holds this row's earlier blocks when l was positive before
                 const bool row_rescale = rescale && had;
-                l_half = l_half * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                l_half = l_half * alpha + ((sum2[0].x + sum2[1].x) + (sum2[0].y + sum2[1].y));
                 // tcgen05.ld/st are warp-collective: the warp rescales together when any of its
                 // rows needs it (the others multiply by 1); each warp of the pair owns D/2 columns
                 if (__any_sync(0xffffffffu, row_rescale)) {
                     const float f = row_rescale ? alpha : 1.f;
-                    const uint32_t qp = q - 1, sp = qp & 1, pp = (qp >> 1) & 1;
+                    const uint32_t qp = q - 1, sp = qp % SB, pp = (qp / SB) & 1;
                     if (!mbar_wait(&p_empty[sp], pp, err)) {  // PV(j-1) has finished writing O
                         ok = false;
                         break;
@@ -602,6 +610,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         tc_fence_after();
     }
     // drain: every MMA this CTA issued has completed before TMEM is released
+    if (warp == kPvW && lane == 0) umma_commit(fin);
     if (warp == kMmaW) {
         if (lane == 0) {
             umma_commit(fin);
