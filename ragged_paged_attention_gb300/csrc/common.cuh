@@ -104,6 +104,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     return r;
 }
 
+// Two int8 -> an f16 pair, exactly: with the exponent field of 1024 (0x6400) an f16's
+// 10-bit mantissa counts units, so 0x6400 | (x + 128) is 1024 + x + 128; subtracting 1152
+// leaves x (every intermediate is an integer below 2048: exact).
+__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t v) {
+    const uint32_t u = (v & 0xFFu) | ((uint32_t)(v & 0xFF00u) << 8);  // bytes to the two halves
+    uint32_t h = (u ^ 0x00800080u) | 0x64006400u;
+    const uint32_t bias = 0x64806480u;                                 // 1152 in both halves
+    asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(h) : "r"(bias));
+    return h;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -304,6 +315,10 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with f16 operands (A and B format fields 0) when `f16`, else bf16.
+__host__ __device__ constexpr uint32_t umma_idesc_16(int M, int N, bool a_mn, bool b_mn, bool f16) {
+    return f16 ? umma_idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10)) : umma_idesc_bf16(M, N, a_mn, b_mn);
 }
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <utility>
@@ -51,6 +52,14 @@ inline void rpa_rates(int head_dim, bool fp8, bool scale, float* pre, float* dec
     const bool conv = fp8 || scale;
     *pre = conv ? (head_dim >= 256 ? 1800.f : 2200.f) : (head_dim >= 256 ? 3000.f : head_dim >= 128 ? 3800.f : 2400.f);
     *dec = conv ? 26.f : 60.f;
+}
+
+// A scale the f16 paths may take: a power of two with e4m3 * scale inside bf16's normal range
+// (bf16(float(x) * scale) is then exactly x * scale, so the scale can move onto S and O).
+inline bool rpa_pow2_scale(float s) {
+    int e = 0;
+    const float m = frexpf(s, &e);
+    return s > 0.f && m == 0.5f && e >= -40 && e <= 40;
 }
 
 // One unit of work for a persistent attention CTA (32 bytes).

@@ -77,17 +77,6 @@ __device__ __forceinline__ uint4 dequant8(const uint8_t* src, float sc) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Two int8 -> an f16 pair, exactly: with the exponent field of 1024 (0x6400) an f16's
-// 10-bit mantissa counts units, so 0x6400 | (x + 128) is 1024 + x + 128; subtracting 1152
-// leaves x (every intermediate is an integer below 2048: exact).
-__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t v) {
-    const uint32_t u = (v & 0xFFu) | ((uint32_t)(v & 0xFF00u) << 8);  // bytes to the two halves
-    uint32_t h = (u ^ 0x00800080u) | 0x64006400u;
-    const uint32_t bias = 0x64806480u;                                 // 1152 in both halves
-    asm("sub.rn.f16x2 %0, %0, %1;\n" : "+r"(h) : "r"(bias));
-    return h;
-}
-
 // 8 one-byte elements (e4m3, or int8 when I8) -> 8 f16 (exact, unscaled), packed in a uint4.
 template <bool I8>
 __device__ __forceinline__ uint4 byte8_to_f16(const uint8_t* src) {
@@ -527,13 +516,6 @@ static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t str
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// A scale the f16 path may take: a power of two with e4m3 * scale inside bf16's normal range.
-static bool pow2_scale(float s) {
-    int e = 0;
-    const float m = frexpf(s, &e);
-    return s > 0.f && m == 0.5f && e >= -40 && e <= 40;
-}
-
 int decode_heads_for(int head_dim, bool fp8) {
     (void)fp8;
     return head_dim >= 256 ? 2 : 4;
@@ -542,7 +524,7 @@ int decode_heads_for(int head_dim, bool fp8) {
 template <int D>
 static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     constexpr int HG = D >= 256 ? 2 : 4;
-    const bool pow2 = pow2_scale(a.k_scale_or_one) && pow2_scale(a.v_scale_or_one);
+    const bool pow2 = rpa_pow2_scale(a.k_scale_or_one) && rpa_pow2_scale(a.v_scale_or_one);
     if (a.kv_int8 && pow2) return launch_decode<D, HG, 1, true, true, true>(a, num_sms, stream, per_sm_out);
     if (a.kv_int8) return launch_decode<D, HG, 1, true, false, true>(a, num_sms, stream, per_sm_out);
     if (a.kv_byte && pow2) return launch_decode<D, HG, 1, true, true>(a, num_sms, stream, per_sm_out);

@@ -47,7 +47,7 @@ struct PreTc {
     static constexpr int kStage = DP * kPanel;           // K (or V) of one block
     // stages of the K ring and of the V ring: as many as fit (P lives in TMEM), V's ring the
     // deeper one when the count is odd (a V slot is held from its load until PV, K's only until QK)
-    static constexpr int kFitS = (232448 - kQ - 2560) / kStage;  // 2.5 KB: barriers, scratch
+    static constexpr int kFitS = (232448 - kQ - 3072) / kStage;  // 3 KB: barriers, scratch, row factors
     static constexpr int kTotS = kFitS > 8 ? 8 : kFitS;
     static constexpr int NSK = kTotS / 2;
     static constexpr int NSV = kTotS - NSK;
@@ -57,7 +57,8 @@ struct PreTc {
     static constexpr int kNumBars = 2 * (NSK + NSV) + 4 * 2 + 3;  // rings, S/P barriers (kSB = 2), q, o, fin
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
-    static constexpr int kOffItem = kOffRed + 2 * 2 * 128 * 4;            // WorkItem (16-byte aligned) + abort flag
+    static constexpr int kOffQmul = kOffRed + 2 * 2 * 128 * 4;           // [128] float: Q row factors (f16 path)
+    static constexpr int kOffItem = kOffQmul + 128 * 4;                  // WorkItem (16-byte aligned) + abort flag
     static constexpr int kSmem = kOffItem + 48;
     static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
     static_assert(NSK >= 2 && NSV >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
@@ -122,10 +123,24 @@ __device__ __forceinline__ uint4 kv_convert(typename KvRaw<FP8>::type raw, float
     }
 }
 
+// Raw chunk of 8 one-byte elements -> 8 f16, exact and unscaled (the f16 path).
+template <bool I8>
+__device__ __forceinline__ uint4 kv_convert_f16(uint2 raw) {
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
+    if constexpr (I8)
+        return make_uint4(s8x2_to_f16x2(h[0]), s8x2_to_f16x2(h[1]), s8x2_to_f16x2(h[2]), s8x2_to_f16x2(h[3]));
+    else
+        return make_uint4(e4m3x2_to_f16x2(h[0]), e4m3x2_to_f16x2(h[1]), e4m3x2_to_f16x2(h[2]), e4m3x2_to_f16x2(h[3]));
+}
+
 template <bool TMA>
 constexpr int prefill_warps() { return 8 + 4 + 2; }  // softmax, producers (2 for K, 2 for V), QK and PV issuers
 
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false>
+// F16 (one-byte caches whose k_scale and v_scale are powers of two): K and V go to the tensor
+// cores as exact f16 values (one convert per pair), each Q row is brought into f16 range by a
+// power of two found from its largest element (its bf16 values stay exact), P is f16, and the
+// row factor with k_scale goes onto the scores, v_scale onto O.
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false>
 __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                           int box_rows, int q_tma, int tail) {
@@ -169,6 +184,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     constexpr int kProdW0 = 8, kProdW1 = 12, kMmaW = kProdW1, kPvW = kProdW1 + 1;
     // (no static shared variables: with the 1024-byte aligned dynamic block they would
     // round up to 1 KB and push the kernel past the 227 KB limit)
+    static_assert(!F16 || (FP8 && !TMA), "the f16 path takes one-byte caches through registers");
+    float* qmul = reinterpret_cast<float*>(smem + T::kOffQmul);
     WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + T::kOffItem);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 32);
 
@@ -262,9 +279,39 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     const bool rv = R < n_rows;
                     const uint8_t* src = reinterpret_cast<const uint8_t*>(
                         a.q + ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D);
+                    float qs = 1.f;
+                    if (F16) {
+                        // the row's largest |q| < 2^ex; 2^-k brings it into [2^14, 2^15) (f16 range)
+                        float mabs = 0.f;
+#pragma unroll 8
+                        for (int c = 0; c < D / 8; ++c) {
+                            const uint4 v = rv ? __ldg(reinterpret_cast<const uint4*>(src + c * 16)) : make_uint4(0, 0, 0, 0);
+                            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(h2[e]);
+                                mabs = fmax3(mabs, fabsf(f.x), fabsf(f.y));
+                            }
+                        }
+                        int ex = 0;
+                        frexpf(mabs, &ex);
+                        const int k = max(-30, min(100, ex - 15));
+                        qs = ldexpf(1.f, -k);
+                        qmul[r] = ldexpf(1.f, k);
+                    }
 #pragma unroll 8
                     for (int c = 0; c < D / 8; ++c) {
-                        const uint4 v = rv ? __ldg(reinterpret_cast<const uint4*>(src + c * 16)) : make_uint4(0, 0, 0, 0);
+                        uint4 v = rv ? __ldg(reinterpret_cast<const uint4*>(src + c * 16)) : make_uint4(0, 0, 0, 0);
+                        if (F16) {
+                            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(h2[e]);
+                                w[e] = pack_f16(f.x * qs, f.y * qs);
+                            }
+                            v = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                         *reinterpret_cast<uint4*>(smem + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
                     }
                 }
@@ -395,8 +442,12 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
 #pragma unroll
                             for (int c = 0; c < kGroup; ++c) {
                                 const int cc = c0 + c;
-                                *reinterpret_cast<uint4*>(stage + (cc >> 3) * T::kPanel + kk * 128 + (((cc & 7) ^ (kk & 7)) << 4)) =
-                                    kv_convert<FP8, SCALE, I8>(raw[c], sc);
+                                uint4 cv;
+                                if constexpr (F16)
+                                    cv = kv_convert_f16<I8>(raw[c]);
+                                else
+                                    cv = kv_convert<FP8, SCALE, I8>(raw[c], sc);
+                                *reinterpret_cast<uint4*>(stage + (cc >> 3) * T::kPanel + kk * 128 + (((cc & 7) ^ (kk & 7)) << 4)) = cv;
                             }
                         }
                     }
@@ -407,7 +458,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         } else if (warp == kMmaW) {
             // ---------------- QK issuer ----------------
             if (lane == 0) {
-                constexpr uint32_t idesc_qk = umma_idesc_bf16(128, BK, false, false);
+                constexpr uint32_t idesc_qk = umma_idesc_16(128, BK, false, false, F16);
                 // descriptors of the operand bases; a byte offset d within shared memory adds
                 // d >> 4 to the start-address field (no carry: every address is below 256 KB)
                 const uint64_t qdesc = umma_desc_sw128(smem_u32(smem), 16, 1024);
@@ -432,7 +483,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         } else if (warp == kPvW) {
             // ---------------- PV issuer ----------------
             if (lane == 0) {
-                constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, false, true);
+                constexpr uint32_t idesc_pv = umma_idesc_16(128, D, false, true, F16);
                 const uint64_t vdesc = umma_desc_sw128(smem_u32(smem + T::kOffV), T::kPanel, 1024);
                 bool ok = true;
                 for (int j = 0; ok && j < nb; ++j) {
@@ -460,7 +511,14 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             const int qpos = rv ? kv_len - q_len + R / G : -1;
             const int wlo = a.sliding_window > 0 ? qpos - a.sliding_window + 1 : INT_MIN;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-            const float scale = a.sm_scale, cap = a.soft_cap, c_log2 = a.sm_scale * kLog2e;
+            // F16: the row's power of two (set by the producers with Q) and k_scale go onto its scores
+            float srow = 1.f;
+            bool q_ok = true;
+            if (F16) {
+                q_ok = mbar_wait(q_full, iph, err);
+                srow = a.k_scale_or_one * qmul[r];
+            }
+            const float scale = a.sm_scale * srow, cap = a.soft_cap, c_log2 = a.sm_scale * srow * kLog2e;
             const float cap_k2 = cap != 0.f ? 2.f * kLog2e / cap : 0.f;
             // without a soft cap (and with a positive scale) the row max is taken on the raw
             // scores and the scale goes into the exponent's one FFMA: 2^(s * c - m)
@@ -468,7 +526,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             const float cs = fold ? c_log2 : 1.f;
             constexpr int HB = T::kHalf;
             float m_use = -INFINITY, l_half = 0.f;
-            bool ok = true;
+            bool ok = q_ok;
             for (int j = 0; ok && j < nb; ++j) {
                 const uint32_t q = jb + j, slot = q % SB, par = (q / SB) & 1;  // S and P buffers
                 if (!mbar_wait(&s_full[slot], par, err)) {
@@ -537,7 +595,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                         a2.x = fast_exp2(a2.x);
                         a2.y = fast_exp2(a2.y);
                         sum2[e & 1] = fadd2(sum2[e & 1], a2);
-                        pk[e] = pack_bf16(a2.x, a2.y);
+                        pk[e] = F16 ? pack_f16(a2.x, a2.y) : pack_bf16(a2.x, a2.y);
                     }
                     tmem_st16_nowait(tmem + lane_off + T::kColP + slot * (BK / 2) + half * (HB / 2) + c16 * 16, pk);
                 }
@@ -580,7 +638,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             }
             if (ok && mbar_wait(o_full, iph, err)) {
                 tc_fence_after();
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                const float inv = l_run > 0.f ? (F16 ? a.v_scale_or_one : 1.f) / l_run : 0.f;
                 __nv_bfloat16* dst = a.out +
                                      ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D +
                                      half * (D / 2);
@@ -649,11 +707,11 @@ static bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t d0, uint6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false>
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false>
 static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
                               const CUtensorMap& tq, int box_rows, int q_tma, int tail) {
     using T = PreTc<D>;
-    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8>;
+    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -683,7 +741,11 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     if (tma && 128 % G == 0)
         q_tma = make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
     if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma, tail);
+    // one-byte caches with power-of-two scales: exact f16 operands, scales on S and O
+    const bool pow2 = rpa_pow2_scale(a.k_scale_or_one) && rpa_pow2_scale(a.v_scale_or_one);
+    if (a.kv_int8 && pow2) return launch_pre<D, true, false, false, true, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     if (a.kv_int8) return launch_pre<D, true, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
+    if (a.kv_byte && pow2) return launch_pre<D, true, false, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     if (a.kv_byte) return launch_pre<D, true, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     if (a.has_scale) return launch_pre<D, false, true, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     return launch_pre<D, false, false, false>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);

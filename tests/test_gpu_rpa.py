@@ -86,12 +86,13 @@ def test_fp8_without_scale_and_bf16_with_scale():
 
 @pytest.mark.parametrize("ks,vs", [(0.5, 4.0), (0.37, 1.7)])
 def test_fp8_scales_and_query_magnitudes(ks, vs):
-    # power-of-two scales take the f16 tensor-core path (exact fp8 -> f16, scales applied to
-    # S and O); other scales dequantise to bf16. Query rows far from unit size exercise the
-    # per-row power-of-two range factor of the f16 path in both directions.
+    # power-of-two scales take the f16 tensor-core paths of decode and prefill (exact fp8 ->
+    # f16, scales applied to S and O); other scales dequantise to bf16. Query rows far from
+    # unit size exercise the per-row power-of-two range factor in both directions (the 9- and
+    # 5-token sequences are prefill tiles, the others decode).
     b = workloads.make_rpa([1, 9, 1, 5], [77, 30, 200, 64], num_q_heads=8, num_kv_heads=2, head_dim=128,
                            page_size=16, seed=17, kv_dtype=torch.float8_e4m3fn, k_scale=ks, v_scale=vs)
-    for (lo, hi), f in zip([(0, 1), (1, 10), (10, 11)], [2e4, 1e-3, 64.0]):
+    for (lo, hi), f in zip([(0, 1), (1, 10), (10, 11), (11, 16)], [2e4, 1e-3, 64.0, 300.0]):
         b.q[lo:hi] = (b.q[lo:hi].float() * f).to(b.q.dtype)
     check(b, TOL_FP8 * vs)
 
