@@ -41,6 +41,13 @@ __host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) 
 // ---------------------------------------------------------------------------
 // Asynchronous copies (cp.async, 16 bytes; src_bytes == 0 writes zeros).
 // ---------------------------------------------------------------------------
+// Quotient of two non-negative 64-bit values: the 32-bit divide when both fit (a much shorter
+// sequence than the 64-bit one, which the planning thread would otherwise run at full latency).
+__device__ __forceinline__ long long div_nn(long long a, long long b) {
+    if ((((unsigned long long)a | (unsigned long long)b) >> 32) == 0) return (long long)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -17,7 +17,12 @@ struct WsHeader;
 constexpr int kMaxDecodeHeads = 4;      // most KV heads a decode CTA covers (one warp each)
 constexpr int kDecodeBK = 16;           // keys per decode pipeline stage
 constexpr int kDecodeRows = 8;          // query rows (q_len x G) per decode item (mma N)
-constexpr int kCuCache = 4096;          // cu_q_lens entries the cache-write kernels stage in shared memory
+constexpr int kCuCache = 4096;          // metadata ints the cache-write kernels stage in shared memory
+// Shared-memory ints the RPA cache write stages (cu_q_lens and kv_lens of every sequence slot),
+// or 0 when they do not fit and it reads them from global memory.
+__host__ __device__ inline int update_cache_ints(int max_num_seqs) {
+    return 2 * max_num_seqs + 1 <= kCuCache ? 2 * max_num_seqs + 1 : 0;
+}
 constexpr int kPrefillRows = 128;       // (token, q-head) rows per prefill item (one TMEM tile)
 constexpr int kMinChunk = 256;          // smallest split-KV chunk (keys)
 constexpr int kMaxDecodeCtas = 2048;    // most decode shares (static, one per CTA, and pooled)

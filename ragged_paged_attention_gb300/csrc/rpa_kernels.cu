@@ -29,7 +29,6 @@ namespace rpa {
 // finishing while the rest of the GPU idles); the pool evens out CTAs that stream faster
 // than others.
 __device__ __forceinline__ void plan_body(const RpaArgs& a) {
-    __shared__ int scan_scratch[40];
     __shared__ long long scan_ll[40];
     __shared__ long long red[32], red_g[32];
     __shared__ float red_f[32];
@@ -64,9 +63,18 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
     // (query, key) pairs
     long long work = 0, ngrp = 0;
     float pre_pairs = 0.f;
+    // this thread's first sequence's shape, kept for pass 2 (its first group of sequences)
+    bool c_ok = false;
+    int c_ql = 0, c_kl = 0;
     for (int s = tid; s < num; s += blockDim.x) {
         int ql, kl;
-        if (seq_shape(a, s, ql, kl) && ql >= 1) {
+        const bool sok = seq_shape(a, s, ql, kl);
+        if (s == tid) {
+            c_ok = sok;
+            c_ql = ql;
+            c_kl = kl;
+        }
+        if (sok && ql >= 1) {
             if (ql * G <= 16) {
                 const int klo = decode_key_begin(a, ql, kl);
                 const long long g = (long long)n_groups * cdiv(ql * G, kDecodeRows);
@@ -91,18 +99,24 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         red_f[tid >> 5] = pre_pairs;
     }
     __syncthreads();
-    if (tid == 0) {
-        long long W = 0, NG = 0;
-        float pp = 0.f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-            W += red[w];
-            NG += red_g[w];
-            pp += red_f[w];
+    // the per-warp partials summed by warp 0 with shuffles (a serial loop over them is a
+    // chain of dependent shared-memory loads)
+    if (tid < 32) {
+        const int nw = (int)(blockDim.x >> 5);
+        long long W = tid < nw ? red[tid] : 0, NG = tid < nw ? red_g[tid] : 0;
+        float pp = tid < nw ? red_f[tid] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) {
+            W += __shfl_xor_sync(0xffffffffu, W, o);
+            NG += __shfl_xor_sync(0xffffffffu, NG, o);
+            pp += __shfl_xor_sync(0xffffffffu, pp, o);
         }
-        red[0] = W;
-        s_pf = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
-        s_db = (float)(W - NG * a.item_cost_keys) * (float)a.decode_heads * 2.f * (float)a.head_dim *
-               (a.kv_byte ? 1.f : 2.f);
+        __syncwarp();
+        if (tid == 0) red[0] = W;
+        if (tid == 0) {
+            s_pf = pp * 4.f * (float)a.num_q_heads * (float)a.head_dim;
+            s_db = (float)(W - NG * a.item_cost_keys) * (float)a.decode_heads * 2.f * (float)a.head_dim *
+                   (a.kv_byte ? 1.f : 2.f);
+        }
     }
     __syncthreads();
     // SMs for the prefill kernel beside decode: the n minimising max(prefill time on n SMs,
@@ -132,16 +146,25 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         }
     }
     __syncthreads();
+    float bt = INFINITY;
+    int bn = S;
+    if (tid < 32) {  // the best of the warps' candidates, by warp 0
+        if (tid < (int)(blockDim.x >> 5)) {
+            bt = best_t[tid];
+            bn = best_n[tid];
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const float t2 = __shfl_xor_sync(0xffffffffu, bt, o);
+            const int n2 = __shfl_xor_sync(0xffffffffu, bn, o);
+            if (t2 < bt || (t2 == bt && n2 < bn)) {
+                bt = t2;
+                bn = n2;
+            }
+        }
+    }
     if (tid == 0) {
         const long long W = red[0];
         const float pre_flops = s_pf, dec_bytes = s_db;
-        float bt = INFINITY;
-        int bn = S;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
-            if (best_t[w] < bt || (best_t[w] == bt && best_n[w] < bn)) {
-                bt = best_t[w];
-                bn = best_n[w];
-            }
         // all SMs to prefill first unless the split beats the serial order by 10%
         int n_pre = S;
         if (pre_flops <= 0.f) {
@@ -157,17 +180,17 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         ctas = max(1, min(ctas, kMaxDecodeCtas / 2));
         // static shares: all but the pool's part of the line, none under kMinChunk keys
         const long long w_static = W * (100 - kPoolPercent) / 100;
-        long long q1 = w_static / ctas / kDecodeBK * kDecodeBK;
+        long long q1 = div_nn(w_static, ctas) / kDecodeBK * kDecodeBK;
         int r = ctas;
         if (q1 < kMinChunk) {
             q1 = kMinChunk;
-            r = (int)min((long long)ctas, w_static / kMinChunk);
+            r = (int)min((long long)ctas, div_nn(w_static, kMinChunk));
         }
         const long long ls = (long long)r * q1;
         // pooled shares: about kPoolPerCta per CTA, at least kMinPoolChunk keys, within the bound
         const long long rest = W - ls;
-        long long q2 = rest / ((long long)kPoolPerCta * ctas);
-        q2 = max(q2, (rest + (kMaxDecodeCtas - r) - 1) / (kMaxDecodeCtas - r));
+        long long q2 = div_nn(rest, (long long)kPoolPerCta * ctas);
+        q2 = max(q2, div_nn(rest + (kMaxDecodeCtas - r) - 1, kMaxDecodeCtas - r));
         q2 = max((long long)kMinPoolChunk, (q2 + kDecodeBK - 1) / kDecodeBK * kDecodeBK);
         // (every share longer than a group's cost holds at least one key)
         q2 = max(q2, (long long)(a.item_cost_keys + kDecodeBK));
@@ -177,13 +200,13 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         s_r = r;
         hdr->chunk_keys = (int)min(q1, (long long)0x7fffffff);
         hdr->dec_ctas = r;
-        hdr->dec_shares = r + (int)((rest + q2 - 1) / q2);
+        hdr->dec_shares = r + (int)div_nn(rest + q2 - 1, q2);
     }
     __syncthreads();
     const long long q1 = s_q1, q2 = s_q2, ls = s_ls;
     const int n_static = s_r;
     // share holding line position p, and where share c starts
-    auto share_of = [&](long long p) { return p < ls ? p / q1 : n_static + (p - ls) / q2; };
+    auto share_of = [&](long long p) { return p < ls ? div_nn(p, q1) : n_static + div_nn(p - ls, q2); };
     auto share_start = [&](long long c) { return c < n_static ? c * q1 : ls + (c - n_static) * q2; };
     // pass 2: item counts, scan, emit
     int dec_base = 0, pre_base = 0;
@@ -192,7 +215,14 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         const int s = s0 + tid;
         int ql = 0, kl = 0, nd = 0, np = 0, klo = 0, nrh = 0;
         long long wk = 0;  // this sequence's decode work (all its groups)
-        bool ok = s < num && seq_shape(a, s, ql, kl);
+        bool ok = false;
+        if (s0 == 0) {
+            ok = s < num && c_ok;
+            ql = c_ql;
+            kl = c_kl;
+        } else {
+            ok = s < num && seq_shape(a, s, ql, kl);
+        }
         if (ok && ql >= 1) {
             if (ql * G <= 16) {
                 klo = decode_key_begin(a, ql, kl);
@@ -213,9 +243,12 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
                 nd += (int)(share_of(kr0 + len - 1) - share_of(kr0) + 1);
             }
         }
-        int tot_d, tot_p;
-        const int od = block_exclusive_scan(nd, scan_scratch, &tot_d);
-        const int op = block_exclusive_scan(np, scan_scratch, &tot_p);
+        // both item counts in one scan: decode in the high word, prefill in the low (each total
+        // is far below 2^31, so the low word never carries)
+        long long tot_dp;
+        const long long odp = block_exclusive_scan(((long long)nd << 32) | (long long)np, scan_ll, &tot_dp);
+        const int od = (int)(odp >> 32), op = (int)(odp & 0xffffffffll);
+        const int tot_d = (int)(tot_dp >> 32), tot_p = (int)(tot_dp & 0xffffffffll);
         // every thread then emits items: a thread per item, not per sequence (a long prefill
         // sequence has hundreds); item idx belongs to the first sequence whose end offset
         // (exclusive prefix + count) exceeds it
@@ -314,7 +347,8 @@ __global__ void __launch_bounds__(1024) rpa_plan_kernel(RpaArgs a) { plan_body(a
 // Cache write: new K/V rows -> their page slots (16-byte copies, bit exact)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, int nblocks) {
-    extern __shared__ int s_cu[];  // cu_q_lens[0..num] when it fits (kCuCache entries)
+    // cu_q_lens[0..max_num_seqs] then kv_lens[0..max_num_seqs), when they fit (update_cache_ints)
+    extern __shared__ int s_cu[];
     __shared__ int s_num;
     // an rpa_forward plan kernel behind may start now: it reads only metadata this kernel does
     // not write, and it ends after this grid has
@@ -337,32 +371,39 @@ __device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, i
             }
         }
     };
-    // the first token's rows are in flight while the metadata arrives
-    const int t_first = block * warps + (threadIdx.x >> 5);
-    uint4 v[kBatch];
-    if (t_first < a.max_num_tokens) load_batch(t_first, lane, v);
+    // the metadata in one round trip, issued first: the sequence count and, for every sequence
+    // slot the arrays have (cu_q_lens holds max_num_seqs + 1 entries, kv_lens max_num_seqs),
+    // the query offsets and KV lengths, read before the count is known
+    const bool cached = update_cache_ints(a.max_num_seqs) > 0;
+    const int ms = a.max_num_seqs;
     if (threadIdx.x == 0) {
         int n = a.num_seqs[0];
-        if (n < 0 || n > a.max_num_seqs) {
+        if (n < 0 || n > ms) {
             set_error(a.err, RPA_DEV_ERR_NUM_SEQS);
             n = 0;
         }
         s_num = n;
     }
+    if (cached) {
+        for (int i = threadIdx.x; i <= ms; i += blockDim.x) s_cu[i] = a.cu_q_lens[i];
+        for (int i = threadIdx.x; i < ms; i += blockDim.x) s_cu[ms + 1 + i] = a.kv_lens[i];
+    }
+    // tokens interleaved over the blocks (warp w of block b starts at token w * nblocks + b),
+    // so a small batch still spreads over every block; the first token's rows are in flight
+    // while the metadata arrives
+    const int t_first = (threadIdx.x >> 5) * nblocks + block;
+    uint4 v[kBatch];
+    if (t_first < a.max_num_tokens) load_batch(t_first, lane, v);
     __syncthreads();
     const int num = s_num;
     if (num == 0) return;
-    // one global round trip for the metadata the per-token search reads
-    const bool cached = num + 1 <= kCuCache;
-    if (cached)
-        for (int i = threadIdx.x; i <= num; i += blockDim.x) s_cu[i] = a.cu_q_lens[i];
-    __syncthreads();
     const int32_t* cu = cached ? s_cu : a.cu_q_lens;
+    const int32_t* kvl = cached ? s_cu + ms + 1 : a.kv_lens;
     const int total = cu[num];
     for (int t = t_first; t < min(total, a.max_num_tokens); t += nblocks * warps) {
         if (t != t_first) load_batch(t, lane, v);
         const int s = seq_of_token(cu, num, t);
-        const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = a.kv_lens[s];
+        const int q_start = cu[s], q_len = cu[s + 1] - q_start, kv_len = kvl[s];
         if (t < q_start || t >= q_start + q_len) continue;
         if (q_len > kv_len) {
             if (lane == 0) set_error(a.err, RPA_DEV_ERR_Q_LEN);
@@ -452,9 +493,10 @@ cudaError_t launch_rpa_forward(const RpaArgs& a, int num_sms, cudaStream_t strea
 }
 
 cudaError_t launch_rpa_forward_update(const RpaArgs& a, const RpaUpdateArgs& u, int num_sms, cudaStream_t stream) {
-    // one warp per new token in 1024-thread blocks, behind the plan's block
-    const int ublocks = max(1, min(cdiv(u.max_num_tokens, 32), num_sms * 2));
-    const int smem = min(u.max_num_seqs + 1, kCuCache) * (int)sizeof(int);
+    // one warp per new token in 1024-thread blocks beside the plan's block, over as many SMs as
+    // the batch fills (the tokens are interleaved over the blocks)
+    const int ublocks = max(1, min(u.max_num_tokens, max(num_sms - 1, min(cdiv(u.max_num_tokens, 32), num_sms * 2))));
+    const int smem = update_cache_ints(u.max_num_seqs) * (int)sizeof(int);
     {
         ProfScope ps("rpa_plan_update", stream);
         rpa_plan_update_kernel<<<1 + ublocks, 1024, smem, stream>>>(a, u);
@@ -467,7 +509,7 @@ cudaError_t launch_rpa_forward_update(const RpaArgs& a, const RpaUpdateArgs& u, 
 cudaError_t launch_rpa_update(const RpaUpdateArgs& a, int num_sms, cudaStream_t stream) {
     const int grid = min(cdiv(a.max_num_tokens, 8), num_sms * 8);
     if (grid <= 0) return cudaSuccess;
-    const int smem = min(a.max_num_seqs + 1, kCuCache) * (int)sizeof(int);
+    const int smem = update_cache_ints(a.max_num_seqs) * (int)sizeof(int);
     ProfScope ps("rpa_update", stream);
     rpa_update_kernel<<<grid, 256, smem, stream>>>(a);
     return cudaGetLastError();
