@@ -300,7 +300,9 @@ static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages,
     a.decode_heads = decode_heads_for(p->head_dim, p->kv_dtype != RPA_DTYPE_BF16);
     a.num_sms = sms;
     a.overlap = prof_enabled() ? 0 : 1;
-    rpa_rates(p->head_dim, a.kv_byte != 0, a.has_scale != 0, &a.pre_flops_per_ns_sm, &a.dec_bytes_per_ns_sm);
+    rpa_rates(p->head_dim, a.kv_byte != 0, a.has_scale != 0,
+              rpa_pow2_scale(a.k_scale_or_one) && rpa_pow2_scale(a.v_scale_or_one), &a.pre_flops_per_ns_sm,
+              &a.dec_bytes_per_ns_sm);
     a.item_cost_keys = rpa_item_cost_keys(a.kv_byte || a.has_scale);
     a.decode_per_sm = rpa_decode_ctas_per_sm(a);
     if (a.decode_per_sm <= 0) return fail(RPA_ERR_CUDA, "decode kernel occupancy query failed");

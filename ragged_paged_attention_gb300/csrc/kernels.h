@@ -53,10 +53,11 @@ constexpr int kPrefillStopPercent = 90;
 // decode bytes per ns per SM while the SMs (not HBM) limit it. Measured on GB300 for head_dim
 // 128 bf16 (Llama-3 batch) and 256 fp8 (Gemma-2 batch); the other entries are scaled from
 // those. Only the SM split depends on them, never a result.
-inline void rpa_rates(int head_dim, bool fp8, bool scale, float* pre, float* dec) {
+inline void rpa_rates(int head_dim, bool fp8, bool scale, bool pow2, float* pre, float* dec) {
     const bool conv = fp8 || scale;
     *pre = conv ? (head_dim >= 256 ? 1800.f : 2200.f) : (head_dim >= 256 ? 3000.f : head_dim >= 128 ? 3800.f : 2400.f);
-    *dec = conv ? 26.f : 60.f;
+    // (one-byte caches with power-of-two scales decode through the f16 fragment path)
+    *dec = conv ? (fp8 && pow2 ? 38.f : 26.f) : 60.f;
 }
 
 // A scale the f16 paths may take: a power of two with e4m3 * scale inside bf16's normal range

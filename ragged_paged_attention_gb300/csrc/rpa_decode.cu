@@ -27,14 +27,15 @@
 
 namespace rpa {
 
-template <int D, int HG, int ESZ, bool CONV>
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
 struct DecTile {
     static constexpr int BK = kDecodeBK;                 // keys per stage
     static constexpr int kSeg = HG * 2 * D * ESZ;        // bytes of one token's segment
     static constexpr int kRow = kSeg + 16;               // padded shared-memory row
     static constexpr int kStage = BK * kRow;
     static constexpr int kConvRow = D * 2 + 16;          // one head's K (then V) in bf16, padded
-    static constexpr int kConv = CONV ? HG * BK * kConvRow : 0;
+    // (the f16 path converts straight into MMA fragments: no conversion rows)
+    static constexpr int kConv = CONV && !F16 ? HG * BK * kConvRow : 0;
     // shared memory per CTA: two stages and (fp8) the conversion rows fit four fp8 or three
     // bf16 CTAs on an SM (with ~150 / ~95 registers a thread); measured on the Gemma-2 and
     // Llama decode batches, occupancy beats deeper rings here
@@ -86,14 +87,45 @@ __device__ __forceinline__ uint4 byte8_to_f16(const uint8_t* src) {
     return make_uint4(e4m3x2_to_f16x2(h[0]), e4m3x2_to_f16x2(h[1]), e4m3x2_to_f16x2(h[2]), e4m3x2_to_f16x2(h[3]));
 }
 
+// Two one-byte elements (the low 16 bits of v) -> an f16 pair, exactly.
+template <bool I8>
+__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t v) {
+    return I8 ? s8x2_to_f16x2((uint16_t)(v & 0xFFFFu)) : e4m3x2_to_f16x2((uint16_t)(v & 0xFFFFu));
+}
+
+// f16 path, fragment layouts.  A dot product is the same under any order of its terms, so K and
+// Q use one permutation of the head dims chosen for the loads: lane (g8, q4) of the S^T = K Q^T
+// MMA reads, per K row, the 16-byte chunks kchunk(q4, i) (spread so a quarter-warp hits eight
+// distinct bank groups), and k-step ks takes bytes 4 (ks & 3).. of chunk kchunk(q4, ks >> 2).
+template <int D>
+__device__ __forceinline__ int kchunk(int q4, int i) {
+    if constexpr (D >= 256)
+        return 2 * q4 + 8 * (i & 1) + (i >> 1);
+    else if constexpr (D == 128)
+        return 2 * q4 + i;
+    else
+        return q4;
+}
+// O^T = V^T P^T permutes the output dims instead (undone by the stores): lane g8 of tile t holds
+// dims vdim(g8, 2t) and vdim(g8, 2t + 1), the bytes 2t, 2t + 1 of its D/8 bytes of each V row
+// (16-byte chunks g8 + 8i, or 8 bytes at 8 g8 when D = 64).
+template <int D>
+__device__ __forceinline__ int vdim(int g8, int j) {
+    if constexpr (D >= 128)
+        return 16 * (g8 + 8 * (j >> 4)) + (j & 15);
+    else
+        return 8 * g8 + j;
+}
+
 // F16 (fp8 or int8 caches whose k_scale and v_scale are powers of two): bf16(float(x) * scale)
 // is then exactly x * scale, so K and V go to the tensor cores as exact f16 values and the
 // scales are applied to S and O instead; each query row is brought into f16 range by a power
-// of two (undone on its scores), which keeps its bf16 values exact. I8: the one-byte elements
-// are int8.
+// of two (undone on its scores), which keeps its bf16 values exact.  The one-byte K and V rows
+// are converted straight into MMA fragments (permuted head dims, see kchunk / vdim): no
+// conversion rows in shared memory, no ldmatrix.  I8: the one-byte elements are int8.
 template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false>
-__global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decode_kernel(RpaArgs a) {
-    using T = DecTile<D, HG, ESZ, CONV>;
+__global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_decode_kernel(RpaArgs a) {
+    using T = DecTile<D, HG, ESZ, CONV, F16>;
     static_assert(!F16 || (CONV && ESZ == 1), "the f16 path takes one-byte caches");
     static_assert(!I8 || (CONV && ESZ == 1), "int8 caches take the converting path");
     constexpr int BK = T::BK, STAGES = T::STAGES;
@@ -236,8 +268,11 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     a.q + ((size_t)(q_start + (rvb ? Rb / G : 0)) * a.num_q_heads + head * G + (rvb ? Rb % G : 0)) * D);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    qb[ks][0] = rvb ? __ldg(qrow + ks * 8 + q4) : 0u;
-                    qb[ks][1] = rvb ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;
+                    // (f16 path: the dims of K's permuted A fragments, kchunk)
+                    const int w0 = F16 ? 8 * kchunk<D>(q4, ks >> 2) + 2 * (ks & 3) : ks * 8 + q4;
+                    const int w1 = F16 ? w0 + 1 : ks * 8 + 4 + q4;
+                    qb[ks][0] = rvb ? __ldg(qrow + w0) : 0u;
+                    qb[ks][1] = rvb ? __ldg(qrow + w1) : 0u;
                 }
             }
             // F16: the row's power-of-two range factor (its 4 lanes hold its D values), the
@@ -300,10 +335,13 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     }
                     __syncwarp();
                 };
-                if (CONV) {
+                if (CONV && !F16) {
                     if (head_ok) convert(0);
                     kbase = vbase = smem_u32(cb);
                     rowb = T::kConvRow;
+                } else if (F16) {
+                    kbase = vbase = 0u;  // (fragments come straight from the stage rows)
+                    rowb = T::kRow;
                 } else {
                     kbase = smem_u32(stg) + warp * 2 * D * 2;
                     vbase = kbase + D * 2;
@@ -313,19 +351,36 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     const int key0 = kb + blk * BK;
                     // S^T [16 keys x 8 rows] = K Q^T; A = K rows (ldmatrix: keys 0-7 / 8-15, dims 0-7 / 8-15)
                     float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                    {
+                    if constexpr (F16) {
+                        // K rows g8 and g8 + 8 of this warp's head, converted into A fragments
+                        const uint8_t* kr0 = stg + g8 * T::kRow + warp * 2 * D;
+                        const uint8_t* kr1 = kr0 + 8 * T::kRow;
+#pragma unroll
+                        for (int i = 0; i < D / 64; ++i) {
+                            const int c = kchunk<D>(q4, i);
+                            const uint4 u0 = *reinterpret_cast<const uint4*>(kr0 + c * 16);
+                            const uint4 u1 = *reinterpret_cast<const uint4*>(kr1 + c * 16);
+                            const uint32_t x0[4] = {u0.x, u0.y, u0.z, u0.w}, x1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                uint32_t ka4[4];
+                                ka4[0] = byte2_to_f16x2<I8>(x0[e]);        // key g8, dims d, d + 1
+                                ka4[1] = byte2_to_f16x2<I8>(x1[e]);        // key g8 + 8
+                                ka4[2] = byte2_to_f16x2<I8>(x0[e] >> 16);  // key g8, dims d + 2, d + 3
+                                ka4[3] = byte2_to_f16x2<I8>(x1[e] >> 16);
+                                mma_f16(sc, ka4, qb[4 * i + e][0], qb[4 * i + e][1]);
+                            }
+                        }
+                    } else {
                         const uint32_t ka = kbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * rowb + (lane >> 4) * 16;
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
                             uint32_t ka4[4];
                             ldsm_x4(ka + ks * 32, ka4[0], ka4[1], ka4[2], ka4[3]);
-                            if (F16)
-                                mma_f16(sc, ka4, qb[ks][0], qb[ks][1]);
-                            else
-                                mma_bf16(sc, ka4, qb[ks][0], qb[ks][1]);
+                            mma_bf16(sc, ka4, qb[ks][0], qb[ks][1]);
                         }
                     }
-                    if (CONV) {
+                    if (CONV && !F16) {
                         __syncwarp();  // every lane is done reading K out of cb
                         convert(1);
                     }
@@ -364,20 +419,73 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                     // P^T as B fragments (k = keys 2*q4.., n = row g8): transpose the 8x8 blocks
                     const uint32_t pb0 = movmatrix_t(F16 ? pack_f16(sc[0], sc[1]) : pack_bf16(sc[0], sc[1]));
                     const uint32_t pb1 = movmatrix_t(F16 ? pack_f16(sc[2], sc[3]) : pack_bf16(sc[2], sc[3]));
-                    // O^T [16 dims x 8 rows] += V^T P^T; A = V^T by a transposing ldmatrix of V rows
-                    const uint32_t va = vbase + ((lane & 7) + ((lane >> 4) << 3)) * rowb + ((lane >> 3) & 1) * 16;
+                    // O^T [16 dims x 8 rows] += V^T P^T
+                    if constexpr (F16) {
+                        // A = V^T from keys 2 q4, 2 q4 + 1, 2 q4 + 8, 2 q4 + 9: a byte permute pairs
+                        // two keys' elements of one dim, one convert makes the f16 pair
+                        const uint8_t* vr = stg + warp * 2 * D + D;
+                        const uint8_t* v0 = vr + (2 * q4) * T::kRow;
+                        const uint8_t* v1 = v0 + T::kRow;
+                        const uint8_t* v2 = v0 + 8 * T::kRow;
+                        const uint8_t* v3 = v2 + T::kRow;
+                        constexpr int kVW = D / 32;  // 32-bit words of this lane's D/8 bytes per row
+                        uint32_t w0[kVW], w1[kVW], w2[kVW], w3[kVW];
+                        if constexpr (D >= 128) {
 #pragma unroll
-                    for (int dm = 0; dm < D / 16; ++dm) {
-                        o[dm][0] *= alpha[0];
-                        o[dm][1] *= alpha[1];
-                        o[dm][2] *= alpha[0];
-                        o[dm][3] *= alpha[1];
-                        uint32_t va4[4];
-                        ldsm_x4_t(va + dm * 32, va4[0], va4[1], va4[2], va4[3]);
-                        if (F16)
-                            mma_f16(o[dm], va4, pb0, pb1);
-                        else
+                            for (int i = 0; i < D / 128; ++i) {
+                                const int off = 16 * (g8 + 8 * i);
+                                const uint4 r0 = *reinterpret_cast<const uint4*>(v0 + off);
+                                const uint4 r1 = *reinterpret_cast<const uint4*>(v1 + off);
+                                const uint4 r2 = *reinterpret_cast<const uint4*>(v2 + off);
+                                const uint4 r3 = *reinterpret_cast<const uint4*>(v3 + off);
+                                w0[4 * i] = r0.x; w0[4 * i + 1] = r0.y; w0[4 * i + 2] = r0.z; w0[4 * i + 3] = r0.w;
+                                w1[4 * i] = r1.x; w1[4 * i + 1] = r1.y; w1[4 * i + 2] = r1.z; w1[4 * i + 3] = r1.w;
+                                w2[4 * i] = r2.x; w2[4 * i + 1] = r2.y; w2[4 * i + 2] = r2.z; w2[4 * i + 3] = r2.w;
+                                w3[4 * i] = r3.x; w3[4 * i + 1] = r3.y; w3[4 * i + 2] = r3.z; w3[4 * i + 3] = r3.w;
+                            }
+                        } else {
+                            const int off = 8 * g8;
+                            const uint2 r0 = *reinterpret_cast<const uint2*>(v0 + off);
+                            const uint2 r1 = *reinterpret_cast<const uint2*>(v1 + off);
+                            const uint2 r2 = *reinterpret_cast<const uint2*>(v2 + off);
+                            const uint2 r3 = *reinterpret_cast<const uint2*>(v3 + off);
+                            w0[0] = r0.x; w0[1] = r0.y; w1[0] = r1.x; w1[1] = r1.y;
+                            w2[0] = r2.x; w2[1] = r2.y; w3[0] = r3.x; w3[1] = r3.y;
+                        }
+#pragma unroll
+                        for (int wd = 0; wd < kVW; ++wd) {
+                            // bytes 4 wd .. 4 wd + 3: tiles 2 wd (bytes 0, 1) and 2 wd + 1 (bytes 2, 3)
+                            const uint32_t lo01 = __byte_perm(w0[wd], w1[wd], 0x5140), hi01 = __byte_perm(w0[wd], w1[wd], 0x7362);
+                            const uint32_t lo23 = __byte_perm(w2[wd], w3[wd], 0x5140), hi23 = __byte_perm(w2[wd], w3[wd], 0x7362);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int dm = 2 * wd + h;
+                                const uint32_t p01 = h ? hi01 : lo01, p23 = h ? hi23 : lo23;
+                                o[dm][0] *= alpha[0];
+                                o[dm][1] *= alpha[1];
+                                o[dm][2] *= alpha[0];
+                                o[dm][3] *= alpha[1];
+                                uint32_t va4[4];
+                                va4[0] = byte2_to_f16x2<I8>(p01);        // dim vdim(g8, 2 dm), keys 2 q4, 2 q4 + 1
+                                va4[1] = byte2_to_f16x2<I8>(p01 >> 16);  // dim vdim(g8, 2 dm + 1)
+                                va4[2] = byte2_to_f16x2<I8>(p23);        // keys 2 q4 + 8, 2 q4 + 9
+                                va4[3] = byte2_to_f16x2<I8>(p23 >> 16);
+                                mma_f16(o[dm], va4, pb0, pb1);
+                            }
+                        }
+                    } else {
+                        // A = V^T by a transposing ldmatrix of V rows
+                        const uint32_t va = vbase + ((lane & 7) + ((lane >> 4) << 3)) * rowb + ((lane >> 3) & 1) * 16;
+#pragma unroll
+                        for (int dm = 0; dm < D / 16; ++dm) {
+                            o[dm][0] *= alpha[0];
+                            o[dm][1] *= alpha[1];
+                            o[dm][2] *= alpha[0];
+                            o[dm][3] *= alpha[1];
+                            uint32_t va4[4];
+                            ldsm_x4_t(va + dm * 32, va4[0], va4[1], va4[2], va4[3]);
                             mma_bf16(o[dm], va4, pb0, pb1);
+                        }
                     }
                 }
                 __syncwarp();
@@ -392,7 +500,22 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
             }
             // (warp-uniform: the movmatrix below is warp-collective)
             if (!__any_sync(0xffffffffu, s_abort != 0) && head_ok) {
-                if (w.num_splits == 1) {
+                if (F16 && w.num_splits == 1) {
+                    // the thread's two columns are query rows 2 q4 + j; each tile's pair of C rows
+                    // is two adjacent head dims (vdim): one 32-bit store per row and tile
+                    const float vs = a.v_scale_or_one;  // (V went in unscaled)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if (!rv[j]) continue;
+                        const int R = rb + 2 * q4 + j;
+                        const float inv = l_run[j] > 0.f ? vs / l_run[j] : 0.f;
+                        __nv_bfloat16* dst = a.out + ((size_t)(q_start + R / G) * a.num_q_heads + head * G + R % G) * D;
+#pragma unroll
+                        for (int dm = 0; dm < D / 16; ++dm)
+                            *reinterpret_cast<uint32_t*>(dst + vdim<D>(g8, 2 * dm)) =
+                                pack_bf16(o[dm][j] * inv, o[dm][2 + j] * inv);
+                    }
+                } else if (w.num_splits == 1) {
                     // normalise per column, transpose each 8x8 block back to rows: thread then
                     // holds row rb + g8, dims 2*q4, 2*q4+1 of the block (32-bit stores)
                     const float vs = F16 ? a.v_scale_or_one : 1.f;  // (F16: V went in unscaled)
@@ -420,8 +543,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
                         const float vs = F16 ? a.v_scale_or_one : 1.f;
 #pragma unroll
                         for (int dm = 0; dm < D / 16; ++dm) {
-                            po[(size_t)r * D + dm * 16 + g8] = o[dm][j] * vs;
-                            po[(size_t)r * D + dm * 16 + 8 + g8] = o[dm][2 + j] * vs;
+                            const int d0 = F16 ? vdim<D>(g8, 2 * dm) : dm * 16 + g8;
+                            const int d1 = F16 ? d0 + 1 : dm * 16 + 8 + g8;
+                            po[(size_t)r * D + d0] = o[dm][j] * vs;
+                            po[(size_t)r * D + d1] = o[dm][2 + j] * vs;
                         }
                         if (g8 == 0) {
                             pml[r * 2] = m_run[j];
@@ -487,7 +612,7 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV>::kThreads) rpa_decod
 // per_sm_out != nullptr: only report the kernel's resident CTAs per SM (no launch)
 template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false>
 static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
-    using T = DecTile<D, HG, ESZ, CONV>;
+    using T = DecTile<D, HG, ESZ, CONV, F16>;
     auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16, I8>;
     static int per_sm = 0;
     if (per_sm == 0) {
