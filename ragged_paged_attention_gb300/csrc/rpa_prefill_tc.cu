@@ -54,12 +54,13 @@ struct PreTc {
     static constexpr int kOffK = kQ;
     static constexpr int kOffV = kOffK + NSK * kStage;
     static constexpr int kOffBar = kOffV + NSV * kStage;
-    static constexpr int kNumBars = 2 * (NSK + NSV) + 4 * 2 + 3;  // rings, S/P barriers (kSB = 2), q, o, fin
+    // rings, S/P barriers (kSB = 2), q_full, o_full, fin, q_empty, o_empty, item ring full/empty [2] each
+    static constexpr int kNumBars = 2 * (NSK + NSV) + 4 * 2 + 3 + 2 + 4;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
     static constexpr int kOffQmul = kOffRed + 2 * 2 * 128 * 4;           // [128] float: Q row factors (f16 path)
-    static constexpr int kOffItem = kOffQmul + 128 * 4;                  // WorkItem (16-byte aligned) + abort flag
-    static constexpr int kSmem = kOffItem + 48;
+    static constexpr int kOffItem = kOffQmul + 128 * 4;                  // [2] WorkItem ring (16-byte aligned) + abort flag
+    static constexpr int kSmem = kOffItem + 2 * 32 + 16;
     static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
     static_assert(NSK >= 2 && NSV >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
     // TMEM: kSB score buffers of BK columns, kSB P buffers of BK/2 columns (bf16 pairs), O.
@@ -175,6 +176,10 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint64_t* q_full = bars_s + 4 * SB;
     uint64_t* o_full = q_full + 1;
     uint64_t* fin = q_full + 2;
+    uint64_t* q_empty = q_full + 3;     // the item's QKs are done and the softmax warps have started it
+    uint64_t* o_empty = q_full + 4;     // the epilogue has read O out of TMEM
+    uint64_t* item_full = q_full + 5;   // [2] ring slot written
+    uint64_t* item_empty = q_full + 7;  // [2] ring slot read by every warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + T::kOffRed);
     // producer warps [8, 12): warps 8-9 stream K, 10-11 V; then the MMA warp
@@ -186,8 +191,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     // round up to 1 KB and push the kernel past the 227 KB limit)
     static_assert(!F16 || (FP8 && !TMA), "the f16 path takes one-byte caches through registers");
     float* qmul = reinterpret_cast<float*>(smem + T::kOffQmul);
-    WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + T::kOffItem);
-    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 32);
+    WorkItem* s_items = reinterpret_cast<WorkItem*>(smem + T::kOffItem);
+    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 64);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WsHeader* hdr = a.hdr;
@@ -214,9 +219,16 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             mbar_init(&p_full[i], T::kSoftWarps * 32);
             mbar_init(&p_empty[i], 1);
         }
-        mbar_init(q_full, (kProdW1 - kProdW0) * 32);  // every producer thread arrives
+        // Q by TMA: the issuing thread alone; through registers: every producer thread
+        mbar_init(q_full, (TMA && q_tma) ? 1 : (kProdW1 - kProdW0) * 32);
         mbar_init(o_full, 1);
-        mbar_init(fin, 2);  // both issuing threads
+        mbar_init(fin, 2);                         // both issuing threads
+        mbar_init(q_empty, 1 + T::kSoftWarps);     // QK issuer's commit + each softmax warp
+        mbar_init(o_empty, T::kSoftWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], prefill_warps<TMA>());
+        }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -226,23 +238,38 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Items reach the warps through a two-slot ring. The first producer thread (its role runs
+    // furthest ahead) takes item n when it gets to it; every warp reads the slot and frees it.
+    // Each role then runs its own item loop: the producers and the QK issuer start item n + 1
+    // while the softmax warps finish item n (its last blocks and its epilogue). The Q buffer
+    // is refilled once item n's QKs are done and the softmax warps have started it (q_empty),
+    // and PV overwrites O once the epilogue has read it (o_empty); the K/V, S and P rings are
+    // indexed by the CTA's running block count and need nothing at item boundaries.
     uint32_t jb = 0;     // key blocks this CTA has processed (ring positions)
-    uint32_t items = 0;  // items this CTA has processed (q_full / o_full phases)
+    uint32_t items = 0;  // items this CTA has processed (ring slots, q / o phases)
     while (true) {
-        if (tid == 0) {
-            s_item.seq = -1;
+        const uint32_t islot = items & 1, iring = (items >> 1) & 1;
+        if (tid == kProdW0 * 32) {
+            WorkItem nw;
+            nw.seq = -1;
+            if (!mbar_wait(&item_empty[islot], iring ^ 1, err)) s_abort = 1;
             // beside decode, take no new item once most decode CTAs with a share are out of
             // work (decode is ending): what is left goes to the launch after decode, on every SM
-            const bool stop = !tail && a.overlap && hdr->dec_ctas > 0 &&
-                              *(volatile const int*)&hdr->next_item[0] >=
-                                  max(1, hdr->dec_ctas * kPrefillStopPercent / 100);
+            const bool stop = s_abort || (!tail && a.overlap && hdr->dec_ctas > 0 &&
+                                          *(volatile const int*)&hdr->next_item[0] >=
+                                              max(1, hdr->dec_ctas * kPrefillStopPercent / 100));
             if (!stop) {
                 const int it = atomicAdd(&hdr->next_item[1], 1);
-                if (it < hdr->num_items[1]) s_item = a.pre_items[it];
+                if (it < hdr->num_items[1]) nw = a.pre_items[it];
             }
+            s_items[islot] = nw;
+            mbar_arrive(&item_full[islot]);
         }
-        __syncthreads();
-        const WorkItem w = s_item;
+        WorkItem w;
+        w.seq = -1;
+        if (mbar_wait(&item_full[islot], iring, err)) w = s_items[islot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (w.seq < 0 || s_abort) break;
         const int s = w.seq;
         const int q_start = a.cu_q_lens[s];
@@ -264,15 +291,21 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             const int pt = tid - kProdW0 * 32;
             if (TMA && q_tma) {
                 // the 128 rows are 128/G consecutive tokens x the G heads of this KV head
-                if (pt == 0) {
-                    mbar_arrive_expect_tx(q_full, D * 256);
+                // issued from a V-streaming thread: its loads have the most slack, while the K
+                // streamers (and the item fetch) run on into this item ahead of its Q
+                if (pt == 64) {
+                    if (mbar_wait(q_empty, iph ^ 1, err)) {  // the previous item's QKs read Q
+                        mbar_arrive_expect_tx(q_full, D * 256);
 #pragma unroll
-                    for (int p = 0; p < T::DP; ++p)
-                        tma_load_3d(smem_u32(smem + p * 16384), &tm_q, 64 * p, kvh * G, q_start + R0 / G, q_full);
-                } else {
-                    mbar_arrive(q_full);
+                        for (int p = 0; p < T::DP; ++p)
+                            tma_load_3d(smem_u32(smem + p * 16384), &tm_q, 64 * p, kvh * G, q_start + R0 / G, q_full);
+                    } else {
+                        s_abort = 1;
+                    }
                 }
             } else {
+                // the previous item's QKs have read Q and its softmax warps its row factors
+                if (!mbar_wait(q_empty, iph ^ 1, err)) s_abort = 1;
                 const int nprod = (kProdW1 - kProdW0) * 32;
                 for (int r = pt; r < 128; r += nprod) {
                     const int R = R0 + r;
@@ -478,6 +511,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     umma_commit(&s_full[sb]);
                     umma_commit(&k_empty[slot]);
                 }
+                umma_commit(q_empty);  // Q may be refilled once these QKs have completed
                 if (!ok) s_abort = 1;
             }
         } else if (warp == kPvW) {
@@ -485,7 +519,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             if (lane == 0) {
                 constexpr uint32_t idesc_pv = umma_idesc_16(128, D, false, true, F16);
                 const uint64_t vdesc = umma_desc_sw128(smem_u32(smem + T::kOffV), T::kPanel, 1024);
-                bool ok = true;
+                // the first PV overwrites O: the previous item's epilogue has read it
+                bool ok = mbar_wait(o_empty, iph ^ 1, err);
                 for (int j = 0; ok && j < nb; ++j) {
                     const uint32_t q = jb + j, pb = q % SB, pp = (q / SB) & 1, slot = q % NSV, par = (q / NSV) & 1;
                     ok = mbar_wait(&p_full[pb], pp, err) && mbar_wait(&v_full[slot], par, err);
@@ -518,6 +553,10 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 q_ok = mbar_wait(q_full, iph, err);
                 srow = a.k_scale_or_one * qmul[r];
             }
+            // this warp has started the item (and read its row factor): the producers may
+            // refill Q for the next one once the QKs are done too
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_empty);
             const float scale = a.sm_scale * srow, cap = a.soft_cap, c_log2 = a.sm_scale * srow * kLog2e;
             const float cap_k2 = cap != 0.f ? 2.f * kLog2e / cap : 0.f;
             // without a soft cap (and with a positive scale) the row max is taken on the raw
@@ -657,16 +696,23 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                             d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                     }
                 }
+                // O has been read: the next item's first PV may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty);
             } else {
                 s_abort = 1;
             }
             tc_fence_before();
         }
+        __syncwarp();  // the issuer warps' idle lanes wait here for lane 0, not at the next slot
         jb += nb;
         ++items;
-        __syncthreads();
-        tc_fence_after();
     }
+    // every role has left its loop (the softmax warps' last TMEM reads included)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     // drain: every MMA this CTA issued has completed before TMEM is released
     if (warp == kPvW && lane == 0) umma_commit(fin);
     if (warp == kMmaW) {
