@@ -112,6 +112,26 @@ def test_prefill_beside_decode_regimes(q_lens, kv_lens, hq, hkv):
     check(b, TOL_BF16, tokens=sample_tokens(b.q_lens))
 
 
+@pytest.mark.parametrize("kv_dtype,d,ps,ks", [(torch.bfloat16, 128, 16, None), (torch.float8_e4m3fn, 256, 32, 0.5),
+                                              (torch.float8_e4m3fn, 128, 16, 0.37)],
+                         ids=["bf16-tma", "fp8-f16", "fp8-dequant"])
+def test_many_short_prefill_items(kv_dtype, d, ps, ks):
+    # 1200 one-block prefill tiles: every CTA runs several items back to back, its producers
+    # and QK issuer already on the next item while the softmax warps finish the current one.
+    # Queries of alternate sequences differ in size by 2^6, so a Q tile or a per-row factor
+    # taken from the wrong item would show at once.
+    rng = np.random.default_rng(31)
+    n = 600
+    kv_lens = [int(x) for x in rng.integers(8, 61, size=n)]
+    extra = {} if ks is None else dict(k_scale=ks, v_scale=ks)
+    b = workloads.make_rpa([8] * n, kv_lens, num_q_heads=8, num_kv_heads=2, head_dim=d, page_size=ps, seed=31,
+                           kv_dtype=kv_dtype, **extra)
+    for s in range(n):
+        f = 8.0 if s % 2 else 0.125
+        b.q[8 * s:8 * s + 8] = (b.q[8 * s:8 * s + 8].float() * f).to(b.q.dtype)
+    check(b, TOL_BF16 if kv_dtype == torch.bfloat16 else TOL_FP8)
+
+
 def test_serialised_launches():
     # with per-kernel timing on, the kernels run one after another (prefill on every SM,
     # decode after it): the same results within tolerance
