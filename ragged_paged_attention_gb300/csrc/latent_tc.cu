@@ -275,16 +275,24 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 // is still busy.
                 const int kk = pt >> 1, hh = pt & 1;
                 const int nch = nqp * 4;  // chunks of this thread (20 or 16)
+                // read_block and page_size are powers of two in practice: shifts and masks then
+                // replace the divisions (two of them 64-bit) this thread runs for every block
+                const bool rb_p2 = (a.read_block & (a.read_block - 1)) == 0, ps_p2 = (a.page_size & (a.page_size - 1)) == 0;
+                const int rb_sh = __ffs(a.read_block) - 1, ps_sh = __ffs(a.page_size) - 1;
                 auto resolve = [&](int j, bool& v) -> const __nv_bfloat16* {
                     const int key = kb + j * BK + kk;
                     v = j < nb && key < ke;
                     if (!v) return nullptr;
                     if (SPARSE) {
-                        const int u = __ldg(a.indices + (size_t)w.seq * a.topk + key / a.read_block);
-                        const long long kp = (long long)u * a.read_block + key % a.read_block;
+                        const int ui = rb_p2 ? key >> rb_sh : key / a.read_block;
+                        const int ur = rb_p2 ? key & (a.read_block - 1) : key % a.read_block;
+                        const int u = __ldg(a.indices + (size_t)w.seq * a.topk + ui);
+                        const long long kp = (long long)u * a.read_block + ur;
                         v = u >= 0 && kp <= qpos && kp < kbound;
                         if (!v) return nullptr;
-                        const int lp = (int)(kp / a.page_size);
+                        // kp >= 0 here (u >= 0)
+                        const int lp = ps_p2 ? (int)(kp >> ps_sh) : (int)(kp / a.page_size);
+                        const int po = ps_p2 ? (int)(kp & (a.page_size - 1)) : (int)(kp % a.page_size);
                         int page;
                         if (a.q_base) {  // packed list: the request's run, clamped to the list's end
                             const long long pidx = min((long long)kbase + lp, (long long)a.max_pages - 1);
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                             v = false;
                             return nullptr;
                         }
-                        return a.cache + ((size_t)page * a.page_size + kp % a.page_size) * a.row_stride;
+                        return a.cache + ((size_t)page * a.page_size + po) * a.row_stride;
                     }
                     const int page = __ldg(a.page_indices + (size_t)seq * a.pages_per_seq + key / a.page_size);
                     if ((unsigned)page >= (unsigned)a.total_num_pages) {
