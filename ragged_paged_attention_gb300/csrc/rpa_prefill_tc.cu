@@ -8,9 +8,9 @@
 //     and V rows of that KV head page by page into 128-byte-swizzled K-major panels.
 //     bf16 caches go by TMA (one 3-D tensor copy per page-sized box and 64-wide panel,
 //     issued by the lanes of two warps per operand, pages looked up one block ahead; the
-//     partial last page is copied by those warps through registers); fp8 / scaled
-//     caches go through registers in warps 4-7 and are dequantised there as
-//     bf16(float(x) * scale).  Rows past the key range are never copied: the stage
+//     partial last page is copied by those warps through registers); one-byte and scaled
+//     caches go through registers in the same warps 8-11 and are converted there
+//     (bf16(float(x) * scale), or exact f16 with power-of-two scales).  Rows past the key range are never copied: the stage
 //     memory is zeroed at start, so such rows hold finite data with zero probability;
 //   * warp 12 issues tcgen05.mma S = Q K^T into one of two TMEM score buffers, warp 13
 //     O += P V into the TMEM output accumulator (V read MN-major from the same panels, P
@@ -27,7 +27,12 @@
 // of NSK / NSV stages, so a K slot frees as soon as its QK is done); per score buffer s_full
 // (QK -> softmax) and s_free (the softmax has loaded the scores: the next QK into that buffer
 // may start while the softmax is still computing); per P buffer p_full (softmax -> PV) and
-// p_empty (PV has read P); q_full, o_full.  Blocks are 128 keys (64 for D = 256).
+// p_empty (PV has read P); q_full, o_full; q_empty (the item's QKs are done and its softmax
+// warps have started it: Q may be refilled) and o_empty (the epilogue has read O: the next
+// item's first PV may overwrite it); item_full/item_empty, a two-slot ring through which the
+// first producer thread hands items to every warp, so each role runs its own item loop and
+// the producers and QK issuer start item n+1 during item n's epilogue.  Blocks are 128 keys
+// (64 for D = 256).
 // Every wait is bounded (common.cuh); on a timeout the CTA records an error and stops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
