@@ -493,6 +493,14 @@ def main():
     step_bytes = acc["decode"][1] + acc["prefill"][1]
     step_flops = acc["decode"][2] + acc["prefill"][2]
     t_roof = roof_time(step_bytes, step_flops, peaks)
+    # the step's other attention kernel against its own bound, from the same per-kernel pass
+    other_roofs = {}
+    if dom != "rpa_prefill_attn" and ktimes.get("rpa_prefill_attn") and pre_flops > 0:
+        s_pre = ktimes["rpa_prefill_attn"][1] / ktimes["rpa_prefill_attn"][0] * 1e-3
+        a_pre = pre_flops / s_pre / 1e12
+        other_roofs["rpa_prefill_attn"] = {"bound": "tensor", "achieved": a_pre, "peak": peaks["bf16_tflops"],
+                                           "unit": "TFLOP/s", "frac": a_pre / peaks["bf16_tflops"],
+                                           "algorithmic_flops_per_launch": pre_flops}
 
     # end to end: pinned host inputs -> device, update + attention, output -> host, every
     # step. Served the way a serving loop would: inputs and outputs double-buffered on the
@@ -576,6 +584,7 @@ def main():
                               "frac": t_roof / (ms * 1e-3), "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
                               "tflops": step_flops / (ms * 1e-3) / 1e12},
             "roofline": roof,
+            "kernel_rooflines": other_roofs,
             "kernels": kernels,
             "gpu_launches": int(n_launch),
             "kernel_timing": "kernels/roofline: separate pass of the same steps with each launch bracketed by "
@@ -640,9 +649,12 @@ def _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report):
     ms, _ = time_steps(fwd, steps, warm, world)
     _, kt = time_steps(fwd, steps, 1, world, timer=True)  # per-kernel pass (serialised)
     dec_us = 1e3 * kt["rpa_decode_attn"][1] / kt["rpa_decode_attn"][0]
+    extra = {"decode_hbm_frac": acc["decode"][1] / (dec_us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    if kt.get("rpa_prefill_attn"):
+        pre_us = 1e3 * kt["rpa_prefill_attn"][1] / kt["rpa_prefill_attn"][0]
+        extra["prefill_tensor_frac"] = acc["prefill"][2] / (pre_us * 1e-6) / 1e12 / peaks["bf16_tflops"]
     report("gemma2_fp8_sw_cap", b.num_tokens, acc["decode"][1] + acc["prefill"][1],
-           acc["decode"][2] + acc["prefill"][2], ms, kt,
-           {"decode_hbm_frac": acc["decode"][1] / (dec_us * 1e-6) / 1e9 / peaks["hbm_gbs"]})
+           acc["decode"][2] + acc["prefill"][2], ms, kt, extra)
     del b, g, out, ws
     torch.cuda.empty_cache()
 
