@@ -156,8 +156,10 @@ RPA_API int rpa_forward(const rpa_params* p, const void* q, const void* kv_pages
  *     GPU that loads the library holds it until the process exits.  Problems whose
  *     rpa_workspace_size() exceeds it are rejected with RPA_ERR_WORKSPACE before any
  *     launch.  The call allocates nothing itself.
- *   - The first call on each device looks up that array's device address (with the
- *     device current); make that first call before any stream capture.
+ *   - Every call looks up the array's device address in the context current on the
+ *     calling thread, so a host application's own (non-primary) context and a device
+ *     reset between calls are both handled.  The first call in a context also loads
+ *     the library's device code there; make that first call before any stream capture.
  *   - All calls share the one array and it keeps the previous call's contents; the
  *     kernels reset what they need.  Calls that overlap on the GPU (two streams, or
  *     two threads) race on it: serialise them.

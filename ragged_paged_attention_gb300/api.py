@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+import re
 import threading
 
 import torch
@@ -216,6 +217,8 @@ def rpa_forward(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_s
         raise ValueError("q and kv_pages head_dim differ")
     if out is None:
         out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must have q's shape {tuple(q.shape)}, got {tuple(out.shape)}")
     _dev(out, "out", torch.bfloat16)
     if workspace is None:
         workspace = Workspace.get(rpa_workspace_size(prm), q.device, "rpa")
@@ -225,7 +228,18 @@ def rpa_forward(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_s
     return out
 
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
+def _header_noalloc_bytes() -> int:
+    """RPA_NOALLOC_SCRATCH_BYTES as ``include/rpa.h`` defines it (the one definition of the
+    size; the binding reads it instead of restating it)."""
+    path = os.path.join(os.path.dirname(_HERE), "include", "rpa.h")
+    with open(path) as f:
+        m = re.search(r"#define\s+RPA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", f.read())
+    if m is None:
+        raise RuntimeError(f"RPA_NOALLOC_SCRATCH_BYTES not found in {path}")
+    return int(m.group(1)) << int(m.group(2))
+
+
+NOALLOC_SCRATCH_BYTES = _header_noalloc_bytes()
 
 
 def rpa_forward_noalloc(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, out, sm_scale=1.0,
@@ -238,6 +252,12 @@ def rpa_forward_noalloc(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs,
     given.  Overlapping calls race on that array; problems needing more than
     ``NOALLOC_SCRATCH_BYTES`` of scratch raise ``RpaError`` (RPA_ERR_WORKSPACE).
     """
+    # shapes first: the C call sees only pointers, so a q narrower than the cache or an
+    # out smaller than q would be read or written past its end
+    if kv_pages.shape[-1] != q.shape[-1]:
+        raise ValueError("q and kv_pages head_dim differ")
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must have q's shape {tuple(q.shape)}, got {tuple(out.shape)}")
     lib = load_library()
     _dev(q, "q", torch.bfloat16)
     _dev(kv_pages, "kv_pages")
@@ -299,6 +319,8 @@ def rpa_forward_update(q, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_le
         raise ValueError("new_k/new_v must be [max_num_tokens, num_kv_heads, head_dim]")
     if out is None:
         out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must have q's shape {tuple(q.shape)}, got {tuple(out.shape)}")
     _dev(out, "out", torch.bfloat16)
     if workspace is None:
         workspace = Workspace.get(rpa_workspace_size(prm), q.device, "rpa")

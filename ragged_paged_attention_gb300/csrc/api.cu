@@ -691,29 +691,20 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = RPA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device with that device
-// current (the host-side name of the array is only a stand-in, never a device address).
+// Device address of g_noalloc_scratch in the context current on this thread (the host-side
+// name of the array is only a stand-in, never a device address). It is looked up on every
+// call rather than cached: a host application may make its own (non-primary) context
+// current, or reset the device between calls, and either gives the array another address.
+// The lookup is a host-side table read once the library's device code is loaded in that
+// context (the first call there loads it).
 void* noalloc_scratch_ptr(int* rc) {
-    static std::mutex mu;
-    static void* ptrs[64] = {nullptr};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
-        *rc = e != cudaSuccess ? cuda_fail(e, "rpa_forward_noalloc: cudaGetDevice")
-                               : fail(RPA_ERR_CUDA, "rpa_forward_noalloc: device index %d out of range", dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+        *rc = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "rpa_forward_noalloc: cudaGetSymbolAddress");
         return nullptr;
     }
-    std::lock_guard<std::mutex> lk(mu);
-    if (!ptrs[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            *rc = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "rpa_forward_noalloc: cudaGetSymbolAddress");
-            return nullptr;
-        }
-        ptrs[dev] = p;
-    }
-    return ptrs[dev];
+    return p;
 }
 
 }  // namespace
