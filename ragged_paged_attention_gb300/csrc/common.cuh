@@ -52,6 +52,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 16 bytes from shared memory (a shared-window address from smem_u32).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     const int n = valid ? 16 : 0;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
@@ -144,6 +151,14 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
 }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mul.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     float2 d;
     asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n add.rn.f32x2 rd, ra, rb;\n"
@@ -169,6 +184,22 @@ __device__ __forceinline__ float fast_rcp(float x) {
 // for the softmax). k2 = 2 * log2(e) / cap. Saturates to +-cap for large |x| (e^(2y) -> inf or 0).
 __device__ __forceinline__ float soft_cap(float x, float cap, float k2) {
     return cap - (2.f * cap) * fast_rcp(fast_exp2(x * k2) + 1.f);
+}
+
+// The soft cap for small arguments, two at a time, in log2 units: for |x| <= |cap| / 4 it returns
+// cap * tanh(x / cap) * log2(e) from the Taylor series of tanh through the y^9 term
+// (tanh y = y - y^3/3 + 2y^5/15 - 17y^7/315 + 62y^9/2835 - ...; the series alternates with
+// shrinking terms there, so the first omitted one, 1382/155925 |y|^11, bounds the truncation:
+// below 2^-26 relative at |y| = 1/4, under float32 rounding).  No special-function unit is used.
+// v = x * log2(e) (the scaled logit in log2 units), ic = 1 / (cap * log2(e)).
+__device__ __forceinline__ float2 soft_cap_small2(float2 v, float ic) {
+    const float2 u = fmul2(v, make_float2(ic, ic));
+    const float2 u2 = fmul2(u, u);
+    float2 p = ffma2(u2, make_float2(62.f / 2835.f, 62.f / 2835.f), make_float2(-17.f / 315.f, -17.f / 315.f));
+    p = ffma2(p, u2, make_float2(2.f / 15.f, 2.f / 15.f));
+    p = ffma2(p, u2, make_float2(-1.f / 3.f, -1.f / 3.f));
+    p = ffma2(p, u2, make_float2(1.f, 1.f));
+    return fmul2(v, p);
 }
 
 // Two e4m3 bytes -> two floats (exact), via the hardware fp8x2 -> f16x2 convert.
@@ -254,12 +285,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// A waiting thread is suspended (for at most kSuspendNs per try) until the phase completes,
+// instead of re-polling the barrier: a dozen warps polling barriers in tight loops fill the
+// shared-memory pipe and delay the loads and stores of the warps doing the work.
+constexpr uint32_t kSuspendNs = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -274,11 +309,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase of `bar` with the given parity; false (and the error bit) on timeout.
+// The global timer is read once every kPollsPerClock polls: reading it is not free, and a
+// dozen warps polling it at once slow the warps that do the work.
+constexpr uint32_t kPollsPerClock = 4;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
+    uint32_t n = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (++n % kPollsPerClock == 0 && global_ns() - t0 > kWaitLimitNs) {
             set_error(err, RPA_DEV_ERR_TIMEOUT);
             return false;
         }
@@ -489,10 +528,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
-        "p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, "
+        "0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -511,8 +550,9 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
+    uint32_t n = 0;
     while (!mbar_try_wait_cluster(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (++n % kPollsPerClock == 0 && global_ns() - t0 > kWaitLimitNs) {
             set_error(err, RPA_DEV_ERR_TIMEOUT);
             return false;
         }

@@ -311,7 +311,10 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
             const int k = owner(e_pend, idx);
             const int kprev = k > 0 ? e_pend[k - 1] : 0;  // this sequence's items start here
             const int tiles = (e_pend[k] - kprev) / a.num_kv_heads;
-            const int rel = idx - kprev, h = rel / tiles, r = rel - h * tiles;
+            // a sequence's tiles longest first (a later tile sees more keys), the KV heads of one
+            // tile together: persistent CTAs take the long items first and the short ones fill
+            // in at the end
+            const int rel = idx - kprev, h = rel % a.num_kv_heads, r = tiles - 1 - rel / a.num_kv_heads;
             WorkItem w;
             w.seq = s0 + k;
             w.head = h;

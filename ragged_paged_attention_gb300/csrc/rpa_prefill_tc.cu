@@ -43,24 +43,38 @@
 
 namespace rpa {
 
-template <int D>
+template <int D, bool RAW = false>
 struct PreTc {
     static constexpr int BK = D >= 256 ? 64 : 128;       // keys per block
     static constexpr int DP = D / 64;                    // 64-wide panels of the head dim
-    static constexpr int kQ = DP * 128 * 128;            // Q tile: DP panels of [128 rows x 128 B]
+    // Q tile: DP panels of [128 rows x 128 B] in shared memory, or (RAW) in TMEM
+    static constexpr int kQ = RAW ? 0 : DP * 128 * 128;
     static constexpr int kPanel = BK * 128;              // one K or V panel: [BK rows x 128 B]
     static constexpr int kStage = DP * kPanel;           // K (or V) of one block
+    // RAW (one-byte caches staged by TMA): a block's raw K (or V) rows as D / 128 halves of
+    // [BK rows x 128 B], 128-byte swizzled like the panels
+    static constexpr int NH = D / 128;
+    static constexpr int kRawHalf = BK * 128;
+    static constexpr int kRaw = RAW ? NH * kRawHalf : 0;
+    static constexpr int kReserve = 3072;                // barriers, scratch, row factors, item ring
     // stages of the K ring and of the V ring: as many as fit (P lives in TMEM), V's ring the
-    // deeper one when the count is odd (a V slot is held from its load until PV, K's only until QK)
-    static constexpr int kFitS = (232448 - kQ - 3072) / kStage;  // 3 KB: barriers, scratch, row factors
+    // deeper one when the count is odd (a V slot is held from its load until PV, K's only until
+    // QK); RAW: two f16 stages each and the raw rings (three stages each) in the rest
+    static constexpr int kFitS = RAW ? 4 : (232448 - kQ - kReserve) / kStage;
     static constexpr int kTotS = kFitS > 8 ? 8 : kFitS;
     static constexpr int NSK = kTotS / 2;
     static constexpr int NSV = kTotS - NSK;
+    static constexpr int NR = RAW ? (232448 - kReserve - kTotS * kStage) / (2 * (kRaw > 0 ? kRaw : 1)) : 0;
     static constexpr int kOffK = kQ;
     static constexpr int kOffV = kOffK + NSK * kStage;
-    static constexpr int kOffBar = kOffV + NSV * kStage;
-    // rings, S/P barriers (kSB = 2), q_full, o_full, fin, q_empty, o_empty, item ring full/empty [2] each
-    static constexpr int kNumBars = 2 * (NSK + NSV) + 4 * 2 + 3 + 2 + 4;
+    static constexpr int kOffRawK = kOffV + NSV * kStage;
+    static constexpr int kOffRawV = kOffRawK + NR * kRaw;
+    static constexpr int kOffBar = kOffRawV + NR * kRaw;
+    // rings (+ raw rings), S/P barriers, q_full, o_full, fin, q_empty, o_empty, item ring full/empty [2] each
+    static constexpr int kNumBars = 2 * (NSK + NSV) + 4 * NR + 4 * 2 + 3 + 2 + 4 + (RAW ? 1 : 0);
+    // RAW: the item's Q tile (DP panels of [128 rows x 128 B]) is staged by TMA in the free K
+    // slot (kQinK panels) and V slot (the rest) of the item's first block
+    static constexpr int kQinK = kStage / 16384;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
     static constexpr int kOffQmul = kOffRed + 2 * 2 * 128 * 4;           // [128] float: Q row factors (f16 path)
@@ -68,16 +82,22 @@ struct PreTc {
     static constexpr int kSmem = kOffItem + 2 * 32 + 16;
     static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
     static_assert(NSK >= 2 && NSV >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
-    // TMEM: kSB score buffers of BK columns, kSB P buffers of BK/2 columns (bf16 pairs), O.
-    // S and P live apart, so QK of block j+2 may overwrite S as soon as the softmax has loaded
-    // block j's scores, while PV of block j still reads P(j) from its own buffer.
-    static constexpr int kSB = 2;
+    static_assert(!RAW || (NR >= 2 && kOffRawK % 1024 == 0 && kOffRawV % 1024 == 0 && (D == 128 || D == 256)),
+                  "raw rings");
+    // TMEM: kSB score buffers of BK columns, two P buffers of BK/2 columns (bf16 pairs), O and
+    // (RAW) Q (D/2 columns of element pairs).  S and P live apart, so QK of block j+kSB may
+    // overwrite S as soon as the softmax has loaded block j's scores, while PV of block j still
+    // reads P(j) from its own buffer.  RAW keeps one score buffer (the softmax loads a block's
+    // scores at once, so the next QK waits only for that) to make room for Q.
+    static constexpr int kSB = RAW ? 1 : 2;
+    static constexpr int kPB = 2;
     static constexpr int kColP = kSB * BK;
-    static constexpr int kColO = kColP + kSB * (BK / 2);
-    static constexpr int kTmemCols = kColO + D <= 256 ? 256 : 512;
+    static constexpr int kColO = kColP + kPB * (BK / 2);
+    static constexpr int kColQ = kColO + D;
+    static constexpr int kTmemCols = (RAW ? kColQ + D / 2 : kColO + D) <= 256 ? 256 : 512;
     static constexpr int kSoftWarps = 8;                 // two per TMEM lane quarter (column halves)
     static constexpr int kHalf = BK / 2;                 // score columns per softmax warp
-    static_assert(kColO + D <= kTmemCols, "TMEM budget");
+    static_assert((RAW ? kColQ + D / 2 : kColO + D) <= kTmemCols, "TMEM budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -139,18 +159,37 @@ __device__ __forceinline__ uint4 kv_convert_f16(uint2 raw) {
         return make_uint4(e4m3x2_to_f16x2(h[0]), e4m3x2_to_f16x2(h[1]), e4m3x2_to_f16x2(h[2]), e4m3x2_to_f16x2(h[3]));
 }
 
-template <bool TMA>
-constexpr int prefill_warps() { return 8 + 4 + 2; }  // softmax, producers (2 for K, 2 for V), QK and PV issuers
+// softmax, producers (2 for K, 2 for V), QK and PV issuers, and (RAW) the raw-row TMA warp
+template <bool RAW>
+constexpr int prefill_warps() { return 8 + 4 + 2 + (RAW ? 1 : 0); }
+
+// 16 raw one-byte values (dims 16c .. 16c+15 of a row) -> two 16-byte chunks of f16 (exact,
+// unscaled: the f16 path) or bf16(float(x) * scale) values.
+template <bool F16, bool I8>
+__device__ __forceinline__ void raw16_convert(uint4 r, float sc, uint4& lo, uint4& hi) {
+    const uint2 a = make_uint2(r.x, r.y), b = make_uint2(r.z, r.w);
+    if constexpr (F16) {
+        lo = kv_convert_f16<I8>(a);
+        hi = kv_convert_f16<I8>(b);
+    } else {
+        lo = kv_convert<true, false, I8>(a, sc);
+        hi = kv_convert<true, false, I8>(b, sc);
+    }
+}
 
 // F16 (one-byte caches whose k_scale and v_scale are powers of two): K and V go to the tensor
 // cores as exact f16 values (one convert per pair), each Q row is brought into f16 range by a
 // power of two found from its largest element (its bf16 values stay exact), P is f16, and the
 // row factor with k_scale goes onto the scores, v_scale onto O.
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false>
-__global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
+// RAW (one-byte caches, page boxes of >= 8 rows): warp 14 lands each block's raw K and V rows
+// by TMA (128-byte swizzled halves of [BK x 128 B]) in rings of NR stages, warps 8-11 convert
+// them shared memory to shared memory into the f16/bf16 panels and put Q into TMEM (the QK
+// MMAs read A from there), and S has one TMEM buffer.
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false>
+__global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
     rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                           int box_rows, int q_tma, int tail) {
-    using T = PreTc<D>;
+    using T = PreTc<D, RAW>;
     constexpr int BK = T::BK;
     // first launch (tail == 0): started early behind the plan kernel, it waits for it, then lets
     // the decode grid behind start; only the plan's share of its CTAs works. Either launch
@@ -172,29 +211,36 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint64_t* v_full = bars + 2 * NSK;             // [NSV] V block landed
     uint64_t* v_empty = bars + 2 * NSK + NSV;      // [NSV] PV of that block done
     uint64_t* const bars_s = bars + 2 * (NSK + NSV);
-    constexpr int SB = T::kSB;
-    static_assert(T::kSB == 2, "barrier layout");
+    constexpr int SB = T::kSB, PB = T::kPB, NR = T::NR;
+    constexpr uint32_t NRd = NR > 0 ? NR : 1;  // ring divisor (the raw rings exist only with RAW)
+    static_assert(T::kPB == 2 && T::kSB <= 2, "barrier layout");
     uint64_t* s_full = bars_s;            // [SB] S buffer written by QK
-    uint64_t* s_free = bars_s + SB;       // [SB] the softmax has loaded that buffer's scores
-    uint64_t* p_full = bars_s + 2 * SB;   // [SB] P buffer written (and O rescaled)
-    uint64_t* p_empty = bars_s + 3 * SB;  // [SB] PV of that buffer's P done (buffer free again)
-    uint64_t* q_full = bars_s + 4 * SB;
+    uint64_t* s_free = bars_s + 2;        // [SB] the softmax has loaded that buffer's scores
+    uint64_t* p_full = bars_s + 4;        // [PB] P buffer written (and O rescaled)
+    uint64_t* p_empty = bars_s + 6;       // [PB] PV of that buffer's P done (buffer free again)
+    uint64_t* q_full = bars_s + 8;
     uint64_t* o_full = q_full + 1;
     uint64_t* fin = q_full + 2;
     uint64_t* q_empty = q_full + 3;     // the item's QKs are done and the softmax warps have started it
     uint64_t* o_empty = q_full + 4;     // the epilogue has read O out of TMEM
     uint64_t* item_full = q_full + 5;   // [2] ring slot written
     uint64_t* item_empty = q_full + 7;  // [2] ring slot read by every warp
+    uint64_t* rawk_full = q_full + 9;             // [NR] (RAW) a block's raw K rows landed
+    uint64_t* rawk_empty = rawk_full + NR;        // [NR] converted (slot free)
+    uint64_t* rawv_full = rawk_full + 2 * NR;     // [NR] raw V rows landed
+    uint64_t* rawv_empty = rawk_full + 3 * NR;    // [NR] converted
+    uint64_t* q_stage = rawk_full + 4 * NR;       // (RAW) the item's Q tile landed in its staging slots
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + T::kOffRed);
     // producer warps [8, 12): warps 8-9 stream K, 10-11 V; then the MMA warp
     // warp 12 issues the QK MMAs (and owns the TMEM allocation), warp 13 the PV MMAs: two issuing
     // threads, so neither stream waits behind the other's inputs (an MMA issue blocks while the
     // tensor pipe's short queue is full)
-    constexpr int kProdW0 = 8, kProdW1 = 12, kMmaW = kProdW1, kPvW = kProdW1 + 1;
+    constexpr int kProdW0 = 8, kProdW1 = 12, kMmaW = kProdW1, kPvW = kProdW1 + 1, kRawW = kProdW1 + 2;
     // (no static shared variables: with the 1024-byte aligned dynamic block they would
     // round up to 1 KB and push the kernel past the 227 KB limit)
     static_assert(!F16 || (FP8 && !TMA), "the f16 path takes one-byte caches through registers");
+    static_assert(!RAW || (FP8 && !TMA && !SCALE), "the raw-staging path is for one-byte caches");
     float* qmul = reinterpret_cast<float*>(smem + T::kOffQmul);
     WorkItem* s_items = reinterpret_cast<WorkItem*>(smem + T::kOffItem);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 64);
@@ -221,9 +267,18 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], T::kSoftWarps * 32);
+        }
+        for (int i = 0; i < PB; ++i) {
             mbar_init(&p_full[i], T::kSoftWarps * 32);
             mbar_init(&p_empty[i], 1);
         }
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(&rawk_full[i], 1);   // the TMA warp's arrive + the copies' bytes
+            mbar_init(&rawk_empty[i], 2);  // one arrival per converting warp
+            mbar_init(&rawv_full[i], 1);
+            mbar_init(&rawv_empty[i], 2);
+        }
+        if (RAW) mbar_init(q_stage, 1);
         // Q by TMA: the issuing thread alone; through registers: every producer thread
         mbar_init(q_full, (TMA && q_tma) ? 1 : (kProdW1 - kProdW0) * 32);
         mbar_init(o_full, 1);
@@ -232,7 +287,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         mbar_init(o_empty, T::kSoftWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&item_full[i], 1);
-            mbar_init(&item_empty[i], prefill_warps<TMA>());
+            mbar_init(&item_empty[i], prefill_warps<RAW>());
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -254,7 +309,8 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
     uint32_t items = 0;  // items this CTA has processed (ring slots, q / o phases)
     while (true) {
         const uint32_t islot = items & 1, iring = (items >> 1) & 1;
-        if (tid == kProdW0 * 32) {
+        // the fetching thread: the first producer thread, or (RAW) the raw-row TMA warp's
+        if (tid == (RAW ? kRawW : kProdW0) * 32) {
             WorkItem nw;
             nw.seq = -1;
             if (!mbar_wait(&item_empty[islot], iring ^ 1, err)) s_abort = 1;
@@ -291,7 +347,232 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
         const int nb = cdiv(ke - kb, BK);
         const uint32_t iph = items & 1;
 
-        if (warp >= kProdW0 && warp < kProdW1) {
+        if (RAW && warp >= kProdW0 && warp < kProdW1) {
+            // ---------------- converters (RAW) ----------------
+            // Q: this warp's 32 rows (its TMEM lane quarter), once the previous item's QKs have
+            // read Q and its softmax warps have started it (q_empty). With q_tma the tile has been
+            // staged by TMA in the item's first K and V slots (128-byte swizzled panels) and is
+            // read from there; otherwise each thread loads its row from global memory.
+            {
+                const int r = (warp - kProdW0) * 32 + lane;
+                const uint32_t lane_off = (uint32_t)((warp - kProdW0) * 32) << 16;
+                if (!mbar_wait(q_empty, iph ^ 1, err)) s_abort = 1;
+                if (q_tma && !mbar_wait(q_stage, iph, err)) s_abort = 1;
+                tc_fence_after();
+                const int R = R0 + r;
+                const bool rv = R < n_rows;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                    a.q + ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D);
+                // this row in the staged tile: panel p at base(p) + r * 128, 16-byte chunk cc of it
+                // at position cc ^ (r % 8)
+                const uint32_t kst = smem_u32(smem + T::kOffK + (jb % NSK) * T::kStage) + r * 128;
+                const uint32_t vst = smem_u32(smem + T::kOffV + (jb % NSV) * T::kStage) + r * 128;
+                // 16-byte chunk c (elements 8c .. 8c+7) of this row; rows past the item are zeros
+                auto qchunk = [&](int c) -> uint4 {
+                    if (!rv) return make_uint4(0, 0, 0, 0);
+                    if (!q_tma) return __ldg(reinterpret_cast<const uint4*>(src + c * 16));
+                    const int p = c >> 3;
+                    return lds128((p < T::kQinK ? kst + p * 16384 : vst + (p - T::kQinK) * 16384) +
+                                  (((c & 7) ^ (r & 7)) << 4));
+                };
+                float qs = 1.f;
+                if (F16) {
+                    // the row's largest |q| < 2^ex; 2^-k brings it into [2^14, 2^15) (f16 range);
+                    // eight chunks in flight, four independent maxima
+                    float m4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D / 8; c0 += 8) {
+                        uint4 v8[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) v8[u] = qchunk(c0 + u);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v8[u]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(h2[e]);
+                                m4[e] = fmax3(m4[e], fabsf(f.x), fabsf(f.y));
+                            }
+                        }
+                    }
+                    const float mabs = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    int ex = 0;
+                    frexpf(mabs, &ex);
+                    const int k = max(-30, min(100, ex - 15));
+                    qs = ldexpf(1.f, -k);
+                    qmul[r] = ldexpf(1.f, k);
+                }
+                // 32 elements (16 TMEM columns of element pairs) per store, two stores per batch
+#pragma unroll 1
+                for (int g = 0; g < D / 32; g += 2) {
+                    uint4 v8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v8[u] = qchunk(g * 4 + u);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 u = v8[h * 4 + c];
+                            if (F16) {
+                                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = __bfloat1622float2(h2[e]);
+                                    w4[e] = pack_f16(f.x * qs, f.y * qs);
+                                }
+                                u = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
+                            v[4 * c] = u.x;
+                            v[4 * c + 1] = u.y;
+                            v[4 * c + 2] = u.z;
+                            v[4 * c + 3] = u.w;
+                        }
+                        tmem_st16_nowait(tmem + lane_off + T::kColQ + (g + h) * 16, v);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                // every converter thread has read the staged tile before block jb's K and V are
+                // converted into the same slots
+                if (q_tma) asm volatile("bar.sync 5, 128;" ::: "memory");
+                mbar_arrive(q_full);
+            }
+            // K (warps 8-9) or V (warps 10-11) of every block: raw rows -> panels. The part's 64
+            // threads work in phases of 8 lanes, each phase one 16-byte raw chunk of 8 consecutive
+            // rows (distinct swizzled positions for the raw reads and the panel writes alike).
+            const int part = (warp - kProdW0) >> 1;
+            const int ph = (((warp - kProdW0) & 1) << 2) | (lane >> 3), l8 = lane & 7;
+            uint64_t* fbar = part ? v_full : k_full;
+            uint64_t* ebar = part ? v_empty : k_empty;
+            uint64_t* rfull = part ? rawv_full : rawk_full;
+            uint64_t* rempty = part ? rawv_empty : rawk_empty;
+            const float sc = part ? a.v_scale_or_one : a.k_scale_or_one;
+            constexpr int kChunks = D / 16;                    // 16-byte raw chunks per row
+            constexpr int kIters = (BK / 8) * kChunks / 8;     // (row group, chunk) pairs per phase
+            constexpr int kCB = kChunks / 8 > 0 ? kChunks / 8 : 1;  // raw halves (8-chunk groups) per row
+            // iteration `it` of a phase covers chunk c = (it % kCB) * 8 + ph of rows
+            // (it / kCB) * 8 + l8: its raw half is it % kCB, its panels (it % kCB) * 2 + ph / 4,
+            // so every address is a per-thread base plus a compile-time offset
+            const uint32_t raw_base = l8 * 128 + ((ph ^ l8) << 4);
+            const uint32_t dst_base = (ph >> 2) * T::kPanel + l8 * 128;
+            const uint32_t pos0 = ((2 * (ph & 3)) ^ l8) << 4, pos1 = ((2 * (ph & 3) + 1) ^ l8) << 4;
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t q = jb + j, slot = part ? q % NSV : q % NSK, par = (part ? q / NSV : q / NSK) & 1;
+                const uint32_t rs = q % NRd, rp = (q / NRd) & 1;
+                if (!mbar_wait(&rfull[rs], rp, err) || !mbar_wait(&ebar[slot], par ^ 1, err)) {
+                    s_abort = 1;
+                    break;
+                }
+                const uint8_t* raw = smem + (part ? T::kOffRawV : T::kOffRawK) + rs * T::kRaw + raw_base;
+                uint8_t* stage = smem + (part ? T::kOffV : T::kOffK) + slot * T::kStage + dst_base;
+                const int nvalid = ke - (kb + j * BK);  // rows of this block inside the key range (>= 1)
+                const bool full = nvalid >= BK;
+                // a batch's raw chunks are all loaded before any is converted and stored (the
+                // compiler cannot tell the raw ring from the panels, so it would otherwise keep
+                // every load behind the previous store)
+                constexpr int kBatch = 8;
+                static_assert(kIters % kBatch == 0, "converter batches");
+#pragma unroll
+                for (int it0 = 0; it0 < kIters; it0 += kBatch) {
+                    uint4 r16[kBatch];
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int it = it0 + u;
+                        const int row = (it / kCB) * 8 + l8;
+                        r16[u] = (full || row < nvalid)
+                                     ? *reinterpret_cast<const uint4*>(raw + (it % kCB) * T::kRawHalf + (it / kCB) * 1024)
+                                     : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int it = it0 + u;
+                        uint4 lo, hi;
+                        raw16_convert<F16, I8>(r16[u], sc, lo, hi);  // zero bytes convert to zeros
+                        uint8_t* drow = stage + (it % kCB) * 2 * T::kPanel + (it / kCB) * 1024;
+                        *reinterpret_cast<uint4*>(drow + pos0) = lo;
+                        *reinterpret_cast<uint4*>(drow + pos1) = hi;
+                    }
+                }
+                fence_proxy_async_smem();  // panels written by threads, read by the tensor core
+                mbar_arrive(&fbar[slot]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rempty[rs]);
+            }
+        } else if (RAW && warp == kRawW) {
+            // ---------------- raw-row TMA (RAW) ----------------
+            // lane l owns box l (box_rows keys of one page) of every block, looked up one block
+            // ahead; a box with any row inside the key range is copied whole (its rows past the
+            // range are slots of the same page, converted to zeros), K then V of each block
+            const int nbox = BK / box_rows;
+            const int lbr = __ffs(box_rows) - 1, lps = __ffs(a.page_size) - 1, pmask_ps = a.page_size - 1;
+            const uint32_t box_bytes = (uint32_t)box_rows * 128 * T::NH;
+            const int* tbl = a.page_indices + (size_t)s * a.pages_per_seq;
+            auto page_of = [&](int j) -> int {
+                const int key = kb + j * BK + lane * box_rows;
+                return (lane < nbox && j < nb && key < ke) ? __ldg(tbl + (key >> lps)) : 0;
+            };
+            int page_next = page_of(0);
+            bool go = true;
+            for (int j = 0; go && j < nb; ++j) {
+                const uint32_t q = jb + j, rs = q % NRd, rp = (q / NRd) & 1;
+                int page = page_next;
+                page_next = page_of(j + 1);
+                const int kbj = kb + j * BK;
+                const int nvb = min(nbox, (ke - kbj + box_rows - 1) >> lbr);  // boxes with a row in range
+                if (lane < nvb && (unsigned)page >= (unsigned)a.total_num_pages) {
+                    set_error(err, RPA_DEV_ERR_PAGE);
+                    page = 0;  // an in-bounds page keeps the barrier's byte count; the error is recorded
+                }
+                const int z0 = (page << lps) + ((kbj + lane * box_rows) & pmask_ps);
+#pragma unroll 1
+                for (int part = 0; part < 2; ++part) {
+                    uint64_t* rfull = part ? rawv_full : rawk_full;
+                    uint64_t* rempty = part ? rawv_empty : rawk_empty;
+                    int g = 1;
+                    if (lane == 0) {
+                        g = mbar_wait(&rempty[rs], rp ^ 1, err);
+                        if (g)
+                            mbar_arrive_expect_tx(&rfull[rs], (uint32_t)nvb * box_bytes);
+                        else
+                            s_abort = 1;
+                    }
+                    if (!__shfl_sync(0xffffffffu, g, 0)) {
+                        go = false;
+                        break;
+                    }
+                    uint8_t* dst = smem + (part ? T::kOffRawV : T::kOffRawK) + rs * T::kRaw + lane * box_rows * 128;
+                    if (lane < nvb) {
+#pragma unroll
+                        for (int h = 0; h < T::NH; ++h)
+                            tma_load_3d(smem_u32(dst + h * T::kRawHalf), &tm_kv, 128 * h, 2 * kvh + part, z0, &rfull[rs]);
+                    }
+                }
+                if (go && j == 0 && q_tma) {
+                    // the item's Q tile into the K and V slots of its first block once those are
+                    // free (QK and PV of block jb - 2 done); the converters read it from there
+                    int g = 1;
+                    if (lane == 0) {
+                        const uint32_t ks = jb % NSK, kp = (jb / NSK) & 1, vs = jb % NSV, vp = (jb / NSV) & 1;
+                        g = mbar_wait(&k_empty[ks], kp ^ 1, err) &&
+                            (T::DP <= T::kQinK || mbar_wait(&v_empty[vs], vp ^ 1, err));
+                        if (g) {
+                            mbar_arrive_expect_tx(q_stage, (uint32_t)D * 256);
+#pragma unroll
+                            for (int p = 0; p < T::DP; ++p) {
+                                uint8_t* qd = p < T::kQinK ? smem + T::kOffK + ks * T::kStage + p * 16384
+                                                           : smem + T::kOffV + vs * T::kStage + (p - T::kQinK) * 16384;
+                                tma_load_3d(smem_u32(qd), &tm_q, 64 * p, kvh * G, q_start + R0 / G, q_stage);
+                            }
+                        } else {
+                            s_abort = 1;
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, g, 0)) go = false;
+                }
+            }
+        } else if (warp >= kProdW0 && warp < kProdW1) {
             // ---------------- producers ----------------
             const int pt = tid - kProdW0 * 32;
             if (TMA && q_tma) {
@@ -509,10 +790,18 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t kb0 = kdesc + (uint64_t)((slot * T::kStage) >> 4);
+                    if constexpr (RAW) {
+                        // Q from TMEM: one K=16 step spans 8 columns of element pairs
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        umma_bf16(tmem + sb * BK, qdesc + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                                  kb0 + (((ks >> 2) * T::kPanel + (ks & 3) * 32) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            umma_bf16_ta(tmem + sb * BK, tmem + T::kColQ + ks * 8,
+                                         kb0 + (((ks >> 2) * T::kPanel + (ks & 3) * 32) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            umma_bf16(tmem + sb * BK, qdesc + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                      kb0 + (((ks >> 2) * T::kPanel + (ks & 3) * 32) >> 4), idesc_qk, ks > 0 ? 1u : 0u);
+                    }
                     umma_commit(&s_full[sb]);
                     umma_commit(&k_empty[slot]);
                 }
@@ -527,7 +816,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 // the first PV overwrites O: the previous item's epilogue has read it
                 bool ok = mbar_wait(o_empty, iph ^ 1, err);
                 for (int j = 0; ok && j < nb; ++j) {
-                    const uint32_t q = jb + j, pb = q % SB, pp = (q / SB) & 1, slot = q % NSV, par = (q / NSV) & 1;
+                    const uint32_t q = jb + j, pb = q % PB, pp = (q / PB) & 1, slot = q % NSV, par = (q / NSV) & 1;
                     ok = mbar_wait(&p_full[pb], pp, err) && mbar_wait(&v_full[slot], par, err);
                     if (!ok) break;
                     tc_fence_after();
@@ -572,8 +861,9 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
             float m_use = -INFINITY, l_half = 0.f;
             bool ok = q_ok;
             for (int j = 0; ok && j < nb; ++j) {
-                const uint32_t q = jb + j, slot = q % SB, par = (q / SB) & 1;  // S and P buffers
-                if (!mbar_wait(&s_full[slot], par, err)) {
+                const uint32_t q = jb + j, sslot = q % SB, spar = (q / SB) & 1;  // S buffer
+                const uint32_t slot = q % PB, par = (q / PB) & 1;                 // P buffer
+                if (!mbar_wait(&s_full[sslot], spar, err)) {
                     ok = false;
                     break;
                 }
@@ -582,16 +872,31 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
 #pragma unroll
                 for (int c = 0; c < HB / 32; ++c) {
                     float t32[32];
-                    tmem_ld32(tmem + lane_off + slot * BK + half * HB + c * 32, t32);
+                    tmem_ld32(tmem + lane_off + sslot * BK + half * HB + c * 32, t32);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) x[c * 32 + i] = t32[i];
                 }
                 tc_fence_before();
-                mbar_arrive(&s_free[slot]);  // QK of block q + SB may overwrite these scores
+                mbar_arrive(&s_free[sslot]);  // QK of block q + SB may overwrite these scores
                 const int key0 = kb + j * BK + half * HB;
                 if (cap != 0.f) {
+                    // small logits (the warp's every |x * scale| <= |cap| / 4): the series form,
+                    // on the FMA pipe; otherwise the exponential identity
+                    float am = 0.f;
 #pragma unroll
-                    for (int i = 0; i < HB; ++i) x[i] = soft_cap(x[i] * scale, cap, cap_k2) * kLog2e;
+                    for (int i = 0; i < HB; i += 2) am = fmax3(am, fabsf(x[i]), fabsf(x[i + 1]));
+                    if (__all_sync(0xffffffffu, am * fabsf(scale) <= 0.25f * fabsf(cap))) {
+                        const float sl2 = scale * kLog2e, ic = 1.f / (cap * kLog2e);
+#pragma unroll
+                        for (int i = 0; i < HB; i += 2) {
+                            const float2 y = soft_cap_small2(fmul2(make_float2(x[i], x[i + 1]), make_float2(sl2, sl2)), ic);
+                            x[i] = y.x;
+                            x[i + 1] = y.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < HB; ++i) x[i] = soft_cap(x[i] * scale, cap, cap_k2) * kLog2e;
+                    }
                 } else if (!fold) {
 #pragma unroll
                     for (int i = 0; i < HB; ++i) x[i] *= c_log2;
@@ -650,7 +955,7 @@ __global__ void __launch_bounds__(prefill_warps<TMA>() * 32, 1)
                 // rows needs it (the others multiply by 1); each warp of the pair owns D/2 columns
                 if (__any_sync(0xffffffffu, row_rescale)) {
                     const float f = row_rescale ? alpha : 1.f;
-                    const uint32_t qp = q - 1, sp = qp % SB, pp = (qp / SB) & 1;
+                    const uint32_t qp = q - 1, sp = qp % PB, pp = (qp / PB) & 1;
                     if (!mbar_wait(&p_empty[sp], pp, err)) {  // PV(j-1) has finished writing O
                         ok = false;
                         break;
@@ -758,11 +1063,25 @@ static bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t d0, uint6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false>
+// 3-D one-byte tensor [d2][d1][d0] (d0 contiguous) with a box of {128, 1, b2}, 128-byte swizzle:
+// half of a raw K or V row per copy (the raw-staging path).
+static bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b2) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0, d0 * d1};
+    const cuuint32_t box[3] = {128, 1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false>
 static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
                               const CUtensorMap& tq, int box_rows, int q_tma, int tail) {
-    using T = PreTc<D>;
-    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16>;
+    using T = PreTc<D, RAW>;
+    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16, RAW>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -770,7 +1089,7 @@ static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream
         configured = true;
     }
     ProfScope ps(tail ? "rpa_prefill_tail" : "rpa_prefill_attn", stream);
-    return launch_pdl(kern, dim3(num_sms), dim3(prefill_warps<TMA>() * 32), T::kSmem, stream, a.overlap && !tail, a,
+    return launch_pdl(kern, dim3(num_sms), dim3(prefill_warps<RAW>() * 32), T::kSmem, stream, a.overlap && !tail, a,
                       tkv, tq, box_rows, q_tma, tail);
 }
 
@@ -794,6 +1113,21 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma, tail);
     // one-byte caches with power-of-two scales: exact f16 operands, scales on S and O
     const bool pow2 = rpa_pow2_scale(a.k_scale_or_one) && rpa_pow2_scale(a.v_scale_or_one);
+    if constexpr (D == 128 || D == 256) {
+        // one-byte caches whose pages tile the block in boxes of >= 8 rows: raw rows by TMA,
+        // converted in shared memory, Q in TMEM
+        bool raw = a.kv_byte && (ps & (ps - 1)) == 0 && box_rows >= 8 && BK / box_rows <= 32;
+        if (raw) raw = make_tmap_u8(&tkv, a.kv_pages, D, C, tokens, box_rows);
+        if (raw) {
+            // Q staged by TMA (boxes of G heads x 128 / G tokens) when G divides the tile
+            const int qt = (128 % G == 0 && make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G)) ? 1 : 0;
+            if (a.kv_int8 && pow2)
+                return launch_pre<D, true, false, false, true, true, true>(a, num_sms, stream, tkv, tq, box_rows, qt, tail);
+            if (a.kv_int8) return launch_pre<D, true, false, false, true, false, true>(a, num_sms, stream, tkv, tq, box_rows, qt, tail);
+            if (pow2) return launch_pre<D, true, false, false, false, true, true>(a, num_sms, stream, tkv, tq, box_rows, qt, tail);
+            return launch_pre<D, true, false, false, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, qt, tail);
+        }
+    }
     if (a.kv_int8 && pow2) return launch_pre<D, true, false, false, true, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     if (a.kv_int8) return launch_pre<D, true, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     if (a.kv_byte && pow2) return launch_pre<D, true, false, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
