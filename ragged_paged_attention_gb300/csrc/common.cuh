@@ -473,6 +473,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// Gather of four rows (y0..y3) of a 2-D tensor map whose box is one row high, columns from x:
+// the rows land one after another at dst (with the map's swizzle), completing on `bar`.
+// A row index outside the tensor lands as zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+        : "memory");
+}
 // ---- thread-block clusters (distributed shared memory) ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&kv_full[i], kv_tma ? 32 : 128);  // TMA: warp 8; registers: all producers
+            mbar_init(&kv_full[i], (kv_tma == 1 || kv_tma == 2) ? 32 : 128);  // MLA TMA: warp 8; gathers: all producers
             mbar_init(&kv_empty[i], 1);
             mbar_init(&vld_full[i], 128);
         }
@@ -199,7 +199,76 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         if (warp >= kProdW0 && warp < kMmaW) {
             // ---------------- producers ----------------
             const int pt = tid - kProdW0 * 32;
-            if (!SPARSE && kv_tma) {
+            if (SPARSE && kv_tma == 3) {
+                // selected rows by TMA gathers: warp w of the four resolves keys 16w .. 16w+15 of
+                // each block (one per lane, one block ahead) and its lanes 0-3 each gather one group
+                // of four rows, one 4-row copy per 64-column panel, straight into the swizzled
+                // panels; a key that is not valid gathers a row past the cache (zeros). Every
+                // block's copies go out as soon as its slot is free, so up to NS blocks are in flight.
+                const int wsub = warp - kProdW0, kk = wsub * 16 + (lane & 15);
+                const bool rb_p2 = (a.read_block & (a.read_block - 1)) == 0, ps_p2 = (a.page_size & (a.page_size - 1)) == 0;
+                const int rb_sh = __ffs(a.read_block) - 1, ps_sh = __ffs(a.page_size) - 1;
+                const int oob_row = a.total_num_pages * a.page_size;  // gathers zeros
+                auto resolve_row = [&](int j, bool& v) -> int {
+                    const int key = kb + j * BK + kk;
+                    v = lane < 16 && j < nb && key < ke;
+                    if (!v) return oob_row;
+                    const int ui = rb_p2 ? key >> rb_sh : key / a.read_block;
+                    const int ur = rb_p2 ? key & (a.read_block - 1) : key % a.read_block;
+                    const int u = __ldg(a.indices + (size_t)w.seq * a.topk + ui);
+                    const long long kp = (long long)u * a.read_block + ur;
+                    v = u >= 0 && kp <= qpos && kp < kbound;
+                    if (!v) return oob_row;
+                    const int lp = ps_p2 ? (int)(kp >> ps_sh) : (int)(kp / a.page_size);
+                    const int po = ps_p2 ? (int)(kp & (a.page_size - 1)) : (int)(kp % a.page_size);
+                    int page;
+                    if (a.q_base) {  // packed list: the request's run, clamped to the list's end
+                        const long long pidx = min((long long)kbase + lp, (long long)a.max_pages - 1);
+                        page = pidx >= 0 ? __ldg(a.page_table + pidx) : -1;
+                    } else {
+                        page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
+                    }
+                    if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                        set_error(err, RPA_DEV_ERR_PAGE);
+                        v = false;
+                        return oob_row;
+                    }
+                    return page * a.page_size + po;
+                };
+                bool v_next;
+                int row_next = resolve_row(0, v_next);
+                const uint32_t grp_bytes = 4u * nqp * 128;  // one group's four rows, every panel
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1;
+                    const bool v = v_next;
+                    const int row = row_next;
+                    row_next = resolve_row(j + 1, v_next);
+                    int g = 1;
+                    if (lane == 0) {
+                        g = mbar_wait(&kv_empty[st], par ^ 1, err);
+                        if (g)
+                            mbar_expect_tx(&kv_full[st], 4 * grp_bytes);
+                        else
+                            s_abort = 1;
+                    }
+                    if (!__shfl_sync(0xffffffffu, g, 0)) break;
+                    if (lane < 16) vld[st * BK + kk] = v ? 1 : 0;
+                    mbar_arrive(&vld_full[st]);  // (read by the softmax through plain loads)
+                    // group gi = lane & 3: the rows of lanes 4gi .. 4gi+3
+                    const int gi = lane & 3;
+                    const int r0 = __shfl_sync(0xffffffffu, row, 4 * gi), r1 = __shfl_sync(0xffffffffu, row, 4 * gi + 1);
+                    const int r2 = __shfl_sync(0xffffffffu, row, 4 * gi + 2), r3 = __shfl_sync(0xffffffffu, row, 4 * gi + 3);
+                    if (lane < 4) {
+                        uint8_t* dst = smem + kOffKV + st * kStage + (wsub * 16 + gi * 4) * 128;
+#pragma unroll
+                        for (int p = 0; p < NQP_MAX; ++p)
+                            if (p < nqp)
+                                tma_gather4(smem_u32(dst + p * kPanel), &tm_kc, lat_panel_col(rank, p), r0, r1, r2, r3,
+                                            &kv_full[st]);
+                    }
+                    mbar_arrive(&kv_full[st]);
+                }
+            } else if (!SPARSE && kv_tma) {
                 if (warp == kProdW0) {
                     const int nbox = BK / box_rows;
                     const size_t tbl = (size_t)seq * a.pages_per_seq;
@@ -859,7 +928,11 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
     memset(&kr, 0, sizeof kr);
     memset(&kc3, 0, sizeof kc3);
     int kv_tma = 0, box_rows = 0;  // without usable key maps the register gather runs
-    if (!SPARSE) {
+    if (SPARSE) {
+        // kv_tma 3: the fused latent rows [rows][row_stride] by 4-row TMA gathers of 64 columns
+        const uint64_t rows = (uint64_t)a.total_num_pages * a.page_size;
+        if (rows < 0x7fffffffull && make_tmap_2d(&kc, a.cache, a.row_stride, rows, a.row_stride, 1)) kv_tma = 3;
+    } else {
         const int ps = a.page_size;
         box_rows = ps < BK ? ps : BK;
         if ((ps & (ps - 1)) == 0 && box_rows >= 8) {
