@@ -370,25 +370,70 @@ def llama_batch():
     return workloads.llama_mixed()
 
 
-def cpu_baseline_rpa(b, seconds, seed=0):
+def cpu_sample(run, total, seconds, n_cal=4, seed=0):
+    """Times ``run(ids)`` -- the oracle on a subset of the ``total`` units (query tokens) of a
+    workload: a calibration call on ``n_cal`` units, then one call on as many uniformly drawn
+    units as fit in about ``seconds``.  Returns (units, seconds taken)."""
+    rng = np.random.default_rng(seed)
+    n_cal = min(n_cal, total)
+    t0 = time.perf_counter()
+    run(np.sort(rng.choice(total, n_cal, replace=False)))
+    cal = time.perf_counter() - t0
+    n = int(max(n_cal, min(total, n_cal * seconds / max(cal, 1e-3))))
+    ids = np.sort(rng.choice(total, n, replace=False))
+    t0 = time.perf_counter()
+    run(ids)
+    return n, time.perf_counter() - t0
+
+
+def cpu_record(n, total, dt, what):
+    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {total} query tokens drawn uniformly from {what}, all heads, float64 C oracle "
+                      f"with OpenMP, {dt:.1f} s"}
+
+
+def cpu_baseline_rpa(b, seconds, seed=0, what="the Llama-3-8B mixed batch"):
     """The float64 oracle on a random sample of the batch's query tokens."""
     import oracle
     oracle.build()
-    rng = np.random.default_rng(seed)
     T = b.num_tokens
-    n_cal = 8
-    t0 = time.perf_counter()
-    oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens),
-               tokens=rng.choice(T, n_cal, replace=False), **b.options())
-    cal = time.perf_counter() - t0
-    n = int(max(8, min(T, n_cal * seconds / max(cal, 1e-3))))
-    toks = np.sort(rng.choice(T, n, replace=False))
-    t0 = time.perf_counter()
-    oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=toks, **b.options())
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} of {T} query tokens drawn uniformly from the Llama-3-8B mixed batch, all heads, "
-                      f"float64 C oracle with OpenMP, {dt:.1f} s"}
+    n, dt = cpu_sample(lambda ids: oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens,
+                                              len(b.q_lens), tokens=ids, **b.options()), T, seconds, 8, seed)
+    return cpu_record(n, T, dt, what)
+
+
+def cpu_baseline_mla(m, seconds, seed=0):
+    """The oracle's update_kv_cache and attention on a random sample of the MLA batch's tokens."""
+    import oracle
+    oracle.build()
+    T = m.num_tokens
+    n, dt = cpu_sample(lambda ids: oracle.mla_forward(m.ql_nope, m.q_pe, m.new_kv_c, m.new_k_pe, m.cache_kv_c,
+                                                      m.cache_k_pe, m.kv_lens, m.page_indices, m.cu_q_lens,
+                                                      m.distribution, tokens=ids, **m.options()),
+                       T, seconds, 4, seed)
+    return cpu_record(n, T, dt, "the DeepSeek-V3 MLA batch (cache update included)")
+
+
+def cpu_baseline_sparse(s, seconds, what, seed=0):
+    """The oracle on a random sample of the sparse batch's queries."""
+    import oracle
+    oracle.build()
+    B, S = s.q.shape[:2]
+    n, dt = cpu_sample(lambda ids: oracle.sparse_mla(s.q, s.cache, s.indices, s.positions, s.page_table,
+                                                     queries=ids, **s.options()), B * S, seconds, 2, seed)
+    return cpu_record(n, B * S, dt, what)
+
+
+def cpu_baseline_sparse_ragged(s, seconds, what, seed=0):
+    """The oracle's self-write and attention on a random sample of the packed batch's tokens."""
+    import oracle
+    oracle.build()
+    T = s.ql.shape[0]
+    cache = oracle.sparse_ragged_write(s.kvc, s.kpe, s.cache, s.loc, page_size=s.page_size)
+    n, dt = cpu_sample(lambda ids: oracle.sparse_mla_ragged(s.ql, s.qpe, cache, s.topk, s.positions, s.seq_lens,
+                                                            s.cu_q_lens, s.cu_kv_lens, s.page_indices, queries=ids,
+                                                            **s.options()), T, seconds, 2, seed)
+    return cpu_record(n, T, dt, what)
 
 
 def run_reference(args, world, rank):
@@ -434,8 +479,10 @@ def main():
     api.load_library()
     peaks, peak_src = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
+    cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
     if args.workload != "llama_mixed":
-        res = run_variants(dev, peaks, args, world, only=args.workload)
+        res = run_variants(dev, peaks, args, world, only=args.workload,
+                           cpu_secs=args.cpu_seconds / 3 if cpu_ok else 0.0)
         if rank == 0:
             v = res[args.workload]
             print(json.dumps({"metric": METRIC, "value": v["tokens_per_s"] * world, "unit": "tokens/s",
@@ -564,7 +611,7 @@ def main():
     # same-run variants (decode/prefill sub-launches are in `kernels`)
     variants = {}
     if not args.no_variants:
-        variants = run_variants(dev, peaks, args, world)
+        variants = run_variants(dev, peaks, args, world, cpu_secs=args.cpu_seconds / 3 if cpu_ok else 0.0)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -601,7 +648,9 @@ def main():
         print(json.dumps(line), flush=True)
 
 
-def run_variants(dev, peaks, args, world, only=None):
+def run_variants(dev, peaks, args, world, only=None, cpu_secs=0.0):
+    """The other workloads, each measured on its own; with cpu_secs > 0 each also carries the
+    oracle timed on a bounded sample of it (about cpu_secs of host time)."""
     from ragged_paged_attention_gb300 import api, workloads
     res = {}
     steps, warm = (max(3, args.steps // 2), 3) if only is None else (args.steps, args.warmup)
@@ -621,20 +670,20 @@ def run_variants(dev, peaks, args, world, only=None):
 
     # Gemma-2-style fp8 KV, sliding window, soft cap
     if want("gemma2_fp8_sw_cap"):
-        _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report)
+        _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report, cpu_secs)
     if want("mla_deepseek_v3"):
-        _variant_mla(dev, peaks, api, workloads, steps, warm, world, report)
+        _variant_mla(dev, peaks, api, workloads, steps, warm, world, report, cpu_secs)
     for phase in ("prefill", "decode"):
         for mode in ("token", "page"):
             if want(f"dsa_sparse_{phase}_{mode}"):
-                _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report)
+                _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report, cpu_secs)
     for mode in ("token", "page"):
         if want(f"dsa_sparse_ragged_{mode}"):
-            _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report)
+            _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report, cpu_secs)
     return res
 
 
-def _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report):
+def _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report, cpu_secs=0.0):
     b = workloads.gemma_options()
     acc = rpa_accounting(b)
     g = b.to(dev)
@@ -653,13 +702,21 @@ def _variant_gemma(dev, peaks, api, workloads, steps, warm, world, report):
     if kt.get("rpa_prefill_attn"):
         pre_us = 1e3 * kt["rpa_prefill_attn"][1] / kt["rpa_prefill_attn"][0]
         extra["prefill_tensor_frac"] = acc["prefill"][2] / (pre_us * 1e-6) / 1e12 / peaks["bf16_tflops"]
+    if cpu_secs > 0:
+        extra["cpu_baseline"] = cpu_baseline_rpa(b, cpu_secs, what="the Gemma-2-style fp8 batch")
     report("gemma2_fp8_sw_cap", b.num_tokens, acc["decode"][1] + acc["prefill"][1],
            acc["decode"][2] + acc["prefill"][2], ms, kt, extra)
     del b, g, out, ws
     torch.cuda.empty_cache()
 
 
-def _variant_mla(dev, peaks, api, workloads, steps, warm, world, report):
+def _mla_call(api, g, out, ws, opts):
+    return lambda: api.mla_rpa_forward(g.ql_nope, g.q_pe, g.new_kv_c, g.new_k_pe, g.cache_kv_c, g.cache_k_pe,
+                                       g.kv_lens, g.page_indices, g.cu_q_lens, g.distribution, out=out, workspace=ws,
+                                       **opts)
+
+
+def _variant_mla(dev, peaks, api, workloads, steps, warm, world, report, cpu_secs=0.0):
     m = workloads.mla_deepseek()
     tok, byt, fl, dec = mla_accounting(m)
     g = m.to(dev)
@@ -667,18 +724,39 @@ def _variant_mla(dev, peaks, api, workloads, steps, warm, world, report):
     prm = api.make_mla_params(g.ql_nope, g.q_pe, g.cache_kv_c, g.cache_k_pe, g.kv_lens, g.page_indices, **opts)
     ws = torch.zeros(api.mla_workspace_size(prm), dtype=torch.uint8, device=dev)
     out = torch.empty_like(g.ql_nope)
-    ms, kt = time_steps(lambda: api.mla_rpa_forward(g.ql_nope, g.q_pe, g.new_kv_c, g.new_k_pe, g.cache_kv_c,
-                                                    g.cache_k_pe, g.kv_lens, g.page_indices, g.cu_q_lens,
-                                                    g.distribution, out=out, workspace=ws, **opts),
-                        steps, warm, world, timer=True)
+    ms, kt = time_steps(_mla_call(api, g, out, ws, opts), steps, warm, world, timer=True)
     att_us = 1e3 * kt["mla_attn"][1] / kt["mla_attn"][0]
-    report("mla_deepseek_v3", tok, byt, fl, ms, kt,
-           {"attn_tensor_frac": fl / (att_us * 1e-6) / 1e12 / peaks["bf16_tflops"]})
+    extra = {"attn_tensor_frac": fl / (att_us * 1e-6) / 1e12 / peaks["bf16_tflops"]}
+    # the decode-only and prefill-only sub-launches: the batch's own sequence lengths, each
+    # class on its own (decode sits near the ridge, prefill is tensor-bound)
+    nd = sum(1 for x in m.q_lens if x == 1)
+    for name, ql, kl in (("decode_sub", m.q_lens[:nd], m.kv_lens_list[:nd]),
+                         ("prefill_sub", m.q_lens[nd:], m.kv_lens_list[nd:])):
+        sub = workloads.make_mla(ql, kl, seed=2003 + len(ql), num_decode=nd if name == "decode_sub" else 0,
+                                 pages_per_seq=m.page_indices.numel() // len(m.q_lens))
+        s_tok, s_byt, s_fl, _ = mla_accounting(sub)
+        gs = sub.to(dev)
+        prm_s = api.make_mla_params(gs.ql_nope, gs.q_pe, gs.cache_kv_c, gs.cache_k_pe, gs.kv_lens, gs.page_indices,
+                                    **opts)
+        ws_s = torch.zeros(api.mla_workspace_size(prm_s), dtype=torch.uint8, device=dev)
+        out_s = torch.empty_like(gs.ql_nope)
+        _, kt_s = time_steps(_mla_call(api, gs, out_s, ws_s, opts), steps, warm, world, timer=True)
+        us = 1e3 * kt_s["mla_attn"][1] / kt_s["mla_attn"][0]
+        t_roof = roof_time(s_byt, s_fl, peaks)
+        extra[name] = {"tokens": s_tok, "attn_us": us, "bytes": s_byt, "flops": s_fl,
+                       "hbm_gbs": s_byt / (us * 1e-6) / 1e9, "tflops": s_fl / (us * 1e-6) / 1e12,
+                       "bound": "hbm" if s_byt / (peaks["hbm_gbs"] * 1e9) >= s_fl / (peaks["bf16_tflops"] * 1e12)
+                       else "tensor", "roofline_frac": t_roof / (us * 1e-6),
+                       "tensor_frac": s_fl / (us * 1e-6) / 1e12 / peaks["bf16_tflops"]}
+        del sub, gs, ws_s, out_s
+    if cpu_secs > 0:
+        extra["cpu_baseline"] = cpu_baseline_mla(m, cpu_secs)
+    report("mla_deepseek_v3", tok, byt, fl, ms, kt, extra)
     del m, g, out, ws
     torch.cuda.empty_cache()
 
 
-def _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report):
+def _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report, cpu_secs=0.0):
     s = workloads.dsa_sparse_ragged(mode=mode)
     tok, byt, fl = sparse_ragged_accounting(s)
     g = s.to(dev)
@@ -692,12 +770,16 @@ def _variant_sparse_ragged(dev, api, workloads, mode, steps, warm, world, report
                                                workspace=ws, **s.options())
 
     ms, kt = time_steps(call, max(3, steps // 2), warm, world, timer=True)
-    report(f"dsa_sparse_ragged_{mode}", tok, byt, fl, ms, kt)
+    extra = None
+    if cpu_secs > 0:
+        extra = {"cpu_baseline": cpu_baseline_sparse_ragged(
+            s, cpu_secs, f"the packed-ragged DSA batch ({mode}-level selection, self-write included)")}
+    report(f"dsa_sparse_ragged_{mode}", tok, byt, fl, ms, kt, extra)
     del s, g, out, ws
     torch.cuda.empty_cache()
 
 
-def _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report):
+def _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report, cpu_secs=0.0):
     s = workloads.dsa_sparse(mode=mode, phase=phase)
     tok, byt, fl = sparse_accounting(s)
     g = s.to(dev)
@@ -708,7 +790,10 @@ def _variant_sparse(dev, api, workloads, phase, mode, steps, warm, world, report
     ms, kt = time_steps(lambda: api.sparse_mla_forward(g.q, g.cache, g.indices, g.positions, g.page_table,
                                                        out=out, workspace=ws, **s.options()),
                         steps if phase == "decode" else max(3, steps // 4), warm, world, timer=True)
-    report(f"dsa_sparse_{phase}_{mode}", tok, byt, fl, ms, kt)
+    extra = None
+    if cpu_secs > 0:
+        extra = {"cpu_baseline": cpu_baseline_sparse(s, cpu_secs, f"the DSA {phase} batch ({mode}-level selection)")}
+    report(f"dsa_sparse_{phase}_{mode}", tok, byt, fl, ms, kt, extra)
     del s, g, out, ws
     torch.cuda.empty_cache()
 

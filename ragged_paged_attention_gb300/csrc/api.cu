@@ -50,6 +50,9 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 float resolve_mask(float m) { return isnan(m) ? -0.7f * 3.402823466e38f : m; }
+// A mask value above -1e30 leaves masked keys real weight (exp(s + mask - m) does not underflow
+// for the logits attention sees), so the kernels then take every key and apply it literally.
+bool mild_mask(float m) { return resolve_mask(m) > -1e30f; }
 
 // ---------------------------- RPA ----------------------------------------
 struct RpaLayout {
@@ -76,8 +79,7 @@ int check_rpa_params(const rpa_params* p) {
     if (p->sliding_window < 0) return fail(RPA_ERR_VALUE, "sliding_window must be positive (0 = none)");
     if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
     if (!isfinite(p->k_scale) || !isfinite(p->v_scale)) return fail(RPA_ERR_VALUE, "k_scale/v_scale must be finite");
-    if (resolve_mask(p->mask_value) > -1e30f)
-        return fail(RPA_ERR_UNSUPPORTED, "mask_value %g > -1e30: masked keys would carry weight", p->mask_value);
+    if (isinf(p->mask_value) && p->mask_value > 0.f) return fail(RPA_ERR_VALUE, "mask_value must not be +inf");
     if ((long long)p->max_num_seqs * p->pages_per_seq > INT32_MAX) return fail(RPA_ERR_SHAPE, "page table too large");
     return RPA_OK;
 }
@@ -137,8 +139,7 @@ int check_mla_params(const mla_params* p) {
     if (!isfinite(p->sm_scale)) return fail(RPA_ERR_VALUE, "sm_scale must be finite");
     if (p->sliding_window < 0) return fail(RPA_ERR_VALUE, "sliding_window must be positive (0 = none)");
     if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
-    if (resolve_mask(p->mask_value) > -1e30f)
-        return fail(RPA_ERR_UNSUPPORTED, "mask_value %g > -1e30: masked keys would carry weight", p->mask_value);
+    if (isinf(p->mask_value) && p->mask_value > 0.f) return fail(RPA_ERR_VALUE, "mask_value must not be +inf");
     if ((long long)p->max_num_seqs * p->pages_per_seq > INT32_MAX) return fail(RPA_ERR_SHAPE, "page table too large");
     return RPA_OK;
 }
@@ -294,6 +295,8 @@ static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages,
     a.sm_scale = p->sm_scale;
     a.soft_cap = p->soft_cap;
     a.sliding_window = p->sliding_window;
+    a.mask_mild = mild_mask(p->mask_value) ? 1 : 0;
+    a.mask_value = resolve_mask(p->mask_value);
     a.has_scale = p->k_scale != 0.f || p->v_scale != 0.f;
     a.k_scale_or_one = p->k_scale != 0.f ? p->k_scale : 1.f;
     a.v_scale_or_one = p->v_scale != 0.f ? p->v_scale : 1.f;
@@ -480,6 +483,8 @@ int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, 
     a.sm_scale = p->sm_scale;
     a.soft_cap = p->soft_cap;
     a.sliding_window = p->sliding_window;
+    a.mask_mild = mild_mask(p->mask_value) ? 1 : 0;
+    a.mask_value = resolve_mask(p->mask_value);
     a.ql_nope = static_cast<const __nv_bfloat16*>(ql_nope);
     a.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
     a.cache_kv_c = static_cast<const __nv_bfloat16*>(cache_kv_c);
@@ -494,6 +499,7 @@ int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, 
     a.lkv_pad = p->lkv_dim_pad;
     a.r_pad = p->r_dim_pad;
     a.out_bf16 = static_cast<__nv_bfloat16*>(out);
+    a.target_items = sms;
     a.total_num_pages = p->total_num_pages;
     a.page_size = p->page_size;
     a.hdr = reinterpret_cast<WsHeader*>(ws);

@@ -94,6 +94,11 @@ struct RpaArgs {
     int kv_int8;
     float sm_scale, soft_cap;
     int sliding_window;
+    // a mask_value that leaves masked keys real weight (above -1e30): every key of a sequence
+    // takes part, a masked one with mask_value added to its logit (the RPA reference's form);
+    // otherwise masked keys are skipped (their weight is exactly zero either way)
+    int mask_mild;
+    float mask_value;
     int has_scale;              // k_scale or v_scale given
     float k_scale_or_one, v_scale_or_one;
     int decode_per_sm;          // decode CTAs resident per SM (occupancy of the chosen kernel)
@@ -133,6 +138,10 @@ constexpr int kLatBK = 64;        // keys per block
 constexpr int kLatDk = 576;       // 512 latent + 64 rope
 constexpr int kLatDv = 512;
 constexpr int kLatMinChunk = 512;
+// most items the MLA plan aims for (the workspace bound); it aims for two per SM (one per CTA of
+// each two-CTA cluster, twice over): a split costs its partial O and a merge, and a decode batch
+// split finer spends more on those than it gains in balance (64 decode queries: 1104 us at up to
+// 512 items, measured)
 constexpr int kLatTargetCtas = 512;
 // sparse MLA splits a query's selected keys only down to about this many items in all (half
 // the two-CTA clusters): its per-item cost (Q slice, pipeline fill, fp32 partial and merge)
@@ -145,6 +154,10 @@ struct LatentArgs {
     int num_heads;
     float sm_scale, soft_cap;
     int sliding_window;
+    // mask_value above -1e30: every key of a sequence takes part and a masked logit is replaced
+    // by mask_value (the MLA reference's form); otherwise masked keys are skipped
+    int mask_mild;
+    float mask_value;
     // MLA
     const __nv_bfloat16* ql_nope;   // [T, H, 512]
     const __nv_bfloat16* q_pe;      // [T, H, 64]
@@ -155,6 +168,7 @@ struct LatentArgs {
     const int32_t* cu_q_lens;
     const int32_t* distribution;
     int max_num_tokens, max_num_seqs, pages_per_seq, lkv_pad, r_pad;
+    int target_items;               // MLA plan: about this many items in all (<= kLatTargetCtas)
     __nv_bfloat16* out_bf16;        // [T, H, 512]
     // sparse
     const __nv_bfloat16* q;         // [B, S, H, 576]
@@ -292,7 +306,7 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu, int num, int t) {
 
 // First key any query of a decode-class sequence can see (aligned down to a stage).
 __device__ __forceinline__ int decode_key_begin(const RpaArgs& a, int ql, int kl) {
-    if (a.sliding_window <= 0) return 0;
+    if (a.sliding_window <= 0 || a.mask_mild) return 0;
     const int lo = kl - ql - a.sliding_window + 1;
     return lo <= 0 ? 0 : lo / kDecodeBK * kDecodeBK;
 }

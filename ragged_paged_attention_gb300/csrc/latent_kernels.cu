@@ -116,8 +116,9 @@ __device__ __forceinline__ bool mla_token(const LatentArgs& a, int num, int t, i
         return false;
     }
     const int qpos = kv_len - q_len + (t - q_start);
-    khi = qpos + 1;
-    klo = a.sliding_window > 0 ? max(0, qpos - a.sliding_window + 1) : 0;
+    // the causal (windowed) range, or every key of the sequence with a mild mask
+    khi = a.mask_mild ? kv_len : qpos + 1;
+    klo = a.sliding_window > 0 && !a.mask_mild ? max(0, qpos - a.sliding_window + 1) : 0;
     klo = klo / kLatBK * kLatBK;
     return true;
 }
@@ -126,6 +127,8 @@ __device__ __forceinline__ void mla_plan_body(const LatentArgs& a) {
     __shared__ int scan_scratch[40];
     __shared__ long long red[32];
     __shared__ int s_num, s_total, s_chunk, s_bad;
+    constexpr int kLenBuckets = 1024;  // item lengths in 64-key blocks (longer ones share the last)
+    __shared__ int hist[kLenBuckets];
     WsHeader* hdr = a.hdr;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -166,7 +169,8 @@ __device__ __forceinline__ void mla_plan_body(const LatentArgs& a) {
     if (tid == 0) {
         long long w = 0;
         for (int i = 0; i < (int)(blockDim.x >> 5); ++i) w += red[i];
-        long long c = (w + kLatTargetCtas - 1) / kLatTargetCtas;
+        const int tgt = max(1, min(kLatTargetCtas, a.target_items));
+        long long c = (w + tgt - 1) / tgt;
         if (c < kLatMinChunk) c = kLatMinChunk;
         c = (c + kLatBK - 1) / kLatBK * kLatBK;
         s_chunk = (int)c;
@@ -174,6 +178,31 @@ __device__ __forceinline__ void mla_plan_body(const LatentArgs& a) {
     }
     __syncthreads();
     const int chunk = s_chunk;
+    // Items are listed longest first (a counting sort on their 64-key blocks, kLenBuckets
+    // buckets): the attention kernel takes them from a queue in list order, so the short ones
+    // fill in at the end. A split group keeps its partials at its group slots (split 0's
+    // running index in token order plus the split), whatever the items' places in the list.
+    auto bucket = [&](int len) { return kLenBuckets - 1 - min(kLenBuckets - 1, (len + kLatBK - 1) / kLatBK); };
+    for (int i = tid; i < kLenBuckets; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int t0 = 0; t0 < total; t0 += blockDim.x) {
+        const int t = t0 + tid;
+        int s = 0, klo = 0, khi = 0;
+        if (t < total && mla_token(a, num, t, s, klo, khi)) {
+            const int nsplit = cdiv(khi - klo, chunk);
+            for (int i = 0; i < nsplit; ++i)
+                atomicAdd(&hist[bucket(min(khi, klo + (i + 1) * chunk) - (klo + i * chunk))], tiles);
+        }
+    }
+    __syncthreads();
+    {
+        // exclusive offsets of the buckets (one thread per bucket: the plan runs 1024 threads)
+        int tot;
+        const int v = tid < kLenBuckets ? hist[tid] : 0;
+        const int o = block_exclusive_scan(v, scan_scratch, &tot);
+        if (tid < kLenBuckets) hist[tid] = o;
+        __syncthreads();
+    }
     int base = 0;
     for (int t0 = 0; t0 < total; t0 += blockDim.x) {
         const int t = t0 + tid;
@@ -183,8 +212,8 @@ __device__ __forceinline__ void mla_plan_body(const LatentArgs& a) {
         const int off = block_exclusive_scan(nsplit * tiles, scan_scratch, &tot) + base;
         for (int h = 0; h < tiles && nsplit; ++h) {
             for (int i = 0; i < nsplit; ++i) {
-                const int it = off + h * nsplit + i;
-                if (it >= a.max_items) break;
+                const int g = off + h * nsplit + i;  // group slot of this split
+                if (g >= a.max_items) break;
                 WorkItem w;
                 w.seq = s;
                 w.head = h * kLatRows;
@@ -194,9 +223,10 @@ __device__ __forceinline__ void mla_plan_body(const LatentArgs& a) {
                 w.first_item = off + h * nsplit;
                 w.num_splits = nsplit;
                 w.split = i;
-                a.items[it] = w;
-                a.tickets[2 * it] = 0;  // one ticket per CTA rank of the cluster pair
-                a.tickets[2 * it + 1] = 0;
+                const int it = atomicAdd(&hist[bucket(w.key_end - w.key_begin)], 1);  // place in the list
+                if (it < a.max_items) a.items[it] = w;
+                a.tickets[2 * g] = 0;  // one ticket per CTA rank of the cluster pair
+                a.tickets[2 * g + 1] = 0;
             }
         }
         base += tot;

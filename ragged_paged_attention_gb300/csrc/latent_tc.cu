@@ -49,12 +49,12 @@ constexpr int kOffSRecv = kOffKV + NS * kStage;    // [2]
 constexpr int kOffPRecv = kOffSRecv + 2 * kSRecv;  // [2]
 constexpr int kOffStat = kOffPRecv + 2 * kPRecv;   // (m, l) of the peer's rows
 constexpr int kOffBar = kOffStat + 64 * 8;
-constexpr int kNumBars = 3 * NS + 20;
+constexpr int kNumBars = 3 * NS + 24;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;
 constexpr int kOffVld = kOffRed + 2 * 2 * 128 * 4;
 constexpr int kOffItem = kOffVld + NS * BK;
-constexpr int kSmem = kOffItem + 48;
+constexpr int kSmem = kOffItem + 64;  // item, abort flag, item index, index ring [2], merge flag
 // TMEM columns: S [128 x 64] fp32 at 0, the Q slice (bf16 pairs, 160 or 128 columns) at 64,
 // P [128 x 64] bf16 pairs at 224, the O half [128 x 256] fp32 at 256.
 constexpr int kColS = 0, kColQ = BK, kColP = 224, kColO = 256;
@@ -94,11 +94,14 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     uint64_t* precv_used = bars + 3 * NS + 15;  // [2] my helper threads have read it
     uint64_t* p_free = bars + 3 * NS + 17;      // [2] the peer has read the P buffer I write next
     uint64_t* stat_full = bars + 3 * NS + 19;   // (m, l) of the peer's rows landed (bytes)
+    uint64_t* itm_full = bars + 3 * NS + 20;    // [2] (MLA, rank 1) the item index from rank 0 landed
+    uint64_t* itm_free = bars + 3 * NS + 22;    // [2] (MLA, rank 0) rank 1 has read that slot's index
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     uint8_t* vld = smem + kOffVld;
     WorkItem& s_item = *reinterpret_cast<WorkItem*>(smem + kOffItem);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + kOffItem + 32);
+    volatile int* s_itm = reinterpret_cast<volatile int*>(smem + kOffItem + 40);  // [2] item index slots
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
@@ -134,6 +137,10 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             mbar_init(&p_free[i], 1);
         }
         mbar_init(stat_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&itm_full[i], 1);  // rank 1 arms the 4 bytes rank 0's st.async delivers
+            mbar_init(&itm_free[i], 1);  // rank 1's release arrive
+        }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -153,27 +160,66 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     }
     const int n_items = SPARSE ? sparse_items : hdr->num_items[2];
     uint32_t jb = 0, items = 0, nstat = 0;
-    for (int it = (int)cluster_id_x(); it < n_items; it += (int)cluster_count_x()) {
+    // Sparse items are dealt round-robin to the clusters (every query selects the same number of
+    // units). MLA items differ in length, so they are taken from a queue that the plan sorted
+    // longest first: rank 0 of a cluster takes the next index and hands it to rank 1 through that
+    // CTA's shared memory (st.async on a two-slot ring, bounded waits on both sides), so both
+    // CTAs work the same item.
+    const uint32_t itm_slot_peer = mapa_shared(smem_u32((const void*)s_itm), peer);
+    const uint32_t itm_full_peer = mapa_shared(smem_u32(itm_full), peer);
+    const uint32_t itm_free_peer = mapa_shared(smem_u32(itm_free), peer);
+    for (uint32_t k = 0;; ++k) {
+        volatile int& s_it = *reinterpret_cast<volatile int*>(smem + kOffItem + 36);
         if (tid == 0) {
-            WorkItem w;
+            int it;
             if (SPARSE) {
-                const int per_q = tiles * a.sparse_splits;
-                const int bs = it / per_q, rem = it % per_q;
-                const int tile = rem / a.sparse_splits, sp = rem % a.sparse_splits;
-                w.seq = bs;
-                w.head = tile * 128;
-                w.row_begin = 0;
-                w.key_begin = sp * sparse_chunk;
-                w.key_end = min(slots, (sp + 1) * sparse_chunk);
-                w.first_item = it - sp;
-                w.num_splits = a.sparse_splits;
-                w.split = sp;
+                it = (int)cluster_id_x() + (int)k * (int)cluster_count_x();
             } else {
-                w = a.items[it];
+                const uint32_t sl = k & 1, ph = (k >> 1) & 1;
+                if (rank == 0) {
+                    it = n_items;
+                    if (mbar_wait_cluster(&itm_free[sl], ph ^ 1, err)) {  // rank 1 has read index k - 2
+                        const int q = atomicAdd(&hdr->next_item[2], 1);
+                        it = q < n_items ? q : n_items;
+                    } else {
+                        s_abort = 1;
+                    }
+                    st_async_f32(itm_slot_peer + sl * 4, __int_as_float(it), itm_full_peer + sl * 8);
+                } else {
+                    mbar_arrive_expect_tx(&itm_full[sl], 4);
+                    if (mbar_wait_cluster(&itm_full[sl], ph, err)) {
+                        it = s_itm[sl];
+                        mbar_arrive_cluster(itm_free_peer + sl * 8);
+                    } else {
+                        it = n_items;
+                        s_abort = 1;
+                    }
+                }
             }
-            s_item = w;
+            s_it = it;
+            if (it < n_items) {
+                WorkItem w;
+                if (SPARSE) {
+                    const int per_q = tiles * a.sparse_splits;
+                    const int bs = it / per_q, rem = it % per_q;
+                    const int tile = rem / a.sparse_splits, sp = rem % a.sparse_splits;
+                    w.seq = bs;
+                    w.head = tile * 128;
+                    w.row_begin = 0;
+                    w.key_begin = sp * sparse_chunk;
+                    w.key_end = min(slots, (sp + 1) * sparse_chunk);
+                    w.first_item = it - sp;
+                    w.num_splits = a.sparse_splits;
+                    w.split = sp;
+                } else {
+                    w = a.items[it];
+                }
+                s_item = w;
+            }
         }
         __syncthreads();
+        const int it = s_it;
+        if (it >= n_items) break;
         const WorkItem w = s_item;
         if (s_abort) break;
         const int h0 = w.head;
@@ -687,11 +733,14 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         const uint8_t* vb = vld + st * BK + half * 32;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) x[i] = vb[i] ? x[i] : -INFINITY;
-                    } else if (!(key0 >= wlo && key0 + 31 < ke)) {
+                    } else if (!(key0 >= wlo && key0 + 31 <= qpos && key0 + 31 < ke)) {
+                        // a mild mask replaces a masked logit of a key in the range by mask_value
+                        const float mrep = a.mask_value * kLog2e;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int key = key0 + i;
-                            x[i] = (key < ke && key >= wlo) ? x[i] : -INFINITY;
+                            const bool vis = key <= qpos && key >= wlo;
+                            x[i] = key < ke ? (vis ? x[i] : a.mask_mild ? mrep : -INFINITY) : -INFINITY;
                         }
                     }
                     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -790,7 +839,9 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     }
                 } else {
                     // split: unnormalised O half + (m, l) to the workspace
-                    float* po = a.partial_o + ((size_t)it * 128 + r) * kLatDv + col0;
+                    // partials live at the group's slot (split 0's index plus the split)
+                    const size_t pslot = (size_t)w.first_item + w.split;
+                    float* po = a.partial_o + (pslot * 128 + r) * kLatDv + col0;
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         float o32[32];
@@ -800,8 +851,8 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         for (int i = 0; i < 8; ++i) d4[i] = make_float4(o32[4 * i], o32[4 * i + 1], o32[4 * i + 2], o32[4 * i + 3]);
                     }
                     if (half == 0) {
-                        a.partial_ml[((size_t)it * 128 + r) * 2] = m_use;
-                        a.partial_ml[((size_t)it * 128 + r) * 2 + 1] = l_run;
+                        a.partial_ml[(pslot * 128 + r) * 2] = m_use;
+                        a.partial_ml[(pslot * 128 + r) * 2 + 1] = l_run;
                     }
                 }
             } else {
@@ -816,46 +867,71 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
         tc_fence_after();
         if (w.num_splits > 1 && !s_abort) {
             // the last CTA of this rank to finish a split group merges the group's halves
-            volatile int& s_last = *reinterpret_cast<volatile int*>(smem + kOffItem + 36);
+            volatile int& s_last = *reinterpret_cast<volatile int*>(smem + kOffItem + 48);
             __threadfence();
             __syncthreads();
             if (tid == 0) s_last = atomicAdd(&a.tickets[w.first_item * 2 + rank], 1) == w.num_splits - 1;
             __syncthreads();
             if (s_last) {
                 __threadfence();
-                if (warp < 8) {
-                    const int r = (warp & 3) * 32 + lane, half = warp >> 2;
-                    const int col0 = (int)rank * 256 + half * 128;
+                // merge: a warp per row at a time; each lane holds one split's (m, l) and two
+                // float4 of this rank's 256 output columns (loads of a row are contiguous), and
+                // four splits' loads are in flight at once
+                const int ns = w.num_splits;
+                const size_t ib = (size_t)w.first_item * 128;
+                const int cbase = (int)rank * 256 + lane * 4;
+                for (int rr = warp; rr < 128; rr += lat::kWarps) {
+                    if (h0 + rr >= H) continue;
                     float M = -INFINITY;
-                    for (int sp = 0; sp < w.num_splits; ++sp)
-                        M = fmaxf(M, __ldcg(a.partial_ml + ((size_t)(w.first_item + sp) * 128 + r) * 2));
+                    for (int s0 = lane; s0 < ns; s0 += 32) M = fmaxf(M, __ldcg(a.partial_ml + ((ib + (size_t)s0 * 128 + rr) * 2)));
+                    M = warp_max(M);
                     const float Mu = M == -INFINITY ? 0.f : M;
                     float L = 0.f;
-                    for (int sp = 0; sp < w.num_splits; ++sp) {
-                        const size_t base = ((size_t)(w.first_item + sp) * 128 + r) * 2;
+                    for (int s0 = lane; s0 < ns; s0 += 32) {
+                        const size_t base = (ib + (size_t)s0 * 128 + rr) * 2;
                         L += fast_exp2(__ldcg(a.partial_ml + base) - Mu) * __ldcg(a.partial_ml + base + 1);
                     }
+                    L = warp_sum(L);
                     const float inv = L > 0.f ? 1.f / L : 0.f;
-                    if (h0 + r < H) {
-                        for (int c4 = 0; c4 < 32; ++c4) {
-                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int sp = 0; sp < w.num_splits; ++sp) {
-                                const size_t base = (size_t)(w.first_item + sp) * 128 + r;
-                                const float f = fast_exp2(__ldcg(a.partial_ml + base * 2) - Mu);
-                                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.partial_o + base * kLatDv + col0 + c4 * 4));
-                                acc.x += f * v.x;
-                                acc.y += f * v.y;
-                                acc.z += f * v.z;
-                                acc.w += f * v.w;
+                    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+                    for (int s0 = 0; s0 < ns; s0 += 32) {
+                        // lane l: the factor of split s0 + l
+                        const int sl = s0 + lane;
+                        const float fl = sl < ns ? fast_exp2(__ldcg(a.partial_ml + (ib + (size_t)sl * 128 + rr) * 2) - Mu) * inv : 0.f;
+                        const int cnt = min(32, ns - s0);
+                        for (int j = 0; j < cnt; j += 4) {
+                            float4 v[8];
+                            float f[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                f[u] = __shfl_sync(0xffffffffu, fl, (j + u) & 31);
+                                const bool in = j + u < cnt;
+                                const float* po = a.partial_o + (ib + (size_t)(s0 + j + u) * 128 + rr) * kLatDv + cbase;
+                                v[2 * u] = in ? __ldcg(reinterpret_cast<const float4*>(po)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                v[2 * u + 1] = in ? __ldcg(reinterpret_cast<const float4*>(po + 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (!in) f[u] = 0.f;
                             }
-                            if (SPARSE) {
-                                *reinterpret_cast<float4*>(a.out_f32 + ((size_t)w.seq * H + h0 + r) * kLatDv + col0 + c4 * 4) =
-                                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                            } else {
-                                *reinterpret_cast<uint2*>(a.out_bf16 + ((size_t)t * H + h0 + r) * kLatDv + col0 + c4 * 4) =
-                                    make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                acc0.x += f[u] * v[2 * u].x;
+                                acc0.y += f[u] * v[2 * u].y;
+                                acc0.z += f[u] * v[2 * u].z;
+                                acc0.w += f[u] * v[2 * u].w;
+                                acc1.x += f[u] * v[2 * u + 1].x;
+                                acc1.y += f[u] * v[2 * u + 1].y;
+                                acc1.z += f[u] * v[2 * u + 1].z;
+                                acc1.w += f[u] * v[2 * u + 1].w;
                             }
                         }
+                    }
+                    if (SPARSE) {
+                        float* o = a.out_f32 + ((size_t)w.seq * H + h0 + rr) * kLatDv + cbase;
+                        *reinterpret_cast<float4*>(o) = acc0;
+                        *reinterpret_cast<float4*>(o + 128) = acc1;
+                    } else {
+                        __nv_bfloat16* o = a.out_bf16 + ((size_t)t * H + h0 + rr) * kLatDv + cbase;
+                        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16(acc0.x, acc0.y), pack_bf16(acc0.z, acc0.w));
+                        *reinterpret_cast<uint2*>(o + 128) = make_uint2(pack_bf16(acc1.x, acc1.y), pack_bf16(acc1.z, acc1.w));
                     }
                 }
                 if (tid == 0) a.tickets[w.first_item * 2 + rank] = 0;

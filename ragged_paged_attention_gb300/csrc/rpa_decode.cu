@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_
                         if (cap != 0.f) x = soft_cap(x, cap, cap_k2);
                         x *= kLog2e;
                         const bool ok = key <= qpos[j] && key >= wlo[j] && key < ke;
-                        x = ok ? x : -INFINITY;
+                        // a mild mask adds mask_value to a masked logit of a key in the range
+                        x = ok ? x : (a.mask_mild && key < ke) ? x + a.mask_value * kLog2e : -INFINITY;
                         sc[e] = x;
                         mx[j] = fmaxf(mx[j], x);
                     }

@@ -341,9 +341,10 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
         const int R0 = w.row_begin;
         const int R1 = min(n_rows, R0 + 128) - 1;
         const int qmin = kv_len - q_len + R0 / G, qmax = kv_len - q_len + R1 / G;
-        int kb = a.sliding_window > 0 ? max(0, qmin - a.sliding_window + 1) : 0;
+        // keys the tile's rows see: the causal (windowed) range, or every key with a mild mask
+        int kb = a.sliding_window > 0 && !a.mask_mild ? max(0, qmin - a.sliding_window + 1) : 0;
         kb = kb / BK * BK;
-        const int ke = qmax + 1;
+        const int ke = a.mask_mild ? kv_len : qmax + 1;
         const int nb = cdiv(ke - kb, BK);
         const uint32_t iph = items & 1;
 
@@ -901,13 +902,18 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
 #pragma unroll
                     for (int i = 0; i < HB; ++i) x[i] *= c_log2;
                 }
-                // the causal / window mask only matters on blocks crossing a row's limits
+                // the causal / window mask only matters on blocks crossing a row's limits; a mild
+                // mask adds mask_value to a masked logit (in x's units: raw scores when the scale
+                // is folded into the exponent, log2 units otherwise) and only keys past the
+                // sequence are dropped
                 const bool inside = key0 >= wlo && key0 + HB - 1 <= qpos;
                 if (__any_sync(0xffffffffu, !inside)) {
+                    const float madd = fold ? a.mask_value / scale : a.mask_value * kLog2e;
 #pragma unroll
                     for (int i = 0; i < HB; ++i) {
                         const int key = key0 + i;
-                        x[i] = (key <= qpos && key >= wlo) ? x[i] : -INFINITY;
+                        const bool vis = key <= qpos && key >= wlo;
+                        x[i] = vis ? x[i] : (a.mask_mild && key < kv_len) ? x[i] + madd : -INFINITY;
                     }
                 }
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};

@@ -52,7 +52,7 @@ def good_rpa():
 
 @pytest.mark.parametrize("field,value,code", [
     ("num_combined_kv_heads", 3, -2), ("num_q_heads", 5, -2), ("head_dim", 96, -5), ("q_dtype", 2, -3),
-    ("kv_dtype", 3, -3), ("sliding_window", -1, -4), ("soft_cap", math.inf, -4), ("mask_value", -1.0, -5),
+    ("kv_dtype", 3, -3), ("sliding_window", -1, -4), ("soft_cap", math.inf, -4), ("mask_value", math.inf, -4),
     ("version", 7, -4), ("struct_size", 4, -4), ("page_size", 0, -2), ("sm_scale", math.nan, -4),
 ])
 def test_rpa_host_validation(lib, field, value, code):

@@ -59,3 +59,12 @@ def test_mla_update_only_bit_exact():
     torch.cuda.synchronize()
     assert torch.equal(g.cache_kv_c.cpu().view(torch.int16), ckv.view(torch.int16))
     assert torch.equal(g.cache_k_pe.cpu().view(torch.int16), ckpe.view(torch.int16))
+
+
+@pytest.mark.parametrize("mask,sw", [(-1.5, None), (-3.0, 100), (0.25, 40)])
+def test_mla_mild_mask_value_replaces(mask, sw):
+    # The MLA reference replaces a masked logit by mask_value; with a value that leaves masked
+    # keys real weight, each query sees every key of its sequence: its future keys (prefill)
+    # and the keys outside the window at mask_value.
+    m = workloads.make_mla([1, 1, 40, 3], [700, 65, 300, 9], seed=24, max_num_tokens=48)
+    run_and_check(m, mask_value=mask, sliding_window=sw)

@@ -265,3 +265,31 @@ def test_int8_kv(ks, vs, d):
     T = b.num_tokens
     scale = float(ref[:T].abs().max())
     assert max_abs(out[:T], ref[:T]) <= 2e-2 * scale
+
+
+@pytest.mark.parametrize("mask", [-1.5, -4.0, 0.5])
+@pytest.mark.parametrize("kind", ["bf16_tma", "fp8_raw", "window_cap", "int8_decode_rows"])
+def test_mild_mask_value_is_added(mask, kind):
+    # The RPA reference adds mask_value to a masked logit. With a value that leaves masked keys
+    # real weight, every key of a sequence takes part: the future keys of a chunk's queries and
+    # the keys outside the window, each with mask_value added after the scale and the soft cap.
+    # Decode rows (q_len * G <= 16, including two-row decode items) and prefill tiles; the bf16
+    # TMA path, the fp8 raw-staging path and the int8 register path.
+    if kind == "bf16_tma":
+        b = workloads.make_rpa([1, 1, 9, 40], [300, 33, 120, 200], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                               page_size=16, seed=41)
+        tol = TOL_BF16
+    elif kind == "fp8_raw":
+        b = workloads.make_rpa([1, 70, 1, 130], [500, 300, 90, 260], num_q_heads=16, num_kv_heads=8, head_dim=256,
+                               page_size=32, seed=42, kv_dtype=torch.float8_e4m3fn, k_scale=0.5, v_scale=0.5)
+        tol = TOL_FP8
+    elif kind == "window_cap":
+        b = workloads.make_rpa([1, 5, 33, 1], [400, 64, 150, 7], num_q_heads=8, num_kv_heads=4, head_dim=128,
+                               page_size=16, seed=43, sliding_window=50, soft_cap=30.0)
+        tol = TOL_BF16
+    else:
+        b = workloads.make_rpa([2, 3, 1, 20], [40, 90, 700, 64], num_q_heads=16, num_kv_heads=4, head_dim=128,
+                               page_size=16, seed=44, kv_dtype=torch.int8, k_scale=1 / 64, v_scale=1 / 64,
+                               sliding_window=30)
+        tol = TOL_BF16
+    check(b, tol, mask_value=mask)
