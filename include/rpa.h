@@ -90,6 +90,14 @@ typedef enum {
 #define RPA_DEV_ERR_TOKENS     0x10u  /* cu_q_lens[num_seqs] > max_num_tokens or not monotone */
 #define RPA_DEV_ERR_POSITION   0x20u  /* sparse: query position outside [0, seq_len) */
 #define RPA_DEV_ERR_TIMEOUT    0x40u  /* a pipeline wait gave up after its time limit (2 s) */
+#define RPA_DEV_ERR_BATCH_KIND 0x80u  /* a sequence of the class rpa_params.batch_kind excludes */
+
+/* rpa_params.batch_kind: what the caller knows of the batch's mix (the MLA v1 page keys its
+ * decode-only, prefill-only and mixed kernels on its `distribution`).  A sequence is decode-class
+ * when q_len * (num_q_heads / num_kv_heads) <= 16, prefill-class otherwise. */
+#define RPA_BATCH_MIXED        0      /* unknown or mixed: every kernel is launched */
+#define RPA_BATCH_DECODE_ONLY  1      /* no prefill-class sequence: the prefill launches are skipped */
+#define RPA_BATCH_PREFILL_ONLY 2      /* no decode-class sequence: the decode launch is skipped */
 
 /* CUDA stream handle (ABI-compatible with cudaStream_t). */
 typedef struct CUstream_st* rpa_stream_t;
@@ -136,6 +144,10 @@ typedef struct {
     float mask_value;            /* NaN = default */
     float k_scale;               /* 0 = none */
     float v_scale;               /* 0 = none */
+    /* RPA_BATCH_*; a sequence the hint excludes is skipped (its rows are not written) and sets
+     * RPA_DEV_ERR_BATCH_KIND.  Optional: a struct_size that ends before this field means
+     * RPA_BATCH_MIXED. */
+    int32_t batch_kind;
 } rpa_params;
 
 /* Bytes of workspace rpa_forward needs for these maxima. */

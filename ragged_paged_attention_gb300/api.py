@@ -51,7 +51,10 @@ class rpa_params(ctypes.Structure):
                 ("max_num_seqs", ctypes.c_int32), ("pages_per_seq", ctypes.c_int32),
                 ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("sm_scale", ctypes.c_float),
                 ("sliding_window", ctypes.c_int32), ("soft_cap", ctypes.c_float), ("mask_value", ctypes.c_float),
-                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float), ("batch_kind", ctypes.c_int32)]
+
+
+BATCH_MIXED, BATCH_DECODE_ONLY, BATCH_PREFILL_ONLY = 0, 1, 2
 
 
 class mla_params(ctypes.Structure):
@@ -181,7 +184,7 @@ def _kv_code(dtype) -> int:
 
 
 def make_rpa_params(q, kv_pages, page_indices, *, sm_scale=1.0, sliding_window=None, soft_cap=None,
-                    mask_value=None, k_scale=None, v_scale=None) -> rpa_params:
+                    mask_value=None, k_scale=None, v_scale=None, batch_kind=BATCH_MIXED) -> rpa_params:
     P, ps, C, D = kv_pages.shape
     max_num_seqs, pps = page_indices.shape
     return rpa_params(
@@ -190,7 +193,7 @@ def make_rpa_params(q, kv_pages, page_indices, *, sm_scale=1.0, sliding_window=N
         max_num_seqs=max_num_seqs, pages_per_seq=pps, q_dtype=BF16, kv_dtype=_kv_code(kv_pages.dtype),
         sm_scale=float(sm_scale), sliding_window=int(_opt(sliding_window, 0)), soft_cap=float(_opt(soft_cap)),
         mask_value=math.nan if mask_value is None else float(mask_value), k_scale=float(_opt(k_scale)),
-        v_scale=float(_opt(v_scale)))
+        v_scale=float(_opt(v_scale)), batch_kind=int(batch_kind))
 
 
 def rpa_workspace_size(params: rpa_params) -> int:
@@ -201,8 +204,10 @@ def rpa_workspace_size(params: rpa_params) -> int:
 
 
 def rpa_forward(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_scale=1.0, sliding_window=None,
-                soft_cap=None, mask_value=None, k_scale=None, v_scale=None, out=None, workspace=None):
-    """Ragged paged attention; returns ``out`` [max_num_tokens, Hq, D] bf16."""
+                soft_cap=None, mask_value=None, k_scale=None, v_scale=None, out=None, workspace=None,
+                batch_kind=BATCH_MIXED):
+    """Ragged paged attention; returns ``out`` [max_num_tokens, Hq, D] bf16.  ``batch_kind``
+    (BATCH_DECODE_ONLY / BATCH_PREFILL_ONLY) lets the library skip the other class's launches."""
     lib = load_library()
     _dev(q, "q", torch.bfloat16)
     _dev(kv_pages, "kv_pages")
@@ -210,7 +215,8 @@ def rpa_forward(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_s
                  ("num_seqs", num_seqs)):
         _dev(t, n, torch.int32)
     prm = make_rpa_params(q, kv_pages, page_indices, sm_scale=sm_scale, sliding_window=sliding_window,
-                          soft_cap=soft_cap, mask_value=mask_value, k_scale=k_scale, v_scale=v_scale)
+                          soft_cap=soft_cap, mask_value=mask_value, k_scale=k_scale, v_scale=v_scale,
+                          batch_kind=batch_kind)
     if kv_lens.numel() != prm.max_num_seqs or cu_q_lens.numel() != prm.max_num_seqs + 1 or num_seqs.numel() != 1:
         raise ValueError("kv_lens must be [max_num_seqs], cu_q_lens [max_num_seqs + 1], num_seqs [1]")
     if kv_pages.shape[-1] != q.shape[-1]:
@@ -297,7 +303,7 @@ def rpa_update_kv_cache(new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens
 
 def rpa_forward_update(q, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_scale=1.0,
                        sliding_window=None, soft_cap=None, mask_value=None, k_scale=None, v_scale=None, out=None,
-                       workspace=None):
+                       workspace=None, batch_kind=BATCH_MIXED):
     """rpa_update_kv_cache then rpa_forward in one call (the cache write shares the plan's
     launch); writes ``kv_pages`` in place and returns ``out``."""
     lib = load_library()
@@ -309,7 +315,8 @@ def rpa_forward_update(q, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_le
                  ("num_seqs", num_seqs)):
         _dev(t, n, torch.int32)
     prm = make_rpa_params(q, kv_pages, page_indices, sm_scale=sm_scale, sliding_window=sliding_window,
-                          soft_cap=soft_cap, mask_value=mask_value, k_scale=k_scale, v_scale=v_scale)
+                          soft_cap=soft_cap, mask_value=mask_value, k_scale=k_scale, v_scale=v_scale,
+                          batch_kind=batch_kind)
     if kv_lens.numel() != prm.max_num_seqs or cu_q_lens.numel() != prm.max_num_seqs + 1 or num_seqs.numel() != 1:
         raise ValueError("kv_lens must be [max_num_seqs], cu_q_lens [max_num_seqs + 1], num_seqs [1]")
     if kv_pages.shape[-1] != q.shape[-1]:

@@ -55,6 +55,11 @@ float resolve_mask(float m) { return isnan(m) ? -0.7f * 3.402823466e38f : m; }
 bool mild_mask(float m) { return resolve_mask(m) > -1e30f; }
 
 // ---------------------------- RPA ----------------------------------------
+// batch_kind, or RPA_BATCH_MIXED when the caller's struct ends before it
+int rpa_batch_kind(const rpa_params* p) {
+    return p->struct_size >= offsetof(rpa_params, batch_kind) + sizeof(int32_t) ? p->batch_kind : RPA_BATCH_MIXED;
+}
+
 struct RpaLayout {
     size_t items_dec, items_pre, tickets, cta_first, pml, po, total;
     int max_dec, max_pre;
@@ -62,7 +67,9 @@ struct RpaLayout {
 
 int check_rpa_params(const rpa_params* p) {
     if (!p) return fail(RPA_ERR_NULL, "params is NULL");
-    if (p->struct_size < sizeof(rpa_params)) return fail(RPA_ERR_VALUE, "rpa_params.struct_size too small");
+    if (p->struct_size < offsetof(rpa_params, batch_kind)) return fail(RPA_ERR_VALUE, "rpa_params.struct_size too small");
+    if (rpa_batch_kind(p) < RPA_BATCH_MIXED || rpa_batch_kind(p) > RPA_BATCH_PREFILL_ONLY)
+        return fail(RPA_ERR_VALUE, "batch_kind %d is not an RPA_BATCH_* value", rpa_batch_kind(p));
     if (p->version != RPA_ABI_VERSION) return fail(RPA_ERR_VALUE, "rpa_params.version %u != %d", p->version, RPA_ABI_VERSION);
     if (p->max_num_tokens <= 0 || p->num_q_heads <= 0 || p->num_combined_kv_heads <= 0 || p->total_num_pages <= 0 ||
         p->page_size <= 0 || p->max_num_seqs <= 0 || p->pages_per_seq <= 0)
@@ -297,6 +304,7 @@ static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages,
     a.sliding_window = p->sliding_window;
     a.mask_mild = mild_mask(p->mask_value) ? 1 : 0;
     a.mask_value = resolve_mask(p->mask_value);
+    a.batch_kind = rpa_batch_kind(p);
     a.has_scale = p->k_scale != 0.f || p->v_scale != 0.f;
     a.k_scale_or_one = p->k_scale != 0.f ? p->k_scale : 1.f;
     a.v_scale_or_one = p->v_scale != 0.f ? p->v_scale : 1.f;

@@ -99,6 +99,7 @@ struct RpaArgs {
     // otherwise masked keys are skipped (their weight is exactly zero either way)
     int mask_mild;
     float mask_value;
+    int batch_kind;             // RPA_BATCH_*: a decode-only or prefill-only batch skips the other launches
     int has_scale;              // k_scale or v_scale given
     float k_scale_or_one, v_scale_or_one;
     int decode_per_sm;          // decode CTAs resident per SM (occupancy of the chosen kernel)
@@ -302,6 +303,12 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu, int num, int t) {
         if (cu[mid] <= t) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// Whether the caller's batch_kind admits a sequence of this class (decode: q_len * G <= 16).
+__device__ __forceinline__ bool kind_allows(const RpaArgs& a, bool decode_class) {
+    return !(a.batch_kind == RPA_BATCH_DECODE_ONLY && !decode_class) &&
+           !(a.batch_kind == RPA_BATCH_PREFILL_ONLY && decode_class);
 }
 
 // First key any query of a decode-class sequence can see (aligned down to a stage).

@@ -74,7 +74,9 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
             c_ql = ql;
             c_kl = kl;
         }
-        if (sok && ql >= 1) {
+        if (sok && ql >= 1 && !kind_allows(a, ql * G <= 16)) {
+            set_error(&a.hdr->error_bits, RPA_DEV_ERR_BATCH_KIND);  // skipped: its launch is not made
+        } else if (sok && ql >= 1) {
             if (ql * G <= 16) {
                 const int klo = decode_key_begin(a, ql, kl);
                 const long long g = (long long)n_groups * cdiv(ql * G, kDecodeRows);
@@ -223,7 +225,7 @@ __device__ __forceinline__ void plan_body(const RpaArgs& a) {
         } else {
             ok = s < num && seq_shape(a, s, ql, kl);
         }
-        if (ok && ql >= 1) {
+        if (ok && ql >= 1 && kind_allows(a, ql * G <= 16)) {
             if (ql * G <= 16) {
                 klo = decode_key_begin(a, ql, kl);
                 nrh = cdiv(ql * G, kDecodeRows);
@@ -477,7 +479,17 @@ cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t stream) {
 // decode started early (programmatic launch) on the rest and finishing after that prefill grid,
 // then the prefill items still queued when decode ran dry, on every SM; otherwise prefill then
 // decode
+// A batch_kind hint drops the launches of the class it excludes: a decode-only batch launches
+// decode alone, a prefill-only batch one prefill grid on every SM, each an ordinary launch behind
+// the plan (it reads the plan's lists at its start, and later work on the stream starts only
+// once it has ended).
 static cudaError_t launch_attention(const RpaArgs& a, int num_sms, cudaStream_t stream) {
+    if (a.batch_kind == RPA_BATCH_DECODE_ONLY) {
+        RpaArgs d = a;
+        d.overlap = 0;
+        return launch_rpa_decode(d, num_sms, stream);
+    }
+    if (a.batch_kind == RPA_BATCH_PREFILL_ONLY) return launch_rpa_prefill(a, num_sms, stream, 2);
     cudaError_t e = launch_rpa_prefill(a, num_sms, stream, 0);
     if (e != cudaSuccess) return e;
     e = launch_rpa_decode(a, num_sms, stream);

@@ -1094,7 +1094,8 @@ static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    ProfScope ps(tail ? "rpa_prefill_tail" : "rpa_prefill_attn", stream);
+    // tail 1: the launch after decode; 2: the only attention launch of a prefill-only batch
+    ProfScope ps(tail == 1 ? "rpa_prefill_tail" : "rpa_prefill_attn", stream);
     return launch_pdl(kern, dim3(num_sms), dim3(prefill_warps<RAW>() * 32), T::kSmem, stream, a.overlap && !tail, a,
                       tkv, tq, box_rows, q_tma, tail);
 }

@@ -107,3 +107,18 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(4, 4, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         api.rpa_forward(q, q, q, q, q, q)
+
+
+def test_batch_kind_is_optional_and_checked(lib):
+    p = good_rpa()
+    n = ctypes.c_size_t(0)
+    p.batch_kind = 3
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == -4
+    p.batch_kind = 2
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    # a caller built against the struct without the field: its struct_size ends before it
+    p.batch_kind = 99
+    p.struct_size = api.rpa_params.batch_kind.offset
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    p.struct_size = api.rpa_params.batch_kind.offset - 4
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == -4

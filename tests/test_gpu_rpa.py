@@ -293,3 +293,60 @@ def test_mild_mask_value_is_added(mask, kind):
                                sliding_window=30)
         tol = TOL_BF16
     check(b, tol, mask_value=mask)
+
+
+def _launches(fn):
+    n0 = api.launch_count()
+    fn()
+    torch.cuda.synchronize()
+    return api.launch_count() - n0
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_batch_kind_hint_skips_the_other_launches(kind):
+    # a batch of one class with the matching hint: the same bits, with the other class's
+    # launches (decode: both prefill grids; prefill: decode and the prefill tail) not made
+    if kind == "decode":
+        b = workloads.make_rpa([1] * 30 + [2], list(range(100, 3100, 100)) + [40], num_q_heads=16, num_kv_heads=4,
+                               head_dim=128, page_size=16, seed=51)
+        hint = api.BATCH_DECODE_ONLY
+    else:
+        b = workloads.make_rpa([200, 37], [900, 300], num_q_heads=16, num_kv_heads=4, head_dim=128, page_size=16,
+                               seed=52)
+        hint = api.BATCH_PREFILL_ONLY
+    g = b.to("cuda")
+    opts = b.options()
+    ref = torch.full_like(g.q, 7.0)
+    n_plain = _launches(lambda: api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens,
+                                                g.num_seqs, out=ref, **opts))
+    out = torch.full_like(g.q, 7.0)
+    ws = torch.zeros(api.rpa_workspace_size(api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)),
+                     dtype=torch.uint8, device="cuda")
+    n_hint = _launches(lambda: api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs,
+                                               out=out, workspace=ws, batch_kind=hint, **opts))
+    assert api.check_device_status(ws) == 0
+    assert n_hint == 2 and n_plain == 4
+    T = b.num_tokens
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    tokens = sample_tokens(b.q_lens)
+    ref64 = oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), tokens=tokens, **opts)
+    assert max_abs(out[tokens], ref64[tokens]) <= TOL_BF16
+    assert (out[T:].float() == 7.0).all()
+
+
+def test_batch_kind_hint_violation_is_reported():
+    # a decode-only hint on a mixed batch: the prefill-class sequence is skipped (its rows stay
+    # unwritten) and reported; the decode rows are computed
+    b = workloads.make_rpa([1, 40, 1], [300, 200, 77], num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                           seed=53)
+    g = b.to("cuda")
+    opts = b.options()
+    ws = torch.zeros(api.rpa_workspace_size(api.make_rpa_params(g.q, g.kv_pages, g.page_indices, **opts)),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.full_like(g.q, 7.0)
+    api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, out=out, workspace=ws,
+                    batch_kind=api.BATCH_DECODE_ONLY, **opts)
+    assert api.check_device_status(ws) & 0x80
+    assert (out[1:41].float() == 7.0).all()
+    ref = oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, 3, tokens=[0, 41], **opts)
+    assert max_abs(out[[0, 41]], ref[[0, 41]]) <= TOL_BF16
