@@ -46,6 +46,7 @@ _lib = None
 BF16 = 1
 E4M3 = 2
 INT8 = 3
+INT4 = 4  # packed two to a byte: a uint8 cache tensor [P, ps, C, D / 2]
 DEFAULT_MASK_VALUE = -0.7 * 3.4028234663852886e38  # -0.7 * float32 max
 
 
@@ -158,6 +159,8 @@ def _load():
         lib.oracle_decode_e4m3.restype = ctypes.c_double
         lib.oracle_decode_int8.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_int8.restype = ctypes.c_double
+        lib.oracle_decode_int4.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_int4.restype = ctypes.c_double
         lib.oracle_round_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.oracle_round_f32_to_bf16.restype = ctypes.c_double
         for f in ("oracle_rpa", "oracle_rpa_update_kv_cache", "oracle_mla_update_kv_cache",
@@ -195,6 +198,8 @@ def _kv_code(dtype: torch.dtype) -> int:
         return E4M3
     if dtype == torch.int8:
         return INT8
+    if dtype == torch.uint8:  # int4 values, two per byte (element 2i in the low nibble of byte i)
+        return INT4
     raise ValueError(f"unsupported kv dtype {dtype}")
 
 
@@ -205,6 +210,8 @@ def _nthreads(n):
 def rpa_params(q, kv_pages, page_indices, *, sm_scale=1.0, sliding_window=None, soft_cap=None,
                mask_value=None, k_scale=None, v_scale=None) -> RpaParams:
     P, ps, C, D = kv_pages.shape
+    if kv_pages.dtype == torch.uint8:  # int4: two values per byte along the head dimension
+        D *= 2
     max_num_seqs, pps = page_indices.shape
     return RpaParams(
         num_q_heads=q.shape[1], num_combined_kv_heads=C, head_dim=D, total_num_pages=P,
@@ -385,6 +392,10 @@ def decode_e4m3(bits: int) -> float:
 
 def decode_int8(bits: int) -> float:
     return _load().oracle_decode_int8(bits)
+
+
+def decode_int4(nibble: int) -> float:
+    return _load().oracle_decode_int4(nibble)
 
 
 def round_f32_to_bf16(x: float) -> float:

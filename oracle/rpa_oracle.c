@@ -48,6 +48,7 @@
 #define ORACLE_BF16 1
 #define ORACLE_E4M3 2
 #define ORACLE_INT8 3
+#define ORACLE_INT4 4
 
 /* ------------------------------------------------------------------ */
 /* Number formats, decoded from their definitions.                     */
@@ -94,9 +95,19 @@ static float f32_round_to_bf16(float f) {
  * value) or, with a scale, multiplies float32(x) by it like any other KV dtype. */
 static float int8_to_f32(uint8_t b) { return (float)(b < 128 ? (int)b : (int)b - 256); }
 
+/* int4: a two's-complement nibble (values -8 .. 7), two to a byte along the head dimension:
+ * element 2i of a row is the low nibble of the row's byte i, element 2i+1 the high nibble (the
+ * v2 kernel's packed integer loads unpack several values from one word the same way, lowest
+ * bits first).  Like int8 it is promoted exactly, or scaled in float32. */
+static float int4_to_f32(uint8_t nib) { return (float)(nib < 8 ? (int)nib : (int)nib - 16); }
+
 static float load_elem(const void* base, size_t idx, int dtype) {
     if (dtype == ORACLE_E4M3) return e4m3_bits_to_f32(((const uint8_t*)base)[idx]);
     if (dtype == ORACLE_INT8) return int8_to_f32(((const uint8_t*)base)[idx]);
+    if (dtype == ORACLE_INT4) {
+        const uint8_t b = ((const uint8_t*)base)[idx >> 1];
+        return int4_to_f32((idx & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 15));
+    }
     return bf16_bits_to_f32(((const uint16_t*)base)[idx]);
 }
 
@@ -115,6 +126,7 @@ static double rpa_kv_value(const void* base, size_t idx, int dtype, float scale)
 double oracle_decode_bf16(uint16_t bits) { return (double)bf16_bits_to_f32(bits); }
 double oracle_decode_e4m3(uint8_t bits) { return (double)e4m3_bits_to_f32(bits); }
 double oracle_decode_int8(uint8_t bits) { return (double)int8_to_f32(bits); }
+double oracle_decode_int4(uint8_t nibble) { return (double)int4_to_f32((uint8_t)(nibble & 15)); }
 double oracle_round_f32_to_bf16(float f) { return (double)f32_round_to_bf16(f); }
 
 /* ------------------------------------------------------------------ */
@@ -263,7 +275,8 @@ int oracle_rpa_update_kv_cache(const oracle_rpa_params* p, const void* new_k, co
                                const int32_t* cu_q_lens, int32_t num_seqs) {
     if (!p || !new_k || !new_v || !kv_pages) return ORACLE_ERR_ARG;
     const int C = p->num_combined_kv_heads, Hkv = C / 2, D = p->head_dim, ps = p->page_size;
-    const size_t esz = p->kv_dtype == ORACLE_BF16 ? 2 : 1;
+    /* bytes of one head row: D elements of 2, 1 or (int4) 1/2 byte */
+    const size_t rowb = p->kv_dtype == ORACLE_BF16 ? (size_t)D * 2 : p->kv_dtype == ORACLE_INT4 ? (size_t)D / 2 : (size_t)D;
     for (int i = 0; i < num_seqs; ++i) {
         const int q_start = cu_q_lens[i], q_len = cu_q_lens[i + 1] - cu_q_lens[i];
         const int kv_len = kv_lens[i];
@@ -274,10 +287,10 @@ int oracle_rpa_update_kv_cache(const oracle_rpa_params* p, const void* new_k, co
             const int32_t page = page_indices[(size_t)i * p->pages_per_seq + pos / ps];
             if (page < 0 || page >= p->total_num_pages) return ORACLE_ERR_PAGE;
             for (int g = 0; g < Hkv; ++g) {
-                const size_t src = ((size_t)(q_start + j) * Hkv + g) * D * esz;
-                const size_t dk = (((size_t)page * ps + pos % ps) * C + 2 * g) * D * esz;
-                memcpy((char*)kv_pages + dk, (const char*)new_k + src, D * esz);
-                memcpy((char*)kv_pages + dk + D * esz, (const char*)new_v + src, D * esz);
+                const size_t src = ((size_t)(q_start + j) * Hkv + g) * rowb;
+                const size_t dk = (((size_t)page * ps + pos % ps) * C + 2 * g) * rowb;
+                memcpy((char*)kv_pages + dk, (const char*)new_k + src, rowb);
+                memcpy((char*)kv_pages + dk + rowb, (const char*)new_v + src, rowb);
             }
         }
     }

@@ -41,6 +41,9 @@ def _randn(rng: np.random.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
     and filled by a thread pool."""
     if dtype == torch.int8:  # integer caches: uniform over the whole byte
         return torch.from_numpy(rng.integers(-128, 128, size=tuple(shape)).astype(np.int8))
+    if dtype == torch.uint8:  # int4 caches: two uniform nibbles per byte (the last dim is halved)
+        shape = tuple(shape[:-1]) + (shape[-1] // 2,)
+        return torch.from_numpy(rng.integers(0, 256, size=shape).astype(np.uint8))
     n = int(np.prod(shape))
     if n <= _CHUNK:
         x = rng.standard_normal(size=n, dtype=np.float32)
@@ -67,6 +70,8 @@ def _fill_nan(t: torch.Tensor) -> None:
         t.view(torch.uint8).fill_(E4M3_NAN)
     elif t.dtype == torch.int8:  # no NaN: the extreme value, which would show in any output
         t.fill_(127)
+    elif t.dtype == torch.uint8:  # int4 pairs: the largest value in both nibbles
+        t.fill_(0x77)
     else:
         t.fill_(float("nan"))
 

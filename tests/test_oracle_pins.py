@@ -74,17 +74,31 @@ def rand_bf16(rng, shape):
     return bf16(rng.standard_normal(shape))
 
 
+def pack_int4(x):
+    """int values in [-8, 7] [..., D] -> uint8 [..., D / 2]: element 2i in the low nibble of
+    byte i, element 2i+1 in the high nibble (two's complement in each nibble)."""
+    u = (x.to(torch.int16) & 15).to(torch.uint8)
+    return (u[..., 0::2] | (u[..., 1::2] << 4)).contiguous()
+
+
 def ragged_case(rng, q_lens, kv_lens, Hq, Hkv, D, ps, sm_scale=None, sw=None, soft_cap=None,
                 dtype=torch.bfloat16, scale=None, mask_value=MASK):
     if dtype == torch.int8:  # the full two's-complement range
         K_list = [torch.from_numpy(rng.integers(-128, 128, size=(k, Hkv, D)).astype(np.int8)) for k in kv_lens]
         V_list = [torch.from_numpy(rng.integers(-128, 128, size=(k, Hkv, D)).astype(np.int8)) for k in kv_lens]
+    elif dtype == "int4":  # the full 4-bit range, held as int8 values on the dense side
+        K_list = [torch.from_numpy(rng.integers(-8, 8, size=(k, Hkv, D)).astype(np.int8)) for k in kv_lens]
+        V_list = [torch.from_numpy(rng.integers(-8, 8, size=(k, Hkv, D)).astype(np.int8)) for k in kv_lens]
     else:
         K_list = [rand_bf16(rng, (k, Hkv, D)).to(dtype) for k in kv_lens]
         V_list = [rand_bf16(rng, (k, Hkv, D)).to(dtype) for k in kv_lens]
     T = sum(q_lens)
     q = rand_bf16(rng, (T, Hq, D))
-    pages, table = page_rpa(K_list, V_list, ps, rng, dtype=dtype)
+    if dtype == "int4":
+        pages, table = page_rpa(K_list, V_list, ps, rng, dtype=torch.int8)
+        pages = pack_int4(pages)  # the oracle reads the packed bytes
+    else:
+        pages, table = page_rpa(K_list, V_list, ps, rng, dtype=dtype)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]), dtype=torch.int32)
     kvl = torch.tensor(kv_lens, dtype=torch.int32)
     sm_scale = 1 / math.sqrt(D) if sm_scale is None else sm_scale
@@ -190,6 +204,35 @@ def test_rpa_int8_bruteforce(scale, sm_scale):
     rng = np.random.default_rng(21)
     out, exp, _ = ragged_case(rng, [1, 3], [20, 11], 4, 2, 16, 8, dtype=torch.int8, scale=scale, sm_scale=sm_scale)
     np.testing.assert_allclose(out, exp, rtol=0, atol=1e-10)
+
+
+def test_int4_decode_all_codes():
+    # two's complement in four bits, decoded from the definition
+    assert [oracle.decode_int4(n) for n in range(16)] == [float(n if n < 8 else n - 16) for n in range(16)]
+
+
+@pytest.mark.parametrize("scale,sm_scale", [(None, 0.02), (1 / 8, None), (0.0123, 0.9)])
+def test_rpa_int4_bruteforce(scale, sm_scale):
+    # int4 K/V unpacked on the dense side by the test's own nibble order: promoted exactly
+    # without a scale, else bf16(float32(x) * scale)
+    rng = np.random.default_rng(23)
+    out, exp, _ = ragged_case(rng, [1, 3, 2], [20, 11, 40], 4, 2, 16, 8, dtype="int4", scale=scale, sm_scale=sm_scale)
+    np.testing.assert_allclose(out, exp, rtol=0, atol=1e-10)
+
+
+def test_int4_one_key_returns_its_value_in_element_order():
+    # a single key returns its value row exactly; the value's nibbles all differ, so a swapped
+    # nibble order or byte order shows in the output's element order
+    D = 16
+    v = torch.tensor([[-8, 7, 1, -1, 2, -2, 3, -3, 4, -4, 5, -5, 6, -6, 0, -7]], dtype=torch.int8)
+    k = torch.zeros(1, D, dtype=torch.int8)
+    pages = torch.zeros(2, 4, 2, D // 2, dtype=torch.uint8)
+    pages[1, 0, 0] = pack_int4(k)[0]
+    pages[1, 0, 1] = pack_int4(v)[0]
+    q = bf16(np.ones((1, 1, D)))
+    out = oracle.rpa(q, pages, torch.tensor([1], dtype=torch.int32), torch.tensor([[1]], dtype=torch.int32),
+                     torch.tensor([0, 1], dtype=torch.int32), 1, sm_scale=0.5)
+    np.testing.assert_array_equal(out[0, 0].numpy(), v[0].double().numpy())
 
 
 def test_rpa_fp8_scaled_bruteforce():
