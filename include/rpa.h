@@ -79,7 +79,11 @@ typedef enum {
     RPA_DTYPE_BF16 = 1,
     RPA_DTYPE_FP8_E4M3 = 2,
     RPA_DTYPE_F32 = 3,
-    RPA_DTYPE_INT8 = 4           /* two's-complement bytes (RPA K/V only) */
+    RPA_DTYPE_INT8 = 4,          /* two's-complement bytes (RPA K/V only) */
+    RPA_DTYPE_INT4 = 5           /* two's-complement 4-bit values, two to a byte along the head
+                                  * dimension: element 2i of a row in the low nibble (bits 0-3) of
+                                  * the row's byte i, element 2i+1 in the high nibble (RPA K/V only;
+                                  * a head row is head_dim / 2 bytes) */
 } rpa_dtype;
 
 /* Bits of the device error word (OR-ed together). */
@@ -122,9 +126,10 @@ typedef struct CUstream_st* rpa_stream_t;
  * KV head h / (num_q_heads / num_kv_heads).  Logits: sm_scale * q.k, then
  * soft_cap * tanh(x / soft_cap) when soft_cap != 0.  When k_scale (v_scale) != 0 the
  * keys (values) are dequantised as bf16(float(k) * k_scale) before the dot products.
- * kv_dtype int8 (the v2 kernel's packed integer KV): the bytes are two's-complement
- * integers, read as their exact value without a scale and dequantised like any other
- * dtype with one. */
+ * kv_dtype int8 and int4 (the v2 kernel's packed integer KV): two's-complement integers, read
+ * as their exact value without a scale and dequantised like any other dtype with one; int4
+ * packs two values a byte (RPA_DTYPE_INT4), so kv_pages (and new_k / new_v) rows are
+ * head_dim / 2 bytes. */
 typedef struct {
     uint32_t struct_size;        /* sizeof(rpa_params) */
     uint32_t version;            /* RPA_ABI_VERSION */
@@ -137,7 +142,7 @@ typedef struct {
     int32_t max_num_seqs;
     int32_t pages_per_seq;
     int32_t q_dtype;             /* RPA_DTYPE_BF16 */
-    int32_t kv_dtype;            /* RPA_DTYPE_BF16, RPA_DTYPE_FP8_E4M3 or RPA_DTYPE_INT8 */
+    int32_t kv_dtype;            /* RPA_DTYPE_BF16, RPA_DTYPE_FP8_E4M3, RPA_DTYPE_INT8 or RPA_DTYPE_INT4 */
     float sm_scale;
     int32_t sliding_window;      /* 0 = none */
     float soft_cap;              /* 0 = none */

@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librpa_gb300.so")
 ABI_VERSION = 1
 
-BF16, FP8_E4M3, F32, INT8 = 1, 2, 3, 4
+BF16, FP8_E4M3, F32, INT8, INT4 = 1, 2, 3, 4, 5
 
 STATUS = {0: "RPA_OK", -1: "RPA_ERR_NULL", -2: "RPA_ERR_SHAPE", -3: "RPA_ERR_DTYPE", -4: "RPA_ERR_VALUE",
           -5: "RPA_ERR_UNSUPPORTED", -6: "RPA_ERR_CUDA", -7: "RPA_ERR_DEVICE_CHECK", -8: "RPA_ERR_WORKSPACE"}
@@ -180,12 +180,20 @@ def _kv_code(dtype) -> int:
         return FP8_E4M3
     if dtype == torch.int8:
         return INT8
+    if dtype == torch.uint8:  # int4 values packed two a byte (element 2i in the low nibble of byte i)
+        return INT4
     raise ValueError(f"unsupported KV dtype {dtype}")
+
+
+def kv_head_dim(kv_pages) -> int:
+    """Head dim of a cache tensor: its last dim, twice that for a packed int4 (uint8) cache."""
+    return kv_pages.shape[-1] * (2 if kv_pages.dtype == torch.uint8 else 1)
 
 
 def make_rpa_params(q, kv_pages, page_indices, *, sm_scale=1.0, sliding_window=None, soft_cap=None,
                     mask_value=None, k_scale=None, v_scale=None, batch_kind=BATCH_MIXED) -> rpa_params:
-    P, ps, C, D = kv_pages.shape
+    P, ps, C, _ = kv_pages.shape
+    D = kv_head_dim(kv_pages)
     max_num_seqs, pps = page_indices.shape
     return rpa_params(
         struct_size=ctypes.sizeof(rpa_params), version=ABI_VERSION, max_num_tokens=q.shape[0],
@@ -219,7 +227,7 @@ def rpa_forward(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, *, sm_s
                           batch_kind=batch_kind)
     if kv_lens.numel() != prm.max_num_seqs or cu_q_lens.numel() != prm.max_num_seqs + 1 or num_seqs.numel() != 1:
         raise ValueError("kv_lens must be [max_num_seqs], cu_q_lens [max_num_seqs + 1], num_seqs [1]")
-    if kv_pages.shape[-1] != q.shape[-1]:
+    if kv_head_dim(kv_pages) != q.shape[-1]:
         raise ValueError("q and kv_pages head_dim differ")
     if out is None:
         out = torch.empty_like(q)
@@ -260,7 +268,7 @@ def rpa_forward_noalloc(q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs,
     """
     # shapes first: the C call sees only pointers, so a q narrower than the cache or an
     # out smaller than q would be read or written past its end
-    if kv_pages.shape[-1] != q.shape[-1]:
+    if kv_head_dim(kv_pages) != q.shape[-1]:
         raise ValueError("q and kv_pages head_dim differ")
     if tuple(out.shape) != tuple(q.shape):
         raise ValueError(f"out must have q's shape {tuple(q.shape)}, got {tuple(out.shape)}")
@@ -319,7 +327,7 @@ def rpa_forward_update(q, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_le
                           batch_kind=batch_kind)
     if kv_lens.numel() != prm.max_num_seqs or cu_q_lens.numel() != prm.max_num_seqs + 1 or num_seqs.numel() != 1:
         raise ValueError("kv_lens must be [max_num_seqs], cu_q_lens [max_num_seqs + 1], num_seqs [1]")
-    if kv_pages.shape[-1] != q.shape[-1]:
+    if kv_head_dim(kv_pages) != q.shape[-1]:
         raise ValueError("q and kv_pages head_dim differ")
     if (new_k.shape != new_v.shape or new_k.shape[0] != q.shape[0] or new_k.shape[1] * 2 != kv_pages.shape[2]
             or new_k.shape[2] != kv_pages.shape[3]):

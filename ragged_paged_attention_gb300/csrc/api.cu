@@ -80,8 +80,9 @@ int check_rpa_params(const rpa_params* p) {
     if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
         return fail(RPA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", p->head_dim);
     if (p->q_dtype != RPA_DTYPE_BF16) return fail(RPA_ERR_DTYPE, "q_dtype must be bf16");
-    if (p->kv_dtype != RPA_DTYPE_BF16 && p->kv_dtype != RPA_DTYPE_FP8_E4M3 && p->kv_dtype != RPA_DTYPE_INT8)
-        return fail(RPA_ERR_DTYPE, "kv_dtype must be bf16, fp8 e4m3 or int8");
+    if (p->kv_dtype != RPA_DTYPE_BF16 && p->kv_dtype != RPA_DTYPE_FP8_E4M3 && p->kv_dtype != RPA_DTYPE_INT8 &&
+        p->kv_dtype != RPA_DTYPE_INT4)
+        return fail(RPA_ERR_DTYPE, "kv_dtype must be bf16, fp8 e4m3, int8 or int4");
     if (!isfinite(p->sm_scale)) return fail(RPA_ERR_VALUE, "sm_scale must be finite");
     if (p->sliding_window < 0) return fail(RPA_ERR_VALUE, "sliding_window must be positive (0 = none)");
     if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
@@ -299,6 +300,7 @@ static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages,
     a.pages_per_seq = p->pages_per_seq;
     a.kv_byte = p->kv_dtype != RPA_DTYPE_BF16;
     a.kv_int8 = p->kv_dtype == RPA_DTYPE_INT8;
+    a.kv_int4 = p->kv_dtype == RPA_DTYPE_INT4;
     a.sm_scale = p->sm_scale;
     a.soft_cap = p->soft_cap;
     a.sliding_window = p->sliding_window;
@@ -351,7 +353,7 @@ static int rpa_update_prepare(const rpa_params* p, const void* new_k, const void
     a.max_num_tokens = p->max_num_tokens;
     a.num_kv_heads = p->num_combined_kv_heads / 2;
     a.head_dim = p->head_dim;
-    a.esz = p->kv_dtype == RPA_DTYPE_BF16 ? 2 : 1;
+    a.row_bytes = p->kv_dtype == RPA_DTYPE_BF16 ? p->head_dim * 2 : p->kv_dtype == RPA_DTYPE_INT4 ? p->head_dim / 2 : p->head_dim;
     a.total_num_pages = p->total_num_pages;
     a.page_size = p->page_size;
     a.max_num_seqs = p->max_num_seqs;

@@ -90,8 +90,9 @@ struct RpaArgs {
     __nv_bfloat16* out;
     int max_num_tokens, num_q_heads, num_kv_heads, head_dim;
     int total_num_pages, page_size, max_num_seqs, pages_per_seq;
-    int kv_byte;                // one-byte K/V elements: e4m3, or int8 when kv_int8
+    int kv_byte;                // narrow K/V elements: e4m3, int8 (kv_int8) or int4 (kv_int4)
     int kv_int8;
+    int kv_int4;                // two 4-bit values a byte, element 2i in the low nibble of byte i
     float sm_scale, soft_cap;
     int sliding_window;
     // a mask_value that leaves masked keys real weight (above -1e30): every key of a sequence
@@ -129,7 +130,7 @@ struct RpaUpdateArgs {
     const int32_t* cu_q_lens;
     const int32_t* num_seqs;
     uint32_t* err;  // may be null
-    int max_num_tokens, num_kv_heads, head_dim, esz;
+    int max_num_tokens, num_kv_heads, head_dim, row_bytes;  // row_bytes: one head row of K or V
     int total_num_pages, page_size, max_num_seqs, pages_per_seq;
 };
 

@@ -27,10 +27,11 @@
 
 namespace rpa {
 
-template <int D, int HG, int ESZ, bool CONV, bool F16 = false>
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I4 = false>
 struct DecTile {
     static constexpr int BK = kDecodeBK;                 // keys per stage
-    static constexpr int kSeg = HG * 2 * D * ESZ;        // bytes of one token's segment
+    // bytes of one token's segment (I4: half a byte an element)
+    static constexpr int kSeg = I4 ? HG * D : HG * 2 * D * ESZ;
     static constexpr int kRow = kSeg + 16;               // padded shared-memory row
     static constexpr int kStage = BK * kRow;
     static constexpr int kConvRow = D * 2 + 16;          // one head's K (then V) in bf16, padded
@@ -74,6 +75,20 @@ __device__ __forceinline__ uint4 dequant8(const uint8_t* src, float sc) {
             const float2 f = __bfloat1622float2(h[e]);
             w[e] = pack_bf16(f.x * sc, f.y * sc);
         }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 8 int4 elements (4 bytes; element 2i in the low nibble of byte i) -> 8 bf16 of
+// bf16(float(x) * scale), packed in a uint4.
+__device__ __forceinline__ uint4 dequant_i4x8(const uint8_t* src, float sc) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int lo = (int)(v << (28 - 8 * e)) >> 28;  // nibble 2e, sign-extended
+        const int hi = (int)(v << (24 - 8 * e)) >> 28;  // nibble 2e + 1
+        w[e] = pack_bf16((float)lo * sc, (float)hi * sc);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -123,11 +138,14 @@ __device__ __forceinline__ int vdim(int g8, int j) {
 // of two (undone on its scores), which keeps its bf16 values exact.  The one-byte K and V rows
 // are converted straight into MMA fragments (permuted head dims, see kchunk / vdim): no
 // conversion rows in shared memory, no ldmatrix.  I8: the one-byte elements are int8.
-template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false>
-__global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_decode_kernel(RpaArgs a) {
-    using T = DecTile<D, HG, ESZ, CONV, F16>;
-    static_assert(!F16 || (CONV && ESZ == 1), "the f16 path takes one-byte caches");
+// I4: int4 caches (two elements a byte), dequantised into the bf16 conversion rows.
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false, bool I4 = false>
+__global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16, I4>::kThreads) rpa_decode_kernel(RpaArgs a) {
+    using T = DecTile<D, HG, ESZ, CONV, F16, I4>;
+    static_assert(!F16 || (CONV && ESZ == 1 && !I4), "the f16 path takes one-byte caches");
     static_assert(!I8 || (CONV && ESZ == 1), "int8 caches take the converting path");
+    static_assert(!I4 || (CONV && !F16 && !I8), "int4 caches take the bf16 converting path");
+    constexpr int kRowB = I4 ? D / 2 : D * ESZ;  // bytes of one head row of K or V
     constexpr int BK = T::BK, STAGES = T::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
@@ -203,7 +221,7 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_
         const int n_blocks = ke > kb ? cdiv(ke - kb, BK) : 0;
         const int h0 = w.head;
         const int seg_heads = min(HG, Hkv - h0);
-        const uint32_t seg_bytes = seg_heads * 2 * D * ESZ;
+        const uint32_t seg_bytes = seg_heads * 2 * kRowB;
 
         if (producer) {
             // lane t < BK owns token t of every stage: it resolves that token's page (the
@@ -239,7 +257,7 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_
                 if (!go) break;
                 if (ok) {
                     const uint8_t* src =
-                        kv + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * h0) * (size_t)(D * ESZ);
+                        kv + (((size_t)page * a.page_size + key % a.page_size) * C + 2 * h0) * (size_t)kRowB;
                     bulk_g2s(smem_u32(stages + st * T::kStage + lane * T::kRow), src, seg_bytes, &full[st]);
                 }
             }
@@ -329,9 +347,9 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_
 #pragma unroll 4
                     for (int i = lane; i < BK * kChunks; i += 32) {
                         const int kk = i / kChunks, c = i % kChunks;
-                        const uint8_t* src = stg + kk * T::kRow + (warp * 2 * D + part * D + c * 8) * ESZ;
+                        const uint8_t* src = stg + kk * T::kRow + (warp * 2 + part) * kRowB + c * 8 * kRowB / D;
                         *reinterpret_cast<uint4*>(cb + kk * T::kConvRow + c * 16) =
-                            F16 ? byte8_to_f16<I8>(src) : dequant8<ESZ, I8>(src, sc);
+                            I4 ? dequant_i4x8(src, sc) : F16 ? byte8_to_f16<I8>(src) : dequant8<ESZ, I8>(src, sc);
                     }
                     __syncwarp();
                 };
@@ -611,10 +629,10 @@ __global__ void __launch_bounds__(DecTile<D, HG, ESZ, CONV, F16>::kThreads) rpa_
 }
 
 // per_sm_out != nullptr: only report the kernel's resident CTAs per SM (no launch)
-template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false>
+template <int D, int HG, int ESZ, bool CONV, bool F16 = false, bool I8 = false, bool I4 = false>
 static cudaError_t launch_decode(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
-    using T = DecTile<D, HG, ESZ, CONV, F16>;
-    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16, I8>;
+    using T = DecTile<D, HG, ESZ, CONV, F16, I4>;
+    auto kern = rpa_decode_kernel<D, HG, ESZ, CONV, F16, I8, I4>;
     static int per_sm = 0;
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -651,6 +669,7 @@ template <int D>
 static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     constexpr int HG = D >= 256 ? 2 : 4;
     const bool pow2 = rpa_pow2_scale(a.k_scale_or_one) && rpa_pow2_scale(a.v_scale_or_one);
+    if (a.kv_int4) return launch_decode<D, HG, 1, true, false, false, true>(a, num_sms, stream, per_sm_out);
     if (a.kv_int8 && pow2) return launch_decode<D, HG, 1, true, true, true>(a, num_sms, stream, per_sm_out);
     if (a.kv_int8) return launch_decode<D, HG, 1, true, false, true>(a, num_sms, stream, per_sm_out);
     if (a.kv_byte && pow2) return launch_decode<D, HG, 1, true, true>(a, num_sms, stream, per_sm_out);

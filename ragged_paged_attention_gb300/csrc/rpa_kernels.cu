@@ -360,7 +360,7 @@ __device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, i
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
     const int Hkv = a.num_kv_heads, C = 2 * Hkv;
-    const int row_chunks = a.head_dim * a.esz / 16;  // 16-byte chunks per head row
+    const int row_chunks = a.row_bytes / 16;  // 16-byte chunks per head row
     const int chunks = Hkv * 2 * row_chunks;
     // one warp per token; each lane moves up to kBatch 16-byte chunks of the token's rows at a
     // time, loaded before the sequence and page lookups (they depend on the token index only)
@@ -372,7 +372,7 @@ __device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, i
             if (i < chunks) {
                 const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
                 v[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(part ? a.new_v : a.new_k) +
-                                                             (((size_t)t * Hkv + head) * a.head_dim * a.esz) + c * 16));
+                                                             (((size_t)t * Hkv + head) * a.row_bytes) + c * 16));
             }
         }
     };
@@ -425,7 +425,7 @@ __device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, i
             continue;
         }
         uint8_t* slot = static_cast<uint8_t*>(a.kv_pages) +
-                        ((size_t)page * a.page_size + pos % a.page_size) * C * a.head_dim * a.esz;
+                        ((size_t)page * a.page_size + pos % a.page_size) * C * a.row_bytes;
         for (int i0 = lane; i0 < chunks; i0 += 32 * kBatch) {
             if (i0 != lane) load_batch(t, i0, v);
 #pragma unroll
@@ -433,7 +433,7 @@ __device__ __forceinline__ void update_body(const RpaUpdateArgs& a, int block, i
                 const int i = i0 + 32 * j;
                 if (i < chunks) {
                     const int head = i / (2 * row_chunks), part = (i / row_chunks) & 1, c = i % row_chunks;
-                    *reinterpret_cast<uint4*>(slot + ((size_t)(2 * head + part) * a.head_dim * a.esz) + c * 16) = v[j];
+                    *reinterpret_cast<uint4*>(slot + ((size_t)(2 * head + part) * a.row_bytes) + c * 16) = v[j];
                 }
             }
         }

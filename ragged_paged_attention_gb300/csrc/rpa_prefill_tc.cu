@@ -149,6 +149,19 @@ __device__ __forceinline__ uint4 kv_convert(typename KvRaw<FP8>::type raw, float
     }
 }
 
+// 8 int4 elements (4 bytes; element 2i in the low nibble of byte i) -> 16 bytes of bf16 of
+// bf16(float(x) * scale).
+__device__ __forceinline__ uint4 kv_convert_i4(uint32_t v, float sc) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int lo = (int)(v << (28 - 8 * e)) >> 28;  // nibble 2e, sign-extended
+        const int hi = (int)(v << (24 - 8 * e)) >> 28;  // nibble 2e + 1
+        w[e] = pack_bf16((float)lo * sc, (float)hi * sc);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Raw chunk of 8 one-byte elements -> 8 f16, exact and unscaled (the f16 path).
 template <bool I8>
 __device__ __forceinline__ uint4 kv_convert_f16(uint2 raw) {
@@ -185,7 +198,8 @@ __device__ __forceinline__ void raw16_convert(uint4 r, float sc, uint4& lo, uint
 // by TMA (128-byte swizzled halves of [BK x 128 B]) in rings of NR stages, warps 8-11 convert
 // them shared memory to shared memory into the f16/bf16 panels and put Q into TMEM (the QK
 // MMAs read A from there), and S has one TMEM buffer.
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false>
+// I4 (int4 caches, two elements a byte): the register path, each 8-element chunk 4 bytes.
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false, bool I4 = false>
 __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
     rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                           int box_rows, int q_tma, int tail) {
@@ -198,12 +212,20 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
         pdl_wait();
         pdl_launch_dependents();
     }
-    {
-        const WsHeader* h = a.hdr;
-        if ((!tail && (int)blockIdx.x >= h->prefill_ctas) || *(volatile const int*)&h->next_item[1] >= h->num_items[1])
-            return;
-    }
     extern __shared__ __align__(1024) uint8_t smem[];
+    {
+        // one decision for the whole CTA: the queue counter moves while other CTAs take items,
+        // so threads reading it on their own could disagree, and a CTA whose item-fetching
+        // thread left would leave its other warps waiting for an item
+        volatile int& s_exit = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 68);
+        if (threadIdx.x == 0) {
+            const WsHeader* h = a.hdr;
+            s_exit = (!tail && (int)blockIdx.x >= h->prefill_ctas) ||
+                     *(volatile const int*)&h->next_item[1] >= h->num_items[1];
+        }
+        __syncthreads();
+        if (s_exit) return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
     constexpr int NSK = T::NSK, NSV = T::NSV;
     uint64_t* k_full = bars;                       // [NSK] K block landed
@@ -240,7 +262,8 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
     // (no static shared variables: with the 1024-byte aligned dynamic block they would
     // round up to 1 KB and push the kernel past the 227 KB limit)
     static_assert(!F16 || (FP8 && !TMA), "the f16 path takes one-byte caches through registers");
-    static_assert(!RAW || (FP8 && !TMA && !SCALE), "the raw-staging path is for one-byte caches");
+    static_assert(!RAW || (FP8 && !TMA && !SCALE && !I4), "the raw-staging path is for one-byte caches");
+    static_assert(!I4 || (FP8 && !TMA && !RAW && !F16 && !I8), "int4 caches take the bf16 register path");
     float* qmul = reinterpret_cast<float*>(smem + T::kOffQmul);
     WorkItem* s_items = reinterpret_cast<WorkItem*>(smem + T::kOffItem);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + T::kOffItem + 64);
@@ -749,8 +772,20 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                             v = false;
                         }
                         const uint8_t* row =
-                            v ? kvp + (((size_t)page[i] * a.page_size + key % a.page_size) * C + 2 * kvh + part) * (size_t)(D * kEsz)
+                            v ? kvp + (((size_t)page[i] * a.page_size + key % a.page_size) * C + 2 * kvh + part) *
+                                          (size_t)(I4 ? D / 2 : D * kEsz)
                               : nullptr;
+                        if constexpr (I4) {
+                            // 8 int4 elements (4 bytes) a chunk: a whole row's loads in flight
+                            uint32_t raw4[kRowChunks];
+#pragma unroll
+                            for (int c = 0; c < kRowChunks; ++c) raw4[c] = v ? __ldg(reinterpret_cast<const uint32_t*>(row + c * 4)) : 0u;
+#pragma unroll
+                            for (int c = 0; c < kRowChunks; ++c)
+                                *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) =
+                                    kv_convert_i4(raw4[c], sc);
+                            continue;
+                        }
                         // loads in flight per pass: a whole row for fp8 (8-byte chunks), 16 chunks for bf16
                         constexpr int kGroup = FP8 ? kRowChunks : (kRowChunks < 16 ? kRowChunks : 16);
 #pragma unroll 1
@@ -1083,11 +1118,11 @@ static bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t d0, uint64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false>
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false, bool I4 = false>
 static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
                               const CUtensorMap& tq, int box_rows, int q_tma, int tail) {
     using T = PreTc<D, RAW>;
-    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16, RAW>;
+    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16, RAW, I4>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -1118,6 +1153,8 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     if (tma && 128 % G == 0)
         q_tma = make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
     if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma, tail);
+    // int4 caches: dequantised to bf16 through registers
+    if (a.kv_int4) return launch_pre<D, true, false, false, false, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     // one-byte caches with power-of-two scales: exact f16 operands, scales on S and O
     const bool pow2 = rpa_pow2_scale(a.k_scale_or_one) && rpa_pow2_scale(a.v_scale_or_one);
     if constexpr (D == 128 || D == 256) {

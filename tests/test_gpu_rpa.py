@@ -350,3 +350,42 @@ def test_batch_kind_hint_violation_is_reported():
     assert (out[1:41].float() == 7.0).all()
     ref = oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, 3, tokens=[0, 41], **opts)
     assert max_abs(out[[0, 41]], ref[[0, 41]]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("ks,vs", [(None, None), (1 / 4, 1 / 8), (0.0123, 0.021)],
+                         ids=["exact", "pow2", "scaled"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_int4_kv(ks, vs, d):
+    # int4 caches (two's-complement nibbles, element 2i in the low nibble of byte i): exact
+    # integers without scales, bf16(float(x) * scale) with them; decode rows (two-row items too)
+    # and prefill tiles, windowed and not
+    hq, hkv = (8, 2) if d < 256 else (4, 2)
+    b = workloads.make_rpa([1, 9, 2, 40], [77, 30, 300, 200], num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                           page_size=16, seed=70 + d, kv_dtype=torch.uint8, k_scale=ks, v_scale=vs,
+                           sliding_window=150 if d == 128 else None,
+                           sm_scale=2.0 / (4.6 * (ks or 1.0) * math.sqrt(d)))  # logits' spread ~2
+    out, bits, _ = run_gpu(b)
+    assert bits == 0
+    ref = oracle.rpa(b.q, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), **b.options())
+    T = b.num_tokens
+    scale = float(ref[:T].abs().max())
+    assert max_abs(out[:T], ref[:T]) <= 2e-2 * scale
+    assert (out[T:].float() == 7.0).all()
+
+
+def test_int4_update_then_attend():
+    # the cache write moves packed bytes unchanged; the fused call attends over them
+    b = workloads.make_rpa([1, 1, 6, 19], [33, 1, 6, 40], num_q_heads=8, num_kv_heads=4, head_dim=128, page_size=16,
+                           seed=18, kv_dtype=torch.uint8, max_num_seqs=6, max_num_tokens=32, extra_pages=4,
+                           k_scale=0.5, v_scale=0.5)
+    n = len(b.q_lens)
+    ref_pages = oracle.rpa_update_kv_cache(b.new_k[:b.num_tokens].contiguous(), b.new_v[:b.num_tokens].contiguous(),
+                                           b.kv_pages, b.kv_lens[:n], b.page_indices[:n], b.cu_q_lens[:n + 1], n)
+    g = b.to("cuda")
+    out = api.rpa_forward_update(g.q, g.new_k, g.new_v, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens,
+                                 g.num_seqs, **b.options())
+    torch.cuda.synchronize()
+    assert torch.equal(g.kv_pages.cpu(), ref_pages)
+    ref = oracle.rpa(b.q, ref_pages, b.kv_lens, b.page_indices, b.cu_q_lens, n, **b.options())
+    T = b.num_tokens
+    assert max_abs(out[:T], ref[:T]) <= 2e-2 * float(ref[:T].abs().max())
