@@ -84,6 +84,8 @@ class MlaParams(ctypes.Structure):
         ("sliding_window", ctypes.c_int32),
         ("soft_cap", ctypes.c_double),
         ("mask_value", ctypes.c_double),
+        ("q_dtype", ctypes.c_int32),
+        ("q_scale", ctypes.c_double),
     ]
 
 
@@ -260,7 +262,7 @@ def rpa_update_kv_cache(new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_lens
 
 
 def mla_params(ql_nope, q_pe, cache_kv_c, cache_k_pe, page_indices, max_num_seqs, *, sm_scale=1.0,
-               sliding_window=None, soft_cap=None, mask_value=None) -> MlaParams:
+               sliding_window=None, soft_cap=None, mask_value=None, q_scale=None) -> MlaParams:
     P = cache_kv_c.shape[0]
     ps = cache_kv_c.shape[1] * cache_kv_c.shape[2]
     return MlaParams(
@@ -269,7 +271,8 @@ def mla_params(ql_nope, q_pe, cache_kv_c, cache_k_pe, page_indices, max_num_seqs
         max_num_seqs=max_num_seqs, pages_per_seq=page_indices.numel() // max_num_seqs,
         sm_scale=float(sm_scale), sliding_window=int(sliding_window or 0),
         soft_cap=float(soft_cap or 0.0),
-        mask_value=DEFAULT_MASK_VALUE if mask_value is None else float(mask_value))
+        mask_value=DEFAULT_MASK_VALUE if mask_value is None else float(mask_value),
+        q_dtype=E4M3 if ql_nope.dtype == torch.float8_e4m3fn else BF16, q_scale=float(q_scale or 0.0))
 
 
 def mla_update_kv_cache(new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,

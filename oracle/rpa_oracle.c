@@ -315,7 +315,15 @@ typedef struct {
     int32_t sliding_window; /* 0 = none */
     double soft_cap;        /* 0 = none */
     double mask_value;      /* replaces masked logits */
+    int32_t q_dtype;        /* ORACLE_BF16, or ORACLE_E4M3 for fp8 queries (ql_nope, q_pe) */
+    double q_scale;         /* 0 = none; else the scores are multiplied by it (after sm_scale) */
 } oracle_mla_params;
+
+/* Query element: bfloat16, or an fp8 e4m3 byte decoded exactly. */
+static double mla_q_elem(const void* base, size_t idx, int dtype) {
+    if (dtype == ORACLE_E4M3) return (double)e4m3_bits_to_f32(((const uint8_t*)base)[idx]);
+    return (double)bf16_bits_to_f32(((const uint16_t*)base)[idx]);
+}
 
 /* new_kv_c: bf16 [*, lkv]; new_k_pe: bf16 [*, r]; caches viewed as
  * [P, ps, lkv_pad] and [P, ps, r_pad] (the [P, ps/pk, pk, D] layout has the
@@ -350,7 +358,7 @@ int oracle_mla_update_kv_cache(const oracle_mla_params* p, const uint16_t* new_k
 /* ql_nope: bf16 [*, H, lkv]; q_pe: bf16 [*, H, r]; caches as above (already
  * updated).  Key = [kv_c | k_pe], value = kv_c, one latent head for all q
  * heads.  Masked logits are replaced by mask_value.  out: float64 [*, H, lkv]. */
-int oracle_mla(const oracle_mla_params* p, const uint16_t* ql_nope, const uint16_t* q_pe,
+int oracle_mla(const oracle_mla_params* p, const void* ql_nope, const void* q_pe,
                const uint16_t* cache_kv_c, const uint16_t* cache_k_pe, const int32_t* kv_lens,
                const int32_t* page_indices, const int32_t* cu_q_lens, int32_t num_seqs,
                const int32_t* tokens, int32_t n_tokens, double* out, int nthreads) {
@@ -384,17 +392,18 @@ int oracle_mla(const oracle_mla_params* p, const uint16_t* ql_nope, const uint16
         const int q_len = cu_q_lens[s + 1] - cu_q_lens[s];
         const int kv_len = kv_lens[s];
         const int q_pos = kv_len - q_len + (t - cu_q_lens[s]);
-        const uint16_t* qn = ql_nope + ((size_t)t * H + h) * L;
-        const uint16_t* qr = q_pe + ((size_t)t * H + h) * R;
+        const size_t qn = ((size_t)t * H + h) * L, qr = ((size_t)t * H + h) * R;  /* element offsets */
         double* x = (double*)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1));
         for (int k = 0; k < kv_len; ++k) {
             const size_t slot = (size_t)page_indices[(size_t)s * pps + k / ps] * ps + k % ps;
             const uint16_t* c = cache_kv_c + slot * p->lkv_dim_pad;
             const uint16_t* r = cache_k_pe + slot * p->r_dim_pad;
             double dot = 0.0;
-            for (int d = 0; d < L; ++d) dot += (double)bf16_bits_to_f32(qn[d]) * bf16_bits_to_f32(c[d]);
-            for (int d = 0; d < R; ++d) dot += (double)bf16_bits_to_f32(qr[d]) * bf16_bits_to_f32(r[d]);
+            for (int d = 0; d < L; ++d) dot += mla_q_elem(ql_nope, qn + d, p->q_dtype) * bf16_bits_to_f32(c[d]);
+            for (int d = 0; d < R; ++d) dot += mla_q_elem(q_pe, qr + d, p->q_dtype) * bf16_bits_to_f32(r[d]);
+            /* the MLA kernel's order: sm_scale, then (fp8 queries) q_scale */
             double v = p->sm_scale * dot;
+            if (p->q_scale != 0.0) v *= p->q_scale;
             if (p->soft_cap != 0.0) v = p->soft_cap * tanh(v / p->soft_cap);
             int masked = q_pos < k;
             if (p->sliding_window > 0 && q_pos - p->sliding_window >= k) masked = 1;

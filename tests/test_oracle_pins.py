@@ -449,6 +449,27 @@ def test_mla_matches_dense_bruteforce():
         np.testing.assert_allclose(out[cu[s]:cu[s + 1]], exp, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("q_scale", [None, 0.5, 0.037])
+def test_mla_fp8_queries_match_dense_bruteforce(q_scale):
+    # fp8 e4m3 queries (torch's decode of the bytes, on the dense side) with the MLA kernel's
+    # q_scale multiplying the scores after sm_scale
+    rng = np.random.default_rng(33)
+    q_lens, kv_lens = [1, 4], [20, 9]
+    ql, qpe, ckv, ckpe, kvl, table, cu, dist, C_list, R_list = mla_case(rng, q_lens, kv_lens)
+    ql8 = (ql.float() * 3).to(torch.float8_e4m3fn)
+    qpe8 = (qpe.float() * 3).to(torch.float8_e4m3fn)
+    sm = 1 / math.sqrt(40)
+    out = oracle.mla(ql8, qpe8, ckv, ckpe, kvl, table, cu, dist, sm_scale=sm, q_scale=q_scale).numpy()
+    for s in range(2):
+        K = torch.cat([C_list[s], R_list[s]], dim=1).to(torch.float64).numpy()[:, None, :]
+        V = C_list[s].to(torch.float64).numpy()[:, None, :]
+        qs = torch.cat([ql8, qpe8], dim=2)[cu[s]:cu[s + 1]].to(torch.float64).numpy()
+        q_pos = kv_lens[s] - q_lens[s] + np.arange(q_lens[s])
+        exp = dense_attention(qs, np.repeat(K, 4, axis=1), np.repeat(V, 4, axis=1), q_pos, sm * (q_scale or 1.0),
+                              mode="replace")
+        np.testing.assert_allclose(out[cu[s]:cu[s + 1]], exp, rtol=0, atol=1e-12)
+
+
 def test_mla_mask_value_replaces_logit():
     rng = np.random.default_rng(31)
     ql, qpe, ckv, ckpe, kvl, table, cu, dist, C_list, R_list = mla_case(rng, [3], [5], H=2)
