@@ -36,11 +36,13 @@
  *   - Optional values use a "none" encoding: sliding_window = 0, soft_cap = 0,
  *     k_scale = v_scale = 0, mask_value = NaN (meaning -0.7 * FLT_MAX, the pages'
  *     DEFAULT_MASK_VALUE).
- *   - Masked logits are given zero softmax weight.  The pages add (RPA) or
- *     substitute (MLA) mask_value; with a mask value at or below -1e30 that weight
- *     underflows to exactly zero in float32 because the key at the query's own
- *     position is always visible, so the two agree.  A mask_value above -1e30 is
- *     rejected with RPA_ERR_UNSUPPORTED.
+ *   - Masking follows the pages: RPA adds mask_value to a masked logit, MLA
+ *     substitutes it.  With a mask value at or below -1e30 a masked key's weight
+ *     underflows to exactly zero in float32 (the key at the query's own position is
+ *     always visible), so the kernels skip masked keys outright.  Any larger finite
+ *     mask_value leaves masked keys real weight: then every key below kv_len takes
+ *     part (future keys of a prefill chunk and keys outside the window alike) with
+ *     mask_value added or substituted.  +inf is rejected with RPA_ERR_VALUE.
  */
 #ifndef RPA_GB300_RPA_H_
 #define RPA_GB300_RPA_H_
@@ -217,8 +219,8 @@ RPA_API int rpa_forward_update(const rpa_params* p, const void* q, const void* n
 /* ---------------------------------------------------------------------- */
 
 /* Layouts (tpu-inference MLA v1, mla_ragged_paged_attention):
- *   ql_nope    [max_num_tokens, num_q_heads, lkv_dim]        bf16
- *   q_pe       [max_num_tokens, num_q_heads, r_dim]          bf16
+ *   ql_nope    [max_num_tokens, num_q_heads, lkv_dim]        bf16, or fp8 e4m3 (q_dtype)
+ *   q_pe       [max_num_tokens, num_q_heads, r_dim]          same dtype as ql_nope
  *   new_kv_c   [max_num_tokens, lkv_dim]                     bf16
  *   new_k_pe   [max_num_tokens, r_dim]                       bf16
  *   cache_kv_c [total_num_pages, page_size / kv_packing, kv_packing, lkv_dim_pad] bf16
@@ -229,7 +231,9 @@ RPA_API int rpa_forward_update(const rpa_params* p, const void* q, const void* n
  *              (decode_end, prefill_end, num_seqs); only distribution[2] bounds the work
  *   out        [max_num_tokens, num_q_heads, lkv_dim]        bf16
  * Key = [kv_c | k_pe], value = kv_c, one latent head shared by all q heads; masked
- * logits are replaced by mask_value (see the header note on masking). */
+ * logits are replaced by mask_value (see the header note on masking).  fp8 queries are
+ * widened exactly to bf16 before the products; the output stays bf16 (the MLA v1 page
+ * writes it in the query dtype, which for fp8 would throw away most of its precision). */
 typedef struct {
     uint32_t struct_size;        /* sizeof(mla_params) */
     uint32_t version;            /* RPA_ABI_VERSION */
@@ -248,6 +252,11 @@ typedef struct {
     int32_t sliding_window;      /* 0 = none */
     float soft_cap;              /* 0 = none */
     float mask_value;            /* NaN = default */
+    /* Optional (read only when struct_size covers them, else bf16 queries): */
+    int32_t q_dtype;             /* RPA_DTYPE_BF16 (0 is taken as bf16) or RPA_DTYPE_FP8_E4M3 for
+                                    ql_nope and q_pe */
+    float q_scale;               /* fp8 queries: every score is multiplied by it after sm_scale
+                                    (0 = 1); must be 0 for bf16 queries */
 } mla_params;
 
 RPA_API int mla_workspace_size(const mla_params* p, size_t* bytes);

@@ -64,7 +64,8 @@ class mla_params(ctypes.Structure):
                 ("r_dim_pad", ctypes.c_int32), ("total_num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("kv_packing", ctypes.c_int32), ("max_num_seqs", ctypes.c_int32),
                 ("pages_per_seq", ctypes.c_int32), ("sm_scale", ctypes.c_float),
-                ("sliding_window", ctypes.c_int32), ("soft_cap", ctypes.c_float), ("mask_value", ctypes.c_float)]
+                ("sliding_window", ctypes.c_int32), ("soft_cap", ctypes.c_float), ("mask_value", ctypes.c_float),
+                ("q_dtype", ctypes.c_int32), ("q_scale", ctypes.c_float)]
 
 
 class sparse_params(ctypes.Structure):
@@ -346,16 +347,18 @@ def rpa_forward_update(q, new_k, new_v, kv_pages, kv_lens, page_indices, cu_q_le
 
 
 def make_mla_params(ql_nope, q_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, *, sm_scale=1.0,
-                    sliding_window=None, soft_cap=None, mask_value=None) -> mla_params:
+                    sliding_window=None, soft_cap=None, mask_value=None, q_scale=None) -> mla_params:
     P, ps_pk, pk, lkv_pad = cache_kv_c.shape
     max_num_seqs = kv_lens.numel()
+    fp8 = ql_nope.dtype == torch.float8_e4m3fn
     return mla_params(
         struct_size=ctypes.sizeof(mla_params), version=ABI_VERSION, max_num_tokens=ql_nope.shape[0],
         num_q_heads=ql_nope.shape[1], lkv_dim=ql_nope.shape[2], r_dim=q_pe.shape[2], lkv_dim_pad=lkv_pad,
         r_dim_pad=cache_k_pe.shape[-1], total_num_pages=P, page_size=ps_pk * pk, kv_packing=pk,
         max_num_seqs=max_num_seqs, pages_per_seq=page_indices.numel() // max_num_seqs, sm_scale=float(sm_scale),
         sliding_window=int(_opt(sliding_window, 0)), soft_cap=float(_opt(soft_cap)),
-        mask_value=math.nan if mask_value is None else float(mask_value))
+        mask_value=math.nan if mask_value is None else float(mask_value),
+        q_dtype=FP8_E4M3 if fp8 else BF16, q_scale=float(_opt(q_scale)) if fp8 else 0.0)
 
 
 def mla_workspace_size(params: mla_params) -> int:
@@ -367,8 +370,11 @@ def mla_workspace_size(params: mla_params) -> int:
 
 def _check_mla(ql_nope, q_pe, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
                distribution):
-    for n, t in (("ql_nope", ql_nope), ("q_pe", q_pe), ("new_kv_c", new_kv_c), ("new_k_pe", new_k_pe),
-                 ("cache_kv_c", cache_kv_c), ("cache_k_pe", cache_k_pe)):
+    qdt = torch.float8_e4m3fn if ql_nope.dtype == torch.float8_e4m3fn else torch.bfloat16
+    for n, t in (("ql_nope", ql_nope), ("q_pe", q_pe)):
+        _dev(t, n, qdt)
+    for n, t in (("new_kv_c", new_kv_c), ("new_k_pe", new_k_pe), ("cache_kv_c", cache_kv_c),
+                 ("cache_k_pe", cache_k_pe)):
         _dev(t, n, torch.bfloat16)
     for n, t in (("kv_lens", kv_lens), ("page_indices", page_indices), ("cu_q_lens", cu_q_lens),
                  ("distribution", distribution)):
@@ -398,16 +404,21 @@ def mla_update_kv_cache(new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, pag
 
 
 def mla_rpa_forward(ql_nope, q_pe, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
-                    distribution, *, sm_scale=1.0, sliding_window=None, soft_cap=None, mask_value=None, out=None,
-                    workspace=None):
-    """MLA update_kv_cache + attention; returns ``out`` [max_num_tokens, H, lkv] bf16 (caches updated in place)."""
+                    distribution, *, sm_scale=1.0, sliding_window=None, soft_cap=None, mask_value=None, q_scale=None,
+                    out=None, workspace=None):
+    """MLA update_kv_cache + attention; returns ``out`` [max_num_tokens, H, lkv] bf16 (caches updated in place).
+
+    ``ql_nope`` and ``q_pe`` are bf16, or both float8_e4m3fn with ``q_scale`` multiplying the
+    scores after ``sm_scale``."""
     lib = load_library()
     _check_mla(ql_nope, q_pe, new_kv_c, new_k_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, cu_q_lens,
                distribution)
+    if q_scale is not None and ql_nope.dtype != torch.float8_e4m3fn:
+        raise ValueError("q_scale applies to float8_e4m3fn queries only")
     prm = make_mla_params(ql_nope, q_pe, cache_kv_c, cache_k_pe, kv_lens, page_indices, sm_scale=sm_scale,
-                          sliding_window=sliding_window, soft_cap=soft_cap, mask_value=mask_value)
+                          sliding_window=sliding_window, soft_cap=soft_cap, mask_value=mask_value, q_scale=q_scale)
     if out is None:
-        out = torch.empty_like(ql_nope)
+        out = torch.empty(ql_nope.shape, dtype=torch.bfloat16, device=ql_nope.device)
     _dev(out, "out", torch.bfloat16)
     if workspace is None:
         workspace = Workspace.get(mla_workspace_size(prm), ql_nope.device, "mla")

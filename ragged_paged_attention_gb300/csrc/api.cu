@@ -132,9 +132,20 @@ struct LatLayout {
     int max_items;
 };
 
+// q_dtype and q_scale sit at the end of mla_params; a caller built against the struct
+// without them passes a struct_size that ends before them and gets bf16 queries
+int mla_q_dtype(const mla_params* p) {
+    if (p->struct_size < offsetof(mla_params, q_dtype) + sizeof(int32_t) || p->q_dtype == 0) return RPA_DTYPE_BF16;
+    return p->q_dtype;
+}
+
+float mla_q_scale(const mla_params* p) {
+    return p->struct_size >= offsetof(mla_params, q_scale) + sizeof(float) ? p->q_scale : 0.f;
+}
+
 int check_mla_params(const mla_params* p) {
     if (!p) return fail(RPA_ERR_NULL, "params is NULL");
-    if (p->struct_size < sizeof(mla_params)) return fail(RPA_ERR_VALUE, "mla_params.struct_size too small");
+    if (p->struct_size < offsetof(mla_params, q_dtype)) return fail(RPA_ERR_VALUE, "mla_params.struct_size too small");
     if (p->version != RPA_ABI_VERSION) return fail(RPA_ERR_VALUE, "mla_params.version %u != %d", p->version, RPA_ABI_VERSION);
     if (p->max_num_tokens <= 0 || p->num_q_heads <= 0 || p->total_num_pages <= 0 || p->page_size <= 0 ||
         p->max_num_seqs <= 0 || p->pages_per_seq <= 0 || p->kv_packing <= 0)
@@ -149,6 +160,12 @@ int check_mla_params(const mla_params* p) {
     if (!isfinite(p->soft_cap)) return fail(RPA_ERR_VALUE, "soft_cap must be finite (0 = none)");
     if (isinf(p->mask_value) && p->mask_value > 0.f) return fail(RPA_ERR_VALUE, "mask_value must not be +inf");
     if ((long long)p->max_num_seqs * p->pages_per_seq > INT32_MAX) return fail(RPA_ERR_SHAPE, "page table too large");
+    const int qd = mla_q_dtype(p);
+    if (qd != RPA_DTYPE_BF16 && qd != RPA_DTYPE_FP8_E4M3)
+        return fail(RPA_ERR_DTYPE, "mla q_dtype %d: queries are bf16 or fp8 e4m3", qd);
+    const float qs = mla_q_scale(p);
+    if (!isfinite(qs) || qs < 0.f) return fail(RPA_ERR_VALUE, "q_scale must be finite and >= 0 (0 = 1)");
+    if (qd == RPA_DTYPE_BF16 && qs != 0.f) return fail(RPA_ERR_VALUE, "q_scale applies to fp8 queries only");
     return RPA_OK;
 }
 
@@ -490,7 +507,9 @@ int mla_rpa_forward(const mla_params* p, const void* ql_nope, const void* q_pe, 
     memset(&a, 0, sizeof a);
     a.sparse = 0;
     a.num_heads = p->num_q_heads;
-    a.sm_scale = p->sm_scale;
+    // fp8 queries: the scores carry q_scale on top of sm_scale (one product, as a float)
+    a.q_fp8 = mla_q_dtype(p) == RPA_DTYPE_FP8_E4M3 ? 1 : 0;
+    a.sm_scale = mla_q_scale(p) != 0.f ? p->sm_scale * mla_q_scale(p) : p->sm_scale;
     a.soft_cap = p->soft_cap;
     a.sliding_window = p->sliding_window;
     a.mask_mild = mild_mask(p->mask_value) ? 1 : 0;

@@ -209,6 +209,21 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
     return __half22float2(hh);
 }
 
+// Eight e4m3 bytes (element 0 in the low byte) -> eight bf16 in the same order, exactly:
+// e4m3 has 3 mantissa bits and an exponent range bf16 covers, so every value survives
+// both the f16 and the bf16 step.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
+    const uint32_t w[2] = {v.x, v.y};
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = e4m3x2_to_float2((uint16_t)(w[i >> 1] >> ((i & 1) * 16)));
+        __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        r[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Swizzled byte offset of 16-byte chunk `c` of row `r` in a tile whose rows are
 // `row_bytes` long (a multiple of 128): XOR of the low three chunk bits with the
 // row index keeps eight consecutive rows of one logical chunk on distinct banks.

@@ -163,6 +163,7 @@ struct LatentArgs {
     // MLA
     const __nv_bfloat16* ql_nope;   // [T, H, 512]
     const __nv_bfloat16* q_pe;      // [T, H, 64]
+    int q_fp8;                      // ql_nope and q_pe hold fp8 e4m3 bytes (same shapes)
     const __nv_bfloat16* cache_kv_c;  // rows of lkv_pad
     const __nv_bfloat16* cache_k_pe;  // rows of r_pad
     const int32_t* kv_lens;

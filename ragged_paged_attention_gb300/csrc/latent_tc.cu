@@ -592,7 +592,14 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 uint4 buf[20];
 #pragma unroll
                 for (int i = 0; i < 20; ++i) {
-                    if (i < nch) {
+                    if (i < nch && !SPARSE && a.q_fp8) {  // fp8 queries: 8 bytes per chunk, widened
+                        const int c = c0 + i, p = c >> 3, cc = c & 7;
+                        const uint8_t* src = (rank == 0 && p == 4)
+                                                 ? reinterpret_cast<const uint8_t*>(a.q_pe) + qrow * 64 + cc * 8
+                                                 : reinterpret_cast<const uint8_t*>(a.ql_nope) + qrow * kLatDv +
+                                                       lat_panel_col(rank, p) + cc * 8;
+                        buf[i] = e4m3x8_to_bf16x8(__ldg(reinterpret_cast<const uint2*>(src)));
+                    } else if (i < nch) {
                         const int c = c0 + i, p = c >> 3, cc = c & 7;
                         const __nv_bfloat16* src = (SPARSE && a.q) ? a.q + qrow * kLatDk + lat_panel_col(rank, p) + cc * 8
                                                    : (rank == 0 && p == 4) ? a.q_pe + qrow * 64 + cc * 8

@@ -188,14 +188,18 @@ class MlaInputs:
     sliding_window: int | None = None
     soft_cap: float | None = None
     mask_value: float | None = None
+    q_scale: float | None = None
 
     @property
     def num_tokens(self) -> int:
         return int(sum(self.q_lens))
 
     def options(self) -> dict:
-        return dict(sm_scale=self.sm_scale, sliding_window=self.sliding_window, soft_cap=self.soft_cap,
+        opts = dict(sm_scale=self.sm_scale, sliding_window=self.sliding_window, soft_cap=self.soft_cap,
                     mask_value=self.mask_value)
+        if self.q_scale is not None:
+            opts["q_scale"] = self.q_scale
+        return opts
 
     def to(self, device) -> "MlaInputs":
         kw = {k: (v.to(device) if isinstance(v, torch.Tensor) else v)
@@ -206,7 +210,9 @@ class MlaInputs:
 def make_mla(q_lens, kv_lens, *, num_q_heads=128, lkv_dim=512, r_dim=64, page_size=64, kv_packing=2,
              seed, num_decode=None, pages_per_seq=None, max_num_seqs=None, max_num_tokens=None,
              extra_pages=0, sm_scale=None, sliding_window=None, soft_cap=None, mask_value=None,
-             poison=True) -> MlaInputs:
+             q_dtype=torch.bfloat16, q_scale=None, poison=True) -> MlaInputs:
+    """``q_dtype=torch.float8_e4m3fn`` draws the queries as N(0, 1) / q_scale (default 1/8)
+    rounded to e4m3: the per-tensor quantised queries whose scores carry q_scale."""
     rng = np.random.Generator(np.random.PCG64(seed))
     q_lens, kv_lens = [int(x) for x in q_lens], [int(x) for x in kv_lens]
     num_seqs = len(q_lens)
@@ -225,6 +231,12 @@ def make_mla(q_lens, kv_lens, *, num_q_heads=128, lkv_dim=512, r_dim=64, page_si
     ckv[..., :lkv_dim] = _randn(rng, (P, page_size, lkv_dim), torch.bfloat16)
     ckpe = torch.zeros((P, page_size, r_pad), dtype=torch.bfloat16)
     ckpe[..., :r_dim] = _randn(rng, (P, page_size, r_dim), torch.bfloat16)
+    if q_dtype == torch.float8_e4m3fn:
+        q_scale = 0.125 if q_scale is None else float(q_scale)
+        ql = (ql.float() / q_scale).to(q_dtype)
+        qpe = (qpe.float() / q_scale).to(q_dtype)
+    elif q_dtype != torch.bfloat16 or q_scale is not None:
+        raise ValueError("MLA queries are bf16, or float8_e4m3fn with a q_scale")
     if poison:
         _fill_nan(ql[T:])
         _fill_nan(qpe[T:])
@@ -257,7 +269,7 @@ def make_mla(q_lens, kv_lens, *, num_q_heads=128, lkv_dim=512, r_dim=64, page_si
         kv_lens=torch.from_numpy(kvl), page_indices=torch.from_numpy(table.reshape(-1).copy()),
         cu_q_lens=torch.from_numpy(cu), distribution=dist, q_lens=q_lens, kv_lens_list=kv_lens,
         sm_scale=(1.0 / math.sqrt(192.0)) if sm_scale is None else float(sm_scale),
-        sliding_window=sliding_window, soft_cap=soft_cap, mask_value=mask_value)
+        sliding_window=sliding_window, soft_cap=soft_cap, mask_value=mask_value, q_scale=q_scale)
 
 
 @dataclasses.dataclass

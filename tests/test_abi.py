@@ -122,3 +122,24 @@ def test_batch_kind_is_optional_and_checked(lib):
     assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
     p.struct_size = api.rpa_params.batch_kind.offset - 4
     assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == -4
+
+
+def test_mla_query_dtype_is_optional_and_checked(lib):
+    m = api.mla_params(struct_size=ctypes.sizeof(api.mla_params), version=1, max_num_tokens=8, num_q_heads=128,
+                       lkv_dim=512, r_dim=64, lkv_dim_pad=512, r_dim_pad=128, total_num_pages=4, page_size=64,
+                       kv_packing=2, max_num_seqs=2, pages_per_seq=2, sm_scale=0.07, sliding_window=0,
+                       soft_cap=0.0, mask_value=math.nan)
+    n = ctypes.c_size_t(0)
+    ws = lambda: lib.mla_workspace_size(ctypes.byref(m), ctypes.byref(n))  # noqa: E731
+    assert ws() == 0  # q_dtype 0 reads as bf16
+    for qd, qs, code in ((api.FP8_E4M3, 0.0, 0), (api.FP8_E4M3, 0.25, 0), (api.BF16, 0.25, -4),
+                         (api.FP8_E4M3, -1.0, -4), (api.FP8_E4M3, math.nan, -4), (api.INT8, 0.0, -3),
+                         (api.F32, 0.0, -3)):
+        m.q_dtype, m.q_scale = qd, qs
+        assert ws() == code, (qd, qs)
+    # a caller built against the struct without the two fields gets bf16 queries
+    m.q_dtype, m.q_scale = 77, -1.0
+    m.struct_size = api.mla_params.q_dtype.offset
+    assert ws() == 0
+    m.struct_size = api.mla_params.q_dtype.offset - 4
+    assert ws() == -4

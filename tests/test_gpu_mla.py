@@ -15,7 +15,7 @@ def run_and_check(m, tokens=None, **over):
     ref, ckv, ckpe = oracle.mla_forward(m.ql_nope, m.q_pe, m.new_kv_c, m.new_k_pe, m.cache_kv_c, m.cache_k_pe,
                                         m.kv_lens, m.page_indices, m.cu_q_lens, m.distribution, tokens=tokens, **opts)
     g = m.to("cuda")
-    out = torch.full_like(g.ql_nope, 7.0)
+    out = torch.full(g.ql_nope.shape, 7.0, dtype=torch.bfloat16, device="cuda")
     prm = api.make_mla_params(g.ql_nope, g.q_pe, g.cache_kv_c, g.cache_k_pe, g.kv_lens, g.page_indices, **opts)
     ws = torch.zeros(api.mla_workspace_size(prm), dtype=torch.uint8, device="cuda")
     api.mla_rpa_forward(g.ql_nope, g.q_pe, g.new_kv_c, g.new_k_pe, g.cache_kv_c, g.cache_k_pe, g.kv_lens,
@@ -68,3 +68,18 @@ def test_mla_mild_mask_value_replaces(mask, sw):
     # and the keys outside the window at mask_value.
     m = workloads.make_mla([1, 1, 40, 3], [700, 65, 300, 9], seed=24, max_num_tokens=48)
     run_and_check(m, mask_value=mask, sliding_window=sw)
+
+
+@pytest.mark.parametrize("q_scale,sw,cap", [(0.125, None, None), (0.03, 100, 25.0), (0.5, None, None)])
+def test_mla_fp8_queries(q_scale, sw, cap):
+    # per-tensor fp8 e4m3 queries: widened exactly in the kernel, scores carry q_scale
+    m = workloads.make_mla([1, 1, 40, 3, 70], [700, 65, 300, 9, 70], seed=25, max_num_tokens=128,
+                           q_dtype=torch.float8_e4m3fn, q_scale=q_scale)
+    assert m.ql_nope.dtype == torch.float8_e4m3fn
+    run_and_check(m, sliding_window=sw, soft_cap=cap)
+
+
+def test_mla_fp8_queries_full_size_sampled():
+    m0 = workloads.mla_deepseek()
+    m = workloads.make_mla(m0.q_lens, m0.kv_lens_list, seed=26, q_dtype=torch.float8_e4m3fn)
+    run_and_check(m, tokens=sample_tokens(m.q_lens, per_chunk=2))

@@ -52,14 +52,18 @@ def test_sparse_duplicates_and_future_units():
 @pytest.mark.parametrize("mode", ["token", "page"])
 def test_sparse_prefill_full_size_sampled(mode):
     s = workloads.dsa_sparse(mode=mode, phase="prefill")
+    # 48 queries: the first and the last, and one drawn from each of 46 equal strata between
+    n = s.positions.numel()
     rng = np.random.default_rng(5)
-    run_and_check(s, queries=sorted(rng.choice(s.positions.numel(), size=12, replace=False).tolist()))
+    edges = np.linspace(1, n - 1, 47).astype(int)
+    mid = [int(rng.integers(lo, max(lo + 1, hi))) for lo, hi in zip(edges[:-1], edges[1:])]
+    run_and_check(s, queries=sorted({0, n - 1, *mid}))
 
 
 @pytest.mark.parametrize("mode", ["token", "page"])
 def test_sparse_decode_full_size_sampled(mode):
     s = workloads.dsa_sparse(mode=mode, phase="decode")
-    run_and_check(s, queries=list(range(0, 64, 5)))
+    run_and_check(s, queries=list(range(s.positions.numel())))  # every query of the batch
 
 
 def test_sparse_split_merge():
@@ -117,5 +121,5 @@ def test_sparse_ragged_full_size_sampled():
     for mode in ("token", "page"):
         s = workloads.dsa_sparse_ragged(mode=mode)
         rng = np.random.default_rng(3)
-        tokens = sorted(rng.choice(s.ql.shape[0], size=24, replace=False).tolist())
+        tokens = sorted(rng.choice(s.ql.shape[0], size=48, replace=False).tolist())
         run_ragged(s, tokens=tokens)
