@@ -79,7 +79,7 @@ struct PreTc {
     static constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;  // [2 parities][2 halves][128 rows] float
     static constexpr int kOffQmul = kOffRed + 2 * 2 * 128 * 4;           // [128] float: Q row factors (f16 path)
     static constexpr int kOffItem = kOffQmul + 128 * 4;                  // [2] WorkItem ring (16-byte aligned) + abort flag
-    static constexpr int kSmem = kOffItem + 2 * 32 + 16;
+    static constexpr int kSmem = kOffItem + 2 * 32 + 16 + 32;  // + each softmax warp's kv_len
     static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffItem % 16 == 0, "shared-memory alignment");
     static_assert(NSK >= 2 && NSV >= 2 && kOffK % 1024 == 0 && kOffV % 1024 == 0, "stages / swizzle-atom alignment");
     static_assert(!RAW || (NR >= 2 && kOffRawK % 1024 == 0 && kOffRawV % 1024 == 0 && (D == 128 || D == 256)),
@@ -199,7 +199,10 @@ __device__ __forceinline__ void raw16_convert(uint4 r, float sc, uint4& lo, uint
 // them shared memory to shared memory into the f16/bf16 panels and put Q into TMEM (the QK
 // MMAs read A from there), and S has one TMEM buffer.
 // I4 (int4 caches, two elements a byte): the register path, each 8-element chunk 4 bytes.
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false, bool I4 = false>
+// MILD: a mask value that leaves masked keys weight (rare: its own, register-path instantiations,
+// so that the common ones carry none of its code)
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false, bool I4 = false,
+          bool MILD = false>
 __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
     rpa_prefill_tc_kernel(RpaArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                           int box_rows, int q_tma, int tail) {
@@ -365,9 +368,9 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
         const int R1 = min(n_rows, R0 + 128) - 1;
         const int qmin = kv_len - q_len + R0 / G, qmax = kv_len - q_len + R1 / G;
         // keys the tile's rows see: the causal (windowed) range, or every key with a mild mask
-        int kb = a.sliding_window > 0 && !a.mask_mild ? max(0, qmin - a.sliding_window + 1) : 0;
+        int kb = a.sliding_window > 0 && !MILD ? max(0, qmin - a.sliding_window + 1) : 0;
         kb = kb / BK * BK;
-        const int ke = a.mask_mild ? kv_len : qmax + 1;
+        const int ke = MILD ? kv_len : qmax + 1;
         const int nb = cdiv(ke - kb, BK);
         const uint32_t iph = items & 1;
 
@@ -876,6 +879,13 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
             const int qpos = rv ? kv_len - q_len + R / G : -1;
             const int wlo = a.sliding_window > 0 ? qpos - a.sliding_window + 1 : INT_MIN;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            // kv_len is needed again only by a mild mask: this warp's copy waits in shared memory
+            // instead of a register held through the block loop
+            volatile int* s_kvl = reinterpret_cast<volatile int*>(smem + T::kOffItem + 80) + warp;
+            if constexpr (MILD) {
+                if (lane == 0) *s_kvl = kv_len;
+                __syncwarp();
+            }
             // F16: the row's power of two (set by the producers with Q) and k_scale go onto its scores
             float srow = 1.f;
             bool q_ok = true;
@@ -943,12 +953,21 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                 // sequence are dropped
                 const bool inside = key0 >= wlo && key0 + HB - 1 <= qpos;
                 if (__any_sync(0xffffffffu, !inside)) {
-                    const float madd = fold ? a.mask_value / scale : a.mask_value * kLog2e;
+                    if constexpr (!MILD) {
 #pragma unroll
-                    for (int i = 0; i < HB; ++i) {
-                        const int key = key0 + i;
-                        const bool vis = key <= qpos && key >= wlo;
-                        x[i] = vis ? x[i] : (a.mask_mild && key < kv_len) ? x[i] + madd : -INFINITY;
+                        for (int i = 0; i < HB; ++i) {
+                            const int key = key0 + i;
+                            x[i] = (key <= qpos && key >= wlo) ? x[i] : -INFINITY;
+                        }
+                    } else {
+                        const float madd = fold ? a.mask_value / scale : a.mask_value * kLog2e;
+                        const int kvl = *s_kvl;
+#pragma unroll
+                        for (int i = 0; i < HB; ++i) {
+                            const int key = key0 + i;
+                            const bool vis = key <= qpos && key >= wlo;
+                            x[i] = vis ? x[i] : key < kvl ? x[i] + madd : -INFINITY;
+                        }
                     }
                 }
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -1118,11 +1137,12 @@ static bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t d0, uint64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false, bool I4 = false>
+template <int D, bool FP8, bool SCALE, bool TMA, bool I8 = false, bool F16 = false, bool RAW = false, bool I4 = false,
+          bool MILD = false>
 static cudaError_t launch_pre(const RpaArgs& a, int num_sms, cudaStream_t stream, const CUtensorMap& tkv,
                               const CUtensorMap& tq, int box_rows, int q_tma, int tail) {
     using T = PreTc<D, RAW>;
-    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16, RAW, I4>;
+    auto kern = rpa_prefill_tc_kernel<D, FP8, SCALE, TMA, I8, F16, RAW, I4, MILD>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
@@ -1146,6 +1166,14 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     // the block, or boxes too small for one lane each, take the register path
     const int box_rows = ps < BK ? ps : BK;
     // (boxes of >= 8 rows keep every TMA destination on a 1024-byte swizzle-atom boundary)
+    if (a.mask_mild) {
+        // mild masks: the register path for every cache type (one-byte caches dequantised to bf16)
+        if (a.kv_int4) return launch_pre<D, true, false, false, false, false, false, true, true>(a, num_sms, stream, tkv, tq, 0, 0, tail);
+        if (a.kv_int8) return launch_pre<D, true, false, false, true, false, false, false, true>(a, num_sms, stream, tkv, tq, 0, 0, tail);
+        if (a.kv_byte) return launch_pre<D, true, false, false, false, false, false, false, true>(a, num_sms, stream, tkv, tq, 0, 0, tail);
+        if (a.has_scale) return launch_pre<D, false, true, false, false, false, false, false, true>(a, num_sms, stream, tkv, tq, 0, 0, tail);
+        return launch_pre<D, false, false, false, false, false, false, false, true>(a, num_sms, stream, tkv, tq, 0, 0, tail);
+    }
     bool tma = !a.kv_byte && !a.has_scale && (ps & (ps - 1)) == 0 && box_rows >= 8 && BK / box_rows <= 32;
     const uint64_t tokens = (uint64_t)a.total_num_pages * ps;
     if (tma) tma = make_tmap_bf16(&tkv, a.kv_pages, D, C, tokens, 1, box_rows);
