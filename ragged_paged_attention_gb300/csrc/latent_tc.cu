@@ -22,10 +22,11 @@
 // its own in flight) passes that on to the peer with one cluster-scope release arrive.
 // Row statistics (m, l) of the owned rows go to the peer once per item.
 // Warps per CTA: 0-7 softmax (two per TMEM lane quarter, 32 of the 64 columns each; a
-// quarter's warps are owners or helpers), 8-11 producers, 12 MMA issuer, 13 signalling.  MLA keys are the causal (windowed) prefix gathered page
-// by page with 2-D TMA boxes (the partial last page through registers); sparse keys are
-// the selected units' rows, gathered through registers with their validity recorded for
-// the softmax.  Items split long key ranges; partials merge by the log-sum-exp rule.
+// quarter's warps are owners or helpers), 8-11 producers, 12 MMA issuer, 13 signalling.
+// MLA keys are the causal (windowed) prefix, brought page by page with TMA boxes (the
+// partial last page through registers); sparse keys are the selected units' rows, four at a
+// time by TMA tile::gather4 copies, with their validity recorded for the softmax.  Items
+// split long key ranges; partials merge by the log-sum-exp rule.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
