@@ -138,7 +138,9 @@ typedef struct {
     int32_t max_num_tokens;
     int32_t num_q_heads;
     int32_t num_combined_kv_heads;
-    int32_t head_dim;            /* 64, 128 or 256 */
+    int32_t head_dim;            /* 64, 128 or 256; 96 or 192 for attention over a bf16 cache without
+                                    scales, with a power-of-two page_size >= 8 and a mask_value at or
+                                    below -1e30 (the cache write takes any of the five) */
     int32_t total_num_pages;
     int32_t page_size;
     int32_t max_num_seqs;

@@ -77,8 +77,8 @@ int check_rpa_params(const rpa_params* p) {
     if (p->num_combined_kv_heads % 2) return fail(RPA_ERR_SHAPE, "num_combined_kv_heads must be even (K and V interleaved)");
     const int hkv = p->num_combined_kv_heads / 2;
     if (p->num_q_heads % hkv) return fail(RPA_ERR_SHAPE, "num_q_heads %d not divisible by num_kv_heads %d", p->num_q_heads, hkv);
-    if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
-        return fail(RPA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", p->head_dim);
+    if (p->head_dim != 64 && p->head_dim != 96 && p->head_dim != 128 && p->head_dim != 192 && p->head_dim != 256)
+        return fail(RPA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 96, 128, 192, 256)", p->head_dim);
     if (p->q_dtype != RPA_DTYPE_BF16) return fail(RPA_ERR_DTYPE, "q_dtype must be bf16");
     if (p->kv_dtype != RPA_DTYPE_BF16 && p->kv_dtype != RPA_DTYPE_FP8_E4M3 && p->kv_dtype != RPA_DTYPE_INT8 &&
         p->kv_dtype != RPA_DTYPE_INT4)
@@ -293,6 +293,16 @@ static int rpa_prepare(const rpa_params* p, const void* q, const void* kv_pages,
         return fail(RPA_ERR_NULL, "a tensor pointer is NULL");
     if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out)) return fail(RPA_ERR_VALUE, "q, kv_pages and out must be 16-byte aligned");
     if (out == q || out == kv_pages) return fail(RPA_ERR_VALUE, "out must not alias q or kv_pages");
+    if (p->head_dim == 96 || p->head_dim == 192) {
+        // the prefill kernel runs these at the next multiple of 128 with the tensor maps'
+        // zero fill for the missing dims, which needs its TMA path
+        const int ps = p->page_size;
+        if (p->kv_dtype != RPA_DTYPE_BF16 || p->k_scale != 0.f || p->v_scale != 0.f || mild_mask(p->mask_value) ||
+            (ps & (ps - 1)) != 0 || ps < 8)
+            return fail(RPA_ERR_UNSUPPORTED,
+                        "head_dim %d attention needs a bf16 cache without scales, a power-of-two page_size >= 8 "
+                        "and a mask_value at or below -1e30", p->head_dim);
+    }
     const RpaLayout L = rpa_layout(p);
     rc = check_workspace(workspace, workspace_bytes, L.total);
     if (rc) return rc;

@@ -681,7 +681,10 @@ static cudaError_t launch_decode_d(const RpaArgs& a, int num_sms, cudaStream_t s
 static cudaError_t decode_dispatch(const RpaArgs& a, int num_sms, cudaStream_t stream, int* per_sm_out) {
     switch (a.head_dim) {
         case 64: return launch_decode_d<64>(a, num_sms, stream, per_sm_out);
+        // head_dim 96 and 192: bf16 caches without scales (the host admits nothing else)
+        case 96: return launch_decode<96, 4, 2, false>(a, num_sms, stream, per_sm_out);
         case 128: return launch_decode_d<128>(a, num_sms, stream, per_sm_out);
+        case 192: return launch_decode<192, 4, 2, false>(a, num_sms, stream, per_sm_out);
         case 256: return launch_decode_d<256>(a, num_sms, stream, per_sm_out);
         default: return cudaErrorInvalidValue;
     }

@@ -623,8 +623,11 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                 for (int r = pt; r < 128; r += nprod) {
                     const int R = R0 + r;
                     const bool rv = R < n_rows;
+                    // rows are a.head_dim wide (below D when the kernel runs at the next multiple
+                    // of 128: the dims past it are zeros)
+                    const int dq8 = a.head_dim / 8;
                     const uint8_t* src = reinterpret_cast<const uint8_t*>(
-                        a.q + ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D);
+                        a.q + ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * a.head_dim);
                     float qs = 1.f;
                     if (F16) {
                         // the row's largest |q| < 2^ex; 2^-k brings it into [2^14, 2^15) (f16 range)
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                     }
 #pragma unroll 8
                     for (int c = 0; c < D / 8; ++c) {
-                        uint4 v = rv ? __ldg(reinterpret_cast<const uint4*>(src + c * 16)) : make_uint4(0, 0, 0, 0);
+                        uint4 v = rv && c < dq8 ? __ldg(reinterpret_cast<const uint4*>(src + c * 16)) : make_uint4(0, 0, 0, 0);
                         if (F16) {
                             const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
                             uint32_t w[4];
@@ -725,8 +728,12 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                             const int tr = i / kCh, c = p0 * 8 + i % kCh;
                             if (c >= D / 8) continue;
                             const int kk = nfull * box_rows + tr;
-                            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                                kvp + ((size_t)(pz0 + tr) * C + 2 * kvh + part) * (size_t)(D * 2) + c * 16));
+                            // dims past a.head_dim (a kernel run at the next multiple of 128) are zeros
+                            const uint4 v = c * 8 < a.head_dim
+                                                ? __ldg(reinterpret_cast<const uint4*>(
+                                                      kvp + ((size_t)(pz0 + tr) * C + 2 * kvh + part) * (size_t)(a.head_dim * 2) +
+                                                      c * 16))
+                                                : make_uint4(0, 0, 0, 0);
                             *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) = v;
                         }
                     }
@@ -1049,14 +1056,15 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                 tc_fence_after();
                 const float inv = l_run > 0.f ? (F16 ? a.v_scale_or_one : 1.f) / l_run : 0.f;
                 __nv_bfloat16* dst = a.out +
-                                     ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) * D +
+                                     ((size_t)(q_start + (rv ? R / G : 0)) * a.num_q_heads + kvh * G + (rv ? R % G : 0)) *
+                                         a.head_dim +
                                      half * (D / 2);
                 // every lane runs the (warp-collective) TMEM loads; only real rows store
 #pragma unroll 1
                 for (int c = 0; c < D / 64; ++c) {
                     float o32[32];
                     tmem_ld32(tmem + lane_off + T::kColO + half * (D / 2) + c * 32, o32);
-                    if (rv) {
+                    if (rv && half * (D / 2) + c * 32 < a.head_dim) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o32[2 * i] * inv, o32[2 * i + 1] * inv);
@@ -1166,6 +1174,7 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     // the block, or boxes too small for one lane each, take the register path
     const int box_rows = ps < BK ? ps : BK;
     // (boxes of >= 8 rows keep every TMA destination on a 1024-byte swizzle-atom boundary)
+    if (a.head_dim != D && (a.mask_mild || a.kv_byte || a.has_scale)) return cudaErrorInvalidValue;
     if (a.mask_mild) {
         // mild masks: the register path for every cache type (one-byte caches dequantised to bf16)
         if (a.kv_int4) return launch_pre<D, true, false, false, false, false, false, true, true>(a, num_sms, stream, tkv, tq, 0, 0, tail);
@@ -1176,11 +1185,14 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
     }
     bool tma = !a.kv_byte && !a.has_scale && (ps & (ps - 1)) == 0 && box_rows >= 8 && BK / box_rows <= 32;
     const uint64_t tokens = (uint64_t)a.total_num_pages * ps;
-    if (tma) tma = make_tmap_bf16(&tkv, a.kv_pages, D, C, tokens, 1, box_rows);
+    // (the maps are a.head_dim wide: at head_dim 96 or 192 the boxes' columns past it read
+    // the fill value, zero, so the kernel runs at D = the next multiple of 128 unchanged)
+    if (tma) tma = make_tmap_bf16(&tkv, a.kv_pages, a.head_dim, C, tokens, 1, box_rows);
     int q_tma = 0;
     if (tma && 128 % G == 0)
-        q_tma = make_tmap_bf16(&tq, a.q, D, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
+        q_tma = make_tmap_bf16(&tq, a.q, a.head_dim, a.num_q_heads, a.max_num_tokens, G, 128 / G) ? 1 : 0;
     if (tma) return launch_pre<D, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, q_tma, tail);
+    if (a.head_dim != D) return cudaErrorInvalidValue;  // (the host admits such shapes only where TMA runs)
     // int4 caches: dequantised to bf16 through registers
     if (a.kv_int4) return launch_pre<D, true, false, false, false, false, false, true>(a, num_sms, stream, tkv, tq, box_rows, 0, tail);
     // one-byte caches with power-of-two scales: exact f16 operands, scales on S and O
@@ -1211,7 +1223,9 @@ static cudaError_t launch_pre_d(const RpaArgs& a, int num_sms, cudaStream_t stre
 cudaError_t launch_rpa_prefill(const RpaArgs& a, int num_sms, cudaStream_t stream, int tail) {
     switch (a.head_dim) {
         case 64: return launch_pre_d<64>(a, num_sms, stream, tail);
+        case 96:
         case 128: return launch_pre_d<128>(a, num_sms, stream, tail);
+        case 192:
         case 256: return launch_pre_d<256>(a, num_sms, stream, tail);
         default: return cudaErrorInvalidValue;
     }

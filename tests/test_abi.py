@@ -51,7 +51,7 @@ def good_rpa():
 
 
 @pytest.mark.parametrize("field,value,code", [
-    ("num_combined_kv_heads", 3, -2), ("num_q_heads", 5, -2), ("head_dim", 96, -5), ("q_dtype", 2, -3),
+    ("num_combined_kv_heads", 3, -2), ("num_q_heads", 5, -2), ("head_dim", 80, -5), ("q_dtype", 2, -3),
     ("kv_dtype", 3, -3), ("sliding_window", -1, -4), ("soft_cap", math.inf, -4), ("mask_value", math.inf, -4),
     ("version", 7, -4), ("struct_size", 4, -4), ("page_size", 0, -2), ("sm_scale", math.nan, -4),
 ])
@@ -143,3 +143,20 @@ def test_mla_query_dtype_is_optional_and_checked(lib):
     assert ws() == 0
     m.struct_size = api.mla_params.q_dtype.offset - 4
     assert ws() == -4
+
+
+def test_head_dim_96_attention_is_bf16_only(lib):
+    # 96 and 192 pass the parameter check (the cache write takes any dtype) but attention at
+    # those widths needs a bf16 cache without scales: refused before anything launches
+    p = good_rpa()
+    p.head_dim = 96
+    n = ctypes.c_size_t(0)
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    ptrs = [ctypes.c_void_p(256 * (i + 1)) for i in range(7)]
+    ws = ctypes.c_void_p(1 << 20)
+    for field, value in (("kv_dtype", 2), ("k_scale", 0.5), ("page_size", 12), ("mask_value", -1.5)):
+        q = good_rpa()
+        q.head_dim = 96
+        setattr(q, field, value)
+        assert lib.rpa_forward(ctypes.byref(q), *ptrs, ws, 1 << 30, None) == -5, field
+        assert b"head_dim 96" in lib.rpa_last_error()

@@ -389,3 +389,40 @@ def test_int4_update_then_attend():
     ref = oracle.rpa(b.q, ref_pages, b.kv_lens, b.page_indices, b.cu_q_lens, n, **b.options())
     T = b.num_tokens
     assert max_abs(out[:T], ref[:T]) <= 2e-2 * float(ref[:T].abs().max())
+
+
+@pytest.mark.parametrize("d", [96, 192])
+@pytest.mark.parametrize("hq,hkv,ps,sw,cap", [(8, 2, 16, None, None), (16, 4, 32, 40, 30.0), (12, 4, 8, None, None),
+                                              (4, 4, 64, 100, None)])
+def test_head_dim_96_and_192(d, hq, hkv, ps, sw, cap):
+    # head_dim that is not a multiple of 64: decode at its own width, prefill at the next multiple
+    # of 128 with the tensor maps' zero fill past the row (G = 3 takes the per-thread Q rows)
+    b = workloads.make_rpa([1, 1, 3, 40, 130, 2], [1, 700, 64, 40, 300, 77], num_q_heads=hq, num_kv_heads=hkv,
+                           head_dim=d, page_size=ps, seed=d + hq + ps, max_num_seqs=8, max_num_tokens=200,
+                           extra_pages=2, sliding_window=sw, soft_cap=cap)
+    check(b, TOL_BF16)
+
+
+def test_head_dim_96_update_then_attend():
+    b = workloads.make_rpa([1, 5, 33], [90, 5, 200], num_q_heads=8, num_kv_heads=2, head_dim=96, page_size=16,
+                           seed=97, extra_pages=2)
+    T = b.num_tokens
+    rng = np.random.default_rng(98)
+    nk = torch.from_numpy(rng.standard_normal((b.q.shape[0], 2, 96), dtype=np.float32)).to(torch.bfloat16)
+    nv = torch.from_numpy(rng.standard_normal((b.q.shape[0], 2, 96), dtype=np.float32)).to(torch.bfloat16)
+    kv_ref = oracle.rpa_update_kv_cache(nk, nv, b.kv_pages, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens))
+    g = b.to("cuda")
+    out = api.rpa_forward_update(g.q, nk.cuda(), nv.cuda(), g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens,
+                                 g.num_seqs, **b.options())
+    torch.cuda.synchronize()
+    assert torch.equal(g.kv_pages.cpu().view(torch.int16), kv_ref.view(torch.int16))
+    ref = oracle.rpa(b.q, kv_ref, b.kv_lens, b.page_indices, b.cu_q_lens, len(b.q_lens), **b.options())
+    assert max_abs(out[:T], ref[:T]) <= TOL_BF16
+
+
+def test_head_dim_96_refuses_what_its_prefill_cannot_run():
+    b = workloads.make_rpa([1, 9], [40, 30], num_q_heads=8, num_kv_heads=2, head_dim=96, page_size=16, seed=99,
+                           kv_dtype=torch.float8_e4m3fn)
+    g = b.to("cuda")
+    with pytest.raises(api.RpaError, match="RPA_ERR_UNSUPPORTED"):
+        api.rpa_forward(g.q, g.kv_pages, g.kv_lens, g.page_indices, g.cu_q_lens, g.num_seqs, **b.options())
