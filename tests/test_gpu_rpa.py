@@ -188,9 +188,11 @@ def test_bad_page_index_sets_device_error():
     assert bits & 0x04
 
 
-@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn, torch.int8])
-def test_update_kv_cache_bit_exact(kv_dtype):
-    b = workloads.make_rpa([1, 1, 6, 19], [33, 1, 6, 40], num_q_heads=8, num_kv_heads=4, head_dim=128, page_size=16,
+@pytest.mark.parametrize("d", [128, 96, 192])
+@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn, torch.int8, torch.uint8])
+def test_update_kv_cache_bit_exact(kv_dtype, d):
+    # (uint8: packed int4; the cache write moves any of the dtypes at any of the head sizes)
+    b = workloads.make_rpa([1, 1, 6, 19], [33, 1, 6, 40], num_q_heads=8, num_kv_heads=4, head_dim=d, page_size=16,
                            seed=18, kv_dtype=kv_dtype, max_num_seqs=6, max_num_tokens=32, extra_pages=4)
     ref = oracle.rpa_update_kv_cache(b.new_k[:b.num_tokens].contiguous(), b.new_v[:b.num_tokens].contiguous(),
                                      b.kv_pages, b.kv_lens[:4], b.page_indices[:4], b.cu_q_lens[:5], 4)
