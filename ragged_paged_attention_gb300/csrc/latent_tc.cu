@@ -60,6 +60,8 @@ constexpr int kSmem = kOffItem + 64;  // item, abort flag, item index, index rin
 // P [128 x 64] bf16 pairs at 224, the O half [128 x 256] fp32 at 256.
 constexpr int kColS = 0, kColQ = BK, kColP = 224, kColO = 256;
 constexpr int kTmemCols = 512;
+// split merges keep their weights [split][128 rows] in the idle key ring (up to this many splits)
+constexpr int kMergeSplits = NS * kStage / (128 * 4);
 constexpr int kWarps = 14;
 constexpr int kProdW0 = 8, kMmaW = 12, kSigW = 13;
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -364,6 +366,9 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                                     tma_load_2d(dst, &tm_kc, lat_panel_col(rank, p), row0, &kv_full[st]);
                             }
                         }
+                        // a partial box (the sequence's last keys): its rows by cp.async, all of
+                        // them in flight at once (rows past the range keep finite stale data,
+                        // whose scores the mask drops)
                         uint32_t pm = __ballot_sync(0xffffffffu, rows > 0 && !full);
                         const bool wrote = pm != 0;
                         while (pm) {
@@ -377,11 +382,14 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                                 const __nv_bfloat16* s_row = (rank == 0 && p == 4)
                                                                   ? a.cache_k_pe + (size_t)(pr0 + r) * a.r_pad
                                                                   : a.cache_kv_c + (size_t)(pr0 + r) * a.lkv_pad + lat_panel_col(rank, p);
-                                const uint4 v = __ldg(reinterpret_cast<const uint4*>(s_row + c * 8));
-                                *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)) = v;
+                                cp_async16(smem_u32(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)), s_row + c * 8, true);
                             }
                         }
-                        if (wrote) fence_proxy_async_smem();  // register-written rows, read by the tensor core
+                        if (wrote) {
+                            cp_async_commit();
+                            cp_async_wait<0>();
+                            fence_proxy_async_smem();  // thread-copied rows, read by the tensor core
+                        }
                         mbar_arrive(&kv_full[st]);
                     }
                 }
@@ -882,64 +890,134 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             __syncthreads();
             if (s_last) {
                 __threadfence();
-                // merge: a warp per row at a time; each lane holds one split's (m, l) and two
-                // float4 of this rank's 256 output columns (loads of a row are contiguous), and
-                // four splits' loads are in flight at once
                 const int ns = w.num_splits;
                 const size_t ib = (size_t)w.first_item * 128;
-                const int cbase = (int)rank * 256 + lane * 4;
-                for (int rr = warp; rr < 128; rr += lat::kWarps) {
-                    if (h0 + rr >= H) continue;
-                    float M = -INFINITY;
-                    for (int s0 = lane; s0 < ns; s0 += 32) M = fmaxf(M, __ldcg(a.partial_ml + ((ib + (size_t)s0 * 128 + rr) * 2)));
-                    M = warp_max(M);
-                    const float Mu = M == -INFINITY ? 0.f : M;
-                    float L = 0.f;
-                    for (int s0 = lane; s0 < ns; s0 += 32) {
-                        const size_t base = (ib + (size_t)s0 * 128 + rr) * 2;
-                        L += fast_exp2(__ldcg(a.partial_ml + base) - Mu) * __ldcg(a.partial_ml + base + 1);
+                if (ns <= kMergeSplits) {
+                    // merge, row-parallel: the key ring is idle between items and holds the
+                    // weights [split][row]. Thread r < 128 owns row r: its splits' (m, l) loads in
+                    // flight together, then the row's max, sum and each split's weight
+                    float* wgt = reinterpret_cast<float*>(smem + kOffKV);
+                    if (tid < 128) {
+                        float M = -INFINITY;
+#pragma unroll 4
+                        for (int s0 = 0; s0 < ns; ++s0) M = fmaxf(M, __ldcg(a.partial_ml + (ib + (size_t)s0 * 128 + tid) * 2));
+                        const float Mu = M == -INFINITY ? 0.f : M;
+                        float L = 0.f;
+#pragma unroll 4
+                        for (int s0 = 0; s0 < ns; ++s0) {
+                            const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.partial_ml + (ib + (size_t)s0 * 128 + tid) * 2));
+                            const float e = fast_exp2(ml.x - Mu);
+                            wgt[s0 * 128 + tid] = e;
+                            L += e * ml.y;
+                        }
+                        const float inv = L > 0.f ? 1.f / L : 0.f;
+                        for (int s0 = 0; s0 < ns; ++s0) wgt[s0 * 128 + tid] *= inv;
                     }
-                    L = warp_sum(L);
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
-                    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-                    for (int s0 = 0; s0 < ns; s0 += 32) {
-                        // lane l: the factor of split s0 + l
-                        const int sl = s0 + lane;
-                        const float fl = sl < ns ? fast_exp2(__ldcg(a.partial_ml + (ib + (size_t)sl * 128 + rr) * 2) - Mu) * inv : 0.f;
-                        const int cnt = min(32, ns - s0);
-                        for (int j = 0; j < cnt; j += 4) {
-                            float4 v[8];
-                            float f[4];
+                    __syncthreads();
+                    // O: this rank's [128 x 256] as 8192 float4 chunks (row c / 64, columns
+                    // 4 (c % 64) of this rank's half); a thread takes eight chunks at a time, their
+                    // eight loads of one split in flight together
+                    constexpr int kPer = 8;
+                    const int nthr = (int)blockDim.x;
+                    for (int c0 = tid; c0 < 128 * 64; c0 += nthr * kPer) {
+                        float4 acc[kPer];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                f[u] = __shfl_sync(0xffffffffu, fl, (j + u) & 31);
-                                const bool in = j + u < cnt;
-                                const float* po = a.partial_o + (ib + (size_t)(s0 + j + u) * 128 + rr) * kLatDv + cbase;
-                                v[2 * u] = in ? __ldcg(reinterpret_cast<const float4*>(po)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                                v[2 * u + 1] = in ? __ldcg(reinterpret_cast<const float4*>(po + 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (!in) f[u] = 0.f;
+                        for (int j = 0; j < kPer; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                        for (int s0 = 0; s0 < ns; ++s0) {
+                            float4 v[kPer];
+#pragma unroll
+                            for (int j = 0; j < kPer; ++j) {
+                                const int c = c0 + j * nthr;
+                                const bool in = c < 128 * 64;
+                                const int rr = in ? c >> 6 : 0;
+                                v[j] = in ? __ldcg(reinterpret_cast<const float4*>(a.partial_o + (ib + (size_t)s0 * 128 + rr) * kLatDv +
+                                                                                   rank * 256 + (c & 63) * 4))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                acc0.x += f[u] * v[2 * u].x;
-                                acc0.y += f[u] * v[2 * u].y;
-                                acc0.z += f[u] * v[2 * u].z;
-                                acc0.w += f[u] * v[2 * u].w;
-                                acc1.x += f[u] * v[2 * u + 1].x;
-                                acc1.y += f[u] * v[2 * u + 1].y;
-                                acc1.z += f[u] * v[2 * u + 1].z;
-                                acc1.w += f[u] * v[2 * u + 1].w;
+                            for (int j = 0; j < kPer; ++j) {
+                                const int c = c0 + j * nthr;
+                                const float f = wgt[s0 * 128 + (c < 128 * 64 ? c >> 6 : 0)];
+                                acc[j].x += f * v[j].x;
+                                acc[j].y += f * v[j].y;
+                                acc[j].z += f * v[j].z;
+                                acc[j].w += f * v[j].w;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < kPer; ++j) {
+                            const int c = c0 + j * nthr;
+                            if (c >= 128 * 64) continue;
+                            const int rr = c >> 6, col = (int)rank * 256 + (c & 63) * 4;
+                            if (h0 + rr >= H) continue;
+                            if (SPARSE) {
+                                *reinterpret_cast<float4*>(a.out_f32 + ((size_t)w.seq * H + h0 + rr) * kLatDv + col) = acc[j];
+                            } else {
+                                *reinterpret_cast<uint2*>(a.out_bf16 + ((size_t)t * H + h0 + rr) * kLatDv + col) =
+                                    make_uint2(pack_bf16(acc[j].x, acc[j].y), pack_bf16(acc[j].z, acc[j].w));
                             }
                         }
                     }
-                    if (SPARSE) {
-                        float* o = a.out_f32 + ((size_t)w.seq * H + h0 + rr) * kLatDv + cbase;
-                        *reinterpret_cast<float4*>(o) = acc0;
-                        *reinterpret_cast<float4*>(o + 128) = acc1;
-                    } else {
-                        __nv_bfloat16* o = a.out_bf16 + ((size_t)t * H + h0 + rr) * kLatDv + cbase;
-                        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16(acc0.x, acc0.y), pack_bf16(acc0.z, acc0.w));
-                        *reinterpret_cast<uint2*>(o + 128) = make_uint2(pack_bf16(acc1.x, acc1.y), pack_bf16(acc1.z, acc1.w));
+                    fence_proxy_async_smem();  // the ring is refilled by TMA for the next item
+                } else {
+                    // (more splits than the ring holds weights for) a warp per row at a time; each
+                    // lane holds one split's (m, l) and two float4 of this rank's 256 output columns,
+                    // four splits' loads in flight at once
+                    const int cbase = (int)rank * 256 + lane * 4;
+                    for (int rr = warp; rr < 128; rr += lat::kWarps) {
+                        if (h0 + rr >= H) continue;
+                        float M = -INFINITY;
+                        for (int s0 = lane; s0 < ns; s0 += 32) M = fmaxf(M, __ldcg(a.partial_ml + ((ib + (size_t)s0 * 128 + rr) * 2)));
+                        M = warp_max(M);
+                        const float Mu = M == -INFINITY ? 0.f : M;
+                        float L = 0.f;
+                        for (int s0 = lane; s0 < ns; s0 += 32) {
+                            const size_t base = (ib + (size_t)s0 * 128 + rr) * 2;
+                            L += fast_exp2(__ldcg(a.partial_ml + base) - Mu) * __ldcg(a.partial_ml + base + 1);
+                        }
+                        L = warp_sum(L);
+                        const float inv = L > 0.f ? 1.f / L : 0.f;
+                        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+                        for (int s0 = 0; s0 < ns; s0 += 32) {
+                            // lane l: the factor of split s0 + l
+                            const int sl = s0 + lane;
+                            const float fl = sl < ns ? fast_exp2(__ldcg(a.partial_ml + (ib + (size_t)sl * 128 + rr) * 2) - Mu) * inv : 0.f;
+                            const int cnt = min(32, ns - s0);
+                            for (int j = 0; j < cnt; j += 4) {
+                                float4 v[8];
+                                float f[4];
+    #pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    f[u] = __shfl_sync(0xffffffffu, fl, (j + u) & 31);
+                                    const bool in = j + u < cnt;
+                                    const float* po = a.partial_o + (ib + (size_t)(s0 + j + u) * 128 + rr) * kLatDv + cbase;
+                                    v[2 * u] = in ? __ldcg(reinterpret_cast<const float4*>(po)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    v[2 * u + 1] = in ? __ldcg(reinterpret_cast<const float4*>(po + 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    if (!in) f[u] = 0.f;
+                                }
+    #pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    acc0.x += f[u] * v[2 * u].x;
+                                    acc0.y += f[u] * v[2 * u].y;
+                                    acc0.z += f[u] * v[2 * u].z;
+                                    acc0.w += f[u] * v[2 * u].w;
+                                    acc1.x += f[u] * v[2 * u + 1].x;
+                                    acc1.y += f[u] * v[2 * u + 1].y;
+                                    acc1.z += f[u] * v[2 * u + 1].z;
+                                    acc1.w += f[u] * v[2 * u + 1].w;
+                                }
+                            }
+                        }
+                        if (SPARSE) {
+                            float* o = a.out_f32 + ((size_t)w.seq * H + h0 + rr) * kLatDv + cbase;
+                            *reinterpret_cast<float4*>(o) = acc0;
+                            *reinterpret_cast<float4*>(o + 128) = acc1;
+                        } else {
+                            __nv_bfloat16* o = a.out_bf16 + ((size_t)t * H + h0 + rr) * kLatDv + cbase;
+                            *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16(acc0.x, acc0.y), pack_bf16(acc0.z, acc0.w));
+                            *reinterpret_cast<uint2*>(o + 128) = make_uint2(pack_bf16(acc1.x, acc1.y), pack_bf16(acc1.z, acc1.w));
+                        }
                     }
                 }
                 if (tid == 0) a.tickets[w.first_item * 2 + rank] = 0;

@@ -721,23 +721,24 @@ __global__ void __launch_bounds__(prefill_warps<RAW>() * 32, 1)
                     }
                     const bool wrote = prow > 0 && p1 > p0;
                     if (wrote) {
-                        // the partial last box: its rows through registers, by the whole warp
+                        // the partial last box: its rows by cp.async, all in flight at once (the
+                        // whole warp; dims past a.head_dim, when the kernel runs at the next
+                        // multiple of 128, are filled with zeros)
                         const int pz0 = __shfl_sync(0xffffffffu, z0, nfull);
                         constexpr int kCh = kPW * 8;  // this warp's 16-byte chunks of a row
                         for (int i = lane; i < prow * kCh; i += 32) {
                             const int tr = i / kCh, c = p0 * 8 + i % kCh;
                             if (c >= D / 8) continue;
                             const int kk = nfull * box_rows + tr;
-                            // dims past a.head_dim (a kernel run at the next multiple of 128) are zeros
-                            const uint4 v = c * 8 < a.head_dim
-                                                ? __ldg(reinterpret_cast<const uint4*>(
-                                                      kvp + ((size_t)(pz0 + tr) * C + 2 * kvh + part) * (size_t)(a.head_dim * 2) +
-                                                      c * 16))
-                                                : make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4*>(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) = v;
+                            const bool in = c * 8 < a.head_dim;
+                            const uint8_t* src = kvp + ((size_t)(pz0 + tr) * C + 2 * kvh + part) * (size_t)(a.head_dim * 2) +
+                                                 (in ? c * 16 : 0);
+                            cp_async16(smem_u32(stage + (c >> 3) * T::kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)), src, in);
                         }
+                        cp_async_commit();
+                        cp_async_wait<0>();
+                        fence_proxy_async_smem();  // thread-copied rows, read by the tensor core
                     }
-                    if (wrote) fence_proxy_async_smem();  // register-written rows, read by the tensor core
                     mbar_arrive(&fbar[slot]);
                 }
             } else {
