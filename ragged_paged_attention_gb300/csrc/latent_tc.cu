@@ -258,40 +258,57 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 const bool rb_p2 = (a.read_block & (a.read_block - 1)) == 0, ps_p2 = (a.page_size & (a.page_size - 1)) == 0;
                 const int rb_sh = __ffs(a.read_block) - 1, ps_sh = __ffs(a.page_size) - 1;
                 const int oob_row = a.total_num_pages * a.page_size;  // gathers zeros
-                auto resolve_row = [&](int j, bool& v) -> int {
-                    const int key = kb + j * BK + kk;
-                    v = lane < 16 && j < nb && key < ke;
-                    if (!v) return oob_row;
-                    const int ui = rb_p2 ? key >> rb_sh : key / a.read_block;
-                    const int ur = rb_p2 ? key & (a.read_block - 1) : key % a.read_block;
-                    const int u = __ldg(a.indices + (size_t)w.seq * a.topk + ui);
+                // A key is resolved in three steps an iteration apart, so that no step waits on
+                // the load of the one before: its unit (index load), then its token, validity and
+                // page-table entry (page load), then its row.
+                auto idx_load = [&](int j, int& u, int& key) {
+                    key = kb + j * BK + kk;
+                    const bool in = lane < 16 && j < nb && key < ke;
+                    const int kc = in ? key : kb;  // a slot of this query: kb < ke when nb > 0
+                    if (!in) key = -1;
+                    u = __ldg(a.indices + (size_t)w.seq * a.topk + (rb_p2 ? kc >> rb_sh : kc / a.read_block));
+                };
+                auto page_load = [&](int u, int key, int& page, int& po, int& st) {
+                    // st: 0 no key, 1 key with a page-table entry (page loaded), 2 key past the table
+                    const int kc = key >= 0 ? key : 0;
+                    const int ur = rb_p2 ? kc & (a.read_block - 1) : kc % a.read_block;
                     const long long kp = (long long)u * a.read_block + ur;
-                    v = u >= 0 && kp <= qpos && kp < kbound;
-                    if (!v) return oob_row;
-                    const int lp = ps_p2 ? (int)(kp >> ps_sh) : (int)(kp / a.page_size);
-                    const int po = ps_p2 ? (int)(kp & (a.page_size - 1)) : (int)(kp % a.page_size);
-                    int page;
+                    const bool v = key >= 0 && u >= 0 && kp <= qpos && kp < kbound;
+                    const long long kpc = v ? kp : 0;
+                    const int lp = ps_p2 ? (int)(kpc >> ps_sh) : (int)(kpc / a.page_size);
+                    po = ps_p2 ? (int)(kpc & (a.page_size - 1)) : (int)(kpc % a.page_size);
+                    long long pidx;
+                    bool pin;
                     if (a.q_base) {  // packed list: the request's run, clamped to the list's end
-                        const long long pidx = min((long long)kbase + lp, (long long)a.max_pages - 1);
-                        page = pidx >= 0 ? __ldg(a.page_table + pidx) : -1;
+                        pidx = min((long long)kbase + lp, (long long)a.max_pages - 1);
+                        pin = pidx >= 0;
                     } else {
-                        page = lp < a.max_pages ? __ldg(a.page_table + (size_t)b * a.max_pages + lp) : -1;
+                        pin = lp < a.max_pages;
+                        pidx = (long long)b * a.max_pages + lp;
                     }
-                    if ((unsigned)page >= (unsigned)a.total_num_pages) {
+                    st = !v ? 0 : pin ? 1 : 2;
+                    page = __ldg(a.page_table + (st == 1 ? pidx : 0));
+                };
+                auto row_of = [&](int page, int po, int st) -> int {
+                    if (st == 0) return oob_row;
+                    const int pg = st == 1 ? page : -1;
+                    if ((unsigned)pg >= (unsigned)a.total_num_pages) {
                         set_error(err, RPA_DEV_ERR_PAGE);
-                        v = false;
                         return oob_row;
                     }
-                    return page * a.page_size + po;
+                    return pg * a.page_size + po;
                 };
-                bool v_next;
-                int row_next = resolve_row(0, v_next);
+                int gu, gkey, gpage, gpo, gst;
+                idx_load(0, gu, gkey);
+                page_load(gu, gkey, gpage, gpo, gst);
+                idx_load(1, gu, gkey);
                 const uint32_t grp_bytes = 4u * nqp * 128;  // one group's four rows, every panel
                 for (int j = 0; j < nb; ++j) {
                     const uint32_t q = jb + j, st = q % NS, par = (q / NS) & 1;
-                    const bool v = v_next;
-                    const int row = row_next;
-                    row_next = resolve_row(j + 1, v_next);
+                    const int row = row_of(gpage, gpo, gst);
+                    const bool v = row != oob_row;
+                    page_load(gu, gkey, gpage, gpo, gst);  // block j + 1
+                    idx_load(j + 2, gu, gkey);
                     int g = 1;
                     if (lane == 0) {
                         g = mbar_wait(&kv_empty[st], par ^ 1, err);
