@@ -50,7 +50,7 @@ constexpr int kOffSRecv = kOffKV + NS * kStage;    // [2]
 constexpr int kOffPRecv = kOffSRecv + 2 * kSRecv;  // [2]
 constexpr int kOffStat = kOffPRecv + 2 * kPRecv;   // (m, l) of the peer's rows
 constexpr int kOffBar = kOffStat + 64 * 8;
-constexpr int kNumBars = 3 * NS + 24;
+constexpr int kNumBars = 3 * NS + 26;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffRed = (kOffTmemSlot + 16 + 127) / 128 * 128;
 constexpr int kOffVld = kOffRed + 2 * 2 * 128 * 4;
@@ -76,7 +76,8 @@ __device__ __forceinline__ int lat_panel_col(int rank, int p) { return rank == 0
 template <bool SPARSE>
 __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     latent_tc_kernel(LatentArgs a, const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_kr,
-                     const __grid_constant__ CUtensorMap tm_kc3, int kv_tma, int box_rows) {
+                     const __grid_constant__ CUtensorMap tm_kc3, const __grid_constant__ CUtensorMap tm_qa,
+                     const __grid_constant__ CUtensorMap tm_qb, int kv_tma, int box_rows, int q_tma) {
     using namespace lat;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -99,6 +100,8 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
     uint64_t* stat_full = bars + 3 * NS + 19;   // (m, l) of the peer's rows landed (bytes)
     uint64_t* itm_full = bars + 3 * NS + 20;    // [2] (MLA, rank 1) the item index from rank 0 landed
     uint64_t* itm_free = bars + 3 * NS + 22;    // [2] (MLA, rank 0) rank 1 has read that slot's index
+    uint64_t* q_land = bars + 3 * NS + 24;      // (Q by TMA) the Q slice's boxes landed in the ring
+    uint64_t* q_free = bars + 3 * NS + 25;      // (Q by TMA) the softmax threads have read them
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     uint8_t* vld = smem + kOffVld;
@@ -140,6 +143,8 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             mbar_init(&p_free[i], 1);
         }
         mbar_init(stat_full, 1);
+        mbar_init(q_land, 1);
+        mbar_init(q_free, 256);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&itm_full[i], 1);  // rank 1 arms the 4 bytes rank 0's st.async delivers
             mbar_init(&itm_free[i], 1);  // rank 1's release arrive
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     idx_load(j + 2, gu, gkey);
                     int g = 1;
                     if (lane == 0) {
-                        g = mbar_wait(&kv_empty[st], par ^ 1, err);
+                        g = mbar_wait(&kv_empty[st], par ^ 1, err) && (j != NS - 2 || !q_tma || mbar_wait(q_free, iph, err));
                         if (g)
                             mbar_expect_tx(&kv_full[st], 4 * grp_bytes);
                         else
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                         for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
                         int g = 1;
                         if (lane == 0) {
-                            g = mbar_wait(&kv_empty[st], par ^ 1, err);
+                            g = mbar_wait(&kv_empty[st], par ^ 1, err) && (j != NS - 2 || !q_tma || mbar_wait(q_free, iph, err));
                             if (g)
                                 mbar_expect_tx(&kv_full[st], bytes);
                             else
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     const bool v = v_next;
                     const __nv_bfloat16* row = row_next;
                     row_next = resolve(j + 1, v_next);
-                    if (!mbar_wait(&kv_empty[st], par ^ 1, err)) {
+                    if (!mbar_wait(&kv_empty[st], par ^ 1, err) || (j == NS - 2 && q_tma && !mbar_wait(q_free, iph, err))) {
                         s_abort = 1;
                         break;
                     }
@@ -610,7 +615,56 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
             const uint32_t precv_peer = mapa_shared(smem_u32(smem + kOffPRecv), peer);
             const uint32_t srecv_full_peer = mapa_shared(smem_u32(srecv_full), peer);
             const uint32_t precv_full_peer = mapa_shared(smem_u32(precv_full), peer);
-            {
+            bool ok = true;
+            if (q_tma) {
+                // Q slice by TMA, 64-row boxes of one 64-dim panel each, into the ring stages of
+                // blocks jb+NS-2 and jb+NS-1 (five boxes a stage): the producers hold back from
+                // those two stages until this CTA's softmax threads have moved the slice on.
+                const uint32_t stA = (jb + NS - 2) % NS, stB = (jb + NS - 1) % NS;
+                auto box_at = [&](int bi) -> uint8_t* {
+                    return smem + kOffKV + (bi < 5 ? stA : stB) * kStage + (bi < 5 ? bi : bi - 5) * kPanel;
+                };
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(q_land, (uint32_t)nqp * 2 * kPanel);
+                    for (int bi = 0; bi < 2 * nqp; ++bi) {
+                        const int p = bi >> 1, y = qrow0 + (bi & 1) * 64;
+                        if (rank == 0 && p == 4 && !(SPARSE && a.q))
+                            tma_load_2d(smem_u32(box_at(bi)), &tm_qb, 0, y, q_land);
+                        else
+                            tma_load_2d(smem_u32(box_at(bi)), &tm_qa, lat_panel_col(rank, p), y, q_land);
+                    }
+                }
+                if (!mbar_wait(q_land, iph, err)) {
+                    s_abort = 1;
+                    ok = false;
+                }
+                // this thread's row, half of its 16-byte chunks, four chunks (16 columns) a store;
+                // 128-byte swizzle: chunk c of box row rr sits at slot c ^ (rr & 7)
+                const int nch = nqp * 4, c0 = half * nch, rr = r & 63;
+#pragma unroll
+                for (int i = 0; i < 20; i += 4) {
+                    if (i < nch) {
+                        uint32_t v[16];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int c = c0 + i + u, p = c >> 3, cc = c & 7;
+                            const int bi = 2 * p + (r >> 6);
+                            const uint8_t* src = box_at(bi) + rr * 128 + ((cc ^ (rr & 7)) << 4);
+                            const uint4 x = *reinterpret_cast<const uint4*>(src);
+                            v[4 * u] = x.x;
+                            v[4 * u + 1] = x.y;
+                            v[4 * u + 2] = x.z;
+                            v[4 * u + 3] = x.w;
+                        }
+                        tmem_st16_nowait(tmem + lane_off + kColQ + (c0 + i) * 4, v);
+                    }
+                }
+                fence_proxy_async_smem();  // these reads before the producers' copies into the stages
+                mbar_arrive(q_free);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(q_full);
+            } else {
                 // Q slice -> TMEM: this thread's row, half of its 16-byte chunks (8 dims = 4
                 // columns each).  The previous item's MMAs have all completed (o_full).
                 const int nch = nqp * 4, c0 = half * nch;
@@ -648,7 +702,6 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                 mbar_arrive(q_full);
             }
             float m_use = -INFINITY, l_half = 0.f;
-            bool ok = true;
             // common tail of a block: once PV of the previous block is done with P and has
             // written O, rescale this row of O by f and store this row's P
             auto finish = [&](uint32_t q, const uint32_t (&pk)[16], float f) -> bool {
@@ -1122,6 +1175,20 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
             if (kv_tma && box_rows == BK && make_tmap_panels(&kc3, a.cache_kv_c, rows, a.lkv_pad)) kv_tma = 2;
         }
     }
+    // Q slices by TMA (bf16 queries): [rows][512 or 576] and the rope part [rows][64], 64-row boxes
+    CUtensorMap qa, qb;
+    memset(&qa, 0, sizeof qa);
+    memset(&qb, 0, sizeof qb);
+    int q_tma = 0;
+    {
+        const uint64_t qrows = SPARSE ? (uint64_t)a.batch * a.num_queries * a.num_heads : (uint64_t)a.max_num_tokens * a.num_heads;
+        if (qrows < 0x7fffffffull) {
+            if (SPARSE && a.q)
+                q_tma = make_tmap_2d(&qa, a.q, kLatDk, qrows, kLatDk, 64);
+            else if (!a.q_fp8)
+                q_tma = make_tmap_2d(&qa, a.ql_nope, kLatDv, qrows, kLatDv, 64) && make_tmap_2d(&qb, a.q_pe, 64, qrows, 64, 64);
+        }
+    }
     auto kern = latent_tc_kernel<SPARSE>;
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg;
@@ -1147,7 +1214,7 @@ static cudaError_t launch_latent_tc(const LatentArgs& a, int num_sms, cudaStream
     }
     cfg.gridDim = dim3(2 * max_clusters);
     ProfScope ps(SPARSE ? "sparse_attn" : "mla_attn", stream);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, kc, kr, kc3, kv_tma, box_rows);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, kc, kr, kc3, qa, qb, kv_tma, box_rows, q_tma);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
