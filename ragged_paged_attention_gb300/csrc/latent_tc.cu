@@ -895,56 +895,64 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                     }
                 }
             }
-            if (ok && mbar_wait(o_full, iph, err)) {
+            // ---- epilogue: this CTA's O half goes row-major through the idle key ring (16-byte
+            // chunks XOR-swizzled by the row, so neither side conflicts), then out a row at a time,
+            // 512 contiguous bytes a warp store.  Every softmax thread reaches the barrier.
+            const bool eok = ok && mbar_wait(o_full, iph, err);
+            if (!eok) s_abort = 1;
+            const bool split = w.num_splits > 1;
+            const bool f32 = SPARSE || split;  // fp32 rows (1 KB), else bf16 rows (512 bytes)
+            const size_t pslot = (size_t)w.first_item + w.split;  // split: the group's slot plus the split
+            uint8_t* tile = smem + kOffKV;
+            if (eok) {
                 tc_fence_after();
-                const bool row_ok = h0 + r < H;
-                const int col0 = (int)rank * 256 + half * 128;
-                if (w.num_splits == 1) {
-                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                const float inv = split ? 1.f : (l_run > 0.f ? 1.f / l_run : 0.f);
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        float o32[32];
-                        tmem_ld32(tmem + lane_off + kColO + half * 128 + c * 32, o32);
-                        if (row_ok) {
-                            if (SPARSE) {
-                                float4* d4 = reinterpret_cast<float4*>(a.out_f32 + ((size_t)w.seq * H + h0 + r) * kLatDv + col0 + c * 32);
+                for (int c = 0; c < 4; ++c) {
+                    float o32[32];
+                    tmem_ld32(tmem + lane_off + kColO + half * 128 + c * 32, o32);
+                    if (f32) {
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    d4[i] = make_float4(o32[4 * i] * inv, o32[4 * i + 1] * inv, o32[4 * i + 2] * inv,
-                                                        o32[4 * i + 3] * inv);
-                            } else {
-                                uint32_t pk[16];
+                        for (int i = 0; i < 8; ++i) {
+                            const int k = half * 32 + c * 8 + i;
+                            *reinterpret_cast<float4*>(tile + r * 1024 + ((k ^ (r & 7)) << 4)) =
+                                make_float4(o32[4 * i] * inv, o32[4 * i + 1] * inv, o32[4 * i + 2] * inv, o32[4 * i + 3] * inv);
+                        }
+                    } else {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(o32[2 * i] * inv, o32[2 * i + 1] * inv);
-                                uint4* d4 = reinterpret_cast<uint4*>(a.out_bf16 + ((size_t)t * H + h0 + r) * kLatDv + col0 + c * 32);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                            }
+                        for (int i = 0; i < 4; ++i) {
+                            const int k = half * 16 + c * 4 + i;
+                            *reinterpret_cast<uint4*>(tile + r * 512 + ((k ^ (r & 7)) << 4)) =
+                                make_uint4(pack_bf16(o32[8 * i] * inv, o32[8 * i + 1] * inv), pack_bf16(o32[8 * i + 2] * inv, o32[8 * i + 3] * inv),
+                                           pack_bf16(o32[8 * i + 4] * inv, o32[8 * i + 5] * inv), pack_bf16(o32[8 * i + 6] * inv, o32[8 * i + 7] * inv));
                         }
                     }
-                } else {
-                    // split: unnormalised O half + (m, l) to the workspace
-                    // partials live at the group's slot (split 0's index plus the split)
-                    const size_t pslot = (size_t)w.first_item + w.split;
-                    float* po = a.partial_o + (pslot * 128 + r) * kLatDv + col0;
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        float o32[32];
-                        tmem_ld32(tmem + lane_off + kColO + half * 128 + c * 32, o32);
-                        float4* d4 = reinterpret_cast<float4*>(po + c * 32);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) d4[i] = make_float4(o32[4 * i], o32[4 * i + 1], o32[4 * i + 2], o32[4 * i + 3]);
-                    }
-                    if (half == 0) {
-                        a.partial_ml[(pslot * 128 + r) * 2] = m_use;
-                        a.partial_ml[(pslot * 128 + r) * 2 + 1] = l_run;
-                    }
                 }
-            } else {
-                s_abort = 1;
+                if (split && half == 0) {
+                    a.partial_ml[(pslot * 128 + r) * 2] = m_use;
+                    a.partial_ml[(pslot * 128 + r) * 2 + 1] = l_run;
+                }
             }
             tc_fence_before();
+            asm volatile("bar.sync 5, 256;" ::: "memory");
+            // rows warp, warp + 8, ...: the lanes take consecutive chunks of a row
+#pragma unroll 1
+            for (int rr = warp; rr < 128; rr += 8) {
+                if (h0 + rr >= H) continue;
+                if (f32) {
+                    float* dst = split ? a.partial_o + (pslot * 128 + rr) * kLatDv + rank * 256
+                                       : a.out_f32 + ((size_t)w.seq * H + h0 + rr) * kLatDv + rank * 256;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int k = hh * 32 + lane;
+                        reinterpret_cast<uint4*>(dst)[k] = *reinterpret_cast<const uint4*>(tile + rr * 1024 + ((k ^ (rr & 7)) << 4));
+                    }
+                } else {
+                    __nv_bfloat16* dst = a.out_bf16 + ((size_t)t * H + h0 + rr) * kLatDv + rank * 256;
+                    reinterpret_cast<uint4*>(dst)[lane] = *reinterpret_cast<const uint4*>(tile + rr * 512 + ((lane ^ (rr & 7)) << 4));
+                }
+            }
+            fence_proxy_async_smem();  // the ring is refilled by TMA for the next item
         }
         jb += nb;
         ++items;
