@@ -388,11 +388,14 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                                     tma_load_2d(dst, &tm_kc, lat_panel_col(rank, p), row0, &kv_full[st]);
                             }
                         }
-                        // a partial box (the sequence's last keys): its rows by cp.async, all of
-                        // them in flight at once (rows past the range keep finite stale data,
-                        // whose scores the mask drops)
+                        // a box that is not full (the sequence's last keys): its rows by cp.async,
+                        // all of them in flight at once.  Past the range the mask drops the scores
+                        // (a select, whatever the bytes), but P = 0 multiplies the value rows, and
+                        // 0 * v is 0 only for finite v: those rows' value panels get zeros (the
+                        // ring's stale bytes may be fp32 words of an output tile or merge weights)
                         uint32_t pm = __ballot_sync(0xffffffffu, rows > 0 && !full);
-                        const bool wrote = pm != 0;
+                        uint32_t pz = __ballot_sync(0xffffffffu, lane < nbox && !full);
+                        const bool wrote = pz != 0;
                         while (pm) {
                             const int src = __ffs(pm) - 1;
                             pm &= pm - 1;
@@ -405,6 +408,15 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                                                                   ? a.cache_k_pe + (size_t)(pr0 + r) * a.r_pad
                                                                   : a.cache_kv_c + (size_t)(pr0 + r) * a.lkv_pad + lat_panel_col(rank, p);
                                 cp_async16(smem_u32(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)), s_row + c * 8, true);
+                            }
+                        }
+                        while (pz) {
+                            const int src = __ffs(pz) - 1;
+                            pz &= pz - 1;
+                            const int prow = __shfl_sync(0xffffffffu, rows, src);
+                            for (int i = lane; i < (box_rows - prow) * 32; i += 32) {
+                                const int kk = src * box_rows + prow + (i >> 5), p = (i >> 3) & 3, c = i & 7;
+                                *reinterpret_cast<uint4*>(stage + p * kPanel + kk * 128 + ((c ^ (kk & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                             }
                         }
                         if (wrote) {
@@ -490,6 +502,11 @@ __global__ void __launch_bounds__(lat::kWarps * 32, 1)
                                 cp_async16(smem_u32(stage + p * kPanel + kk * 128 + ((cc ^ (kk & 7)) << 4)), src, true);
                             }
                         }
+                    } else {
+                        // a key that is not valid: zeros in its value panels (its P is 0, and
+                        // 0 * v is 0 only for finite v)
+                        for (int c = hh * 16; c < hh * 16 + 16; ++c)
+                            *reinterpret_cast<uint4*>(stage + (c >> 3) * kPanel + kk * 128 + (((c & 7) ^ (kk & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                     }
                     cp_async_commit();
                     if (SPARSE) {

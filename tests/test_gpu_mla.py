@@ -44,6 +44,15 @@ def test_mla_prefill_from_zero_and_short_keys():
     run_and_check(m)
 
 
+@pytest.mark.parametrize("page_size", [64, 16])
+def test_mla_short_items_after_split_items(page_size):
+    # a long decode row (split items: fp32 partials, merged) beside a causal prefill whose rows
+    # see 1..256 keys: short items follow long ones on the same CTAs, and a block that is not
+    # full must hold zeros, never stale shared-memory bytes, past its keys
+    m = workloads.make_mla([1, 256], [24000, 256], seed=27, page_size=page_size)
+    run_and_check(m)
+
+
 def test_mla_full_size_sampled():
     m = workloads.mla_deepseek()
     run_and_check(m, tokens=sample_tokens(m.q_lens, per_chunk=4))
