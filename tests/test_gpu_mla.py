@@ -53,6 +53,14 @@ def test_mla_short_items_after_split_items(page_size):
     run_and_check(m)
 
 
+@pytest.mark.parametrize("page_size", [12, 4])
+def test_mla_register_gather_page_sizes(page_size):
+    # page sizes that no TMA box fits (not a power of two, or under 8 rows): the key rows come
+    # through the register-gather instantiation
+    m = workloads.make_mla([1, 1, 40], [700, 65, 300], seed=28, page_size=page_size, max_num_tokens=48)
+    run_and_check(m)
+
+
 def test_mla_full_size_sampled():
     m = workloads.mla_deepseek()
     run_and_check(m, tokens=sample_tokens(m.q_lens, per_chunk=4))
